@@ -1,0 +1,298 @@
+"""Seeded synthetic inputs for the batched draft-verify step.
+
+This module is the one piece that the CUDA library's tests and the CPU
+oracle both consume.  It holds none of the verify method's arithmetic: it
+builds logit rows, picks temperatures, and draws draft tokens from the
+drafter's own law (by the Gumbel-max trick, argmax_t(y_t / T + G_t) with
+G_t standard Gumbel, which is a draw from softmax(y / T) without forming
+it; or by the inverse CDF of a probability vector this module itself
+constructed).  It never normalises a logit row, never evaluates an
+acceptance test and never samples a residual.
+
+Logit recipe ("Speculative Decoding and EAGLE-3" lesson, "Build it" step 6:
+the draft is the target perturbed by noise of a chosen amplitude): a target
+row is Zipf-shaped, z_t = -s ln(rank_t) + N(0, 0.3) with the ranks a fresh
+random permutation of 1..V per row; its draft row is z + N(0, sigma).  Rows
+are built in float32/float64 and cast to the storage dtype last, so both
+sides see the same quantised values.
+
+The five named workloads follow the method statement's five configurations:
+
+  tiny-f32         B=1,   N=4, V=1024,   fp32, sigma 0.5, T 1
+  single-bf16      B=1,   N=5, V=128256, bf16, sigma tuned so that the mean
+                   sum_t min(p, q) over rows is about 0.8; T 1 (or 0)
+  batch64-bf16     B=64,  N=7, V=128256, bf16, sigma_b ~ U[0.2, 1.5],
+                   T_b uniform over {0, 0.7, 1.0}
+  mixture-bf16     B=16,  N=3, V=163840, bf16, half of the 64 target rows
+                   peaked (top-1 mass 0.95 on a Zipf-0.8 base), half flat
+                   Zipf-0.8; sigma 0.4, T 1
+  alpha09-f32      B=256, N=8, V=32000,  fp32, drafts built with per-position
+                   overlap sum_t min(p, q) = 0.9 exactly in real arithmetic;
+                   T 1; draft tokens redrawn for every verify seed
+"""
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+DTYPES = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+# Draft noise for the single-request V=128256 workload, chosen by bisection
+# on the oracle's mean overlap sum_t min(p, q) (target 0.8).  The script
+# that finds it is tests/golden/make_single_bf16_sigma.py; a CPU test checks
+# that the value still gives 0.80 +- 0.01.
+SINGLE_BF16_SIGMA = 0.47816771268844604
+
+
+@dataclasses.dataclass
+class Workload:
+    """One batch of verify inputs on the host (torch CPU tensors)."""
+
+    name: str
+    dtype: str                  # "bf16" | "f32"
+    target: torch.Tensor        # [B, N+1, V]
+    draft: torch.Tensor         # [B, N, V]
+    tokens: torch.Tensor        # [B, N] int32
+    temperature: torch.Tensor   # [B] float32
+    seed: int                   # verify seed
+
+    @property
+    def shape(self):
+        b, n1, v = self.target.shape
+        return b, n1 - 1, v
+
+    def raw(self):
+        """(target, draft) as numpy arrays in the oracle's input form:
+        uint16 bit patterns for bf16, float32 values for fp32."""
+        if self.dtype == "bf16":
+            return (self.target.view(torch.int16).numpy().view(np.uint16),
+                    self.draft.view(torch.int16).numpy().view(np.uint16))
+        return self.target.numpy(), self.draft.numpy()
+
+    def bytes_read(self):
+        """Logit bytes one full verify pass reads: every target row, plus the
+        draft rows of requests with T > 0."""
+        b, n, v = self.shape
+        esize = self.target.element_size()
+        sampled = int((self.temperature > 0).sum())
+        return (b * (n + 1) + sampled * n) * v * esize
+
+
+# --------------------------------------------------------------------------
+# Building blocks
+# --------------------------------------------------------------------------
+
+def _gen(seed):
+    g = torch.Generator()
+    g.manual_seed(int(seed))
+    return g
+
+
+def _neg_log_rank(gen, rows, vocab):
+    """-ln(rank_t) per row, with ranks a fresh random permutation of 1..V."""
+    out = torch.empty(rows, vocab, dtype=torch.float64)
+    base = -torch.log(torch.arange(1, vocab + 1, dtype=torch.float64))
+    for r in range(rows):
+        perm = torch.randperm(vocab, generator=gen)
+        out[r, perm] = base
+    return out
+
+
+def _gumbel_argmax(gen, logits_f64, temperature):
+    """One draw from softmax(logits / T) per row via argmax(logits/T + G),
+    G standard Gumbel; argmax of the logits when T == 0 (first index on
+    ties)."""
+    rows = logits_f64.shape[0]
+    out = np.zeros(rows, dtype=np.int32)
+    for r in range(rows):
+        x = logits_f64[r]
+        if temperature == 0:
+            out[r] = int(np.argmax(x))
+            continue
+        u = torch.rand(x.shape[0], generator=gen, dtype=torch.float64).numpy()
+        u = np.clip(u, 1e-300, 1.0 - 1e-16)
+        g = -np.log(-np.log(u))
+        out[r] = int(np.argmax(x / temperature + g))
+    return out
+
+
+def _widen(t):
+    """Stored logits as float64 (exact)."""
+    return t.to(torch.float64).numpy()
+
+
+def _zipf_rows(gen, rows, vocab, s, noise):
+    z = s * _neg_log_rank(gen, rows, vocab)
+    if noise:
+        z += noise * torch.randn(rows, vocab, generator=gen, dtype=torch.float64)
+    return z
+
+
+def make_zipf(batch, n, vocab, dtype, *, gen_seed, verify_seed=0, s=1.1,
+              target_noise=0.3, sigma=0.5, temperatures=1.0, name="zipf"):
+    """Zipf-shaped target rows, draft = target + N(0, sigma_b), tokens drawn
+    from the drafter at each request's temperature.
+
+    ``sigma`` and ``temperatures`` are a scalar or one value per request.
+    """
+    gen = _gen(gen_seed)
+    sig = np.broadcast_to(np.asarray(sigma, dtype=np.float64), (batch,))
+    temps = np.broadcast_to(np.asarray(temperatures, dtype=np.float32), (batch,)).copy()
+    tdt = DTYPES[dtype]
+    target = torch.empty(batch, n + 1, vocab, dtype=tdt)
+    draft = torch.empty(batch, n, vocab, dtype=tdt)
+    tokens = np.zeros((batch, n), dtype=np.int32)
+    for b in range(batch):
+        z = _zipf_rows(gen, n + 1, vocab, s, target_noise)
+        target[b] = z.to(tdt)
+        if n == 0:
+            continue
+        y = z[:n] + float(sig[b]) * torch.randn(n, vocab, generator=gen, dtype=torch.float64)
+        draft[b] = y.to(tdt)
+        tokens[b] = _gumbel_argmax(gen, _widen(draft[b]), float(temps[b]))
+    return Workload(name, dtype, target, draft, torch.from_numpy(tokens),
+                    torch.from_numpy(temps), int(verify_seed))
+
+
+def make_random(batch, n, vocab, dtype, *, gen_seed, verify_seed=0, temps=(0.0, 0.7, 1.0),
+                sigma=(0.2, 1.5), s=1.1):
+    """A small mixed batch for parity tests: per-request sigma ~ U[sigma],
+    per-request T uniform over ``temps``."""
+    gen = _gen(gen_seed + 7919)
+    lo, hi = sigma
+    sig = (lo + (hi - lo) * torch.rand(batch, generator=gen, dtype=torch.float64)).numpy()
+    pick = torch.randint(0, len(temps), (batch,), generator=gen).numpy()
+    tv = np.asarray(temps, dtype=np.float32)[pick]
+    return make_zipf(batch, n, vocab, dtype, gen_seed=gen_seed, verify_seed=verify_seed,
+                     s=s, sigma=sig, temperatures=tv, name=f"random-{dtype}-B{batch}-N{n}-V{vocab}")
+
+
+# --------------------------------------------------------------------------
+# The five named workloads
+# --------------------------------------------------------------------------
+
+def tiny_f32():
+    """B=1, N=4, V=1024, fp32, sigma 0.5, T 1, verify seed 0."""
+    return make_zipf(1, 4, 1024, "f32", gen_seed=1001, verify_seed=0, sigma=0.5,
+                     temperatures=1.0, name="tiny-f32")
+
+
+def single_bf16(temperature=1.0, sigma=None):
+    """B=1, N=5, V=128256, bf16, sigma tuned for mean overlap ~0.8."""
+    sig = SINGLE_BF16_SIGMA if sigma is None else sigma
+    return make_zipf(1, 5, 128256, "bf16", gen_seed=1002, verify_seed=0, sigma=sig,
+                     temperatures=temperature, name=f"single-bf16-T{temperature:g}")
+
+
+def batch64_bf16(verify_seed=0, gen_seed=1003):
+    """B=64, N=7, V=128256, bf16; sigma_b ~ U[0.2, 1.5]; T_b from {0, 0.7, 1}."""
+    gen = _gen(gen_seed + 104729)
+    sig = (0.2 + 1.3 * torch.rand(64, generator=gen, dtype=torch.float64)).numpy()
+    pick = torch.randint(0, 3, (64,), generator=gen).numpy()
+    temps = np.array([0.0, 0.7, 1.0], dtype=np.float32)[pick]
+    return make_zipf(64, 7, 128256, "bf16", gen_seed=gen_seed, verify_seed=verify_seed,
+                     sigma=sig, temperatures=temps, name="batch64-bf16")
+
+
+def mixture_bf16(verify_seed=0):
+    """B=16, N=3, V=163840, bf16: half of the 64 target rows peaked (top-1
+    mass 0.95 over a Zipf-0.8 base), half flat Zipf-0.8; sigma 0.4; T 1."""
+    batch, n, vocab = 16, 3, 163840
+    gen = _gen(1004)
+    rows = batch * (n + 1)
+    peaked = torch.zeros(rows, dtype=torch.bool)
+    peaked[torch.randperm(rows, generator=gen)[: rows // 2]] = True
+    tdt = torch.bfloat16
+    target = torch.empty(batch, n + 1, vocab, dtype=tdt)
+    draft = torch.empty(batch, n, vocab, dtype=tdt)
+    tokens = np.zeros((batch, n), dtype=np.int32)
+    for b in range(batch):
+        nlr = _neg_log_rank(gen, n + 1, vocab)          # -ln(rank)
+        z = 0.8 * nlr                                    # flat Zipf-0.8 logits
+        for j in range(n + 1):
+            if not peaked[b * (n + 1) + j]:
+                continue
+            # Probability vector: rank 1 gets 0.95, the rest share 0.05 in
+            # Zipf-0.8 proportions; the logits are its logarithm.
+            w = torch.exp(z[j])                          # rank^-0.8
+            top = int(torch.argmax(nlr[j]))
+            rest = w.clone()
+            rest[top] = 0.0
+            q = 0.05 * rest / rest.sum()
+            q[top] = 0.95
+            z[j] = torch.log(q)
+        target[b] = z.to(tdt)
+        y = z[:n] + 0.4 * torch.randn(n, vocab, generator=gen, dtype=torch.float64)
+        draft[b] = y.to(tdt)
+        tokens[b] = _gumbel_argmax(gen, _widen(draft[b]), 1.0)
+    temps = np.ones(batch, dtype=np.float32)
+    return Workload("mixture-bf16", "bf16", target, draft, torch.from_numpy(tokens),
+                    torch.from_numpy(temps), int(verify_seed))
+
+
+class Alpha09:
+    """B=256, N=8, V=32000, fp32 rows with sum_t min(p_j, q_j) = 0.9.
+
+    Per row the target law q is built directly as a probability vector
+    (Zipf-1.1 weights times log-normal(0, 0.3) noise, divided by their sum);
+    a random set S with q(S) >= 0.2 is chosen by walking a random token order;
+    the draft law is p = q (1 - 0.1/q(S)) on S and q (1 + 0.1/(1 - q(S)))
+    off S, so the total-variation distance is 0.1.  Logits are ln q and ln p
+    stored as float32.  ``tokens(s)`` redraws every d_{b,j} ~ p_{b,j} for
+    verify seed s by the inverse CDF of this module's own p.
+    """
+
+    batch, n, vocab = 256, 8, 32000
+    alpha = 0.9
+
+    def __init__(self, gen_seed=1005):
+        gen = _gen(gen_seed)
+        b, n, v = self.batch, self.n, self.vocab
+        self.q = np.zeros((b, n + 1, v))
+        self.p = np.zeros((b, n, v))
+        base = torch.arange(1, v + 1, dtype=torch.float64) ** -1.1
+        for i in range(b):
+            for j in range(n + 1):
+                w = torch.empty(v, dtype=torch.float64)
+                w[torch.randperm(v, generator=gen)] = base
+                w *= torch.exp(0.3 * torch.randn(v, generator=gen, dtype=torch.float64))
+                q = (w / w.sum()).numpy()
+                self.q[i, j] = q
+                if j == n:
+                    continue
+                order = torch.randperm(v, generator=gen).numpy()
+                k = int(np.searchsorted(np.cumsum(q[order]), 0.2)) + 1
+                in_s = np.zeros(v, dtype=bool)
+                in_s[order[:k]] = True
+                qs = q[in_s].sum()
+                p = np.where(in_s, q * (1.0 - 0.1 / qs), q * (1.0 + 0.1 / (1.0 - qs)))
+                self.p[i, j] = p
+        self.target = torch.from_numpy(np.log(self.q).astype(np.float32))
+        self.draft = torch.from_numpy(np.log(self.p).astype(np.float32))
+        self._cdf = np.cumsum(self.p, axis=2)
+        self.temperature = torch.ones(b, dtype=torch.float32)
+
+    def tokens(self, verify_seed):
+        gen = _gen(50000 + int(verify_seed))
+        u = torch.rand(self.batch, self.n, generator=gen, dtype=torch.float64).numpy()
+        out = np.zeros((self.batch, self.n), dtype=np.int32)
+        for i in range(self.batch):
+            for j in range(self.n):
+                c = self._cdf[i, j]
+                t = int(np.searchsorted(c, u[i, j] * c[-1], side="right"))
+                out[i, j] = min(t, self.vocab - 1)
+        return torch.from_numpy(out)
+
+    def workload(self, verify_seed):
+        return Workload("alpha09-f32", "f32", self.target, self.draft,
+                        self.tokens(verify_seed), self.temperature, int(verify_seed))
+
+
+NAMED = {
+    "tiny-f32": tiny_f32,
+    "single-bf16": single_bf16,
+    "batch64-bf16": batch64_bf16,
+    "mixture-bf16": mixture_bf16,
+}
