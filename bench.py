@@ -1,0 +1,387 @@
+"""Benchmark of the batched draft-verify step on the batch64-bf16 workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload: B=64 requests, N=7 drafts, V=128256 vocabulary, bf16 logits,
+per-request draft noise sigma ~ U[0.2, 1.5] and temperature from
+{0, 0.7, 1.0} (synthetic, seeded).  One step = one spec_verify call over the
+whole batch (row statistics, walk, residual/bonus sampling).
+
+Metric: verified draft positions per second (B*N per step), plus the
+achieved HBM bandwidth of the row-statistics kernel against the measured
+copy bandwidth of the GPU.  Under torchrun each rank verifies its own batch
+(weak scaling, no collective on the data path); the timed region is
+bracketed by barriers and the slowest rank's time is used.
+
+--impl reference times the CPU oracle (float64, one host thread) on the same
+metric, a bounded sample of requests per step.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft positions/sec"
+UNIT = "positions/s"
+WORKLOAD = "batch64-bf16"
+PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC = os.path.join(ROOT, "profiles", "rowstats_traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--copies", type=int, default=3, help="rotating input copies in HBM")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def csrc_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "speculative_decoding_verification_73_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_per_launch():
+    """DRAM bytes per row-statistics launch from the committed ncu summary, or
+    None if the kernel sources changed since it was taken."""
+    try:
+        with open(TRAFFIC) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("csrc_hash") != csrc_hash():
+        return None
+    return t.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        self.t0 = time.time()
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t_begin, t_end):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        # samples are 50 ms apart; attribute them to the timed region by order
+        n = len(rows)
+        span = max(time.time() - self.t0, 1e-9)
+        sel = []
+        for i, r in enumerate(rows):
+            t = self.t0 + span * (i + 0.5) / max(n, 1)
+            if t_begin - 0.05 <= t <= t_end + 0.05:
+                sel.append(r)
+        if not sel and rows:
+            sel = rows[-max(1, n // 4):]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in sel if num(r[1]) is not None]
+        mx = [num(r[2]) for r in sel if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in sel for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sel)}
+
+
+# --------------------------------------------------------------------------- ours
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_verification_73_gb300 import binding, build, workloads
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build.build()
+    dev = torch.device("cuda", local)
+
+    wl = workloads.batch64_bf16(verify_seed=rank)
+    B, N, V = wl.shape
+    copies = max(1, args.copies)
+    target = [wl.target.to(dev) for _ in range(copies)]
+    draft = [wl.draft.to(dev) for _ in range(copies)]
+    tokens = wl.tokens.to(dev)
+    temperature = wl.temperature.to(dev)
+    stream = torch.cuda.current_stream(dev)
+    sv = binding.SpecVerify(B, N, V, torch.bfloat16, stream=stream, device=dev)
+    out_t = sv.out_tokens[: B * (N + 1)].view(B, N + 1)
+    out_a, out_k = sv.out_accept[:B], sv.out_kv[:B]
+
+    # the timed loop calls the C ABI directly with pointers prepared once
+    lib = binding.load()
+    import ctypes
+    P = ctypes.c_void_p
+    ptrs = [(P(target[c].data_ptr()), P(draft[c].data_ptr())) for c in range(copies)]
+    p_tok, p_temp = P(tokens.data_ptr()), P(temperature.data_ptr())
+    p_ot, p_oa, p_ok = P(out_t.data_ptr()), P(out_a.data_ptr()), P(out_k.data_ptr())
+
+    def step(i):
+        zt, yt = ptrs[i % copies]
+        rc = lib.spec_verify(sv.ctx, B, N, V, zt, yt, p_tok, p_temp, ctypes.c_uint64(i), p_ot, p_oa, p_ok)
+        if rc != 0:
+            raise binding.SpecVerifyError(rc, "spec_verify")
+
+    for i in range(args.warmup):
+        step(i)
+    code, _ = sv.get_error()
+    assert code == 0, binding.strerror(code)
+    binding.spec_verify_profile_read(sv.ctx)  # clear
+    binding.spec_verify_profile(sv.ctx, True)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t_begin = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_end = time.time()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    kernel_ms, calls = binding.spec_verify_profile_read(sv.ctx)
+    binding.spec_verify_profile(sv.ctx, False)
+    time.sleep(0.2)
+    clk = clocks.stop(t_begin, t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    positions = B * N * args.steps * world
+    value = positions / (elapsed_ms / 1e3)
+    bytes_per_launch = wl.bytes_read()
+    rowstats_ms = kernel_ms["rowstats"] / max(calls, 1)
+    achieved = bytes_per_launch / (rowstats_ms / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    # ---- end to end through the C ABI with host buffers (pinned), rank-local
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 200))
+    h_target = wl.target.pin_memory()
+    h_draft = wl.draft.pin_memory()
+    h_tokens = wl.tokens.pin_memory()
+    h_temp = wl.temperature.pin_memory()
+    h_out_t = torch.empty(B, N + 1, dtype=torch.int32).pin_memory()
+    h_out_a = torch.empty(B, dtype=torch.int32).pin_memory()
+    h_out_k = torch.empty(B, dtype=torch.int32).pin_memory()
+    d_target, d_draft = target[0], draft[0]
+    h2d = sum(t.numel() * t.element_size() for t in (h_target, h_draft, h_tokens, h_temp))
+    d2h = sum(t.numel() * t.element_size() for t in (h_out_t, h_out_a, h_out_k))
+
+    def e2e_step(i):
+        d_target.copy_(h_target, non_blocking=True)
+        d_draft.copy_(h_draft, non_blocking=True)
+        tokens.copy_(h_tokens, non_blocking=True)
+        temperature.copy_(h_temp, non_blocking=True)
+        binding.spec_verify(sv.ctx, d_target, d_draft, tokens, temperature, i, out_t, out_a, out_k)
+        h_out_t.copy_(out_t, non_blocking=True)
+        h_out_a.copy_(out_a, non_blocking=True)
+        h_out_k.copy_(out_k, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = B * N * e2e_steps * world / (e2e_ms / 1e3)
+    code, _ = sv.get_error()
+    assert code == 0, binding.strerror(code)
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 logits, f32 accumulate",
+        "data": "synthetic (seeded Zipf logits, Gaussian draft noise)",
+        "config": {
+            "workload": WORKLOAD, "B": B, "N": N, "V": V, "logits": "bf16",
+            "temperatures": "per request from {0, 0.7, 1.0}",
+            "sampled_requests": int((wl.temperature > 0).sum()),
+            "bytes_read_per_step": bytes_per_launch,
+            "l2": f"inputs larger than L2: {bytes_per_launch / 1e6:.0f} MB read per step, "
+                  f"{copies} rotating copies",
+            "parallelism": f"replicas x{world} (requests shard, no collective)",
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "rowstats", "achieved": achieved, "peak": peak,
+            "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic_per_launch(), "algorithmic_bytes_per_launch": bytes_per_launch,
+            "avg_launch_us": rowstats_ms * 1e3,
+        },
+        "kernel_us_per_step": {k: v / max(calls, 1) * 1e3 for k, v in kernel_ms.items()},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": calls * binding.spec_verify_launches_per_call(),
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, budget_s=12.0)
+    sv.close()
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+# --------------------------------------------------------------------------- oracle
+
+def oracle_requests(wl, idx):
+    """Run the CPU oracle on the listed requests of a workload."""
+    from oracle import verify as ov
+    z, y = wl.raw()
+    d = wl.tokens.numpy()
+    t = wl.temperature.numpy()
+    for b in idx:
+        ov.verify_request(z[b], y[b], d[b], t[b], wl.seed, b, wl.dtype)
+
+
+def cpu_baseline(wl, budget_s):
+    """The oracle, as it stands, on whole requests of the workload until the
+    budget is spent; one host thread (numpy float64)."""
+    B, N, _ = wl.shape
+    done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        oracle_requests(wl, [done % B])
+        done += 1
+    el = time.perf_counter() - t0
+    return {"value": done * N / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} requests of {WORKLOAD} (request i = step i mod {B}), "
+                      f"{el:.1f} s, float64 numpy on 1 host thread"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from speculative_decoding_verification_73_gb300 import workloads
+    wl = workloads.batch64_bf16()
+    B, N, V = wl.shape
+    # time one request to size the per-step sample so the run stays within ~3 minutes
+    t0 = time.perf_counter()
+    oracle_requests(wl, [0])
+    per_req = time.perf_counter() - t0
+    per_step = max(1, min(B, int(150.0 / max(args.steps + args.warmup, 1) / max(per_req, 1e-3))))
+    for i in range(args.warmup):
+        oracle_requests(wl, [(i * per_step + k) % B for k in range(per_step)])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_requests(wl, [(i * per_step + k) % B for k in range(per_step)])
+    el = time.perf_counter() - t0
+    value = per_step * N * args.steps / el
+    sample = f"{per_step} request(s) of {WORKLOAD} per step (rotating), float64 numpy, 1 host thread"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "N": N, "V": V, "logits": "bf16"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

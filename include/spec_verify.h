@@ -1,0 +1,183 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 batched draft-verify step of
+ * speculative decoding.
+ *
+ * What one call computes (the "Speculative Decoding and EAGLE-3" lesson,
+ * factory.pai-world.com, sections "Invariant: Leviathan rejection
+ * sampling", "Build it" steps 1-4 and "KV cache rollback"):
+ *
+ *   for each request b (independently):
+ *     q_j = softmax(target_logits[b, j-1, :] / T_b)   j = 1..N+1  (verifier)
+ *     p_j = softmax(draft_logits [b, j-1, :] / T_b)   j = 1..N    (drafter)
+ *     walk j = 1..N left to right:
+ *        accept d_j iff p_j(d_j) == 0 or u_j < min(1, q_j(d_j) / p_j(d_j))
+ *        at the first rejection j*: emit one token sampled from the residual
+ *        (q_j* - p_j*)_+ / ||(q_j* - p_j*)_+||_1 (from q_j* if that is all 0)
+ *     if all N are accepted: emit a bonus token sampled from q_{N+1}
+ *   T_b == 0 is the greedy argmax-match path: d_j is accepted iff it equals
+ *   argmax target_logits[b, j-1, :] (lowest index on ties); the token after
+ *   the accepted prefix is the argmax of the next target row; draft logits
+ *   are not read.
+ *
+ * Random numbers: Philox4x32-10 (Salmon et al., "Parallel Random Numbers:
+ * As Easy as 1, 2, 3", SC'11) with key = (seed low 32 bits, seed high 32
+ * bits) and counter = (b, j, draw, 0); draw 0 is the accept test at 1-based
+ * position j, draw 1 is the correction at j* or the bonus at j = N+1;
+ * u = (word0 >> 8) * 2^-24.  Samples use the inverse CDF in vocabulary
+ * order: the smallest t whose running sum exceeds u times the total.
+ *
+ * Layout: every tensor is dense row-major, caller-owned DEVICE memory
+ * (cudaMalloc / torch CUDA tensors on the context's device).  Logits are
+ * float32 or bfloat16 as fixed at init.  Rows whose byte offset is a
+ * multiple of 16 (V * sizeof(elem) % 16 == 0 and 16-byte aligned bases)
+ * take the vectorised path; any other V works through a scalar path.
+ *
+ * Calls are asynchronous on the stream given at init and never block the
+ * host.  The library never aborts, traps or prints.  A single context must
+ * not be used from two host threads at once; calls on one context are
+ * ordered by its stream (the workspace is reused by the next call).
+ */
+#ifndef SPEC_VERIFY_H_
+#define SPEC_VERIFY_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------ */
+#define SV_OK          0  /* success                                          */
+#define SV_EINVAL      1  /* host check: null pointer, size or dtype out of range */
+#define SV_EBADTEMP    2  /* device check: a temperature is negative, NaN, inf
+                             or a positive subnormal                           */
+#define SV_EBADTOKEN   3  /* device check: a draft token outside [0, V)        */
+#define SV_EBADLOGIT   4  /* device check: a row that is read holds NaN or +inf,
+                             or all of its entries are -inf                    */
+#define SV_ECUDA       5  /* a CUDA runtime call failed                        */
+
+/* Bits of the device error word (spec_verify_get_error).  A request that
+ * fails a device check gets out_tokens = -1 everywhere, out_accept_len = -1
+ * and out_kv_len = 0; the checks run in the order temperature, tokens,
+ * logits and only the first failing one is recorded for the request. */
+#define SV_ERRBIT_TEMP   1u
+#define SV_ERRBIT_TOKEN  2u
+#define SV_ERRBIT_LOGIT  4u
+
+/* ---- logit element types ---------------------------------------------- */
+#define SV_F32   0
+#define SV_BF16  1
+
+/* Limits of one context. */
+#define SV_MAX_N 255            /* drafts per request                       */
+#define SV_MAX_V (1 << 26)      /* vocabulary size                          */
+
+typedef struct spec_verify_ctx spec_verify_ctx;   /* opaque, library-owned */
+
+/*
+ * spec_verify_init -- create a context on the current CUDA device.
+ *
+ *   ctx          out: the new context (NULL on failure)
+ *   max_B        1 .. 2^20 requests per call
+ *   max_N        0 .. SV_MAX_N drafts per request
+ *   max_V        1 .. SV_MAX_V vocabulary size
+ *   dtype        SV_F32 or SV_BF16: element type of both logit tensors
+ *   cuda_stream  cudaStream_t the calls are enqueued on (NULL = legacy
+ *                default stream)
+ *
+ * Allocates the whole device workspace once (per-row partial statistics,
+ * per-request walk results and sampling sums; a few MB at most) and zeroes
+ * the parts that must start at zero.  Returns SV_OK, SV_EINVAL or SV_ECUDA.
+ */
+int spec_verify_init(spec_verify_ctx** ctx, int max_B, int max_N, int max_V,
+                     int dtype, void* cuda_stream);
+
+/*
+ * spec_verify -- one batched verify step.
+ *
+ *   B, N, V          0 <= B <= max_B, 0 <= N <= max_N, 1 <= V <= max_V
+ *   target_logits    [B, N+1, V] dtype: rows j = 0..N give q_1..q_{N+1}
+ *   draft_logits     [B, N, V] dtype: rows j = 0..N-1 give p_1..p_N
+ *                    (may be NULL only when N == 0)
+ *   draft_tokens     [B, N] int32, each in [0, V)
+ *   temperature      [B] float32: 0 = greedy, else finite and >= 2^-126
+ *   seed             64-bit Philox key
+ *   out_tokens       [B, N+1] int32: the a_b accepted drafts, then the
+ *                    correction or bonus token, then -1 padding
+ *   out_accept_len   [B] int32: a_b in [0, N], drafts accepted
+ *   out_kv_len       [B] int32: a_b + 1, KV entries of this verify window to
+ *                    commit (the verified input token plus the accepted
+ *                    drafts; the lesson's "KV cache rollback": the logical
+ *                    length stops right after the correction token)
+ *
+ * B == 0 is a no-op.  Returns SV_OK, SV_EINVAL (nothing enqueued) or
+ * SV_ECUDA.  Device-detected input errors do not change the return value:
+ * they mark the request's outputs (see SV_ERRBIT_*) and are read with
+ * spec_verify_get_error.
+ */
+int spec_verify(spec_verify_ctx* ctx, int B, int N, int V,
+                const void* target_logits, const void* draft_logits,
+                const int32_t* draft_tokens, const float* temperature,
+                uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len,
+                int32_t* out_kv_len);
+
+/*
+ * spec_verify_get_error -- wait for the context's stream, then return the
+ * first device-detected error since the last read (SV_EBADTEMP,
+ * SV_EBADTOKEN, SV_EBADLOGIT in that priority) or SV_OK, and clear it.
+ * bits (may be NULL) receives the OR of SV_ERRBIT_* flags.
+ */
+int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits);
+
+/*
+ * spec_verify_debug_stats -- copy the row statistics of the last
+ * spec_verify call (same B, N; enqueued on the context's stream) into
+ * caller-owned device buffers, for parity checks:
+ *   accept_prob  [B, N] float32: min(1, q_j(d_j) / p_j(d_j)) (1 when
+ *                p_j(d_j) == 0); NaN for greedy or failed requests
+ *   log_z        [B, 2N+1] float32: per request, log sum_t exp(x_t / T) of
+ *                target rows 0..N then draft rows 0..N-1 (natural log);
+ *                NaN where the row was not normalised
+ * Returns SV_OK, SV_EINVAL or SV_ECUDA.
+ */
+int spec_verify_debug_stats(spec_verify_ctx* ctx, int B, int N,
+                            float* accept_prob, float* log_z);
+
+/*
+ * Kernel timing for benchmarks.  With profiling on, every spec_verify call
+ * records CUDA events around each kernel it launches on the context's
+ * stream.  spec_verify_profile_read waits for the stream and returns, for
+ * the calls since the last read, the summed device time in milliseconds of
+ * each of the SV_NUM_KERNELS kernels (row statistics, walk, sampling) and
+ * the number of calls; it then clears the sums.
+ */
+#define SV_NUM_KERNELS 3
+int spec_verify_profile(spec_verify_ctx* ctx, int enable);
+int spec_verify_profile_read(spec_verify_ctx* ctx, double* ms_per_kernel,
+                             int* calls);
+
+/* Number of kernel launches one spec_verify call with B > 0 makes. */
+int spec_verify_launches_per_call(void);
+
+/*
+ * spec_verify_debug_philox -- test hook.  For i < n, writes the four
+ * Philox4x32-10 output words of counter (ctr3[3i], ctr3[3i+1], ctr3[3i+2], 0)
+ * under key (seed low 32 bits, seed high 32 bits) to out4[4i .. 4i+3],
+ * using the same device function as the walk.  ctr3 and out4 are device
+ * buffers; enqueued on cuda_stream.  Returns SV_OK, SV_EINVAL or SV_ECUDA.
+ */
+int spec_verify_debug_philox(uint64_t seed, const uint32_t* ctr3, uint32_t* out4, int n,
+                             void* cuda_stream);
+
+/* Release the context and its workspace (waits for its stream first).
+ * NULL is accepted.  Returns SV_OK or SV_ECUDA. */
+int spec_verify_destroy(spec_verify_ctx* ctx);
+
+/* Static, human-readable text for a return code. */
+const char* spec_verify_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H_ */

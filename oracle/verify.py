@@ -325,12 +325,17 @@ def acceptance_probabilities(target, draft, drafts, temperature, dtype):
     probs = np.full((batch, n), np.nan)
     logz_t = np.full((batch, n + 1), np.nan)
     logz_d = np.full((batch, n), np.nan)
+    vocab = target.shape[2]
     for b in range(batch):
         t = float(np.float32(temperature[b]))
         if t == 0.0 or not temperature_is_valid(t):
             continue
+        if any(int(x) < 0 or int(x) >= vocab for x in np.asarray(drafts[b]).reshape(-1)[:n]):
+            continue
         z = logits_to_f64(target[b], dtype)
         y = logits_to_f64(draft[b], dtype) if n > 0 else None
+        if not all(row_is_valid(r) for r in z) or (n > 0 and not all(row_is_valid(r) for r in y)):
+            continue
         for j in range(n + 1):
             logz_t[b, j] = log_partition(z[j], t)
         for j in range(n):

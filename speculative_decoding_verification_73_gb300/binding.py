@@ -1,0 +1,224 @@
+"""Python binding of libspecverify (argument marshalling only).
+
+The functions carry the C ABI's names and take torch CUDA tensors; every
+step of the verify path runs in the library's CUDA kernels.  If the
+library has not been built this module raises on first use: there is no
+CPU fallback.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libspecverify.so")
+
+SV_OK, SV_EINVAL, SV_EBADTEMP, SV_EBADTOKEN, SV_EBADLOGIT, SV_ECUDA = range(6)
+SV_ERRBIT_TEMP, SV_ERRBIT_TOKEN, SV_ERRBIT_LOGIT = 1, 2, 4
+SV_F32, SV_BF16 = 0, 1
+SV_NUM_KERNELS = 3
+SV_MAX_N = 255
+KERNEL_NAMES = ("rowstats", "walk", "sample")
+
+_DTYPE_CODE = {torch.float32: SV_F32, torch.bfloat16: SV_BF16}
+
+#: every symbol include/spec_verify.h declares
+EXPORTS = (
+    "spec_verify_init", "spec_verify", "spec_verify_get_error", "spec_verify_debug_stats",
+    "spec_verify_profile", "spec_verify_profile_read", "spec_verify_launches_per_call",
+    "spec_verify_debug_philox", "spec_verify_destroy", "spec_verify_strerror",
+)
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (code {code})")
+
+
+def load():
+    """Load the shared library (once) and declare its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"libspecverify.so is not built ({LIB_PATH}); run "
+            "`python -m speculative_decoding_verification_73_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    c_int, c_void, c_u64 = ctypes.c_int, ctypes.c_void_p, ctypes.c_uint64
+    lib.spec_verify_init.argtypes = [ctypes.POINTER(c_void), c_int, c_int, c_int, c_int, c_void]
+    lib.spec_verify.argtypes = [c_void, c_int, c_int, c_int, c_void, c_void, c_void, c_void,
+                                c_u64, c_void, c_void, c_void]
+    lib.spec_verify_get_error.argtypes = [c_void, ctypes.POINTER(ctypes.c_uint32)]
+    lib.spec_verify_debug_stats.argtypes = [c_void, c_int, c_int, c_void, c_void]
+    lib.spec_verify_profile.argtypes = [c_void, c_int]
+    lib.spec_verify_profile_read.argtypes = [c_void, ctypes.POINTER(ctypes.c_double),
+                                             ctypes.POINTER(c_int)]
+    lib.spec_verify_launches_per_call.argtypes = []
+    lib.spec_verify_debug_philox.argtypes = [c_u64, c_void, c_void, c_int, c_void]
+    lib.spec_verify_destroy.argtypes = [c_void]
+    lib.spec_verify_strerror.argtypes = [c_int]
+    lib.spec_verify_strerror.restype = ctypes.c_char_p
+    for name in EXPORTS:
+        if name != "spec_verify_strerror":
+            getattr(lib, name).restype = c_int
+    _lib = lib
+    return lib
+
+
+def strerror(code):
+    return load().spec_verify_strerror(int(code)).decode()
+
+
+def _check(code, where):
+    if code != SV_OK:
+        raise SpecVerifyError(code, where)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def spec_verify_init(max_B, max_N, max_V, dtype, stream=None):
+    """Create a context; returns its opaque handle (a ctypes void pointer)."""
+    code = _DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    ctx = ctypes.c_void_p()
+    _check(load().spec_verify_init(ctypes.byref(ctx), int(max_B), int(max_N), int(max_V), code,
+                                   _stream_handle(stream)), "spec_verify_init")
+    return ctx
+
+
+def _require(t, name, shape, dtypes):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if tuple(t.shape) != tuple(shape) and t.numel() != int(np_prod(shape)):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}")
+
+
+def np_prod(shape):
+    n = 1
+    for s in shape:
+        n *= int(s)
+    return n
+
+
+def spec_verify(ctx, target_logits, draft_logits, draft_tokens, temperature, seed,
+                out_tokens, out_accept_len, out_kv_len):
+    """Enqueue one verify step; shapes are taken from ``target_logits``.
+    Tensors must be contiguous CUDA tensors in the documented layouts."""
+    B, n1, V = target_logits.shape
+    logit_dt = (torch.float32, torch.bfloat16)
+    _require(target_logits, "target_logits", (B, n1, V), logit_dt)
+    if n1 > 1:
+        _require(draft_logits, "draft_logits", (B, n1 - 1, V), (target_logits.dtype,))
+        _require(draft_tokens, "draft_tokens", (B, n1 - 1), (torch.int32,))
+    _require(temperature, "temperature", (B,), (torch.float32,))
+    _require(out_tokens, "out_tokens", (B, n1), (torch.int32,))
+    _require(out_accept_len, "out_accept_len", (B,), (torch.int32,))
+    _require(out_kv_len, "out_kv_len", (B,), (torch.int32,))
+    _check(load().spec_verify(ctx, int(B), int(n1 - 1), int(V), _ptr(target_logits),
+                              _ptr(draft_logits), _ptr(draft_tokens), _ptr(temperature),
+                              ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF), _ptr(out_tokens),
+                              _ptr(out_accept_len), _ptr(out_kv_len)), "spec_verify")
+
+
+def spec_verify_get_error(ctx):
+    """(code, bits) of the device-detected input errors since the last read."""
+    bits = ctypes.c_uint32(0)
+    code = load().spec_verify_get_error(ctx, ctypes.byref(bits))
+    if code == SV_ECUDA or code == SV_EINVAL:
+        raise SpecVerifyError(code, "spec_verify_get_error")
+    return code, int(bits.value)
+
+
+def spec_verify_debug_stats(ctx, B, N, device=None):
+    """(accept_prob [B, N], log_z [B, 2N+1]) of the last call, as CUDA tensors."""
+    acc = torch.empty(B, N, dtype=torch.float32, device=device or "cuda")
+    lz = torch.empty(B, 2 * N + 1, dtype=torch.float32, device=device or "cuda")
+    _check(load().spec_verify_debug_stats(ctx, int(B), int(N), _ptr(acc), _ptr(lz)),
+           "spec_verify_debug_stats")
+    return acc, lz
+
+
+def spec_verify_profile(ctx, enable):
+    _check(load().spec_verify_profile(ctx, int(bool(enable))), "spec_verify_profile")
+
+
+def spec_verify_profile_read(ctx):
+    """({kernel name: summed ms}, calls) since the last read."""
+    ms = (ctypes.c_double * SV_NUM_KERNELS)()
+    calls = ctypes.c_int(0)
+    _check(load().spec_verify_profile_read(ctx, ms, ctypes.byref(calls)), "spec_verify_profile_read")
+    return dict(zip(KERNEL_NAMES, list(ms))), int(calls.value)
+
+
+def spec_verify_launches_per_call():
+    return int(load().spec_verify_launches_per_call())
+
+
+def spec_verify_debug_philox(seed, counters, stream=None):
+    """Philox4x32-10 words for counters [n, 3] (uint32 values in an int32 or
+    int64 CUDA tensor); returns [n, 4] int64 tensor of the 32-bit words."""
+    ctr = counters.to(torch.int32).contiguous()
+    n = ctr.shape[0]
+    out = torch.empty(n, 4, dtype=torch.int32, device=ctr.device)
+    _check(load().spec_verify_debug_philox(ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF),
+                                           _ptr(ctr), _ptr(out), int(n), _stream_handle(stream)),
+           "spec_verify_debug_philox")
+    return out.to(torch.int64) & 0xFFFFFFFF
+
+
+def spec_verify_destroy(ctx):
+    _check(load().spec_verify_destroy(ctx), "spec_verify_destroy")
+
+
+class SpecVerify:
+    """A context plus preallocated outputs: ``sv(target, draft, tokens, T, seed)``
+    returns (out_tokens, out_accept_len, out_kv_len) as CUDA tensors."""
+
+    def __init__(self, max_B, max_N, max_V, dtype, stream=None, device=None):
+        self.max_B, self.max_N, self.max_V, self.dtype = max_B, max_N, max_V, dtype
+        self.device = torch.device(device or "cuda")
+        self.stream = stream
+        self.ctx = spec_verify_init(max_B, max_N, max_V, dtype, stream)
+        self.out_tokens = torch.empty(max_B * (max_N + 1), dtype=torch.int32, device=self.device)
+        self.out_accept = torch.empty(max_B, dtype=torch.int32, device=self.device)
+        self.out_kv = torch.empty(max_B, dtype=torch.int32, device=self.device)
+
+    def __call__(self, target, draft, tokens, temperature, seed):
+        B, n1, _ = target.shape
+        toks = self.out_tokens[: B * n1].view(B, n1)
+        acc, kv = self.out_accept[:B], self.out_kv[:B]
+        spec_verify(self.ctx, target, draft, tokens, temperature, seed, toks, acc, kv)
+        return toks, acc, kv
+
+    def get_error(self):
+        return spec_verify_get_error(self.ctx)
+
+    def debug_stats(self, B, N):
+        return spec_verify_debug_stats(self.ctx, B, N, self.device)
+
+    def close(self):
+        if self.ctx is not None:
+            spec_verify_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

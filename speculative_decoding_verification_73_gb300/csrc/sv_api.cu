@@ -1,0 +1,267 @@
+// C ABI of libspecverify: context, argument checks, workspace and launches.
+// The operation itself is documented in include/spec_verify.h.
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/spec_verify.h"
+#include "sv_internal.cuh"
+
+struct spec_verify_ctx {
+  int max_B, max_N, max_V, dtype;
+  int device;
+  cudaStream_t stream;
+  void* ws;  // one cudaMalloc holding the whole workspace
+  sv::Workspace w;
+  // profiling
+  bool profile;
+  std::vector<cudaEvent_t> events;  // SV_NUM_KERNELS + 1 per recorded call
+  int recorded;                     // calls whose events are in `events`
+  double ms[SV_NUM_KERNELS];
+  int calls;
+};
+
+namespace {
+
+constexpr int kMaxB = 1 << 20;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int flush_profile(spec_verify_ctx* ctx) {
+  if (ctx->recorded == 0) return SV_OK;
+  if (cudaStreamSynchronize(ctx->stream) != cudaSuccess) return SV_ECUDA;
+  const int per = SV_NUM_KERNELS + 1;
+  for (int c = 0; c < ctx->recorded; ++c) {
+    for (int k = 0; k < SV_NUM_KERNELS; ++k) {
+      float ms = 0.f;
+      if (cudaEventElapsedTime(&ms, ctx->events[c * per + k], ctx->events[c * per + k + 1]) !=
+          cudaSuccess)
+        return SV_ECUDA;
+      ctx->ms[k] += ms;
+    }
+  }
+  ctx->calls += ctx->recorded;
+  ctx->recorded = 0;
+  return SV_OK;
+}
+
+cudaEvent_t* profile_slot(spec_verify_ctx* ctx) {
+  const int per = SV_NUM_KERNELS + 1;
+  constexpr int kMaxRecorded = 4096;
+  if (ctx->recorded == kMaxRecorded && flush_profile(ctx) != SV_OK) return nullptr;
+  const size_t need = static_cast<size_t>(ctx->recorded + 1) * per;
+  while (ctx->events.size() < need) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    ctx->events.push_back(e);
+  }
+  return ctx->events.data() + static_cast<size_t>(ctx->recorded) * per;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* spec_verify_strerror(int code) {
+  switch (code) {
+    case SV_OK: return "success";
+    case SV_EINVAL: return "invalid argument (null pointer, size or dtype out of range)";
+    case SV_EBADTEMP: return "a temperature is negative, NaN, infinite or subnormal";
+    case SV_EBADTOKEN: return "a draft token is outside [0, V)";
+    case SV_EBADLOGIT: return "a logit row holds NaN or +inf, or has no finite entry";
+    case SV_ECUDA: return "a CUDA runtime call failed";
+    default: return "unknown error code";
+  }
+}
+
+int spec_verify_launches_per_call(void) { return SV_NUM_KERNELS; }
+
+int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int dtype,
+                     void* cuda_stream) {
+  if (out == nullptr) return SV_EINVAL;
+  *out = nullptr;
+  if (max_B < 1 || max_B > kMaxB || max_N < 0 || max_N > SV_MAX_N || max_V < 1 ||
+      max_V > SV_MAX_V || (dtype != SV_F32 && dtype != SV_BF16))
+    return SV_EINVAL;
+  spec_verify_ctx* ctx = new (std::nothrow) spec_verify_ctx();
+  if (ctx == nullptr) return SV_ECUDA;
+  ctx->max_B = max_B;
+  ctx->max_N = max_N;
+  ctx->max_V = max_V;
+  ctx->dtype = dtype;
+  ctx->stream = static_cast<cudaStream_t>(cuda_stream);
+  if (cudaGetDevice(&ctx->device) != cudaSuccess) {
+    delete ctx;
+    return SV_ECUDA;
+  }
+  const int s1 = ceil_div(max_V, sv::row_chunk_elems(dtype));
+  const int s3 = ceil_div(max_V, sv::sample_chunk_elems(dtype));
+  const size_t rows = static_cast<size_t>(max_B) * (2 * static_cast<size_t>(max_N) + 1);
+  size_t off = 0;
+  const size_t o_part = off;
+  off = align_up(off + rows * s1 * sizeof(sv::Partial), 256);
+  const size_t o_jobs = off;
+  off = align_up(off + static_cast<size_t>(max_B) * sizeof(sv::Job), 256);
+  const size_t o_sums = off;
+  off = align_up(off + static_cast<size_t>(max_B) * s3 * sizeof(float), 256);
+  const size_t o_cnt = off;
+  off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
+  const size_t o_err = off;
+  off = align_up(off + sizeof(unsigned), 256);
+  const size_t zero_bytes = off - o_cnt;  // counters and error word start at zero
+  const size_t o_acc = off;
+  off = align_up(off + static_cast<size_t>(max_B) * (max_N > 0 ? max_N : 1) * sizeof(float), 256);
+  const size_t o_lz = off;
+  off = align_up(off + rows * sizeof(float), 256);
+  if (cudaMalloc(&ctx->ws, off) != cudaSuccess) {
+    delete ctx;
+    return SV_ECUDA;
+  }
+  char* base = static_cast<char*>(ctx->ws);
+  ctx->w.partials = reinterpret_cast<sv::Partial*>(base + o_part);
+  ctx->w.jobs = reinterpret_cast<sv::Job*>(base + o_jobs);
+  ctx->w.chunk_sums = reinterpret_cast<float*>(base + o_sums);
+  ctx->w.counters = reinterpret_cast<unsigned*>(base + o_cnt);
+  ctx->w.err = reinterpret_cast<unsigned*>(base + o_err);
+  ctx->w.dbg_accept = reinterpret_cast<float*>(base + o_acc);
+  ctx->w.dbg_logz = reinterpret_cast<float*>(base + o_lz);
+  if (cudaMemsetAsync(base + o_cnt, 0, zero_bytes, ctx->stream) != cudaSuccess ||
+      cudaStreamSynchronize(ctx->stream) != cudaSuccess) {
+    cudaFree(ctx->ws);
+    delete ctx;
+    return SV_ECUDA;
+  }
+  *out = ctx;
+  return SV_OK;
+}
+
+int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_logits,
+                const void* draft_logits, const int32_t* draft_tokens, const float* temperature,
+                uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len,
+                int32_t* out_kv_len) {
+  if (ctx == nullptr) return SV_EINVAL;
+  if (B < 0 || B > ctx->max_B || N < 0 || N > ctx->max_N || V < 1 || V > ctx->max_V)
+    return SV_EINVAL;
+  if (B == 0) return SV_OK;
+  if (target_logits == nullptr || temperature == nullptr || out_tokens == nullptr ||
+      out_accept_len == nullptr || out_kv_len == nullptr)
+    return SV_EINVAL;
+  if (N > 0 && (draft_logits == nullptr || draft_tokens == nullptr)) return SV_EINVAL;
+
+  const size_t esize = ctx->dtype == SV_BF16 ? 2 : 4;
+  const bool vec = (static_cast<size_t>(V) * esize) % 16 == 0 && aligned16(target_logits) &&
+                   (N == 0 || aligned16(draft_logits));
+  sv::Problem p;
+  p.B = B;
+  p.N = N;
+  p.V = V;
+  p.target = target_logits;
+  p.draft = draft_logits;
+  p.tokens = draft_tokens;
+  p.temperature = temperature;
+  p.seed = seed;
+  p.out_tokens = out_tokens;
+  p.out_accept = out_accept_len;
+  p.out_kv = out_kv_len;
+  sv::Workspace w = ctx->w;
+  w.S1 = ceil_div(V, sv::row_chunk_elems(ctx->dtype));
+  w.S3 = ceil_div(V, sv::sample_chunk_elems(ctx->dtype));
+
+  cudaEvent_t* ev = nullptr;
+  if (ctx->profile) {
+    ev = profile_slot(ctx);
+    if (ev == nullptr) return SV_ECUDA;
+    if (cudaEventRecord(ev[0], ctx->stream) != cudaSuccess) return SV_ECUDA;
+  }
+  if (sv::launch_rowstats(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
+  if (ev && cudaEventRecord(ev[1], ctx->stream) != cudaSuccess) return SV_ECUDA;
+  if (sv::launch_walk(ctx->dtype, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
+  if (ev && cudaEventRecord(ev[2], ctx->stream) != cudaSuccess) return SV_ECUDA;
+  if (sv::launch_sample(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
+  if (ev) {
+    if (cudaEventRecord(ev[3], ctx->stream) != cudaSuccess) return SV_ECUDA;
+    ctx->recorded += 1;
+  }
+  return SV_OK;
+}
+
+int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits) {
+  if (ctx == nullptr) return SV_EINVAL;
+  unsigned word = 0;
+  if (cudaMemcpyAsync(&word, ctx->w.err, sizeof(word), cudaMemcpyDeviceToHost, ctx->stream) !=
+          cudaSuccess ||
+      cudaMemsetAsync(ctx->w.err, 0, sizeof(unsigned), ctx->stream) != cudaSuccess ||
+      cudaStreamSynchronize(ctx->stream) != cudaSuccess)
+    return SV_ECUDA;
+  if (bits) *bits = word;
+  if (word & SV_ERRBIT_TEMP) return SV_EBADTEMP;
+  if (word & SV_ERRBIT_TOKEN) return SV_EBADTOKEN;
+  if (word & SV_ERRBIT_LOGIT) return SV_EBADLOGIT;
+  return SV_OK;
+}
+
+int spec_verify_debug_stats(spec_verify_ctx* ctx, int B, int N, float* accept_prob,
+                            float* log_z) {
+  if (ctx == nullptr || B < 1 || B > ctx->max_B || N < 0 || N > ctx->max_N) return SV_EINVAL;
+  if (N > 0 && accept_prob != nullptr &&
+      cudaMemcpyAsync(accept_prob, ctx->w.dbg_accept, sizeof(float) * B * N,
+                      cudaMemcpyDeviceToDevice, ctx->stream) != cudaSuccess)
+    return SV_ECUDA;
+  if (log_z != nullptr &&
+      cudaMemcpyAsync(log_z, ctx->w.dbg_logz, sizeof(float) * B * (2 * N + 1),
+                      cudaMemcpyDeviceToDevice, ctx->stream) != cudaSuccess)
+    return SV_ECUDA;
+  return SV_OK;
+}
+
+int spec_verify_profile(spec_verify_ctx* ctx, int enable) {
+  if (ctx == nullptr) return SV_EINVAL;
+  if (!enable && ctx->profile && flush_profile(ctx) != SV_OK) return SV_ECUDA;
+  ctx->profile = enable != 0;
+  return SV_OK;
+}
+
+int spec_verify_profile_read(spec_verify_ctx* ctx, double* ms_per_kernel, int* calls) {
+  if (ctx == nullptr) return SV_EINVAL;
+  if (flush_profile(ctx) != SV_OK) return SV_ECUDA;
+  for (int k = 0; k < SV_NUM_KERNELS; ++k) {
+    if (ms_per_kernel) ms_per_kernel[k] = ctx->ms[k];
+    ctx->ms[k] = 0.0;
+  }
+  if (calls) *calls = ctx->calls;
+  ctx->calls = 0;
+  return SV_OK;
+}
+
+int spec_verify_destroy(spec_verify_ctx* ctx) {
+  if (ctx == nullptr) return SV_OK;
+  int rc = SV_OK;
+  if (cudaStreamSynchronize(ctx->stream) != cudaSuccess) rc = SV_ECUDA;
+  for (cudaEvent_t e : ctx->events) cudaEventDestroy(e);
+  if (cudaFree(ctx->ws) != cudaSuccess) rc = SV_ECUDA;
+  delete ctx;
+  return rc;
+}
+
+/* Test hook: Philox4x32-10 words for n counters (c0, c1, c2, 0) under a
+ * 64-bit seed, computed by the same device function the walk uses.
+ * ctr3: device [n, 3] uint32; out4: device [n, 4] uint32. */
+int spec_verify_debug_philox(uint64_t seed, const uint32_t* ctr3, uint32_t* out4, int n,
+                             void* cuda_stream) {
+  if (n < 0 || (n > 0 && (ctr3 == nullptr || out4 == nullptr))) return SV_EINVAL;
+  return sv::launch_philox_probe(seed, ctr3, out4, n, static_cast<cudaStream_t>(cuda_stream)) ==
+                 cudaSuccess
+             ? SV_OK
+             : SV_ECUDA;
+}
+
+}  // extern "C"

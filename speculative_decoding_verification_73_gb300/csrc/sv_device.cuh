@@ -1,0 +1,203 @@
+// Device-side helpers of libspecverify: element access, streaming loads,
+// block reductions, the temperature rule and Philox4x32-10.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "sv_internal.cuh"
+
+namespace sv {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------- numbers
+
+// 2^x on the SFU (PTX ex2.approx.ftz.f32): results below 2^-126 flush to 0,
+// 2^-inf = 0, NaN stays NaN.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// max that propagates NaN (PTX max.NaN.f32).
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Temperature rule: 0 is greedy, a finite value >= 2^-126 is sampled,
+// anything else (negative, NaN, inf, subnormal) is invalid.
+__device__ __forceinline__ int temp_mode(float t) {
+  if (t == 0.0f) return kModeGreedy;
+  if (t >= 1.17549435e-38f && t <= 3.40282347e38f) return kModeSampled;
+  return kModeInvalid;
+}
+
+// k = log2(e) / T, correctly rounded; every kernel derives it the same way.
+__device__ __forceinline__ float scale_of(float t) { return __fdiv_rn(1.44269504088896341f, t); }
+
+// ---------------------------------------------------------------- loads
+
+// 16-byte read-only load that does not allocate in L1 (each byte of a row
+// is read once by the row-statistics pass).
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+  static constexpr int kVec = 4;                       // elements per 16 bytes
+  static constexpr uint32_t kNegInfWord = 0xff800000u; // one -inf per word
+  static __device__ __forceinline__ float get(const uint4& v, int e) {
+    return __uint_as_float(word(v, e));
+  }
+  static __device__ __forceinline__ float vmax_nan(const uint4& v) {
+    return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                    fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
+  static __device__ __forceinline__ float load1(const float* p) { return __ldg(p); }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  static constexpr uint32_t kNegInfWord = 0xff80ff80u; // two bf16 -inf
+  // Element e of the 16 bytes: element 2i is the low half of word i.
+  static __device__ __forceinline__ float get(const uint4& v, int e) {
+    const uint32_t w = word(v, e >> 1);
+    return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+  }
+  static __device__ __forceinline__ float vmax_nan(const uint4& v) {
+    const uint32_t m = bmax2_nan(bmax2_nan(v.x, v.y), bmax2_nan(v.z, v.w));
+    return fmax_nan(__uint_as_float(m << 16), __uint_as_float(m & 0xffff0000u));
+  }
+  static __device__ __forceinline__ float load1(const __nv_bfloat16* p) {
+    const unsigned short bits = __ldg(reinterpret_cast<const unsigned short*>(p));
+    return __uint_as_float(static_cast<uint32_t>(bits) << 16);
+  }
+};
+
+// ---------------------------------------------------------------- reductions
+// Each takes its own shared scratch of kThreads/32 slots so that back-to-back
+// reductions need no trailing barrier; every thread gets the result.
+
+__device__ __forceinline__ float block_max_nan(float v, float* scratch) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(kFull, v, o));
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = scratch[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) v = fmax_nan(v, scratch[w]);
+  return v;
+}
+
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = scratch[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) v += scratch[w];
+  return v;
+}
+
+__device__ __forceinline__ int block_min_int(int v, int* scratch) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(kFull, v, o));
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = scratch[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) v = min(v, scratch[w]);
+  return v;
+}
+
+__device__ __forceinline__ int block_max_int(int v, int* scratch) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(kFull, v, o));
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = scratch[0];
+#pragma unroll
+  for (int w = 1; w < kThreads / 32; ++w) v = max(v, scratch[w]);
+  return v;
+}
+
+// Exclusive prefix sum over the CTA in thread order (fp32); *total gets the
+// CTA-wide sum.  scratch holds kThreads/32 floats.
+__device__ __forceinline__ float block_exclusive_scan(float v, float* scratch, float* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  float before = 0.f, all = 0.f;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const float t = scratch[w];
+    if (w < warp) before += t;
+    all += t;
+  }
+  *total = all;
+  return before + incl - v;
+}
+
+// ---------------------------------------------------------------- Philox
+// Philox4x32-10 as defined by Salmon, Moraes, Dror and Shaw, "Parallel
+// Random Numbers: As Easy as 1, 2, 3" (SC'11): per round the products
+// M0*x0 and M1*x2 are split into high and low words, the output is
+// (hi1 ^ x1 ^ k0, lo1, hi0 ^ x3 ^ k1, lo0), and the key advances by the
+// Weyl increments between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint2 key) {
+  constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+  constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      key.x += kW0;
+      key.y += kW1;
+    }
+    const uint32_t hi0 = __umulhi(kM0, x.x), lo0 = kM0 * x.x;
+    const uint32_t hi1 = __umulhi(kM1, x.z), lo1 = kM1 * x.z;
+    x = make_uint4(hi1 ^ x.y ^ key.x, lo1, hi0 ^ x.w ^ key.y, lo0);
+  }
+  return x;
+}
+
+// The uniform of (request b, 1-based position j, draw): (word0 >> 8) * 2^-24,
+// exact in float32.
+__device__ __forceinline__ float philox_uniform(unsigned long long seed, uint32_t b, uint32_t j,
+                                                uint32_t draw) {
+  const uint2 key = make_uint2(static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  const uint4 r = philox4x32_10(make_uint4(b, j, draw, 0u), key);
+  return static_cast<float>(r.x >> 8) * 5.9604644775390625e-8f;  // 2^-24
+}
+
+}  // namespace sv

@@ -1,0 +1,86 @@
+// Internal declarations shared by the kernels and the C-ABI layer of
+// libspecverify.  Nothing here is part of the public interface.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sv {
+
+constexpr int kThreads = 256;           // threads per CTA, every kernel
+constexpr int kRowChunkBytes = 32768;   // row-statistics: bytes of one row chunk per CTA
+constexpr int kSampleChunkBytes = 16384;// sampler: bytes of one row chunk per CTA
+constexpr int kWalkMaxThreads = 256;    // walk: one thread per row of a request (N+1 <= 256)
+
+constexpr int kModeInvalid = 0;
+constexpr int kModeGreedy = 1;
+constexpr int kModeSampled = 2;
+
+constexpr unsigned kErrTemp = 1u;
+constexpr unsigned kErrToken = 2u;
+constexpr unsigned kErrLogit = 4u;
+
+// Statistics of one chunk of one logit row (16 bytes).
+//   sampled row: a = c = fl(M * k) with M the chunk maximum and k = log2(e)/T,
+//                s = sum over the chunk of 2^(x*k - c)   (NaN marks a bad chunk)
+//   greedy row : a = chunk maximum M, s = 0 (NaN if a NaN was seen),
+//                idx = lowest index holding M
+struct Partial {
+  float a;
+  float s;
+  int idx;
+  int pad;
+};
+
+constexpr int kJobNone = 0;
+constexpr int kJobResidual = 1;
+constexpr int kJobBonus = 2;
+
+// What the walk leaves for the sampler, one per request.
+//   q_t = 2^(z_t*k - cq) * inv_sq, p_t = 2^(y_t*k - cp) * inv_sp
+struct Job {
+  int kind;     // kJob*
+  int row;      // 0-based row of the correction (first rejected) or bonus row
+  float u;      // uniform of the sampling draw
+  float k;      // log2(e) / T
+  float cq, inv_sq;
+  float cp, inv_sp;
+};
+
+struct Problem {
+  int B, N, V;
+  const void* target;        // [B, N+1, V]
+  const void* draft;         // [B, N, V]
+  const int32_t* tokens;     // [B, N]
+  const float* temperature;  // [B]
+  unsigned long long seed;
+  int32_t* out_tokens;       // [B, N+1]
+  int32_t* out_accept;       // [B]
+  int32_t* out_kv;           // [B]
+};
+
+struct Workspace {
+  Partial* partials;     // [rows = B(2N+1), S1]
+  Job* jobs;             // [B]
+  float* chunk_sums;     // [B, S3]
+  unsigned* counters;    // [B], zero between calls
+  unsigned* err;         // [1], OR of kErr* bits
+  float* dbg_accept;     // [B, N]
+  float* dbg_logz;       // [B, 2N+1]
+  int S1;                // row-statistics chunks per row for this call's V
+  int S3;                // sampler chunks per row for this call's V
+};
+
+// dtype codes match SV_F32 / SV_BF16
+cudaError_t launch_rowstats(int dtype, bool vec, const Problem& p, const Workspace& w,
+                            cudaStream_t s);
+cudaError_t launch_walk(int dtype, const Problem& p, const Workspace& w, cudaStream_t s);
+cudaError_t launch_sample(int dtype, bool vec, const Problem& p, const Workspace& w,
+                          cudaStream_t s);
+cudaError_t launch_philox_probe(unsigned long long seed, const uint32_t* ctr3, uint32_t* out4,
+                                int n, cudaStream_t s);
+
+inline int row_chunk_elems(int dtype) { return kRowChunkBytes / (dtype == 1 ? 2 : 4); }
+inline int sample_chunk_elems(int dtype) { return kSampleChunkBytes / (dtype == 1 ? 2 : 4); }
+
+}  // namespace sv

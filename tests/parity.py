@@ -1,0 +1,90 @@
+"""GPU-vs-oracle comparison under the method's tolerances (test helper).
+
+* greedy requests: tokens, accept length and KV length bit-exact;
+* sampled requests: bit-exact, except where the oracle's decision at the
+  point of divergence had its uniform within WINDOW (1e-5) of its threshold
+  (|u - min(1, q/p)| for an accept test, the distance of u to the edges of
+  the chosen bucket of the normalised CDF for a correction / bonus draw);
+  every such mismatch is logged, and mismatches must stay below 1e-5 of the
+  verified positions;
+* error requests: identical error bits and the -1 / 0 markers.
+"""
+
+import math
+
+import numpy as np
+
+WINDOW = 1e-5
+
+
+def oracle_inputs(wl):
+    z, y = wl.raw()
+    return z, y, wl.tokens.numpy(), wl.temperature.numpy()
+
+
+def run_oracle(wl, seed=None):
+    from oracle import verify as ov
+    z, y, d, t = oracle_inputs(wl)
+    return ov.verify(z, y, d, t, wl.seed if seed is None else seed, wl.dtype)
+
+
+def near_threshold_count(res):
+    return sum(1 for decs in res.decisions for dec in decs if dec.distance() < WINDOW)
+
+
+def compare(res, tokens, accept, kv, temperature, n, label=""):
+    """Check GPU outputs (numpy) against an oracle Result.  Returns the list
+    of logged in-window mismatches."""
+    tokens = np.asarray(tokens).reshape(res.tokens.shape)
+    accept = np.asarray(accept).reshape(-1)
+    kv = np.asarray(kv).reshape(-1)
+    temperature = np.asarray(temperature).reshape(-1)
+    logged = []
+    for b in range(res.tokens.shape[0]):
+        same = (np.array_equal(tokens[b], res.tokens[b]) and accept[b] == res.accept_len[b]
+                and kv[b] == res.kv_len[b])
+        if same:
+            continue
+        where = f"{label} request {b}: gpu a={accept[b]} kv={kv[b]} tok={tokens[b].tolist()} " \
+                f"oracle a={res.accept_len[b]} kv={res.kv_len[b]} tok={res.tokens[b].tolist()}"
+        assert res.request_errors[b] == 0, "error request differs: " + where
+        assert float(temperature[b]) != 0.0, "greedy request differs: " + where
+        assert kv[b] == accept[b] + 1, where
+        decs = res.decisions[b]
+        if accept[b] != res.accept_len[b]:
+            j = min(int(accept[b]), int(res.accept_len[b])) + 1
+            dec = [x for x in decs if x.kind == "accept" and x.j == j]
+        else:
+            dec = [x for x in decs if x.kind in ("residual", "bonus")]
+            # the accepted prefix must agree exactly
+            a = int(accept[b])
+            assert np.array_equal(tokens[b, :a], res.tokens[b, :a]), where
+        assert dec, "no oracle decision at the divergence: " + where
+        dist = dec[0].distance()
+        assert dist < WINDOW, f"mismatch outside the 1e-5 window (distance {dist:.3g}): " + where
+        logged.append((label, b, dec[0].kind, dec[0].j, dist))
+        print("near-threshold mismatch:", where, f"distance={dist:.3g}")
+    positions = tokens.shape[0] * max(n, 1)
+    assert len(logged) < max(1.0, 1e-5 * positions) or len(logged) == 0, \
+        f"{len(logged)} mismatches over {positions} positions"
+    return logged
+
+
+def rel_close(gpu, ref, rtol=WINDOW):
+    """|gpu - ref| <= rtol * max(|ref|, 1) elementwise, NaN where ref is NaN."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    nan = np.isnan(ref)
+    if not np.array_equal(nan, np.isnan(gpu)):
+        return False
+    d = np.abs(gpu[~nan] - ref[~nan])
+    return bool(np.all(d <= rtol * np.maximum(np.abs(ref[~nan]), 1.0)))
+
+
+def max_rel(gpu, ref):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    m = ~np.isnan(ref)
+    if not m.any():
+        return 0.0
+    return float(np.max(np.abs(gpu[m] - ref[m]) / np.maximum(np.abs(ref[m]), 1.0)))
