@@ -15,13 +15,14 @@ How the verify step draws (a reading; the pages define no generator):
 
     key     = (seed mod 2^32, seed div 2^32)
     counter = (request b, position j (1-based), draw, 0)
-    draw 0  = the accept test at position j
+    draw 0  = the accept test at position j: u = uniform of word 0
     draw 1  = the correction at the first rejected position j*, or the
-              bonus at position j = N + 1
-    u       = (word0 >> 8) * 2^-24          in [0, 1 - 2^-24]
+              bonus at position j = N + 1: four uniforms, one per word,
+              one for each level of the grouped inverse CDF
+    uniform of a word w = (w >> 8) * 2^-24     in [0, 1 - 2^-24]
 
-u has 24 significant bits, so it is exact in both float32 and float64 and
-both sides of a comparison see the same number.
+A uniform has 24 significant bits, so it is exact in both float32 and
+float64 and both sides of a comparison see the same number.
 
 Everything here is vectorised over numpy uint64 arrays so that it also
 works on scalars.
@@ -83,6 +84,14 @@ def uniform(seed, b, j, draw):
     if np.ndim(u) == 0:
         return float(u)
     return u
+
+
+def uniforms4(seed, b, j, draw):
+    """The four uniforms of (request b, position j, draw), one per output
+    word, as a tuple of Python floats."""
+    k0, k1 = split_seed(seed)
+    words = philox4x32_10(b, j, draw, 0, k0, k1)
+    return tuple(float(int(w) >> 8) * 2.0 ** -24 for w in words)
 
 
 ACCEPT_DRAW = 0

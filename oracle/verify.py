@@ -26,8 +26,14 @@ Readings of points the pages leave open:
 * a valid T is 0 (greedy) or a finite float32 >= 2^-126; anything else
   (negative, NaN, inf, subnormal) is a per-request temperature error;
 * the uniform u is the Philox draw in ``oracle.philox``;
-* the inverse CDF returns the smallest vocabulary index t whose running
-  sum exceeds u; if rounding leaves none, the largest t with mass > 0;
+* a correction or bonus token is drawn by a grouped inverse CDF: the
+  vocabulary is split into blocks of 2^13 consecutive tokens, each block
+  into blocks of 2^8, then 2^4, then single tokens; at each of these four
+  levels one sub-block is chosen by inverse CDF over the sub-blocks' masses
+  (smallest index whose running sum exceeds u times the total; the last
+  one with mass if rounding leaves none), each level with its own uniform.
+  This draws exactly from the normalised residual (or q), and each
+  decision compares u against at most max(V / 2^13, 32) bucket edges;
 * greedy ties go to the lowest vocabulary index; draft logits are not read
   at T = 0; a draft is accepted iff it equals the row's argmax, and the
   emitted token after the first mismatch (or after N matches) is the
@@ -131,23 +137,54 @@ def residual(q, p):
     return raw / s
 
 
-def sample(dist, u):
-    """Inverse CDF of a distribution over vocabulary indices.
+def sample(masses, u):
+    """Inverse CDF over a short list of masses.
 
-    Returns ``(t, margin)``: t is the smallest index whose running sum
-    C_t exceeds u (largest index with mass > 0 if none does, which only
-    rounding can cause), and margin = min(|u - C_{t-1}|, |u - C_t|) is how
-    far u sits from the edges of t's bucket (C_{-1} = 0).
+    Returns ``(c, margin)``: c is the smallest index whose running sum C_c
+    exceeds u times the total (the last index with mass > 0 if none does,
+    which only rounding can cause), and margin = min(|u - C_{c-1}/M|,
+    |u - C_c/M|) is how far u sits from the edges of c's bucket in units of
+    the total M (C_{-1} = 0).
     """
-    c = np.cumsum(dist)
-    above = np.nonzero(c > u)[0]
+    c_sum = np.cumsum(masses)
+    total = c_sum[-1]
+    above = np.nonzero(c_sum > u * total)[0]
     if len(above):
-        t = int(above[0])
+        c = int(above[0])
     else:
-        t = int(np.nonzero(dist > 0)[0][-1])
-    lo = c[t - 1] if t > 0 else 0
-    margin = min(abs(u - lo), abs(u - c[t]))
-    return t, margin
+        c = int(np.nonzero(masses > 0)[0][-1])
+    lo = c_sum[c - 1] if c > 0 else 0
+    margin = min(abs(u - lo / total), abs(u - c_sum[c] / total))
+    return c, margin
+
+
+# Token groups of the grouped inverse CDF: level 1 splits the vocabulary
+# into blocks of 2^13 consecutive tokens, level 2 a block into blocks of
+# 2^8, level 3 into blocks of 2^4, level 4 into single tokens.
+LEVEL_SHIFTS = (13, 8, 4, 0)
+
+
+def sample_grouped(dist, us):
+    """Draw a token from ``dist`` (any non-negative masses) with four
+    uniforms, one per level: at each level the current block is split into
+    consecutive sub-blocks (sizes 2^13, 2^8, 2^4, 1) and one is chosen by
+    ``sample`` over their masses.  The chance of token t is the product of
+    its blocks' conditional masses, which telescopes to dist[t] / sum(dist),
+    so this is an exact draw from the normalised ``dist``.
+
+    Returns ``(t, margins)`` with the margin of each level's choice.
+    """
+    lo, hi = 0, len(dist)
+    margins = []
+    for level, shift in enumerate(LEVEL_SHIFTS):
+        size = 1 << shift
+        starts = list(range(lo, hi, size))
+        masses = np.array([np.sum(dist[s:min(s + size, hi)]) for s in starts], dtype=dist.dtype)
+        c, margin = sample(masses, us[level])
+        margins.append(margin)
+        lo = starts[c]
+        hi = min(lo + size, hi)
+    return lo, margins
 
 
 # --------------------------------------------------------------------------
@@ -158,7 +195,8 @@ class Decision:
     """One random decision of the walk, for near-threshold bookkeeping.
 
     kind is "accept" (threshold = min(1, q/p), or None when p(d) <= 0),
-    "residual" or "bonus" (margin = distance of u to its bucket edges).
+    "residual" or "bonus" (margin = for each level of the grouped inverse
+    CDF, the distance of that level's uniform to its bucket edges).
     """
 
     __slots__ = ("kind", "j", "u", "threshold", "margin", "taken")
@@ -167,13 +205,16 @@ class Decision:
         self.kind, self.j, self.u = kind, j, u
         self.threshold, self.margin, self.taken = threshold, margin, taken
 
-    def distance(self):
-        """How close u came to flipping this decision."""
+    def distance(self, level=None):
+        """How close the uniform(s) came to flipping this decision (at one
+        level of a sampling decision, or the closest level)."""
         if self.kind == "accept":
             if self.threshold is None:
                 return math.inf
             return abs(self.u - self.threshold)
-        return self.margin
+        if level is not None:
+            return self.margin[level]
+        return min(self.margin)
 
     def __repr__(self):
         return (f"Decision({self.kind}, j={self.j}, u={self.u!r}, "
@@ -184,9 +225,10 @@ def walk(q_rows, p_rows, drafts, draw_uniform):
     """The sampled chain for one request.
 
     q_rows: N+1 verifier distributions q_1..q_{N+1}; p_rows: N draft
-    distributions p_1..p_N; drafts: d_1..d_N; draw_uniform(j, draw) gives
-    the uniform for 1-based position j and draw 0 (accept) or 1
-    (correction / bonus).
+    distributions p_1..p_N; drafts: d_1..d_N; draw_uniform(j, draw) gives,
+    for 1-based position j, the uniform of draw 0 (accept) or the four
+    uniforms of draw 1 (correction / bonus, one per level of
+    ``sample_grouped``).
 
     Returns (tokens, accepted, kv_len, decisions): tokens are the accepted
     drafts followed by one correction or bonus token.
@@ -205,16 +247,25 @@ def walk(q_rows, p_rows, drafts, draw_uniform):
             continue
         r = residual(q_rows[j - 1], p_rows[j - 1])
         u2 = draw_uniform(j, philox.SAMPLE_DRAW)
-        t, margin = sample(r, u2)
+        t, margin = sample_grouped(r, u2)
         decisions.append(Decision("residual", j, u2, margin=margin, taken=t))
         tokens.append(t)
         accepted = j - 1
         return tokens, accepted, accepted + 1, decisions
     u2 = draw_uniform(n + 1, philox.SAMPLE_DRAW)
-    t, margin = sample(q_rows[n], u2)
+    t, margin = sample_grouped(q_rows[n], u2)
     decisions.append(Decision("bonus", n + 1, u2, margin=margin, taken=t))
     tokens.append(t)
     return tokens, n, n + 1, decisions
+
+
+def philox_draws(seed, b):
+    """The uniform provider of request b for ``walk``."""
+    def draw(j, kind):
+        if kind == philox.ACCEPT_DRAW:
+            return philox.uniform(seed, b, j, kind)
+        return philox.uniforms4(seed, b, j, kind)
+    return draw
 
 
 def argmax_lowest(x):
@@ -263,8 +314,7 @@ def verify_request(z_raw, y_raw, drafts, temperature, seed, b, dtype):
     q_rows = [softmax(z[j], t) for j in range(n + 1)]
     p_rows = [softmax(y[j], t) for j in range(n)]
     tokens, a, kv, decisions = walk(
-        q_rows, p_rows, drafts,
-        lambda j, draw: philox.uniform(seed, b, j, draw))
+        q_rows, p_rows, drafts, philox_draws(seed, b))
     return 0, tokens, a, kv, decisions
 
 

@@ -47,7 +47,9 @@ def enumerate_law(q_rows, p_rows, grid):
             continue
         for utup in itertools.product(us, repeat=n + 1):
             def draw(j, kind, utup=utup):
-                return utup[j - 1] if kind == 0 else utup[n]
+                # V <= 16: the first three levels of the grouped inverse CDF
+                # have a single block, so only the last uniform matters
+                return utup[j - 1] if kind == 0 else (Fr(0), Fr(0), Fr(0), utup[n])
             tokens, a, kv, _ = ov.walk(q_rows, p_rows, list(drafts), draw)
             key = (tuple(int(t) for t in tokens), a, kv)
             law[key] = law.get(key, Fr(0)) + w_d / grid ** (n + 1)
@@ -150,7 +152,7 @@ def test_rejected_draft_never_reemitted(law_a):
             continue
         for u0, u1 in itertools.product(us, us):
             tokens, a, _, _ = ov.walk(Q_A, P_A, [d1, 0],
-                                      lambda j, kind: u0 if kind == 0 else u1)
+                                      lambda j, kind: u0 if kind == 0 else (0, 0, 0, u1))
             if a == 0:
                 assert tokens[0] != d1
 
@@ -184,7 +186,56 @@ def test_sample_inverse_cdf_edges():
     assert ov.sample(dist, Fr(3, 12) - Fr(1, 10 ** 6))[0] == 1
     assert ov.sample(dist, Fr(3, 12))[0] == 3      # C_1 = 3/12 is not > 3/12
     assert ov.sample(dist, Fr(11, 12))[0] == 3
-    # rounding past the end falls back to the last index with mass
+    # unnormalised masses: the comparison is against u times the total
     assert ov.sample(np.array([0.5, 0.25, 0.0]), 0.9)[0] == 1
+    assert ov.sample(np.array([0.5, 0.25, 0.0]), 0.5)[0] == 0
     t, margin = ov.sample(dist, Fr(1, 12))
     assert t == 1 and margin == Fr(1, 12)
+    # a zero-mass index is never chosen
+    for k in range(12):
+        assert ov.sample(fr_row(0, 4, 0, 0, 8, 0), Fr(k, 12))[0] in (1, 4)
+
+
+def _grouped_fixture():
+    """300 tokens: level 2 splits them into [0, 256) and [256, 300) with
+    conditional masses 1/3, 2/3; level 3 blocks of 16 get 1/16 each in the
+    first block and 1/4, 1/4, 1/2 in the second; level 4 tokens get
+    multiples of 1/16 of their block (with zeros).  Every level's edges are
+    then multiples of 1/3, 1/16 and 1/16."""
+    dist = [Fr(0)] * 300
+    tok_pattern = [0, 2, 1, 0, 3, 0, 0, 1, 2, 2, 0, 1, 0, 2, 1, 1]   # sums to 16
+    tok_short = [4, 0, 2, 2, 0, 4, 1, 3, 0, 0, 0, 0]                 # 12 tokens, sums to 16
+    for g in range(16):                      # block [0, 256): 16 blocks of 16
+        for i in range(16):
+            dist[16 * g + i] = Fr(1, 3) * Fr(1, 16) * Fr(tok_pattern[(i + g) % 16], 16)
+    second = [Fr(1, 4), Fr(1, 4), Fr(1, 2)]  # blocks [256,272), [272,288), [288,300)
+    for g in range(3):
+        n = 16 if g < 2 else 12
+        pat = tok_pattern if g < 2 else tok_short
+        for i in range(n):
+            dist[256 + 16 * g + i] = Fr(2, 3) * second[g] * Fr(pat[(i + g) % n] if g < 2 else pat[i], 16)
+    return np.array(dist, dtype=object)
+
+
+def test_grouped_sampler_is_exact_over_three_levels():
+    dist = _grouped_fixture()
+    assert sum(dist) == 1
+    law = {}
+    for u2 in range(3):
+        for u3 in range(16):
+            for u4 in range(16):
+                t, _ = ov.sample_grouped(dist, (Fr(0), Fr(u2, 3), Fr(u3, 16), Fr(u4, 16)))
+                law[t] = law.get(t, Fr(0)) + Fr(1, 3 * 16 * 16)
+    for t in range(300):
+        assert law.get(t, Fr(0)) == dist[t], t
+
+
+def test_grouped_sampler_levels_and_scale_invariance():
+    dist = _grouped_fixture()
+    us = (Fr(1, 7), Fr(1, 2), Fr(5, 16), Fr(3, 16))
+    t, margins = ov.sample_grouped(dist, us)
+    t2, margins2 = ov.sample_grouped(dist * 5, us)        # unnormalised masses
+    assert t == t2 and margins == margins2
+    assert len(margins) == 4
+    assert margins[0] == min(us[0], 1 - us[0])             # one block at level 1
+    assert 256 <= t < 300                                  # u2 = 1/2 > 1/3 picks the 2nd block

@@ -198,8 +198,7 @@ def test_leviathan_chi_square_like_lesson_step5():
     ud = rng.random((steps, n))
     for s in range(steps):
         drafts = [min(int(np.searchsorted(cdfs[j], ud[s, j], side="right")), v - 1) for j in range(n)]
-        tokens, _, _, _ = ov.walk(q_rows, p_rows, drafts,
-                                  lambda j, draw, s=s: philox.uniform(777, s, j, draw))
+        tokens, _, _, _ = ov.walk(q_rows, p_rows, drafts, ov.philox_draws(777, s))
         first[tokens[0]] += 1
     direct = np.bincount(np.searchsorted(np.cumsum(q_rows[0]), rng.random(steps), side="right"),
                          minlength=v)[:v]
@@ -232,8 +231,7 @@ def test_alpha09_mean_tokens_per_call():
     for seed in range(100):
         d = wl.tokens(seed).numpy()
         for b in range(256):
-            _, a, _, _ = ov.walk(q_rows[b], p_rows[b], d[b],
-                                 lambda j, draw, b=b, seed=seed: philox.uniform(seed, b, j, draw))
+            _, a, _, _ = ov.walk(q_rows[b], p_rows[b], d[b], ov.philox_draws(seed, b))
             total += a + 1
             count += 1
     closed = (1 - 0.9 ** 9) / (1 - 0.9)
@@ -255,3 +253,22 @@ def test_single_bf16_sigma_gives_overlap_08():
     zf, yf = ov.logits_to_f64(z[0], "bf16"), ov.logits_to_f64(y[0], "bf16")
     al = [float(np.sum(np.minimum(ov.softmax(zf[j], 1.0), ov.softmax(yf[j], 1.0)))) for j in range(5)]
     assert abs(np.mean(al) - 0.8) < 0.01
+
+
+def test_grouped_sampler_chi_square_across_level1_blocks():
+    """float64: draws with Philox uniforms over V = 20000 (three level-1
+    blocks, ragged tail) follow the normalised masses."""
+    rng = np.random.default_rng(21)
+    v = 20000
+    w = rng.random(v) ** 8                      # skewed masses, many tiny
+    w[5000:5100] = 0.0
+    bins = np.minimum(np.arange(v) // 400, 49)  # 50 bins of ~400 tokens
+    p_bin = np.bincount(bins, weights=w, minlength=50) / w.sum()
+    counts = np.zeros(50)
+    n = 20000
+    for s in range(n):
+        t, _ = ov.sample_grouped(w, philox.uniforms4(99, s, 1, 1))
+        assert w[t] > 0
+        counts[bins[t]] += 1
+    chi2 = float(np.sum((counts - n * p_bin) ** 2 / (n * p_bin)))
+    assert chi2 < 85.4   # 49 degrees of freedom, 99.9%
