@@ -191,6 +191,21 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint2 key) {
   return x;
 }
 
+__device__ __forceinline__ float word_uniform(uint32_t w) {
+  return static_cast<float>(w >> 8) * 5.9604644775390625e-8f;  // 2^-24
+}
+
+// The four uniforms of (request b, 1-based position j, draw), one per word.
+__device__ __forceinline__ void philox_uniforms4(unsigned long long seed, uint32_t b, uint32_t j,
+                                                 uint32_t draw, float u[4]) {
+  const uint2 key = make_uint2(static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  const uint4 r = philox4x32_10(make_uint4(b, j, draw, 0u), key);
+  u[0] = word_uniform(r.x);
+  u[1] = word_uniform(r.y);
+  u[2] = word_uniform(r.z);
+  u[3] = word_uniform(r.w);
+}
+
 // The uniform of (request b, 1-based position j, draw): (word0 >> 8) * 2^-24,
 // exact in float32.
 __device__ __forceinline__ float philox_uniform(unsigned long long seed, uint32_t b, uint32_t j,

@@ -9,7 +9,9 @@ namespace sv {
 
 constexpr int kThreads = 256;           // threads per CTA, every kernel
 constexpr int kRowChunkBytes = 32768;   // row-statistics: bytes of one row chunk per CTA
-constexpr int kSampleChunkBytes = 16384;// sampler: bytes of one row chunk per CTA
+constexpr int kLevel1 = 8192;           // tokens per level-1 block of the grouped inverse CDF
+constexpr int kLevel2 = 256;            // tokens per level-2 block
+constexpr int kLevel3 = 16;             // tokens per level-3 block
 constexpr int kWalkMaxThreads = 256;    // walk: one thread per row of a request (N+1 <= 256)
 
 constexpr int kModeInvalid = 0;
@@ -37,14 +39,15 @@ constexpr int kJobResidual = 1;
 constexpr int kJobBonus = 2;
 
 // What the walk leaves for the sampler, one per request.
-//   q_t = 2^(z_t*k - cq) * inv_sq, p_t = 2^(y_t*k - cp) * inv_sp
+//   q_t = 2^(z_t*k - cq) * inv_sq
+//   log2(q_t / p_t) = (z_t - y_t)*k - (dhi + dlo)
 struct Job {
   int kind;     // kJob*
   int row;      // 0-based row of the correction (first rejected) or bonus row
-  float u;      // uniform of the sampling draw
+  float u[4];   // uniforms of the sampling draw, one per level
   float k;      // log2(e) / T
   float cq, inv_sq;
-  float cp, inv_sp;
+  float dhi, dlo;
 };
 
 struct Problem {
@@ -62,13 +65,13 @@ struct Problem {
 struct Workspace {
   Partial* partials;     // [rows = B(2N+1), S1]
   Job* jobs;             // [B]
-  float* chunk_sums;     // [B, S3]
+  float* chunk_sums;     // [B, S3]: residual mass of each level-1 block
   unsigned* counters;    // [B], zero between calls
   unsigned* err;         // [1], OR of kErr* bits
   float* dbg_accept;     // [B, N]
   float* dbg_logz;       // [B, 2N+1]
   int S1;                // row-statistics chunks per row for this call's V
-  int S3;                // sampler chunks per row for this call's V
+  int S3;                // level-1 blocks per row for this call's V
 };
 
 // dtype codes match SV_F32 / SV_BF16
@@ -81,6 +84,6 @@ cudaError_t launch_philox_probe(unsigned long long seed, const uint32_t* ctr3, u
                                 int n, cudaStream_t s);
 
 inline int row_chunk_elems(int dtype) { return kRowChunkBytes / (dtype == 1 ? 2 : 4); }
-inline int sample_chunk_elems(int dtype) { return kSampleChunkBytes / (dtype == 1 ? 2 : 4); }
+inline int sample_chunk_elems(int) { return kLevel1; }
 
 }  // namespace sv

@@ -1,18 +1,28 @@
-// Correction / bonus sampling by inverse CDF, touching only the one row (or
-// row pair) per request that the walk selected.
+// Correction / bonus sampling, touching only the one row (or row pair) per
+// request that the walk selected.
 //
 // "Speculative Decoding and EAGLE-3" lesson, "Invariant: Leviathan rejection
 // sampling" and "Build it" step 2: after a rejection at position j the token
 // comes from the residual r_t = (q_j(t) - p_j(t))_+ normalised by its sum
 // (from q_j itself if that sum is 0); after a full acceptance it comes from
-// q_{N+1}.  The sample is the smallest vocabulary index t whose running sum
-// of r exceeds u * sum(r).
+// q_{N+1}.
 //
-// Grid: B x S3 CTAs, one per (request, 16 KB chunk).  Each CTA sums r over its
-// chunk; the last CTA of a request to finish (counted with an atomic, no
-// waiting) turns the chunk sums into a prefix, finds the chunk holding
-// u * sum(r), rescans only that chunk with a CTA-wide scan, and writes the
-// token.  It then resets the request's counter for the next call.
+// The draw is a grouped inverse CDF with one uniform per level: the
+// vocabulary is split into level-1 blocks of 8192 consecutive tokens, a block
+// into 32 blocks of 256, those into 16 blocks of 16, and those into tokens;
+// at each level the sub-block is the smallest index whose running mass
+// exceeds u_level times the level's total (the last one with mass if
+// rounding leaves none).  The law is exactly r / sum(r), and every decision
+// compares a uniform against at most a few dozen float32 edges.
+//
+// Grid: B x S3 CTAs, one per (request, level-1 block).  Each CTA sums r over
+// its block; the last CTA of a request to finish (counted with an atomic, no
+// waiting) picks the level-1 block, rescans only that block for levels 2-4,
+// writes the token and resets the request's counter for the next call.
+//
+// r_t is evaluated as q_t * (1 - 2^-d_t) with d_t = log2(q_t / p_t) taken from
+// the logit difference and computed with expm1, so that it keeps its relative
+// precision when q_t and p_t nearly cancel.
 
 #include <climits>
 #include <cuda_bf16.h>
@@ -22,23 +32,23 @@
 namespace sv {
 namespace {
 
-// r_t from one target value (and one draft value when has_p).  Both the
-// chunk sums and the rescan evaluate exactly this expression.
+// r_t from one target value (and one draft value when has_p).  The block
+// masses and the rescan evaluate exactly this expression.
 __device__ __forceinline__ float resid(float zt, float yt, const Job& job, bool has_p) {
   const float q = ex2(fmaf(zt, job.k, -job.cq)) * job.inv_sq;
   if (!has_p) return q;
-  const float pr = ex2(fmaf(yt, job.k, -job.cp)) * job.inv_sp;
-  return fmaxf(q - pr, 0.f);
+  const float d = fmaf(zt - yt, job.k, -job.dhi) - job.dlo;  // log2(q_t / p_t)
+  return d > 0.f ? q * -expm1f(d * -0.693147180559945309f) : 0.f;
 }
 
 template <typename T, bool kVecPath>
-__device__ float chunk_sum(const T* z, const T* y, int beg, int end, const Job& job, bool has_p,
-                           float* scratch) {
+__device__ float block_mass(const T* z, const T* y, int beg, int end, const Job& job, bool has_p,
+                            float* scratch) {
   using E = Elem<T>;
   float s = 0.f;
   if (kVecPath) {
     constexpr int kVec = E::kVec;
-    constexpr int kPer = kSampleChunkBytes / 16 / kThreads;
+    constexpr int kPer = kLevel1 / kVec / kThreads;
     const uint4* zp = reinterpret_cast<const uint4*>(z + beg);
     const uint4* yp = reinterpret_cast<const uint4*>(y + beg);
     const int nv = (end - beg) / kVec;
@@ -47,7 +57,8 @@ __device__ float chunk_sum(const T* z, const T* y, int beg, int end, const Job& 
     for (int i = 0; i < kPer; ++i) {
       const int v = threadIdx.x + i * kThreads;
       const bool in = v < nv;
-      zr[i] = in ? __ldg(zp + v) : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+      zr[i] = in ? __ldg(zp + v)
+                 : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
       yr[i] = (in && has_p) ? __ldg(yp + v) : zr[i];
     }
 #pragma unroll
@@ -65,17 +76,57 @@ __device__ float chunk_sum(const T* z, const T* y, int beg, int end, const Job& 
   return block_sum(s, scratch);
 }
 
+// Inverse CDF over n masses, evaluated by one whole warp (all lanes get the
+// result): the smallest c with running sum C_c > u * C_{n-1}; if none, the
+// last c with mass > 0; -1 if every mass is 0.  Masses are read through
+// `get(i)`.  Tiles of 32 are scanned in index order twice (total, then the
+// crossing) with identical arithmetic.
+template <typename Get>
+__device__ int warp_pick(Get get, int n, float u) {
+  const int lane = threadIdx.x & 31;
+  float carry = 0.f;
+  int last_pos = -1;
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    const float m = i < n ? get(i) : 0.f;
+    float incl = m;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned pos = __ballot_sync(kFull, m > 0.f);
+    if (pos) last_pos = base + 31 - __clz(pos);
+    carry += __shfl_sync(kFull, incl, 31);
+  }
+  if (last_pos < 0) return -1;
+  const float target = u * carry;
+  carry = 0.f;
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    const float m = i < n ? get(i) : 0.f;
+    float incl = m;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned hit = __ballot_sync(kFull, i < n && carry + incl > target);
+    if (hit) return base + __ffs(hit) - 1;
+    carry += __shfl_sync(kFull, incl, 31);
+  }
+  return last_pos;
+}
+
 template <typename T, bool kVecPath>
 __global__ void __launch_bounds__(kThreads) sample_kernel(Problem p, Workspace w) {
   using E = Elem<T>;
-  constexpr int kChunk = kSampleChunkBytes / static_cast<int>(sizeof(T));
-  constexpr int kSeg = kChunk / kThreads;  // contiguous elements per thread in the rescan
+  constexpr int kSeg = kLevel1 / kThreads;  // 32 contiguous tokens per thread in the rescan
   __shared__ float red[kThreads / 32];
-  __shared__ float red2[kThreads / 32];
-  __shared__ int red_i[kThreads / 32];
-  __shared__ int red_j[kThreads / 32];
-  __shared__ int s_last;
-  __shared__ float s_sel[3];  // chunk index (as bits), prefix before it, target
+  __shared__ float s_l2[kLevel1 / kLevel2];         // 32 level-2 masses
+  __shared__ float s_l3[kLevel1 / kLevel3];         // 512 level-3 masses
+  __shared__ float s_l4[kLevel3];                   // 16 token masses
+  __shared__ int s_last, s_sel, s_g2, s_g3, s_tok;
   const int S3 = w.S3;
   const int b = blockIdx.x / S3;
   const int c = blockIdx.x - b * S3;
@@ -89,8 +140,8 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(Problem p, Workspace w
   bool has_p = job.kind == kJobResidual;
   float* sums = w.chunk_sums + static_cast<size_t>(b) * S3;
 
-  const int beg = c * kChunk;
-  const float part = chunk_sum<T, kVecPath>(z, y, beg, min(V, beg + kChunk), job, has_p, red);
+  const int beg = c * kLevel1;
+  const float part = block_mass<T, kVecPath>(z, y, beg, min(V, beg + kLevel1), job, has_p, red);
   if (threadIdx.x == 0) {
     sums[c] = part;
     __threadfence();
@@ -101,65 +152,41 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(Problem p, Workspace w
   if (!s_last) return;
   __threadfence();
 
-  // ---- last CTA of request b: locate the chunk, then the token.
+  // ---- last CTA of request b.  Level 1: pick the block.
   for (int pass = 0; pass < 2; ++pass) {
-    if (threadIdx.x == 0) {
-      float prefix = 0.f;
-      for (int i = 0; i < S3; ++i) prefix += __ldcg(sums + i);
-      const float total = prefix;
-      const float target = job.u * total;
-      int sel = -1, last_pos = -1;
-      float before = 0.f, before_last = 0.f, run = 0.f;
-      for (int i = 0; i < S3; ++i) {
-        const float v = __ldcg(sums + i);
-        if (v > 0.f) {
-          last_pos = i;
-          before_last = run;
-        }
-        if (sel < 0 && run + v > target) {
-          sel = i;
-          before = run;
-        }
-        run += v;
-      }
-      if (sel < 0) {  // rounding put the target at or past the end
-        sel = last_pos;
-        before = before_last;
-      }
-      s_sel[0] = __int_as_float(total > 0.f ? sel : -1);
-      s_sel[1] = before;
-      s_sel[2] = target;
+    if (threadIdx.x < 32) {
+      const int sel = warp_pick([&](int i) { return __ldcg(sums + i); }, S3, job.u[0]);
+      if (threadIdx.x == 0) s_sel = sel;
     }
     __syncthreads();
-    if (__float_as_int(s_sel[0]) >= 0) break;
-    // The residual has no mass: sample from q instead (recompute every chunk).
-    if (!has_p || pass == 1) break;
+    if (s_sel >= 0 || !has_p || pass == 1) break;
+    // The residual has no mass: sample from q instead.
     has_p = false;
     for (int i = 0; i < S3; ++i) {
-      const int bi = i * kChunk;
-      const float v = chunk_sum<T, kVecPath>(z, y, bi, min(V, bi + kChunk), job, false, red);
+      const int bi = i * kLevel1;
+      const float v = block_mass<T, kVecPath>(z, y, bi, min(V, bi + kLevel1), job, false, red);
       if (threadIdx.x == 0) sums[i] = v;
       __syncthreads();
     }
     __threadfence_block();
   }
-  const int sel = __float_as_int(s_sel[0]);
+  const int sel = s_sel;
   int token = 0;
   if (sel >= 0) {
-    const float before = s_sel[1], target = s_sel[2];
-    const int cbeg = sel * kChunk;
-    const int cend = min(V, cbeg + kChunk);
+    // Rescan the chosen block: thread t holds tokens [32t, 32t + 32) of it.
+    const int cbeg = sel * kLevel1;
+    const int cend = min(V, cbeg + kLevel1);
     const int t0 = cbeg + threadIdx.x * kSeg;
     float r[kSeg];
     if (kVecPath) {
       constexpr int kVec = E::kVec;
-      constexpr int kVecs = kSeg / kVec;
 #pragma unroll
-      for (int i = 0; i < kVecs; ++i) {
+      for (int i = 0; i < kSeg / kVec; ++i) {
         const int e0 = t0 + i * kVec;
         const bool in = e0 < cend;
         const uint4 zv = in ? __ldg(reinterpret_cast<const uint4*>(z + e0))
-                            : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+                            : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord,
+                                         E::kNegInfWord);
         const uint4 yv = (in && has_p) ? __ldg(reinterpret_cast<const uint4*>(y + e0)) : zv;
 #pragma unroll
         for (int e = 0; e < kVec; ++e) r[i * kVec + e] = resid(E::get(zv, e), E::get(yv, e), job, has_p);
@@ -168,28 +195,50 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(Problem p, Workspace w
 #pragma unroll
       for (int i = 0; i < kSeg; ++i) {
         const int t = t0 + i;
-        if (t < cend) {
-          r[i] = resid(E::load1(z + t), has_p ? E::load1(y + t) : 0.f, job, has_p);
-        } else {
-          r[i] = 0.f;
-        }
+        r[i] = t < cend ? resid(E::load1(z + t), has_p ? E::load1(y + t) : 0.f, job, has_p) : 0.f;
       }
     }
-    float mine = 0.f;
+    float h0 = 0.f, h1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < kSeg; ++i) mine += r[i];
-    float total;
-    float run = before + block_exclusive_scan(mine, red2, &total);
-    int hit = INT_MAX, lastpos = -1;
-#pragma unroll
-    for (int i = 0; i < kSeg; ++i) {
-      run += r[i];
-      if (hit == INT_MAX && run > target) hit = t0 + i;
-      if (r[i] > 0.f) lastpos = t0 + i;
+    for (int i = 0; i < kLevel3; ++i) {
+      h0 += r[i];
+      h1 += r[kLevel3 + i];
     }
-    hit = block_min_int(hit, red_i);
-    lastpos = block_max_int(lastpos, red_j);
-    token = hit != INT_MAX ? hit : lastpos;
+    s_l3[2 * threadIdx.x] = h0;
+    s_l3[2 * threadIdx.x + 1] = h1;
+    // level-2 mass: the 8 consecutive threads of one 256-token block
+    float m2 = h0 + h1;
+    m2 += __shfl_xor_sync(kFull, m2, 1);
+    m2 += __shfl_xor_sync(kFull, m2, 2);
+    m2 += __shfl_xor_sync(kFull, m2, 4);
+    if ((threadIdx.x & 7) == 0) s_l2[threadIdx.x >> 3] = m2;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // a chosen block has mass > 0, so each level below finds a sub-block
+      // with mass; max(.., 0) only keeps the indices in range regardless
+      const int g2 = max(warp_pick([&](int i) { return s_l2[i]; }, kLevel1 / kLevel2, job.u[1]), 0);
+      const int g3 = max(warp_pick([&](int i) { return s_l3[g2 * (kLevel2 / kLevel3) + i]; },
+                                   kLevel2 / kLevel3, job.u[2]),
+                         0);
+      if (threadIdx.x == 0) {
+        s_g2 = g2;
+        s_g3 = g3;
+      }
+    }
+    __syncthreads();
+    // the 16 token masses of the chosen level-3 block live in one thread
+    const int blk3 = s_g2 * (kLevel2 / kLevel3) + s_g3;   // level-3 block within the level-1 block
+    if (threadIdx.x == (blk3 >> 1)) {
+#pragma unroll
+      for (int i = 0; i < kLevel3; ++i) s_l4[i] = (blk3 & 1) ? r[kLevel3 + i] : r[i];
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int g4 = max(warp_pick([&](int i) { return s_l4[i]; }, kLevel3, job.u[3]), 0);
+      if (threadIdx.x == 0) s_tok = cbeg + blk3 * kLevel3 + g4;
+    }
+    __syncthreads();
+    token = s_tok;
   }
   if (threadIdx.x == 0) {
     p.out_tokens[static_cast<size_t>(b) * (N + 1) + job.row] = token;

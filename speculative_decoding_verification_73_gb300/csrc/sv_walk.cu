@@ -206,12 +206,15 @@ __global__ void __launch_bounds__(kWalkMaxThreads) walk_kernel(Problem p, Worksp
     Job job;
     job.kind = a < N ? kJobResidual : kJobBonus;
     job.row = a;
-    job.u = philox_uniform(p.seed, b, a + 1, 1);
+    philox_uniforms4(p.seed, b, a + 1, 1, job.u);
     job.k = k;
     job.cq = q.c;
     job.inv_sq = static_cast<float>(1.0 / q.s);
-    job.cp = a < N ? pn.c : 0.f;
-    job.inv_sp = a < N ? static_cast<float>(1.0 / pn.s) : 0.f;
+    // log2 Z_q - log2 Z_p as a float pair, so that log2(q_t / p_t) keeps its
+    // precision when q_t and p_t are close
+    const double dl = a < N ? q.l2z - pn.l2z : 0.0;
+    job.dhi = static_cast<float>(dl);
+    job.dlo = static_cast<float>(dl - static_cast<double>(job.dhi));
     w.jobs[b] = job;
     p.out_accept[b] = a;
     p.out_kv[b] = a + 1;

@@ -3,16 +3,19 @@
 * greedy requests: tokens, accept length and KV length bit-exact;
 * sampled requests: bit-exact, except where the oracle's decision at the
   point of divergence had its uniform within WINDOW (1e-5) of its threshold
-  (|u - min(1, q/p)| for an accept test, the distance of u to the edges of
-  the chosen bucket of the normalised CDF for a correction / bonus draw);
-  every such mismatch is logged, and mismatches must stay below 1e-5 of the
-  verified positions;
+  (|u - min(1, q/p)| for an accept test; for a correction / bonus draw, the
+  distance of that level's uniform to the edges of the chosen sub-block at
+  the first level of the grouped inverse CDF where the two tokens' blocks
+  differ); every such mismatch is logged, and mismatches must stay below
+  1e-5 of the verified positions;
 * error requests: identical error bits and the -1 / 0 markers.
 """
 
 import math
 
 import numpy as np
+
+from oracle.verify import LEVEL_SHIFTS
 
 WINDOW = 1e-5
 
@@ -54,13 +57,17 @@ def compare(res, tokens, accept, kv, temperature, n, label=""):
         if accept[b] != res.accept_len[b]:
             j = min(int(accept[b]), int(res.accept_len[b])) + 1
             dec = [x for x in decs if x.kind == "accept" and x.j == j]
+            assert dec, "no oracle decision at the divergence: " + where
+            dist = dec[0].distance()
         else:
             dec = [x for x in decs if x.kind in ("residual", "bonus")]
+            assert dec, "no oracle decision at the divergence: " + where
             # the accepted prefix must agree exactly
             a = int(accept[b])
             assert np.array_equal(tokens[b, :a], res.tokens[b, :a]), where
-        assert dec, "no oracle decision at the divergence: " + where
-        dist = dec[0].distance()
+            t_gpu, t_ref = int(tokens[b, a]), int(res.tokens[b, a])
+            level = next(lv for lv, sh in enumerate(LEVEL_SHIFTS) if (t_gpu >> sh) != (t_ref >> sh))
+            dist = dec[0].distance(level)
         assert dist < WINDOW, f"mismatch outside the 1e-5 window (distance {dist:.3g}): " + where
         logged.append((label, b, dec[0].kind, dec[0].j, dist))
         print("near-threshold mismatch:", where, f"distance={dist:.3g}")
