@@ -228,7 +228,7 @@ def run_ours(args):
     positions = B * N * args.steps * world
     value = positions / (elapsed_ms / 1e3)
     bytes_per_launch = wl.bytes_read()
-    rowstats_ms = kernel_ms["rowstats"] / max(calls, 1)
+    rowstats_ms = kernel_ms["rowstats_walk"] / max(calls, 1)
     achieved = bytes_per_launch / (rowstats_ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
 
@@ -297,7 +297,7 @@ def run_ours(args):
             "parallelism": f"replicas x{world} (requests shard, no collective)",
         },
         "roofline": {
-            "bound": "hbm", "kernel": "rowstats", "achieved": achieved, "peak": peak,
+            "bound": "hbm", "kernel": "rowstats_walk", "achieved": achieved, "peak": peak,
             "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s", "frac": achieved / peak,
             "traffic": traffic_per_launch(), "algorithmic_bytes_per_launch": bytes_per_launch,
             "avg_launch_us": rowstats_ms * 1e3,

@@ -148,10 +148,12 @@ int spec_verify_debug_stats(spec_verify_ctx* ctx, int B, int N,
  * records CUDA events around each kernel it launches on the context's
  * stream.  spec_verify_profile_read waits for the stream and returns, for
  * the calls since the last read, the summed device time in milliseconds of
- * each of the SV_NUM_KERNELS kernels (row statistics, walk, sampling) and
- * the number of calls; it then clears the sums.
+ * each of the SV_NUM_KERNELS kernels and the number of calls; it then
+ * clears the sums.  Kernel 0 streams every logit row once (row statistics)
+ * and runs each request's accept/reject walk as its last chunk finishes;
+ * kernel 1 samples the correction / bonus tokens.
  */
-#define SV_NUM_KERNELS 3
+#define SV_NUM_KERNELS 2
 int spec_verify_profile(spec_verify_ctx* ctx, int enable);
 int spec_verify_profile_read(spec_verify_ctx* ctx, double* ms_per_kernel,
                              int* calls);

@@ -17,9 +17,9 @@ LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 SV_OK, SV_EINVAL, SV_EBADTEMP, SV_EBADTOKEN, SV_EBADLOGIT, SV_ECUDA = range(6)
 SV_ERRBIT_TEMP, SV_ERRBIT_TOKEN, SV_ERRBIT_LOGIT = 1, 2, 4
 SV_F32, SV_BF16 = 0, 1
-SV_NUM_KERNELS = 3
+SV_NUM_KERNELS = 2
 SV_MAX_N = 255
-KERNEL_NAMES = ("rowstats", "walk", "sample")
+KERNEL_NAMES = ("rowstats_walk", "sample")
 
 _DTYPE_CODE = {torch.float32: SV_F32, torch.bfloat16: SV_BF16}
 

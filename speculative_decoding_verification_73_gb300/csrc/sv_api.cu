@@ -115,6 +115,8 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   off = align_up(off + static_cast<size_t>(max_B) * s3 * sizeof(float), 256);
   const size_t o_cnt = off;
   off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
+  const size_t o_wcnt = off;
+  off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
   const size_t o_err = off;
   off = align_up(off + sizeof(unsigned), 256);
   const size_t zero_bytes = off - o_cnt;  // counters and error word start at zero
@@ -131,6 +133,7 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   ctx->w.jobs = reinterpret_cast<sv::Job*>(base + o_jobs);
   ctx->w.chunk_sums = reinterpret_cast<float*>(base + o_sums);
   ctx->w.counters = reinterpret_cast<unsigned*>(base + o_cnt);
+  ctx->w.walk_counters = reinterpret_cast<unsigned*>(base + o_wcnt);
   ctx->w.err = reinterpret_cast<unsigned*>(base + o_err);
   ctx->w.dbg_accept = reinterpret_cast<float*>(base + o_acc);
   ctx->w.dbg_logz = reinterpret_cast<float*>(base + o_lz);
@@ -184,11 +187,9 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
   }
   if (sv::launch_rowstats(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
   if (ev && cudaEventRecord(ev[1], ctx->stream) != cudaSuccess) return SV_ECUDA;
-  if (sv::launch_walk(ctx->dtype, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
-  if (ev && cudaEventRecord(ev[2], ctx->stream) != cudaSuccess) return SV_ECUDA;
   if (sv::launch_sample(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
   if (ev) {
-    if (cudaEventRecord(ev[3], ctx->stream) != cudaSuccess) return SV_ECUDA;
+    if (cudaEventRecord(ev[2], ctx->stream) != cudaSuccess) return SV_ECUDA;
     ctx->recorded += 1;
   }
   return SV_OK;

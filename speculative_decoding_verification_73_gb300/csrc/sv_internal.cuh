@@ -12,7 +12,8 @@ constexpr int kRowChunkBytes = 32768;   // row-statistics: bytes of one row chun
 constexpr int kLevel1 = 8192;           // tokens per level-1 block of the grouped inverse CDF
 constexpr int kLevel2 = 256;            // tokens per level-2 block
 constexpr int kLevel3 = 16;             // tokens per level-3 block
-constexpr int kWalkMaxThreads = 256;    // walk: one thread per row of a request (N+1 <= 256)
+// The walk runs on the row-statistics CTA of kThreads threads, one thread per
+// row of a request, so N + 1 <= kThreads.
 
 constexpr int kModeInvalid = 0;
 constexpr int kModeGreedy = 1;
@@ -66,7 +67,8 @@ struct Workspace {
   Partial* partials;     // [rows = B(2N+1), S1]
   Job* jobs;             // [B]
   float* chunk_sums;     // [B, S3]: residual mass of each level-1 block
-  unsigned* counters;    // [B], zero between calls
+  unsigned* counters;    // [B], sampler chunk counts, zero between calls
+  unsigned* walk_counters;  // [B], row-statistics chunk counts, zero between calls
   unsigned* err;         // [1], OR of kErr* bits
   float* dbg_accept;     // [B, N]
   float* dbg_logz;       // [B, 2N+1]
@@ -77,7 +79,6 @@ struct Workspace {
 // dtype codes match SV_F32 / SV_BF16
 cudaError_t launch_rowstats(int dtype, bool vec, const Problem& p, const Workspace& w,
                             cudaStream_t s);
-cudaError_t launch_walk(int dtype, const Problem& p, const Workspace& w, cudaStream_t s);
 cudaError_t launch_sample(int dtype, bool vec, const Problem& p, const Workspace& w,
                           cudaStream_t s);
 cudaError_t launch_philox_probe(unsigned long long seed, const uint32_t* ctr3, uint32_t* out4,

@@ -14,11 +14,16 @@
 // loads up front (8 per thread), so a CTA has 32 KB in flight; the chunk
 // maximum is reduced over the CTA first, and every exponent then uses that
 // one reference, so no per-thread rescaling is needed.
+//
+// The CTA that finishes the last chunk of a request (counted with an atomic
+// per request; nothing waits) then runs that request's accept/reject walk,
+// so walks overlap the other requests' streaming.
 
 #include <climits>
 #include <cuda_bf16.h>
 
 #include "sv_device.cuh"
+#include "sv_walk.cuh"
 
 namespace sv {
 namespace {
@@ -177,25 +182,44 @@ __device__ void chunk_scalar(const T* row, int beg, int end, bool greedy, float 
 
 template <typename T, bool kVecPath>
 __global__ void __launch_bounds__(kThreads) rowstats_kernel(Problem p, Workspace w) {
+  __shared__ int s_last;
   const int S1 = w.S1;
   const int row = blockIdx.x / S1;
   const int chunk = blockIdx.x - row * S1;
   const RowRef r = locate_row(p, row);
   const float t = p.temperature[r.b];
   const int mode = temp_mode(t);
-  if (mode == kModeInvalid || (mode == kModeGreedy && r.draft)) return;  // CTA-uniform
-  const T* base = static_cast<const T*>(r.draft ? p.draft : p.target) + r.offset;
-  constexpr int kChunk = kRowChunkBytes / static_cast<int>(sizeof(T));
-  const int beg = chunk * kChunk;
-  const int end = min(p.V, beg + kChunk);
-  const bool greedy = mode == kModeGreedy;
-  const float k = greedy ? 0.f : scale_of(t);
-  Partial* slot = w.partials + static_cast<size_t>(row) * S1 + chunk;
-  if (kVecPath) {
-    chunk_vec<T>(base, beg, end, greedy, k, slot);
-  } else {
-    chunk_scalar<T>(base, beg, end, greedy, k, slot);
+  if (mode == kModeGreedy && r.draft) return;  // CTA-uniform; not counted
+  if (mode == kModeInvalid && r.draft) return;
+  if (mode != kModeInvalid) {
+    const T* base = static_cast<const T*>(r.draft ? p.draft : p.target) + r.offset;
+    constexpr int kChunk = kRowChunkBytes / static_cast<int>(sizeof(T));
+    const int beg = chunk * kChunk;
+    const int end = min(p.V, beg + kChunk);
+    const bool greedy = mode == kModeGreedy;
+    const float k = greedy ? 0.f : scale_of(t);
+    Partial* slot = w.partials + static_cast<size_t>(row) * S1 + chunk;
+    if (kVecPath) {
+      chunk_vec<T>(base, beg, end, greedy, k, slot);
+    } else {
+      chunk_scalar<T>(base, beg, end, greedy, k, slot);
+    }
   }
+  // Count this chunk for its request: target rows always, draft rows only
+  // when the request is sampled.  The CTA that brings the count to its total
+  // runs the walk.
+  if (threadIdx.x == 0) {
+    const unsigned total =
+        static_cast<unsigned>(S1) * static_cast<unsigned>(p.N + 1 + (mode == kModeSampled ? p.N : 0));
+    __threadfence();
+    const unsigned prev = atomicAdd(w.walk_counters + r.b, 1u);
+    s_last = prev + 1 == total;
+    if (s_last) w.walk_counters[r.b] = 0u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  walk_request<T>(p, w, r.b);
 }
 
 }  // namespace

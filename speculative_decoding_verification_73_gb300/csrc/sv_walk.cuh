@@ -1,0 +1,215 @@
+// The accept/reject walk of one request, run by the CTA that finishes the
+// request's last row chunk (see sv_rowstats.cu); thread j handles row j.
+//
+// Thread j merges the row-statistics partials of target row j (and, for a
+// sampled request, draft row j), checks the inputs, and evaluates position
+// j+1 of the chain.  "Speculative Decoding and EAGLE-3" lesson:
+//   * "Build it", step 1: a draft with p(d) = 0 is accepted; otherwise it is
+//     accepted iff u < min(1, q(d) / p(d));
+//   * "Invariant: Leviathan rejection sampling": the walk goes left to right
+//     and stops at the first rejection; if all N are accepted a bonus token
+//     comes from q_{N+1};
+//   * "KV cache rollback" / "Build it" step 4: the committed KV length stops
+//     right after the correction token, i.e. accepted + 1 entries of this
+//     window.
+// Greedy requests (T = 0) accept d_j iff it equals the argmax of target row
+// j; the emitted token after the prefix is the argmax of the next row.
+//
+// All arithmetic is float32 (double-precision transcendentals are very slow
+// on this part).  The acceptance ratio is formed as
+//   log2(q(d)/p(d)) = (z_d - y_d) k - (c_q - c_p) + log2(s_p / s_q),
+// so every term stays small when q(d) and p(d) are close.  The correction /
+// bonus token of a sampled request is left to the sampler as a Job.
+#pragma once
+
+#include <climits>
+
+#include "sv_device.cuh"
+
+namespace sv {
+
+// log2 sum_t 2^(x_t k) = c + log2(s)
+struct RowNorm {
+  float c;
+  float s;
+  bool ok;
+};
+
+__device__ __forceinline__ RowNorm merge_sampled(const Partial* parts, int S1) {
+  float c = -INFINITY;
+  bool bad = false;
+  for (int i = 0; i < S1; ++i) {
+    const float4 pt = __ldcg(reinterpret_cast<const float4*>(parts + i));
+    if (pt.y != pt.y) bad = true;
+    c = fmaxf(c, pt.x);
+  }
+  RowNorm r;
+  r.c = c;
+  r.s = 0.f;
+  if (!bad && c > -INFINITY) {
+    for (int i = 0; i < S1; ++i) {
+      const float4 pt = __ldcg(reinterpret_cast<const float4*>(parts + i));
+      if (pt.x > -INFINITY) r.s += pt.y * exp2f(pt.x - c);
+    }
+  }
+  r.ok = !bad && c > -INFINITY && c < INFINITY && r.s > 0.f && r.s < INFINITY;
+  return r;
+}
+
+struct RowMax {
+  int idx;
+  bool ok;
+};
+
+__device__ __forceinline__ RowMax merge_greedy(const Partial* parts, int S1) {
+  float best = -INFINITY;
+  int idx = INT_MAX;
+  bool bad = false;
+  for (int i = 0; i < S1; ++i) {
+    const int4 pt = __ldcg(reinterpret_cast<const int4*>(parts + i));
+    const float a = __int_as_float(pt.x), s = __int_as_float(pt.y);
+    if (s != s || a != a) bad = true;
+    if (a > best) {  // chunks are in index order: strict > keeps the lowest index
+      best = a;
+      idx = pt.z;
+    }
+  }
+  RowMax r;
+  r.idx = idx;
+  r.ok = !bad && best > -INFINITY && best < INFINITY;
+  return r;
+}
+
+// Error-free sum: s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+template <typename T>
+__device__ __forceinline__ void walk_request(const Problem& p, const Workspace& w, int b) {
+  const int j = threadIdx.x;
+  const int N = p.N, V = p.V, S1 = w.S1;
+  const bool row_thread = j <= N;
+  const bool pos_thread = j < N;
+
+  __shared__ int s_bad_token, s_bad_logit, s_first;
+  if (j == 0) {
+    s_bad_token = 0;
+    s_bad_logit = 0;
+    s_first = N;
+  }
+  __syncthreads();
+
+  const float t = p.temperature[b];
+  const int mode = temp_mode(t);
+  int d = -1;
+  if (pos_thread) {
+    d = p.tokens[static_cast<size_t>(b) * N + j];
+    if (d < 0 || d >= V) atomicOr(&s_bad_token, 1);
+  }
+
+  const size_t trow = static_cast<size_t>(b) * (N + 1) + j;  // target row
+  const size_t drow = static_cast<size_t>(p.B) * (N + 1) +    // draft row, as numbered
+                      static_cast<size_t>(b) * N + j;         // in the partials array
+  RowNorm q{}, pn{};
+  RowMax g{};
+  if (mode == kModeGreedy && row_thread) {
+    g = merge_greedy(w.partials + trow * S1, S1);
+    if (!g.ok) atomicOr(&s_bad_logit, 1);
+  } else if (mode == kModeSampled && row_thread) {
+    q = merge_sampled(w.partials + trow * S1, S1);
+    if (!q.ok) atomicOr(&s_bad_logit, 1);
+    if (pos_thread) {
+      pn = merge_sampled(w.partials + drow * S1, S1);
+      if (!pn.ok) atomicOr(&s_bad_logit, 1);
+    }
+  }
+  __syncthreads();
+
+  unsigned err = 0;
+  if (mode == kModeInvalid)
+    err = kErrTemp;
+  else if (s_bad_token)
+    err = kErrToken;
+  else if (s_bad_logit)
+    err = kErrLogit;
+
+  int32_t* out_tok = p.out_tokens + static_cast<size_t>(b) * (N + 1);
+  float* dbg_acc = w.dbg_accept + static_cast<size_t>(b) * N;
+  float* dbg_lz = w.dbg_logz + static_cast<size_t>(b) * (2 * N + 1);
+  const float qnan = __int_as_float(0x7fc00000);
+  constexpr float kLn2 = 0.693147180559945309f;
+
+  if (err || mode == kModeGreedy) {
+    int a = -1;
+    if (!err) {
+      if (pos_thread && d != g.idx) atomicMin(&s_first, j);
+      __syncthreads();
+      a = s_first;
+    }
+    if (row_thread) {
+      out_tok[j] = (!err && j <= a) ? g.idx : -1;
+      dbg_lz[j] = qnan;
+      if (pos_thread) {
+        dbg_acc[j] = qnan;
+        dbg_lz[N + 1 + j] = qnan;
+      }
+    }
+    if (j == 0) {
+      p.out_accept[b] = err ? -1 : a;
+      p.out_kv[b] = err ? 0 : a + 1;
+      w.jobs[b].kind = kJobNone;
+      if (err) atomicOr(w.err, err);
+    }
+    return;
+  }
+
+  // Sampled request.
+  const float k = scale_of(t);
+  if (pos_thread) {
+    const float zd = Elem<T>::load1(static_cast<const T*>(p.target) + trow * V + d);
+    const float yd = Elem<T>::load1(static_cast<const T*>(p.draft) +
+                                    (static_cast<size_t>(b) * N + j) * V + d);
+    float thr = 1.f;
+    bool accepted = true;
+    if (yd != -INFINITY) {  // p(d) > 0
+      const float lr = fmaf(zd - yd, k, -(q.c - pn.c)) + log2f(pn.s / q.s);  // log2 q(d)/p(d)
+      thr = fminf(1.f, exp2f(lr));
+      accepted = philox_uniform(p.seed, b, j + 1, 0) < thr;
+    }
+    dbg_acc[j] = thr;
+    dbg_lz[N + 1 + j] = (pn.c + log2f(pn.s)) * kLn2;
+    if (!accepted) atomicMin(&s_first, j);
+  }
+  if (row_thread) dbg_lz[j] = (q.c + log2f(q.s)) * kLn2;
+  __syncthreads();
+  const int a = s_first;
+  if (row_thread) out_tok[j] = j < a ? d : -1;
+  if (j == a) {
+    Job job;
+    job.kind = a < N ? kJobResidual : kJobBonus;
+    job.row = a;
+    philox_uniforms4(p.seed, b, a + 1, 1, job.u);
+    job.k = k;
+    job.cq = q.c;
+    job.inv_sq = 1.f / q.s;
+    // log2 Z_q - log2 Z_p = (c_q - c_p) + log2(s_q / s_p) as a float pair,
+    // so that log2(q_t / p_t) keeps its precision when q_t and p_t are close
+    float hi = 0.f, lo = 0.f;
+    if (a < N) {
+      float d1, e1, e2;
+      two_sum(q.c, -pn.c, d1, e1);
+      two_sum(d1, log2f(q.s / pn.s), hi, e2);
+      lo = e1 + e2;
+    }
+    job.dhi = hi;
+    job.dlo = lo;
+    w.jobs[b] = job;
+    p.out_accept[b] = a;
+    p.out_kv[b] = a + 1;
+  }
+}
+
+}  // namespace sv

@@ -45,7 +45,7 @@ def test_strerror_and_launch_count(lib):
     for code in range(1, 6):
         assert binding.strerror(code) != "unknown error code"
     assert binding.strerror(99) == "unknown error code"
-    assert binding.spec_verify_launches_per_call() == binding.SV_NUM_KERNELS == 3
+    assert binding.spec_verify_launches_per_call() == binding.SV_NUM_KERNELS == 2
 
 
 def test_host_argument_checks_need_no_gpu(lib):
