@@ -64,7 +64,7 @@ struct Problem {
 };
 
 struct Workspace {
-  Partial* partials;     // [rows = B(2N+1), S1]
+  Partial* partials;     // [B][2N+1][S1]: target rows 0..N, then draft rows 0..N-1
   Job* jobs;             // [B]
   float* chunk_sums;     // [B, S3]: residual mass of each level-1 block
   unsigned* counters;    // [B], sampler chunk counts, zero between calls

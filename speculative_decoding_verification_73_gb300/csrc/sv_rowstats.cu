@@ -34,19 +34,17 @@ struct RowRef {
   size_t offset;  // element offset of the row in its tensor
 };
 
+// CTAs are numbered request-major: request b owns rows b(2N+1) .. b(2N+1)+2N,
+// its N+1 target rows first, then its N draft rows, so a request's chunks are
+// streamed together and its walk runs soon after.
 __device__ __forceinline__ RowRef locate_row(const Problem& p, int row) {
-  const int tgt_rows = p.B * (p.N + 1);
+  const int per = 2 * p.N + 1;
   RowRef r;
-  if (row < tgt_rows) {
-    r.b = row / (p.N + 1);
-    r.draft = false;
-    r.offset = static_cast<size_t>(row) * p.V;
-  } else {
-    const int r2 = row - tgt_rows;
-    r.b = r2 / p.N;
-    r.draft = true;
-    r.offset = static_cast<size_t>(r2) * p.V;
-  }
+  r.b = row / per;
+  const int i = row - r.b * per;
+  r.draft = i > p.N;
+  r.offset = r.draft ? (static_cast<size_t>(r.b) * p.N + (i - p.N - 1)) * p.V
+                     : (static_cast<size_t>(r.b) * (p.N + 1) + i) * p.V;
   return r;
 }
 

@@ -21,8 +21,8 @@
 // writes the token and resets the request's counter for the next call.
 //
 // r_t is evaluated as q_t * (1 - 2^-d_t) with d_t = log2(q_t / p_t) taken from
-// the logit difference and computed with expm1, so that it keeps its relative
-// precision when q_t and p_t nearly cancel.
+// the logit difference, so that it keeps its relative precision when q_t and
+// p_t nearly cancel.
 
 #include <climits>
 #include <cuda_bf16.h>
@@ -32,13 +32,29 @@
 namespace sv {
 namespace {
 
+// 1 - 2^-d for d > 0, to full float precision: for d >= 1/2 directly (no
+// cancellation), below that from the Taylor series of 1 - e^-x at x = d ln 2
+// (x < 0.35; the first omitted term is below 1.6e-8 of the value).
+__device__ __forceinline__ float one_minus_exp2_neg(float d) {
+  const float x = d * 0.693147180559945309f;
+  float poly = 1.f / 5040.f;
+  poly = fmaf(poly, x, -1.f / 720.f);
+  poly = fmaf(poly, x, 1.f / 120.f);
+  poly = fmaf(poly, x, -1.f / 24.f);
+  poly = fmaf(poly, x, 1.f / 6.f);
+  poly = fmaf(poly, x, -0.5f);
+  poly = fmaf(poly, x, 1.f);
+  const float small = poly * x;
+  return d < 0.5f ? small : 1.f - ex2(-d);
+}
+
 // r_t from one target value (and one draft value when has_p).  The block
 // masses and the rescan evaluate exactly this expression.
 __device__ __forceinline__ float resid(float zt, float yt, const Job& job, bool has_p) {
   const float q = ex2(fmaf(zt, job.k, -job.cq)) * job.inv_sq;
   if (!has_p) return q;
   const float d = fmaf(zt - yt, job.k, -job.dhi) - job.dlo;  // log2(q_t / p_t)
-  return d > 0.f ? q * -expm1f(d * -0.693147180559945309f) : 0.f;
+  return d > 0.f ? q * one_minus_exp2_neg(d) : 0.f;
 }
 
 template <typename T, bool kVecPath>

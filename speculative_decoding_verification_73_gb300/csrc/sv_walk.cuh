@@ -35,24 +35,38 @@ struct RowNorm {
   bool ok;
 };
 
+// Partials are loaded kBatch at a time with every load issued before any is
+// used, so a row costs ceil(S1 / kBatch) L2 round trips, not S1.
+constexpr int kBatch = 8;
+
 __device__ __forceinline__ RowNorm merge_sampled(const Partial* parts, int S1) {
-  float c = -INFINITY;
+  float c = -INFINITY, s = 0.f;
   bool bad = false;
-  for (int i = 0; i < S1; ++i) {
-    const float4 pt = __ldcg(reinterpret_cast<const float4*>(parts + i));
-    if (pt.y != pt.y) bad = true;
-    c = fmaxf(c, pt.x);
+  for (int i0 = 0; i0 < S1; i0 += kBatch) {
+    float4 pt[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      pt[i] = i0 + i < S1 ? __ldcg(reinterpret_cast<const float4*>(parts + i0 + i))
+                          : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+    float cb = c;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (pt[i].y != pt[i].y) bad = true;
+      cb = fmaxf(cb, pt[i].x);
+    }
+    if (cb > -INFINITY) {
+      float sb = c > -INFINITY ? s * exp2f(c - cb) : 0.f;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+        if (pt[i].x > -INFINITY) sb += pt[i].y * exp2f(pt[i].x - cb);
+      s = sb;
+      c = cb;
+    }
   }
   RowNorm r;
   r.c = c;
-  r.s = 0.f;
-  if (!bad && c > -INFINITY) {
-    for (int i = 0; i < S1; ++i) {
-      const float4 pt = __ldcg(reinterpret_cast<const float4*>(parts + i));
-      if (pt.x > -INFINITY) r.s += pt.y * exp2f(pt.x - c);
-    }
-  }
-  r.ok = !bad && c > -INFINITY && c < INFINITY && r.s > 0.f && r.s < INFINITY;
+  r.s = s;
+  r.ok = !bad && c > -INFINITY && c < INFINITY && s > 0.f && s < INFINITY;
   return r;
 }
 
@@ -65,13 +79,20 @@ __device__ __forceinline__ RowMax merge_greedy(const Partial* parts, int S1) {
   float best = -INFINITY;
   int idx = INT_MAX;
   bool bad = false;
-  for (int i = 0; i < S1; ++i) {
-    const int4 pt = __ldcg(reinterpret_cast<const int4*>(parts + i));
-    const float a = __int_as_float(pt.x), s = __int_as_float(pt.y);
-    if (s != s || a != a) bad = true;
-    if (a > best) {  // chunks are in index order: strict > keeps the lowest index
-      best = a;
-      idx = pt.z;
+  for (int i0 = 0; i0 < S1; i0 += kBatch) {
+    int4 pt[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      pt[i] = i0 + i < S1 ? __ldcg(reinterpret_cast<const int4*>(parts + i0 + i))
+                          : make_int4(__float_as_int(-INFINITY), 0, INT_MAX, 0);
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const float a = __int_as_float(pt[i].x), sv = __int_as_float(pt[i].y);
+      if (sv != sv || a != a) bad = true;
+      if (a > best) {  // chunks are in index order: strict > keeps the lowest index
+        best = a;
+        idx = pt[i].z;
+      }
     }
   }
   RowMax r;
@@ -104,25 +125,33 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
 
   const float t = p.temperature[b];
   const int mode = temp_mode(t);
+  const size_t trow = static_cast<size_t>(b) * (N + 1) + j;  // target row in its tensor
   int d = -1;
+  float zd = 0.f, yd = 0.f;
   if (pos_thread) {
     d = p.tokens[static_cast<size_t>(b) * N + j];
-    if (d < 0 || d >= V) atomicOr(&s_bad_token, 1);
+    if (d < 0 || d >= V) {
+      atomicOr(&s_bad_token, 1);
+    } else if (mode == kModeSampled) {
+      // issue the two logit loads early; they are used after the merges
+      zd = Elem<T>::load1(static_cast<const T*>(p.target) + trow * V + d);
+      yd = Elem<T>::load1(static_cast<const T*>(p.draft) + (static_cast<size_t>(b) * N + j) * V + d);
+    }
   }
-
-  const size_t trow = static_cast<size_t>(b) * (N + 1) + j;  // target row
-  const size_t drow = static_cast<size_t>(p.B) * (N + 1) +    // draft row, as numbered
-                      static_cast<size_t>(b) * N + j;         // in the partials array
+  // partials are request-major: [b][target rows 0..N, draft rows 0..N-1][S1]
+  const Partial* req_parts = w.partials + static_cast<size_t>(b) * (2 * N + 1) * S1;
+  const size_t trow_p = static_cast<size_t>(j);
+  const size_t drow_p = static_cast<size_t>(N + 1 + j);
   RowNorm q{}, pn{};
   RowMax g{};
   if (mode == kModeGreedy && row_thread) {
-    g = merge_greedy(w.partials + trow * S1, S1);
+    g = merge_greedy(req_parts + trow_p * S1, S1);
     if (!g.ok) atomicOr(&s_bad_logit, 1);
   } else if (mode == kModeSampled && row_thread) {
-    q = merge_sampled(w.partials + trow * S1, S1);
+    q = merge_sampled(req_parts + trow_p * S1, S1);
     if (!q.ok) atomicOr(&s_bad_logit, 1);
     if (pos_thread) {
-      pn = merge_sampled(w.partials + drow * S1, S1);
+      pn = merge_sampled(req_parts + drow_p * S1, S1);
       if (!pn.ok) atomicOr(&s_bad_logit, 1);
     }
   }
@@ -169,9 +198,6 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
   // Sampled request.
   const float k = scale_of(t);
   if (pos_thread) {
-    const float zd = Elem<T>::load1(static_cast<const T*>(p.target) + trow * V + d);
-    const float yd = Elem<T>::load1(static_cast<const T*>(p.draft) +
-                                    (static_cast<size_t>(b) * N + j) * V + d);
     float thr = 1.f;
     bool accepted = true;
     if (yd != -INFINITY) {  // p(d) > 0

@@ -35,9 +35,10 @@ def near_threshold_count(res):
     return sum(1 for decs in res.decisions for dec in decs if dec.distance() < WINDOW)
 
 
-def compare(res, tokens, accept, kv, temperature, n, label=""):
+def compare(res, tokens, accept, kv, temperature, n, label="", quota=True):
     """Check GPU outputs (numpy) against an oracle Result.  Returns the list
-    of logged in-window mismatches."""
+    of logged in-window mismatches; with quota=False the caller checks the
+    mismatch count against its own total of positions."""
     tokens = np.asarray(tokens).reshape(res.tokens.shape)
     accept = np.asarray(accept).reshape(-1)
     kv = np.asarray(kv).reshape(-1)
@@ -71,10 +72,15 @@ def compare(res, tokens, accept, kv, temperature, n, label=""):
         assert dist < WINDOW, f"mismatch outside the 1e-5 window (distance {dist:.3g}): " + where
         logged.append((label, b, dec[0].kind, dec[0].j, dist))
         print("near-threshold mismatch:", where, f"distance={dist:.3g}")
-    positions = tokens.shape[0] * max(n, 1)
-    assert len(logged) < max(1.0, 1e-5 * positions) or len(logged) == 0, \
-        f"{len(logged)} mismatches over {positions} positions"
+    if quota:
+        check_quota(len(logged), tokens.shape[0] * max(n, 1))
     return logged
+
+
+def check_quota(mismatches, positions):
+    """Mismatches must stay below 1e-5 of the verified draft positions."""
+    assert mismatches == 0 or mismatches < 1e-5 * positions, \
+        f"{mismatches} mismatches over {positions} positions"
 
 
 def rel_close(gpu, ref, rtol=WINDOW):
