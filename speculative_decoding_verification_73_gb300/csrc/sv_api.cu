@@ -15,6 +15,7 @@
 struct spec_verify_ctx {
   int max_B, max_N, max_V, dtype;
   int device;
+  int ring_ctas;  // CTAs of the streaming row-statistics kernel (one per SM)
   cudaStream_t stream;
   void* ws;  // one cudaMalloc holding the whole workspace
   sv::Workspace w;
@@ -79,6 +80,7 @@ const char* spec_verify_strerror(int code) {
     case SV_EBADTOKEN: return "a draft token is outside [0, V)";
     case SV_EBADLOGIT: return "a logit row holds NaN or +inf, or has no finite entry";
     case SV_ECUDA: return "a CUDA runtime call failed";
+    case SV_ETIMEOUT: return "a bounded wait inside a kernel gave up (outputs of that call are invalid)";
     default: return "unknown error code";
   }
 }
@@ -99,23 +101,23 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   ctx->max_V = max_V;
   ctx->dtype = dtype;
   ctx->stream = static_cast<cudaStream_t>(cuda_stream);
-  if (cudaGetDevice(&ctx->device) != cudaSuccess) {
+  int sms = 0;
+  if (cudaGetDevice(&ctx->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess ||
+      sv::prepare_rowstats(max_B) != cudaSuccess) {
     delete ctx;
     return SV_ECUDA;
   }
+  ctx->ring_ctas = sms;
   const int s1 = ceil_div(max_V, sv::row_chunk_elems(dtype));
   const int s3 = ceil_div(max_V, sv::sample_chunk_elems(dtype));
   const size_t rows = static_cast<size_t>(max_B) * (2 * static_cast<size_t>(max_N) + 1);
   size_t off = 0;
   const size_t o_part = off;
   off = align_up(off + rows * s1 * sizeof(sv::Partial), 256);
-  const size_t o_jobs = off;
-  off = align_up(off + static_cast<size_t>(max_B) * sizeof(sv::Job), 256);
   const size_t o_sums = off;
   off = align_up(off + static_cast<size_t>(max_B) * s3 * sizeof(float), 256);
   const size_t o_cnt = off;
-  off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
-  const size_t o_wcnt = off;
   off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
   const size_t o_err = off;
   off = align_up(off + sizeof(unsigned), 256);
@@ -130,10 +132,8 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   }
   char* base = static_cast<char*>(ctx->ws);
   ctx->w.partials = reinterpret_cast<sv::Partial*>(base + o_part);
-  ctx->w.jobs = reinterpret_cast<sv::Job*>(base + o_jobs);
   ctx->w.chunk_sums = reinterpret_cast<float*>(base + o_sums);
   ctx->w.counters = reinterpret_cast<unsigned*>(base + o_cnt);
-  ctx->w.walk_counters = reinterpret_cast<unsigned*>(base + o_wcnt);
   ctx->w.err = reinterpret_cast<unsigned*>(base + o_err);
   ctx->w.dbg_accept = reinterpret_cast<float*>(base + o_acc);
   ctx->w.dbg_logz = reinterpret_cast<float*>(base + o_lz);
@@ -185,7 +185,8 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
     if (ev == nullptr) return SV_ECUDA;
     if (cudaEventRecord(ev[0], ctx->stream) != cudaSuccess) return SV_ECUDA;
   }
-  if (sv::launch_rowstats(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
+  if (sv::launch_rowstats(ctx->dtype, vec, ctx->ring_ctas, p, w, ctx->stream) != cudaSuccess)
+    return SV_ECUDA;
   if (ev && cudaEventRecord(ev[1], ctx->stream) != cudaSuccess) return SV_ECUDA;
   if (sv::launch_sample(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
   if (ev) {
@@ -207,6 +208,7 @@ int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits) {
   if (word & SV_ERRBIT_TEMP) return SV_EBADTEMP;
   if (word & SV_ERRBIT_TOKEN) return SV_EBADTOKEN;
   if (word & SV_ERRBIT_LOGIT) return SV_EBADLOGIT;
+  if (word & SV_ERRBIT_TIMEOUT) return SV_ETIMEOUT;
   return SV_OK;
 }
 

@@ -8,12 +8,14 @@
 namespace sv {
 
 constexpr int kThreads = 256;           // threads per CTA, every kernel
-constexpr int kRowChunkBytes = 32768;   // row-statistics: bytes of one row chunk per CTA
+constexpr int kRowChunkBytes = 32768;   // row-statistics: bytes of one row chunk
+constexpr int kRingStages = 6;          // row-statistics ring: chunks in flight per SM
+constexpr int kRingMaxB = 4096;         // ring kernel keeps per-request counts in shared memory
 constexpr int kLevel1 = 8192;           // tokens per level-1 block of the grouped inverse CDF
 constexpr int kLevel2 = 256;            // tokens per level-2 block
 constexpr int kLevel3 = 16;             // tokens per level-3 block
-// The walk runs on the row-statistics CTA of kThreads threads, one thread per
-// row of a request, so N + 1 <= kThreads.
+// The walk runs on a CTA of kThreads threads, one thread per row of a
+// request, so N + 1 <= kThreads.
 
 constexpr int kModeInvalid = 0;
 constexpr int kModeGreedy = 1;
@@ -22,6 +24,7 @@ constexpr int kModeSampled = 2;
 constexpr unsigned kErrTemp = 1u;
 constexpr unsigned kErrToken = 2u;
 constexpr unsigned kErrLogit = 4u;
+constexpr unsigned kErrTimeout = 8u;
 
 // Statistics of one chunk of one logit row (16 bytes).
 //   sampled row: a = c = fl(M * k) with M the chunk maximum and k = log2(e)/T,
@@ -39,7 +42,7 @@ constexpr int kJobNone = 0;
 constexpr int kJobResidual = 1;
 constexpr int kJobBonus = 2;
 
-// What the walk leaves for the sampler, one per request.
+// What the walk leaves for the sampler (in shared memory of each CTA).
 //   q_t = 2^(z_t*k - cq) * inv_sq
 //   log2(q_t / p_t) = (z_t - y_t)*k - (dhi + dlo)
 struct Job {
@@ -65,10 +68,8 @@ struct Problem {
 
 struct Workspace {
   Partial* partials;     // [B][2N+1][S1]: target rows 0..N, then draft rows 0..N-1
-  Job* jobs;             // [B]
   float* chunk_sums;     // [B, S3]: residual mass of each level-1 block
   unsigned* counters;    // [B], sampler chunk counts, zero between calls
-  unsigned* walk_counters;  // [B], row-statistics chunk counts, zero between calls
   unsigned* err;         // [1], OR of kErr* bits
   float* dbg_accept;     // [B, N]
   float* dbg_logz;       // [B, 2N+1]
@@ -76,8 +77,11 @@ struct Workspace {
   int S3;                // level-1 blocks per row for this call's V
 };
 
-// dtype codes match SV_F32 / SV_BF16
-cudaError_t launch_rowstats(int dtype, bool vec, const Problem& p, const Workspace& w,
+// dtype codes match SV_F32 / SV_BF16.  ring_ctas > 0 selects the streaming
+// ring kernel (aligned rows, B <= kRingMaxB) with that many CTAs.
+size_t ring_smem_bytes(int B);
+cudaError_t prepare_rowstats(int max_B);
+cudaError_t launch_rowstats(int dtype, bool vec, int ring_ctas, const Problem& p, const Workspace& w,
                             cudaStream_t s);
 cudaError_t launch_sample(int dtype, bool vec, const Problem& p, const Workspace& w,
                           cudaStream_t s);

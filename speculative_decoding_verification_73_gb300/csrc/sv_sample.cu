@@ -1,5 +1,5 @@
-// Correction / bonus sampling, touching only the one row (or row pair) per
-// request that the walk selected.
+// The accept/reject walk and the correction / bonus sampling, touching only
+// the one row (or row pair) per request that the walk selected.
 //
 // "Speculative Decoding and EAGLE-3" lesson, "Invariant: Leviathan rejection
 // sampling" and "Build it" step 2: after a rejection at position j the token
@@ -15,10 +15,12 @@
 // rounding leaves none).  The law is exactly r / sum(r), and every decision
 // compares a uniform against at most a few dozen float32 edges.
 //
-// Grid: B x S3 CTAs, one per (request, level-1 block).  Each CTA sums r over
-// its block; the last CTA of a request to finish (counted with an atomic, no
-// waiting) picks the level-1 block, rescans only that block for levels 2-4,
-// writes the token and resets the request's counter for the next call.
+// Grid: B x S3 CTAs, one per (request, level-1 block).  Each CTA first runs
+// the request's accept/reject walk itself from the row-statistics partials
+// (cheap; no CTA waits for another), then sums r over its block; the last CTA
+// of a request to finish (counted with an atomic, no waiting) picks the
+// level-1 block, rescans only that block for levels 2-4, writes the token and
+// resets the request's counter for the next call.
 //
 // r_t is evaluated as q_t * (1 - 2^-d_t) with d_t = log2(q_t / p_t) taken from
 // the logit difference, so that it keeps its relative precision when q_t and
@@ -28,6 +30,7 @@
 #include <cuda_bf16.h>
 
 #include "sv_device.cuh"
+#include "sv_walk.cuh"
 
 namespace sv {
 namespace {
@@ -143,10 +146,16 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(Problem p, Workspace w
   __shared__ float s_l3[kLevel1 / kLevel3];         // 512 level-3 masses
   __shared__ float s_l4[kLevel3];                   // 16 token masses
   __shared__ int s_last, s_sel, s_g2, s_g3, s_tok;
+  __shared__ Job s_job;
   const int S3 = w.S3;
   const int b = blockIdx.x / S3;
   const int c = blockIdx.x - b * S3;
-  const Job job = w.jobs[b];
+  // Only sampled requests need the other blocks; the first block of every
+  // request writes its outputs.
+  if (c != 0 && temp_mode(p.temperature[b]) != kModeSampled) return;  // CTA-uniform
+  walk_request<T>(p, w, b, c == 0, &s_job);
+  __syncthreads();
+  const Job job = s_job;
   if (job.kind == kJobNone) return;  // CTA-uniform
   const int N = p.N, V = p.V;
   const T* z = static_cast<const T*>(p.target) + (static_cast<size_t>(b) * (N + 1) + job.row) * V;

@@ -1,5 +1,7 @@
-// The accept/reject walk of one request, run by the CTA that finishes the
-// request's last row chunk (see sv_rowstats.cu); thread j handles row j.
+// The accept/reject walk of one request, run by each sampler CTA of the
+// request (see sv_sample.cu); thread j handles row j.  Every CTA of a request
+// computes the same result from the row-statistics partials; only the one
+// asked to (write_outputs) stores the outputs.
 //
 // Thread j merges the row-statistics partials of target row j (and, for a
 // sampled request, draft row j), checks the inputs, and evaluates position
@@ -109,7 +111,8 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
 }
 
 template <typename T>
-__device__ __forceinline__ void walk_request(const Problem& p, const Workspace& w, int b) {
+__device__ __forceinline__ void walk_request(const Problem& p, const Workspace& w, int b,
+                                             bool write_outputs, Job* job_out) {
   const int j = threadIdx.x;
   const int N = p.N, V = p.V, S1 = w.S1;
   const bool row_thread = j <= N;
@@ -178,20 +181,22 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
       __syncthreads();
       a = s_first;
     }
-    if (row_thread) {
-      out_tok[j] = (!err && j <= a) ? g.idx : -1;
-      dbg_lz[j] = qnan;
-      if (pos_thread) {
-        dbg_acc[j] = qnan;
-        dbg_lz[N + 1 + j] = qnan;
+    if (write_outputs) {
+      if (row_thread) {
+        out_tok[j] = (!err && j <= a) ? g.idx : -1;
+        dbg_lz[j] = qnan;
+        if (pos_thread) {
+          dbg_acc[j] = qnan;
+          dbg_lz[N + 1 + j] = qnan;
+        }
+      }
+      if (j == 0) {
+        p.out_accept[b] = err ? -1 : a;
+        p.out_kv[b] = err ? 0 : a + 1;
+        if (err) atomicOr(w.err, err);
       }
     }
-    if (j == 0) {
-      p.out_accept[b] = err ? -1 : a;
-      p.out_kv[b] = err ? 0 : a + 1;
-      w.jobs[b].kind = kJobNone;
-      if (err) atomicOr(w.err, err);
-    }
+    if (j == 0) job_out->kind = kJobNone;
     return;
   }
 
@@ -205,14 +210,16 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
       thr = fminf(1.f, exp2f(lr));
       accepted = philox_uniform(p.seed, b, j + 1, 0) < thr;
     }
-    dbg_acc[j] = thr;
-    dbg_lz[N + 1 + j] = (pn.c + log2f(pn.s)) * kLn2;
+    if (write_outputs) {
+      dbg_acc[j] = thr;
+      dbg_lz[N + 1 + j] = (pn.c + log2f(pn.s)) * kLn2;
+    }
     if (!accepted) atomicMin(&s_first, j);
   }
-  if (row_thread) dbg_lz[j] = (q.c + log2f(q.s)) * kLn2;
+  if (write_outputs && row_thread) dbg_lz[j] = (q.c + log2f(q.s)) * kLn2;
   __syncthreads();
   const int a = s_first;
-  if (row_thread) out_tok[j] = j < a ? d : -1;
+  if (write_outputs && row_thread) out_tok[j] = j < a ? d : -1;
   if (j == a) {
     Job job;
     job.kind = a < N ? kJobResidual : kJobBonus;
@@ -232,9 +239,11 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
     }
     job.dhi = hi;
     job.dlo = lo;
-    w.jobs[b] = job;
-    p.out_accept[b] = a;
-    p.out_kv[b] = a + 1;
+    *job_out = job;
+    if (write_outputs) {
+      p.out_accept[b] = a;
+      p.out_kv[b] = a + 1;
+    }
   }
 }
 
