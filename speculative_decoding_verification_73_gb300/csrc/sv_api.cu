@@ -109,7 +109,7 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
     return SV_ECUDA;
   }
   ctx->ring_ctas = sms;
-  const int s1 = ceil_div(max_V, sv::row_chunk_elems(dtype));
+  const int s1 = ceil_div(max_V, sv::row_chunk_elems(dtype, true));  // the finer chunking
   const int s3 = ceil_div(max_V, sv::sample_chunk_elems(dtype));
   const size_t rows = static_cast<size_t>(max_B) * (2 * static_cast<size_t>(max_N) + 1);
   size_t off = 0;
@@ -175,8 +175,9 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
   p.out_tokens = out_tokens;
   p.out_accept = out_accept_len;
   p.out_kv = out_kv_len;
+  const bool ring = vec && B <= sv::kRingMaxB && ctx->ring_ctas > 0;
   sv::Workspace w = ctx->w;
-  w.S1 = ceil_div(V, sv::row_chunk_elems(ctx->dtype));
+  w.S1 = ceil_div(V, sv::row_chunk_elems(ctx->dtype, ring));
   w.S3 = ceil_div(V, sv::sample_chunk_elems(ctx->dtype));
 
   cudaEvent_t* ev = nullptr;
@@ -185,7 +186,8 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
     if (ev == nullptr) return SV_ECUDA;
     if (cudaEventRecord(ev[0], ctx->stream) != cudaSuccess) return SV_ECUDA;
   }
-  if (sv::launch_rowstats(ctx->dtype, vec, ctx->ring_ctas, p, w, ctx->stream) != cudaSuccess)
+  if (sv::launch_rowstats(ctx->dtype, vec, ring ? ctx->ring_ctas : 0, p, w, ctx->stream) !=
+      cudaSuccess)
     return SV_ECUDA;
   if (ev && cudaEventRecord(ev[1], ctx->stream) != cudaSuccess) return SV_ECUDA;
   if (sv::launch_sample(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;

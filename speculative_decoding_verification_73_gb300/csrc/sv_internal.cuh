@@ -8,8 +8,10 @@
 namespace sv {
 
 constexpr int kThreads = 256;           // threads per CTA, every kernel
-constexpr int kRowChunkBytes = 32768;   // row-statistics: bytes of one row chunk
-constexpr int kRingStages = 6;          // row-statistics ring: chunks in flight per SM
+constexpr int kRowChunkBytes = 32768;   // row statistics, direct kernel: bytes of one row chunk
+constexpr int kRingChunkBytes = 8192;   // row statistics, ring kernel: bytes of one row chunk
+constexpr int kRingStages = 24;         // ring kernel: shared-memory stages per SM (192 KB)
+constexpr int kRingWarps = 16;          // ring kernel: consumer warps per CTA
 constexpr int kRingMaxB = 4096;         // ring kernel keeps per-request counts in shared memory
 constexpr int kLevel1 = 8192;           // tokens per level-1 block of the grouped inverse CDF
 constexpr int kLevel2 = 256;            // tokens per level-2 block
@@ -88,7 +90,9 @@ cudaError_t launch_sample(int dtype, bool vec, const Problem& p, const Workspace
 cudaError_t launch_philox_probe(unsigned long long seed, const uint32_t* ctr3, uint32_t* out4,
                                 int n, cudaStream_t s);
 
-inline int row_chunk_elems(int dtype) { return kRowChunkBytes / (dtype == 1 ? 2 : 4); }
+inline int row_chunk_elems(int dtype, bool ring) {
+  return (ring ? kRingChunkBytes : kRowChunkBytes) / (dtype == 1 ? 2 : 4);
+}
 inline int sample_chunk_elems(int) { return kLevel1; }
 
 }  // namespace sv

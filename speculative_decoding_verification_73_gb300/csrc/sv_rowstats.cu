@@ -12,20 +12,22 @@
 //
 // Rows are numbered request-major: request b owns rows b(2N+1) .. b(2N+1)+2N,
 // its N+1 target rows first, then its N draft rows.  A row is cut into
-// 32 KB chunks; partials[row][chunk] receives each chunk's statistics.
+// chunks; partials[row][chunk] receives each chunk's statistics.
 //
-// Two kernels compute the same partials:
-//  * ring: one persistent CTA per SM streams its share of the chunks
-//    through a ring of kRingStages shared-memory stages filled by bulk
-//    copies (cp.async.bulk) that complete on mbarriers, so several chunks
-//    per SM are always in flight while the CTA reduces the current one.  The
-//    active chunks (the draft rows of greedy requests are skipped) are dealt
-//    out round robin: chunk k of the request-major list goes to CTA k mod G.
-//  * direct: one CTA per chunk reading global memory with 16-byte loads (or
-//    scalar loads when rows are not 16-byte aligned); used when the ring's
-//    requirements (aligned rows, B <= kRingMaxB) do not hold.
-// In both, the chunk maximum is reduced over the CTA first and every
-// exponent then uses that one reference.
+// Two kernels compute the partials:
+//  * ring (8 KB chunks): one persistent CTA per SM.  A producer warp streams
+//    the CTA's share of the chunks through kRingStages shared-memory stages
+//    with bulk copies (cp.async.bulk) that complete on "full" mbarriers;
+//    kRingWarps consumer warps each reduce whole chunks on their own (warp
+//    shuffles only, no CTA barrier) and release the stage on an "empty"
+//    mbarrier.  The active chunks (draft rows of greedy requests are
+//    skipped) are dealt round robin: chunk k of the request-major list goes
+//    to CTA k mod G, and a CTA's m-th chunk to consumer warp m mod kRingWarps.
+//  * direct (32 KB chunks): one CTA per chunk reading global memory with
+//    16-byte loads (or scalar loads when rows are not 16-byte aligned); used
+//    when the ring's requirements (aligned rows, B <= kRingMaxB) do not hold.
+// In both, a chunk's maximum is found first and every exponent uses that one
+// reference.
 
 #include <climits>
 #include <cuda_bf16.h>
@@ -37,6 +39,7 @@ namespace {
 
 constexpr int kPer = kRowChunkBytes / 16 / kThreads;  // 16-byte vectors per thread per chunk
 constexpr unsigned kWaitTries = 1u << 22;              // mbarrier polls before giving up
+
 
 struct RowRef {
   bool draft;
@@ -206,6 +209,9 @@ __global__ void __launch_bounds__(kThreads) rowstats_direct_kernel(Problem p, Wo
 
 // ------------------------------------------------------------------ ring
 
+constexpr int kRingThreads = (kRingWarps + 1) * 32;  // consumer warps + one producer warp
+constexpr int kWarpVecs = kRingChunkBytes / 16 / 32;  // 16-byte vectors per lane per chunk
+
 // Chunks a request contributes: none for an invalid temperature (the walk
 // reports it), the target rows for a greedy request, all rows otherwise.
 __device__ __forceinline__ unsigned request_chunks(int mode, int N, int S1) {
@@ -232,22 +238,104 @@ __device__ __forceinline__ Item decode_item(unsigned k, const unsigned* prefix,
   return it;
 }
 
+__device__ __forceinline__ float warp_max_nan(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmax_nan(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+__device__ __forceinline__ int warp_min_int(int v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = min(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+// One warp reduces one chunk held in shared memory (nv 16-byte vectors, the
+// chunk starting at element beg of its row): two passes over the stage,
+// the chunk maximum first, then the exponent sum or the argmax.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 1) rowstats_ring_kernel(Problem p, Workspace w) {
+__device__ __forceinline__ Partial warp_chunk_partial(const uint4* stage, int nv, int beg, bool greedy,
+                                                      float k) {
   using E = Elem<T>;
-  constexpr int kChunk = kRowChunkBytes / static_cast<int>(sizeof(T));
+  constexpr int kVec = E::kVec;
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+#pragma unroll 8
+  for (int i = 0; i < kWarpVecs; ++i) {
+    const int v = lane + i * 32;
+    if (v < nv) m = fmax_nan(m, E::vmax_nan(stage[v]));
+  }
+  const float cmax = warp_max_nan(m);
+  Partial out;
+  out.pad = 0;
+  if (greedy) {
+    int idx = INT_MAX;
+    if (m == cmax) {  // lowest index of this lane holding the chunk maximum
+      for (int i = 0; i < kWarpVecs && idx == INT_MAX; ++i) {
+        const int v = lane + i * 32;
+        if (v >= nv) break;
+        const uint4 x = stage[v];
+#pragma unroll
+        for (int e = 0; e < kVec; ++e)
+          if (idx == INT_MAX && E::get(x, e) == cmax) idx = beg + v * kVec + e;
+      }
+    }
+    out.idx = warp_min_int(idx);
+    out.a = cmax;
+    out.s = (cmax != cmax) ? __int_as_float(0x7fc00000) : 0.f;
+  } else {
+    float c;
+    float s = 0.f;
+    const bool ok = sampled_reference(cmax, k, &c);
+    if (ok) {
+#pragma unroll 4
+      for (int i = 0; i < kWarpVecs; ++i) {
+        const int v = lane + i * 32;
+        if (v < nv) {
+          const uint4 x = stage[v];
+#pragma unroll
+          for (int e = 0; e < kVec; ++e) s += ex2(fmaf(E::get(x, e), k, -c));
+        }
+      }
+    }
+    s = warp_sum(s);
+    if (!ok) {
+      if (cmax == -INFINITY) {
+        c = -INFINITY;
+        s = 0.f;
+      } else {
+        s = __int_as_float(0x7fc00000);
+      }
+    }
+    out.a = c;
+    out.s = s;
+    out.idx = 0;
+  }
+  return out;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kRingThreads, 1) rowstats_ring_kernel(Problem p, Workspace w) {
+  using E = Elem<T>;
+  constexpr int kChunk = kRingChunkBytes / static_cast<int>(sizeof(T));
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingStages * kRowChunkBytes);
-  unsigned* prefix = reinterpret_cast<unsigned*>(bars + kRingStages);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRingStages * kRingChunkBytes);
+  uint64_t* empty = full + kRingStages;
+  unsigned* prefix = reinterpret_cast<unsigned*>(empty + kRingStages);
   unsigned char* modes = reinterpret_cast<unsigned char*>(prefix + p.B + 1);
-  __shared__ unsigned scan_scratch[kThreads / 32];
-  __shared__ int s_abort;
+  __shared__ unsigned scan_scratch[32];
 
   const int B = p.B, N = p.N, S1 = w.S1;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Per-request active chunk counts and their exclusive prefix.
-  const int per_thread = (B + kThreads - 1) / kThreads;
+  // Per-request active chunk counts and their exclusive prefix (whole CTA).
+  const int nthreads = blockDim.x;
+  const int per_thread = (B + nthreads - 1) / nthreads;
   const int b0 = threadIdx.x * per_thread;
   unsigned local = 0;
   for (int i = 0; i < per_thread; ++i) {
@@ -258,8 +346,20 @@ __global__ void __launch_bounds__(kThreads, 1) rowstats_ring_kernel(Problem p, W
       local += request_chunks(mode, N, S1);
     }
   }
-  unsigned total;
-  unsigned run = block_exclusive_scan_u32(local, scan_scratch, &total);
+  unsigned incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned t = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) scan_scratch[warp] = incl;
+  __syncthreads();
+  unsigned run = incl - local, total = 0;
+  for (int q = 0; q < (nthreads >> 5); ++q) {
+    const unsigned t = scan_scratch[q];
+    if (q < warp) run += t;
+    total += t;
+  }
   for (int i = 0; i < per_thread; ++i) {
     const int b = b0 + i;
     if (b < B) {
@@ -269,8 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1) rowstats_ring_kernel(Problem p, W
   }
   if (threadIdx.x == 0) {
     prefix[B] = total;
-    s_abort = 0;
-    for (int s = 0; s < kRingStages; ++s) mbar_init(smem_u32(bars + s), 1);
+    for (int s = 0; s < kRingStages; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(empty + s), 1);
+    }
     fence_mbar_init();
   }
   __syncthreads();
@@ -278,76 +380,61 @@ __global__ void __launch_bounds__(kThreads, 1) rowstats_ring_kernel(Problem p, W
   const unsigned G = gridDim.x, g = blockIdx.x;
   const unsigned my_items = total > g ? (total - g + G - 1) / G : 0u;
 
-  // Producer (thread 0): start the copy of this CTA's m-th chunk into stage
-  // m % kRingStages.
-  int pcursor = 0;
-  auto issue = [&](unsigned m) {
-    if (m >= my_items) return;
-    const Item it = decode_item(g + m * G, prefix, modes, pcursor, S1);
-    const RowRef r = row_of(p, it.b, it.slot);
-    const T* src = static_cast<const T*>(r.draft ? p.draft : p.target) + r.offset +
-                   static_cast<size_t>(it.chunk) * kChunk;
-    const int n = min(p.V - it.chunk * kChunk, kChunk);
-    const uint32_t bytes = static_cast<uint32_t>(n) * sizeof(T);
-    const int s = static_cast<int>(m % kRingStages);
-    const uint32_t bar = smem_u32(bars + s);
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_copy_g2s(smem_u32(ring + s * kRowChunkBytes), src, bytes, bar);
-  };
-  if (threadIdx.x == 0) {
-    for (unsigned m = 0; m + 1 < kRingStages; ++m) issue(m);
+  if (warp == kRingWarps) {
+    // Producer: one lane issues the bulk copy of item m into stage
+    // m % kRingStages once the consumer of item m - kRingStages released it.
+    if (lane == 0) {
+      int cursor = 0;
+      for (unsigned m = 0; m < my_items; ++m) {
+        const int s = static_cast<int>(m % kRingStages);
+        const unsigned use = m / kRingStages;
+        if (use > 0 && !mbar_wait_bounded(smem_u32(empty + s), (use - 1) & 1u, kWaitTries)) {
+          atomicOr(w.err, kErrTimeout);
+          break;
+        }
+        fence_proxy_async_smem();
+        const Item it = decode_item(g + m * G, prefix, modes, cursor, S1);
+        const RowRef r = row_of(p, it.b, it.slot);
+        const T* src = static_cast<const T*>(r.draft ? p.draft : p.target) + r.offset +
+                       static_cast<size_t>(it.chunk) * kChunk;
+        const int n = min(p.V - it.chunk * kChunk, kChunk);
+        const uint32_t bytes = static_cast<uint32_t>(n) * sizeof(T);
+        const uint32_t bar = smem_u32(full + s);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_copy_g2s(smem_u32(ring + s * kRingChunkBytes), src, bytes, bar);
+      }
+    }
+    return;
   }
 
-  int ccursor = 0;
-  unsigned m = 0;
-  for (; m < my_items; ++m) {
-    if (threadIdx.x == 0) {
-      // Refill the stage consumed in iteration m - 1.  Every thread has
-      // passed that iteration's last barrier, so its reads of the stage are
-      // done; the proxy fence orders them before the bulk copy's writes.
-      fence_proxy_async_smem();
-      issue(m + kRingStages - 1);
-    }
-    const Item it = decode_item(g + m * G, prefix, modes, ccursor, S1);
+  // Consumers: warp q reduces items q, q + kRingWarps, ... of this CTA.
+  int cursor = 0;
+  for (unsigned m = warp; m < my_items; m += kRingWarps) {
+    const Item it = decode_item(g + m * G, prefix, modes, cursor, S1);
     const int s = static_cast<int>(m % kRingStages);
-    const uint32_t parity = (m / kRingStages) & 1u;
-    if (!mbar_wait_bounded(smem_u32(bars + s), parity, kWaitTries)) {
+    const bool ready = mbar_wait_bounded(smem_u32(full + s), (m / kRingStages) & 1u, kWaitTries);
+    if (ready) {
+      const int beg = it.chunk * kChunk;
+      const int nv = (min(p.V, beg + kChunk) - beg) / E::kVec;
+      const float k = it.greedy ? 0.f : scale_of(p.temperature[it.b]);
+      const Partial out = warp_chunk_partial<T>(
+          reinterpret_cast<const uint4*>(ring + s * kRingChunkBytes), nv, beg, it.greedy, k);
+      if (lane == 0) {
+        const size_t row = static_cast<size_t>(it.b) * (2 * N + 1) + it.slot;
+        w.partials[row * S1 + it.chunk] = out;
+      }
+    } else if (lane == 0) {
       atomicOr(w.err, kErrTimeout);
-      s_abort = 1;
     }
-    __syncthreads();
-    if (s_abort) break;
-    const int beg = it.chunk * kChunk;
-    const int nv = (min(p.V, beg + kChunk) - beg) / E::kVec;
-    const uint4* stage = reinterpret_cast<const uint4*>(ring + s * kRowChunkBytes);
-    uint4 raw[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int v = threadIdx.x + i * kThreads;
-      raw[i] = v < nv ? stage[v]
-                      : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
-    }
-    const float k = it.greedy ? 0.f : scale_of(p.temperature[it.b]);
-    const Partial out = chunk_partial<T>(raw, beg, it.greedy, k);
-    if (threadIdx.x == 0) {
-      const size_t row = static_cast<size_t>(it.b) * (2 * N + 1) + it.slot;
-      w.partials[row * S1 + it.chunk] = out;
-    }
-  }
-  if (s_abort && threadIdx.x == 0) {
-    // Do not leave while copies into this CTA's shared memory may still be
-    // in flight: wait (bounded) on every copy issued after the one that
-    // timed out.
-    const unsigned issued = min(my_items, m + kRingStages);  // items m .. m+kRingStages-1 may be in flight
-    for (unsigned q = m; q < issued; ++q)
-      mbar_wait_bounded(smem_u32(bars + q % kRingStages), (q / kRingStages) & 1u, kWaitTries);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(empty + s));
   }
 }
 
 }  // namespace
 
 size_t ring_smem_bytes(int B) {
-  return static_cast<size_t>(kRingStages) * kRowChunkBytes + kRingStages * sizeof(uint64_t) +
+  return static_cast<size_t>(kRingStages) * kRingChunkBytes + 2 * kRingStages * sizeof(uint64_t) +
          (static_cast<size_t>(B) + 1) * sizeof(unsigned) + static_cast<size_t>(B);
 }
 
@@ -368,9 +455,9 @@ cudaError_t launch_rowstats(int dtype, bool vec, int ring_ctas, const Problem& p
   if (vec && ring_ctas > 0 && p.B <= kRingMaxB) {
     const size_t smem = ring_smem_bytes(p.B);
     if (dtype == 1)
-      rowstats_ring_kernel<__nv_bfloat16><<<ring_ctas, kThreads, smem, s>>>(p, w);
+      rowstats_ring_kernel<__nv_bfloat16><<<ring_ctas, kRingThreads, smem, s>>>(p, w);
     else
-      rowstats_ring_kernel<float><<<ring_ctas, kThreads, smem, s>>>(p, w);
+      rowstats_ring_kernel<float><<<ring_ctas, kRingThreads, smem, s>>>(p, w);
     return cudaGetLastError();
   }
   const dim3 grid(static_cast<unsigned>(blocks));
