@@ -55,8 +55,6 @@ extern "C" {
 #define SV_EBADLOGIT   4  /* device check: a row that is read holds NaN or +inf,
                              or all of its entries are -inf                    */
 #define SV_ECUDA       5  /* a CUDA runtime call failed                        */
-#define SV_ETIMEOUT    6  /* device: a bounded wait for an asynchronous copy gave
-                             up; the outputs of that call are not valid        */
 
 /* Bits of the device error word (spec_verify_get_error).  A request that
  * fails a device check gets out_tokens = -1 everywhere, out_accept_len = -1
@@ -65,7 +63,6 @@ extern "C" {
 #define SV_ERRBIT_TEMP   1u
 #define SV_ERRBIT_TOKEN  2u
 #define SV_ERRBIT_LOGIT  4u
-#define SV_ERRBIT_TIMEOUT 8u
 
 /* ---- logit element types ---------------------------------------------- */
 #define SV_F32   0
@@ -127,8 +124,7 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V,
 /*
  * spec_verify_get_error -- wait for the context's stream, then return the
  * first device-detected error since the last read (SV_EBADTEMP,
- * SV_EBADTOKEN, SV_EBADLOGIT, SV_ETIMEOUT in that priority) or SV_OK, and
- * clear it.
+ * SV_EBADTOKEN, SV_EBADLOGIT in that priority) or SV_OK, and clear it.
  * bits (may be NULL) receives the OR of SV_ERRBIT_* flags.
  */
 int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits);

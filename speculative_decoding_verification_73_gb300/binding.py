@@ -14,8 +14,8 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 
-SV_OK, SV_EINVAL, SV_EBADTEMP, SV_EBADTOKEN, SV_EBADLOGIT, SV_ECUDA, SV_ETIMEOUT = range(7)
-SV_ERRBIT_TEMP, SV_ERRBIT_TOKEN, SV_ERRBIT_LOGIT, SV_ERRBIT_TIMEOUT = 1, 2, 4, 8
+SV_OK, SV_EINVAL, SV_EBADTEMP, SV_EBADTOKEN, SV_EBADLOGIT, SV_ECUDA = range(6)
+SV_ERRBIT_TEMP, SV_ERRBIT_TOKEN, SV_ERRBIT_LOGIT = 1, 2, 4
 SV_F32, SV_BF16 = 0, 1
 SV_NUM_KERNELS = 2
 SV_MAX_N = 255
@@ -140,7 +140,7 @@ def spec_verify_get_error(ctx):
     """(code, bits) of the device-detected input errors since the last read."""
     bits = ctypes.c_uint32(0)
     code = load().spec_verify_get_error(ctx, ctypes.byref(bits))
-    if code in (SV_ECUDA, SV_EINVAL, SV_ETIMEOUT):
+    if code in (SV_ECUDA, SV_EINVAL):
         raise SpecVerifyError(code, "spec_verify_get_error")
     return code, int(bits.value)
 

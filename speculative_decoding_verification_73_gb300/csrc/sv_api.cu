@@ -15,7 +15,6 @@
 struct spec_verify_ctx {
   int max_B, max_N, max_V, dtype;
   int device;
-  int ring_ctas;  // CTAs of the streaming row-statistics kernel (one per SM)
   cudaStream_t stream;
   void* ws;  // one cudaMalloc holding the whole workspace
   sv::Workspace w;
@@ -80,7 +79,6 @@ const char* spec_verify_strerror(int code) {
     case SV_EBADTOKEN: return "a draft token is outside [0, V)";
     case SV_EBADLOGIT: return "a logit row holds NaN or +inf, or has no finite entry";
     case SV_ECUDA: return "a CUDA runtime call failed";
-    case SV_ETIMEOUT: return "a bounded wait inside a kernel gave up (outputs of that call are invalid)";
     default: return "unknown error code";
   }
 }
@@ -101,15 +99,11 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   ctx->max_V = max_V;
   ctx->dtype = dtype;
   ctx->stream = static_cast<cudaStream_t>(cuda_stream);
-  int sms = 0;
-  if (cudaGetDevice(&ctx->device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess ||
-      sv::prepare_rowstats(max_B) != cudaSuccess) {
+  if (cudaGetDevice(&ctx->device) != cudaSuccess) {
     delete ctx;
     return SV_ECUDA;
   }
-  ctx->ring_ctas = sms;
-  const int s1 = ceil_div(max_V, sv::row_chunk_elems(dtype, true));  // the finer chunking
+  const int s1 = ceil_div(max_V, sv::row_chunk_elems(dtype));
   const int s3 = ceil_div(max_V, sv::sample_chunk_elems(dtype));
   const size_t rows = static_cast<size_t>(max_B) * (2 * static_cast<size_t>(max_N) + 1);
   size_t off = 0;
@@ -175,9 +169,8 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
   p.out_tokens = out_tokens;
   p.out_accept = out_accept_len;
   p.out_kv = out_kv_len;
-  const bool ring = vec && B <= sv::kRingMaxB && ctx->ring_ctas > 0;
   sv::Workspace w = ctx->w;
-  w.S1 = ceil_div(V, sv::row_chunk_elems(ctx->dtype, ring));
+  w.S1 = ceil_div(V, sv::row_chunk_elems(ctx->dtype));
   w.S3 = ceil_div(V, sv::sample_chunk_elems(ctx->dtype));
 
   cudaEvent_t* ev = nullptr;
@@ -186,8 +179,7 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
     if (ev == nullptr) return SV_ECUDA;
     if (cudaEventRecord(ev[0], ctx->stream) != cudaSuccess) return SV_ECUDA;
   }
-  if (sv::launch_rowstats(ctx->dtype, vec, ring ? ctx->ring_ctas : 0, p, w, ctx->stream) !=
-      cudaSuccess)
+  if (sv::launch_rowstats(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess)
     return SV_ECUDA;
   if (ev && cudaEventRecord(ev[1], ctx->stream) != cudaSuccess) return SV_ECUDA;
   if (sv::launch_sample(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
@@ -210,7 +202,6 @@ int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits) {
   if (word & SV_ERRBIT_TEMP) return SV_EBADTEMP;
   if (word & SV_ERRBIT_TOKEN) return SV_EBADTOKEN;
   if (word & SV_ERRBIT_LOGIT) return SV_EBADLOGIT;
-  if (word & SV_ERRBIT_TIMEOUT) return SV_ETIMEOUT;
   return SV_OK;
 }
 

@@ -193,70 +193,6 @@ __device__ __forceinline__ unsigned block_exclusive_scan_u32(unsigned v, unsigne
   return before + incl - v;
 }
 
-// ---------------------------------------------------------------- async copies
-// Bulk global->shared copies completed on an mbarrier (PTX cp.async.bulk,
-// mbarrier.*), used by the streaming row-statistics kernel.
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-// Make initialised barriers visible to the async proxy.
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-// Order this thread's earlier generic-proxy shared-memory accesses before
-// later async-proxy (bulk copy) accesses.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// One arrival that also expects `bytes` of transaction (0 completes the
-// phase at once).
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Wait for the phase of the given parity to complete, at most max_tries
-// polls; returns false if it did not.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t max_tries) {
-  for (uint32_t i = 0; i < max_tries; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-
-// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
-// global to this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                              uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- Philox
 // Philox4x32-10 as defined by Salmon, Moraes, Dror and Shaw, "Parallel
 // Random Numbers: As Easy as 1, 2, 3" (SC'11): per round the products

@@ -8,11 +8,8 @@
 namespace sv {
 
 constexpr int kThreads = 256;           // threads per CTA, every kernel
-constexpr int kRowChunkBytes = 32768;   // row statistics, direct kernel: bytes of one row chunk
-constexpr int kRingChunkBytes = 8192;   // row statistics, ring kernel: bytes of one row chunk
-constexpr int kRingStages = 24;         // ring kernel: shared-memory stages per SM (192 KB)
-constexpr int kRingWarps = 16;          // ring kernel: consumer warps per CTA
-constexpr int kRingMaxB = 4096;         // ring kernel keeps per-request counts in shared memory
+constexpr int kSpanBytes = 65536;       // row statistics: bytes of a row one CTA reduces
+constexpr int kGroup = 4;               // row statistics: 16-byte loads per thread in flight
 constexpr int kLevel1 = 8192;           // tokens per level-1 block of the grouped inverse CDF
 constexpr int kLevel2 = 256;            // tokens per level-2 block
 constexpr int kLevel3 = 16;             // tokens per level-3 block
@@ -26,7 +23,6 @@ constexpr int kModeSampled = 2;
 constexpr unsigned kErrTemp = 1u;
 constexpr unsigned kErrToken = 2u;
 constexpr unsigned kErrLogit = 4u;
-constexpr unsigned kErrTimeout = 8u;
 
 // Statistics of one chunk of one logit row (16 bytes).
 //   sampled row: a = c = fl(M * k) with M the chunk maximum and k = log2(e)/T,
@@ -75,24 +71,19 @@ struct Workspace {
   unsigned* err;         // [1], OR of kErr* bits
   float* dbg_accept;     // [B, N]
   float* dbg_logz;       // [B, 2N+1]
-  int S1;                // row-statistics chunks per row for this call's V
+  int S1;                // row-statistics spans per row for this call's V
   int S3;                // level-1 blocks per row for this call's V
 };
 
-// dtype codes match SV_F32 / SV_BF16.  ring_ctas > 0 selects the streaming
-// ring kernel (aligned rows, B <= kRingMaxB) with that many CTAs.
-size_t ring_smem_bytes(int B);
-cudaError_t prepare_rowstats(int max_B);
-cudaError_t launch_rowstats(int dtype, bool vec, int ring_ctas, const Problem& p, const Workspace& w,
+// dtype codes match SV_F32 / SV_BF16; vec selects 16-byte loads (aligned rows).
+cudaError_t launch_rowstats(int dtype, bool vec, const Problem& p, const Workspace& w,
                             cudaStream_t s);
 cudaError_t launch_sample(int dtype, bool vec, const Problem& p, const Workspace& w,
                           cudaStream_t s);
 cudaError_t launch_philox_probe(unsigned long long seed, const uint32_t* ctr3, uint32_t* out4,
                                 int n, cudaStream_t s);
 
-inline int row_chunk_elems(int dtype, bool ring) {
-  return (ring ? kRingChunkBytes : kRowChunkBytes) / (dtype == 1 ? 2 : 4);
-}
+inline int row_chunk_elems(int dtype) { return kSpanBytes / (dtype == 1 ? 2 : 4); }
 inline int sample_chunk_elems(int) { return kLevel1; }
 
 }  // namespace sv
