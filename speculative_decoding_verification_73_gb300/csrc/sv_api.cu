@@ -111,11 +111,9 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   off = align_up(off + rows * s1 * sizeof(sv::Partial), 256);
   const size_t o_sums = off;
   off = align_up(off + static_cast<size_t>(max_B) * s3 * sizeof(float), 256);
-  const size_t o_cnt = off;
-  off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
   const size_t o_err = off;
   off = align_up(off + sizeof(unsigned), 256);
-  const size_t zero_bytes = off - o_cnt;  // counters and error word start at zero
+  const size_t zero_bytes = off - o_err;  // the error word starts at zero
   const size_t o_acc = off;
   off = align_up(off + static_cast<size_t>(max_B) * (max_N > 0 ? max_N : 1) * sizeof(float), 256);
   const size_t o_lz = off;
@@ -127,11 +125,10 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   char* base = static_cast<char*>(ctx->ws);
   ctx->w.partials = reinterpret_cast<sv::Partial*>(base + o_part);
   ctx->w.chunk_sums = reinterpret_cast<float*>(base + o_sums);
-  ctx->w.counters = reinterpret_cast<unsigned*>(base + o_cnt);
   ctx->w.err = reinterpret_cast<unsigned*>(base + o_err);
   ctx->w.dbg_accept = reinterpret_cast<float*>(base + o_acc);
   ctx->w.dbg_logz = reinterpret_cast<float*>(base + o_lz);
-  if (cudaMemsetAsync(base + o_cnt, 0, zero_bytes, ctx->stream) != cudaSuccess ||
+  if (cudaMemsetAsync(base + o_err, 0, zero_bytes, ctx->stream) != cudaSuccess ||
       cudaStreamSynchronize(ctx->stream) != cudaSuccess) {
     cudaFree(ctx->ws);
     delete ctx;

@@ -46,6 +46,32 @@ __device__ __forceinline__ int temp_mode(float t) {
 // k = log2(e) / T, correctly rounded; every kernel derives it the same way.
 __device__ __forceinline__ float scale_of(float t) { return __fdiv_rn(1.44269504088896341f, t); }
 
+// Packed pairs of floats in one 64-bit register and the paired float
+// instructions of this architecture (PTX fma/mul/add .f32x2).
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // ---------------------------------------------------------------- loads
 
 // 16-byte read-only load that does not allocate in L1 (each byte of a row
@@ -77,6 +103,12 @@ struct Elem<float> {
                     fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
   }
   static __device__ __forceinline__ float load1(const float* p) { return __ldg(p); }
+  static constexpr int kPairs = 2;  // float pairs per 16 bytes
+  // pair i of the 16 bytes: elements 2i, 2i+1
+  static __device__ __forceinline__ uint64_t pair(const uint4& v, int i) {
+    return i == 0 ? f2pack(__uint_as_float(v.x), __uint_as_float(v.y))
+                  : f2pack(__uint_as_float(v.z), __uint_as_float(v.w));
+  }
 };
 
 template <>
@@ -95,6 +127,11 @@ struct Elem<__nv_bfloat16> {
   static __device__ __forceinline__ float load1(const __nv_bfloat16* p) {
     const unsigned short bits = __ldg(reinterpret_cast<const unsigned short*>(p));
     return __uint_as_float(static_cast<uint32_t>(bits) << 16);
+  }
+  static constexpr int kPairs = 4;
+  static __device__ __forceinline__ uint64_t pair(const uint4& v, int i) {
+    const uint32_t w = word(v, i);
+    return f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
   }
 };
 

@@ -13,6 +13,7 @@ constexpr int kGroup = 4;               // row statistics: 16-byte loads per thr
 constexpr int kLevel1 = 8192;           // tokens per level-1 block of the grouped inverse CDF
 constexpr int kLevel2 = 256;            // tokens per level-2 block
 constexpr int kLevel3 = 16;             // tokens per level-3 block
+constexpr int kSampleCluster = 8;       // sampler: CTAs (one cluster) per request
 // The walk runs on a CTA of kThreads threads, one thread per row of a
 // request, so N + 1 <= kThreads.
 
@@ -67,7 +68,6 @@ struct Problem {
 struct Workspace {
   Partial* partials;     // [B][2N+1][S1]: target rows 0..N, then draft rows 0..N-1
   float* chunk_sums;     // [B, S3]: residual mass of each level-1 block
-  unsigned* counters;    // [B], sampler chunk counts, zero between calls
   unsigned* err;         // [1], OR of kErr* bits
   float* dbg_accept;     // [B, N]
   float* dbg_logz;       // [B, 2N+1]

@@ -104,10 +104,11 @@ __device__ Partial chunk_partial_scalar(const T* row, int beg, int end, bool gre
 // the next group's loads issued before the current group is reduced, and
 // keeps a running maximum with its sum rescaled whenever the maximum grows
 // (or, for a greedy row, the running maximum and its lowest index).  The
-// threads' states are merged once at the end.
-template <typename T>
-__device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int end, bool greedy,
-                                                    float k) {
+// threads' states are merged once at the end.  kFull: the span is complete,
+// so no vector needs a bounds check.  Exponent arguments and sums use the
+// paired float instructions, two elements per instruction.
+template <typename T, bool kGreedy, bool kFull>
+__device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int end, float k) {
   using E = Elem<T>;
   constexpr int kVec = E::kVec;
   constexpr int kVecs = kSpanBytes / 16 / kThreads;  // vectors per thread
@@ -116,20 +117,21 @@ __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int e
   __shared__ float red_g[kThreads / 32];
   __shared__ int red_i[kThreads / 32];
   const uint4* vp = reinterpret_cast<const uint4*>(row + beg);
-  const int nv = (end - beg) / kVec;
+  const int nv = kFull ? kVecs * kThreads : (end - beg) / kVec;
   const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
 
   uint4 buf[2][kGroup];
 #pragma unroll
   for (int u = 0; u < kGroup; ++u) {
     const int v = threadIdx.x + u * kThreads;
-    buf[0][u] = v < nv ? ld_stream16(vp + v) : pad;
+    buf[0][u] = (kFull || v < nv) ? ld_stream16(vp + v) : pad;
   }
-  float m = -INFINITY;   // running maximum (raw logits)
-  float c = -INFINITY;   // fl(m k), the exponent reference of s
-  float s = 0.f;         // sum of 2^(x k - c) so far
-  bool bad = false;      // a NaN / +inf / out-of-range maximum was seen
-  int idx = INT_MAX;     // greedy: lowest index holding m
+  float m = -INFINITY;      // running maximum (raw logits)
+  float c = -INFINITY;      // fl(m k), the exponent reference of the sum
+  uint64_t s2 = f2pack(0.f, 0.f);  // sum of 2^(x k - c), two lanes
+  bool bad = false;         // a NaN / +inf / out-of-range maximum was seen
+  int idx = INT_MAX;        // greedy: lowest index holding m
+  const uint64_t k2 = f2pack(k, k);
 #pragma unroll
   for (int gi = 0; gi < kGroups; ++gi) {
     const int cur = gi & 1;
@@ -137,14 +139,14 @@ __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int e
 #pragma unroll
       for (int u = 0; u < kGroup; ++u) {
         const int v = threadIdx.x + ((gi + 1) * kGroup + u) * kThreads;
-        buf[cur ^ 1][u] = v < nv ? ld_stream16(vp + v) : pad;
+        buf[cur ^ 1][u] = (kFull || v < nv) ? ld_stream16(vp + v) : pad;
       }
     }
     float gm = E::vmax_nan(buf[cur][0]);
 #pragma unroll
     for (int u = 1; u < kGroup; ++u) gm = fmax_nan(gm, E::vmax_nan(buf[cur][u]));
     if (gm != gm) bad = true;
-    if (greedy) {
+    if (kGreedy) {
       if (gm > m) {  // strict: an equal value later in the row keeps the earlier index
         m = gm;
         idx = INT_MAX;
@@ -161,27 +163,36 @@ __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int e
       if (gm > m) {
         const float cn = gm * k;
         if (gm == INFINITY || !(fabsf(cn) <= 3.40282347e38f)) bad = true;
-        s = c > -INFINITY ? s * ex2(c - cn) : 0.f;
+        const float r = c > -INFINITY ? ex2(c - cn) : 0.f;
+        s2 = f2mul(s2, f2pack(r, r));
         c = cn;
         m = gm;
       }
       if (m > -INFINITY && !bad) {
+        const uint64_t nc2 = f2pack(-c, -c);
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
 #pragma unroll
-          for (int e = 0; e < kVec; ++e) s += ex2(fmaf(E::get(buf[cur][u], e), k, -c));
+          for (int e = 0; e < E::kPairs; ++e) {
+            float a0, a1;
+            f2unpack(f2fma(E::pair(buf[cur][u], e), k2, nc2), a0, a1);
+            s2 = f2add(s2, f2pack(ex2(a0), ex2(a1)));
+          }
         }
       }
     }
   }
   Partial out;
   out.pad = 0;
-  if (greedy) {
+  if (kGreedy) {
     const float best = block_max_nan(bad ? __int_as_float(0x7fc00000) : m, red_f);
     out.idx = block_min_int(m == best ? idx : INT_MAX, red_i);
     out.a = best;
     out.s = (best != best) ? __int_as_float(0x7fc00000) : 0.f;
   } else {
+    float s_lo, s_hi;
+    f2unpack(s2, s_lo, s_hi);
+    const float s = s_lo + s_hi;
     // merge (c, s) over the CTA; any bad thread makes the span bad
     const float cmax = block_max_nan(bad ? __int_as_float(0x7fc00000) : c, red_f);
     float part = 0.f;
@@ -211,8 +222,16 @@ __global__ void __launch_bounds__(kThreads, 5) rowstats_kernel(Problem p, Worksp
   const int end = min(p.V, beg + kSpan);
   const bool greedy = mode == kModeGreedy;
   const float k = greedy ? 0.f : scale_of(p.temperature[b]);
-  const Partial out = kVecPath ? span_partial_vec<T>(base, beg, end, greedy, k)
-                               : chunk_partial_scalar<T>(base, beg, end, greedy, k);
+  Partial out;
+  if (!kVecPath) {
+    out = chunk_partial_scalar<T>(base, beg, end, greedy, k);
+  } else if (end - beg == kSpan) {
+    out = greedy ? span_partial_vec<T, true, true>(base, beg, end, k)
+                 : span_partial_vec<T, false, true>(base, beg, end, k);
+  } else {
+    out = greedy ? span_partial_vec<T, true, false>(base, beg, end, k)
+                 : span_partial_vec<T, false, false>(base, beg, end, k);
+  }
   if (threadIdx.x == 0) w.partials[static_cast<size_t>(row) * S1 + span] = out;
 }
 

@@ -15,13 +15,14 @@
 // rounding leaves none).  The law is exactly r / sum(r), and every decision
 // compares a uniform against at most a few dozen float32 edges.
 //
-// Grid: B x S3 CTAs, one per (request, level-1 block).  Each CTA first runs
+// Grid: one cluster of kSampleCluster CTAs per request.  Every CTA first runs
 // the request's accept/reject walk itself from the row-statistics partials
-// (cheap; no CTA waits for another), then sums r over its block; the last CTA
-// of a request to finish (counted with an atomic, no waiting) picks the
-// level-1 block, rescans only that block for levels 2-4, writes the token and
-// resets the request's counter for the next call.
-//
+// (cheap, and no CTA waits for another to get it); rank 0 writes the walk's
+// outputs.  For a sampled request each CTA then sums r over its share of the
+// level-1 blocks (blocks rank, rank + cluster, ...), the cluster meets at one
+// hardware cluster barrier, and rank 0 picks the level-1 block, rescans only
+// that block for levels 2-4 and writes the token.
+
 // r_t is evaluated as q_t * (1 - 2^-d_t) with d_t = log2(q_t / p_t) taken from
 // the logit difference, so that it keeps its relative precision when q_t and
 // p_t nearly cancel.
@@ -137,26 +138,41 @@ __device__ int warp_pick(Get get, int n, float u) {
   return last_pos;
 }
 
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Hardware barrier over all threads of all CTAs of the cluster; orders the
+// memory accesses before it (release) with those after it (acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
 template <typename T, bool kVecPath>
-__global__ void __launch_bounds__(kThreads) sample_kernel(Problem p, Workspace w) {
+__global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kThreads)
+    sample_kernel(Problem p, Workspace w) {
   using E = Elem<T>;
   constexpr int kSeg = kLevel1 / kThreads;  // 32 contiguous tokens per thread in the rescan
   __shared__ float red[kThreads / 32];
   __shared__ float s_l2[kLevel1 / kLevel2];         // 32 level-2 masses
   __shared__ float s_l3[kLevel1 / kLevel3];         // 512 level-3 masses
   __shared__ float s_l4[kLevel3];                   // 16 token masses
-  __shared__ int s_last, s_sel, s_g2, s_g3, s_tok;
+  __shared__ int s_sel, s_g2, s_g3, s_tok;
   __shared__ Job s_job;
   const int S3 = w.S3;
-  const int b = blockIdx.x / S3;
-  const int c = blockIdx.x - b * S3;
-  // Only sampled requests need the other blocks; the first block of every
-  // request writes its outputs.
-  if (c != 0 && temp_mode(p.temperature[b]) != kModeSampled) return;  // CTA-uniform
-  walk_request<T>(p, w, b, c == 0, &s_job);
+  const int b = blockIdx.x / kSampleCluster;
+  const unsigned rank = cluster_rank();
+  // Only sampled requests need the other CTAs of the cluster (the choice is
+  // the same in every CTA of a cluster, so either all of them reach the
+  // cluster barrier below or none does); rank 0 writes the outputs.
+  if (rank != 0 && temp_mode(p.temperature[b]) != kModeSampled) return;
+  walk_request<T>(p, w, b, rank == 0, &s_job);
   __syncthreads();
   const Job job = s_job;
-  if (job.kind == kJobNone) return;  // CTA-uniform
+  if (job.kind == kJobNone) return;  // identical in every CTA of the cluster
   const int N = p.N, V = p.V;
   const T* z = static_cast<const T*>(p.target) + (static_cast<size_t>(b) * (N + 1) + job.row) * V;
   const T* y = job.kind == kJobResidual
@@ -165,18 +181,17 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(Problem p, Workspace w
   bool has_p = job.kind == kJobResidual;
   float* sums = w.chunk_sums + static_cast<size_t>(b) * S3;
 
-  const int beg = c * kLevel1;
-  const float part = block_mass<T, kVecPath>(z, y, beg, min(V, beg + kLevel1), job, has_p, red);
-  if (threadIdx.x == 0) {
-    sums[c] = part;
-    __threadfence();
-    const unsigned prev = atomicAdd(w.counters + b, 1u);
-    s_last = prev == static_cast<unsigned>(S3 - 1);
+  // Level-1 block masses: this CTA takes blocks rank, rank + cluster, ...
+  for (int c = static_cast<int>(rank); c < S3; c += kSampleCluster) {
+    const int beg = c * kLevel1;
+    const float part = block_mass<T, kVecPath>(z, y, beg, min(V, beg + kLevel1), job, has_p, red);
+    if (threadIdx.x == 0) sums[c] = part;
   }
-  __syncthreads();
-  if (!s_last) return;
   __threadfence();
+  cluster_sync();
+  if (rank != 0) return;
 
+  // ---- rank 0 of request b.  Level 1: pick the block.
   // ---- last CTA of request b.  Level 1: pick the block.
   for (int pass = 0; pass < 2; ++pass) {
     if (threadIdx.x < 32) {
@@ -265,17 +280,14 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(Problem p, Workspace w
     __syncthreads();
     token = s_tok;
   }
-  if (threadIdx.x == 0) {
-    p.out_tokens[static_cast<size_t>(b) * (N + 1) + job.row] = token;
-    w.counters[b] = 0u;
-  }
+  if (threadIdx.x == 0) p.out_tokens[static_cast<size_t>(b) * (N + 1) + job.row] = token;
 }
 
 }  // namespace
 
 cudaError_t launch_sample(int dtype, bool vec, const Problem& p, const Workspace& w,
                           cudaStream_t s) {
-  const long long blocks = static_cast<long long>(p.B) * w.S3;
+  const long long blocks = static_cast<long long>(p.B) * kSampleCluster;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const dim3 grid(static_cast<unsigned>(blocks));
