@@ -57,6 +57,23 @@ def dist_env():
     return world, rank, local
 
 
+def ranks_max(value, device=None):
+    """Max of a float over all ranks (the slowest rank's time); identity
+    when torch.distributed is not initialised."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step, steps, world, max_ms):
+    """Units processed by all ranks divided by the slowest rank's time."""
+    return units_per_rank_step * steps * world / (max_ms / 1e3)
+
+
 def csrc_hash():
     h = hashlib.sha256()
     d = os.path.join(ROOT, "speculative_decoding_verification_73_gb300", "csrc")
@@ -220,13 +237,8 @@ def run_ours(args):
     binding.spec_verify_profile(sv.ctx, False)
     time.sleep(0.2)
     clk = clocks.stop(t_begin, t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-
-    positions = B * N * args.steps * world
-    value = positions / (elapsed_ms / 1e3)
+    elapsed_ms = ranks_max(elapsed_ms, dev)
+    value = whole_job_rate(B * N, args.steps, world, elapsed_ms)
     bytes_per_launch = wl.bytes_read()
     rowstats_ms = kernel_ms["rowstats_walk"] / max(calls, 1)
     achieved = bytes_per_launch / (rowstats_ms / 1e3) / 1e9
@@ -266,11 +278,8 @@ def run_ours(args):
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = B * N * e2e_steps * world / (e2e_ms / 1e3)
+    e2e_ms = ranks_max(e2e_ms, dev)
+    e2e_value = whole_job_rate(B * N, e2e_steps, world, e2e_ms)
     code, _ = sv.get_error()
     assert code == 0, binding.strerror(code)
 
