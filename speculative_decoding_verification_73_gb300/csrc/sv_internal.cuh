@@ -8,8 +8,11 @@
 namespace sv {
 
 constexpr int kThreads = 256;           // threads per CTA, every kernel
-constexpr int kSpanBytes = 65536;       // row statistics: bytes of a row one CTA reduces
-constexpr int kGroup = 4;               // row statistics: 16-byte loads per thread in flight
+constexpr int kSpanBytes = 65536;       // row statistics, span kernel: bytes of a row one CTA reduces
+constexpr int kGroup = 4;               // row statistics: 16-byte loads per thread per group
+constexpr int kStreamMaxB = 2048;       // stream kernel keeps per-request row counts in shared memory
+constexpr int kStreamCtasPerSm = 2;     // stream kernel: resident CTAs per SM
+constexpr int kStreamStages = 5;        // stream kernel: cp.async groups per warp (4 in flight)
 constexpr int kLevel1 = 8192;           // tokens per level-1 block of the grouped inverse CDF
 constexpr int kLevel2 = 256;            // tokens per level-2 block
 constexpr int kLevel3 = 16;             // tokens per level-3 block
@@ -65,19 +68,45 @@ struct Problem {
   int32_t* out_kv;           // [B]
 };
 
+constexpr int kLayoutSpan = 0;    // partials[b][2N+1][S1]
+constexpr int kLayoutStream = 1;  // partials[range][2], see sv_rowstats.cu
+
 struct Workspace {
-  Partial* partials;     // [B][2N+1][S1]: target rows 0..N, then draft rows 0..N-1
+  Partial* partials;     // row-statistics partials, laid out as `layout` says
+  unsigned* row_prefix;  // [B+1] stream layout: active rows before request b
+  float* tok_logit;      // [B][2N+1] stream layout: logit at the row's draft token
   float* chunk_sums;     // [B, S3]: residual mass of each level-1 block
   unsigned* err;         // [1], OR of kErr* bits
   float* dbg_accept;     // [B, N]
   float* dbg_logz;       // [B, 2N+1]
-  int S1;                // row-statistics spans per row for this call's V
+  int layout;            // kLayout*
+  int S1;                // span layout: spans per row for this call's V
+  int stream_warps;      // stream layout: warps of the row-statistics launch
   int S3;                // level-1 blocks per row for this call's V
 };
 
+// Byte ranges of the stream layout.  The active rows (target rows 0..N of
+// every valid request, draft rows 0..N-1 of sampled ones; request-major) are
+// concatenated into one byte stream of total = rows * row_bytes bytes, cut
+// into ranges of range_bytes (a multiple of 16, at most one row) so that
+// every warp of the launch gets one range (or a few when rows are small).
+// Range rho covers [rho * range_bytes, ...) and touches at most two rows;
+// its partial for the first row it touches is partials[2 rho], for the
+// second partials[2 rho + 1].
+__host__ __device__ inline unsigned long long stream_range_bytes(unsigned long long total,
+                                                                 unsigned long long row_bytes,
+                                                                 unsigned long long warps) {
+  unsigned long long r = ((total + warps - 1) / warps + 15) / 16 * 16;
+  if (r > row_bytes) r = row_bytes;
+  return r < 16 ? 16 : r;
+}
+
 // dtype codes match SV_F32 / SV_BF16; vec selects 16-byte loads (aligned rows).
+// The layout and stream_warps fields of w must match what the launch uses:
+// stream layout iff vec && B <= kStreamMaxB, with stream_warps = grid * 8.
 cudaError_t launch_rowstats(int dtype, bool vec, const Problem& p, const Workspace& w,
                             cudaStream_t s);
+cudaError_t prepare_rowstats();  // once per device, before the first launch
 cudaError_t launch_sample(int dtype, bool vec, const Problem& p, const Workspace& w,
                           cudaStream_t s);
 cudaError_t launch_philox_probe(unsigned long long seed, const uint32_t* ctr3, uint32_t* out4,

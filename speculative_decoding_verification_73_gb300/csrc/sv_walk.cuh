@@ -38,22 +38,24 @@ struct RowNorm {
 };
 
 // Partials are loaded kBatch at a time with every load issued before any is
-// used, so a row costs ceil(S1 / kBatch) L2 round trips, not S1.
+// used, so a row costs ceil(n / kBatch) L2 round trips, not n.  `at(i)` gives
+// the address of the row's i-th partial.
 constexpr int kBatch = 8;
 
-__device__ __forceinline__ RowNorm merge_sampled(const Partial* parts, int S1) {
+template <typename At>
+__device__ __forceinline__ RowNorm merge_sampled(At at, int n) {
   float c = -INFINITY, s = 0.f;
   bool bad = false;
-  for (int i0 = 0; i0 < S1; i0 += kBatch) {
+  for (int i0 = 0; i0 < n; i0 += kBatch) {
     float4 pt[kBatch];
 #pragma unroll
     for (int i = 0; i < kBatch; ++i)
-      pt[i] = i0 + i < S1 ? __ldcg(reinterpret_cast<const float4*>(parts + i0 + i))
-                          : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+      pt[i] = i0 + i < n ? __ldcg(reinterpret_cast<const float4*>(at(i0 + i)))
+                         : make_float4(-INFINITY, 0.f, 0.f, 0.f);
     float cb = c;
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
-      if (pt[i].y != pt[i].y) bad = true;
+      if (pt[i].y != pt[i].y || pt[i].x != pt[i].x) bad = true;
       cb = fmaxf(cb, pt[i].x);
     }
     if (cb > -INFINITY) {
@@ -77,21 +79,24 @@ struct RowMax {
   bool ok;
 };
 
-__device__ __forceinline__ RowMax merge_greedy(const Partial* parts, int S1) {
+// Greedy rows: partials come in increasing index order, so strict > keeps
+// the lowest index among equal maxima.
+template <typename At>
+__device__ __forceinline__ RowMax merge_greedy(At at, int n) {
   float best = -INFINITY;
   int idx = INT_MAX;
   bool bad = false;
-  for (int i0 = 0; i0 < S1; i0 += kBatch) {
+  for (int i0 = 0; i0 < n; i0 += kBatch) {
     int4 pt[kBatch];
 #pragma unroll
     for (int i = 0; i < kBatch; ++i)
-      pt[i] = i0 + i < S1 ? __ldcg(reinterpret_cast<const int4*>(parts + i0 + i))
-                          : make_int4(__float_as_int(-INFINITY), 0, INT_MAX, 0);
+      pt[i] = i0 + i < n ? __ldcg(reinterpret_cast<const int4*>(at(i0 + i)))
+                         : make_int4(__float_as_int(-INFINITY), 0, INT_MAX, 0);
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const float a = __int_as_float(pt[i].x), sv = __int_as_float(pt[i].y);
       if (sv != sv || a != a) bad = true;
-      if (a > best) {  // chunks are in index order: strict > keeps the lowest index
+      if (a > best) {
         best = a;
         idx = pt[i].z;
       }
@@ -100,6 +105,42 @@ __device__ __forceinline__ RowMax merge_greedy(const Partial* parts, int S1) {
   RowMax r;
   r.idx = idx;
   r.ok = !bad && best > -INFINITY && best < INFINITY;
+  return r;
+}
+
+// Where the partials of row `slot` of request b live, for either layout.
+struct RowParts {
+  const Partial* base;  // span layout: partials of the row, contiguous
+  int n;                // number of partials
+  unsigned long long first, rq;  // stream layout: first range, row start / range bytes
+  unsigned long long rb;
+  bool stream;
+  __device__ __forceinline__ const Partial* operator()(int i) const {
+    if (!stream) return base + i;
+    const unsigned long long rho = first + static_cast<unsigned long long>(i);
+    return base + 2 * rho + (rho * rb < rq ? 1 : 0);
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ RowParts row_parts(const Problem& p, const Workspace& w, int b, int slot) {
+  RowParts r;
+  if (w.layout == kLayoutSpan) {
+    r.stream = false;
+    r.base = w.partials + (static_cast<size_t>(b) * (2 * p.N + 1) + slot) * w.S1;
+    r.n = w.S1;
+    return r;
+  }
+  r.stream = true;
+  r.base = w.partials;
+  const unsigned long long row_bytes = static_cast<unsigned long long>(p.V) * sizeof(T);
+  const unsigned long long total = static_cast<unsigned long long>(__ldcg(w.row_prefix + p.B)) * row_bytes;
+  r.rb = stream_range_bytes(total, row_bytes, static_cast<unsigned long long>(w.stream_warps));
+  const unsigned long long q = static_cast<unsigned long long>(__ldcg(w.row_prefix + b)) + slot;
+  r.rq = q * row_bytes;
+  r.first = r.rq / r.rb;
+  const unsigned long long last = (r.rq + row_bytes - 1) / r.rb;
+  r.n = static_cast<int>(last - r.first + 1);
   return r;
 }
 
@@ -114,7 +155,7 @@ template <typename T>
 __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& w, int b,
                                              bool write_outputs, Job* job_out) {
   const int j = threadIdx.x;
-  const int N = p.N, V = p.V, S1 = w.S1;
+  const int N = p.N, V = p.V;
   const bool row_thread = j <= N;
   const bool pos_thread = j < N;
 
@@ -136,25 +177,30 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
     if (d < 0 || d >= V) {
       atomicOr(&s_bad_token, 1);
     } else if (mode == kModeSampled) {
-      // issue the two logit loads early; they are used after the merges
-      zd = Elem<T>::load1(static_cast<const T*>(p.target) + trow * V + d);
-      yd = Elem<T>::load1(static_cast<const T*>(p.draft) + (static_cast<size_t>(b) * N + j) * V + d);
+      if (w.layout == kLayoutStream) {
+        // the row-statistics pass stored the logits at the draft token
+        const float* tl = w.tok_logit + static_cast<size_t>(b) * (2 * N + 1);
+        zd = __ldcg(tl + j);
+        yd = __ldcg(tl + N + 1 + j);
+      } else {
+        zd = Elem<T>::load1(static_cast<const T*>(p.target) + trow * V + d);
+        yd = Elem<T>::load1(static_cast<const T*>(p.draft) + (static_cast<size_t>(b) * N + j) * V + d);
+      }
     }
   }
-  // partials are request-major: [b][target rows 0..N, draft rows 0..N-1][S1]
-  const Partial* req_parts = w.partials + static_cast<size_t>(b) * (2 * N + 1) * S1;
-  const size_t trow_p = static_cast<size_t>(j);
-  const size_t drow_p = static_cast<size_t>(N + 1 + j);
   RowNorm q{}, pn{};
   RowMax g{};
   if (mode == kModeGreedy && row_thread) {
-    g = merge_greedy(req_parts + trow_p * S1, S1);
+    const RowParts tp = row_parts<T>(p, w, b, j);
+    g = merge_greedy(tp, tp.n);
     if (!g.ok) atomicOr(&s_bad_logit, 1);
   } else if (mode == kModeSampled && row_thread) {
-    q = merge_sampled(req_parts + trow_p * S1, S1);
+    const RowParts tp = row_parts<T>(p, w, b, j);
+    q = merge_sampled(tp, tp.n);
     if (!q.ok) atomicOr(&s_bad_logit, 1);
     if (pos_thread) {
-      pn = merge_sampled(req_parts + drow_p * S1, S1);
+      const RowParts dp = row_parts<T>(p, w, b, N + 1 + j);
+      pn = merge_sampled(dp, dp.n);
       if (!pn.ok) atomicOr(&s_bad_logit, 1);
     }
   }
