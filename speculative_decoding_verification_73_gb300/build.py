@@ -33,9 +33,9 @@ def sources():
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _compile(src, verbose):
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-    cmd = [nvcc(), *ARCH, *FLAGS, "-c", src, "-o", obj]
+def _compile(src, verbose, build_dir=BUILD, defines=()):
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc(), *ARCH, *FLAGS, *[f"-D{d}" for d in defines], "-c", src, "-o", obj]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     proc = subprocess.run(cmd, capture_output=True, text=True)
@@ -44,27 +44,30 @@ def _compile(src, verbose):
     return obj, proc.stderr
 
 
-def build(force=False, verbose=False):
-    """Compile and link; skip when the library is newer than every source."""
+def build(force=False, verbose=False, defines=(), out=LIB):
+    """Compile and link; skip when the library is newer than every source.
+    `defines` (NAME=VALUE strings) override the kernels' tuning constants;
+    `out` names the library file (its objects go to a folder beside it)."""
     srcs = sources()
     heads = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
     heads.append(os.path.join(os.path.dirname(PKG), "include", "spec_verify.h"))
     newest = max(os.path.getmtime(f) for f in srcs + heads)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest:
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    if not force and not defines and os.path.exists(out) and os.path.getmtime(out) >= newest:
+        return out
+    build_dir = BUILD if out == LIB else out + ".objs"
+    os.makedirs(build_dir, exist_ok=True)
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        results = list(ex.map(lambda s: _compile(s, verbose), srcs))
+        results = list(ex.map(lambda s: _compile(s, verbose, build_dir, defines), srcs))
     if verbose:
         for _, log in results:
             sys.stderr.write(log)
-    tmp = LIB + ".tmp"
+    tmp = out + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp] + [o for o, _ in results]
     proc = subprocess.run(cmd, capture_output=True, text=True)
     if proc.returncode != 0:
         raise RuntimeError(f"link failed:\n{proc.stdout}\n{proc.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -114,8 +114,8 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   size_t off = 0;
   // partials: span layout rows * s1, stream layout 2 per byte range (at most
   // max(warps, rows) + 1 ranges)
-  const size_t stream_parts = 2 * ((rows > static_cast<size_t>(ctx->stream_warps)
-                                        ? rows : static_cast<size_t>(ctx->stream_warps)) + 1);
+  const size_t stream_ranges = static_cast<size_t>(ctx->stream_warps) * sv::kStreamRanges;
+  const size_t stream_parts = 2 * ((rows > stream_ranges ? rows : stream_ranges) + 1);
   const size_t n_parts = rows * s1 > stream_parts ? rows * s1 : stream_parts;
   const size_t o_part = off;
   off = align_up(off + n_parts * sizeof(sv::Partial), 256);
@@ -184,7 +184,8 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
   p.out_kv = out_kv_len;
   sv::Workspace w = ctx->w;
   w.S1 = ceil_div(V, sv::row_chunk_elems(ctx->dtype));
-  w.layout = (vec && B <= sv::kStreamMaxB) ? sv::kLayoutStream : sv::kLayoutSpan;
+  w.layout = (sv::kLayoutChoice != 1 && vec && B <= sv::kStreamMaxB) ? sv::kLayoutStream
+                                                                     : sv::kLayoutSpan;
   w.stream_warps = ctx->stream_warps;
   w.S3 = ceil_div(V, sv::sample_chunk_elems(ctx->dtype));
 

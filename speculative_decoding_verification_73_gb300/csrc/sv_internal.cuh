@@ -8,11 +8,37 @@
 namespace sv {
 
 constexpr int kThreads = 256;           // threads per CTA, every kernel
-constexpr int kSpanBytes = 65536;       // row statistics, span kernel: bytes of a row one CTA reduces
-constexpr int kGroup = 4;               // row statistics: 16-byte loads per thread per group
-constexpr int kStreamMaxB = 2048;       // stream kernel keeps per-request row counts in shared memory
-constexpr int kStreamCtasPerSm = 2;     // stream kernel: resident CTAs per SM
-constexpr int kStreamStages = 5;        // stream kernel: cp.async groups per warp (4 in flight)
+// Tuning constants of the row-statistics kernels; each can be overridden at
+// build time with -D<name>=<value> (the build script's `defines`).
+#ifndef SV_SPAN_BYTES
+#define SV_SPAN_BYTES 65536
+#endif
+#ifndef SV_GROUP
+#define SV_GROUP 4
+#endif
+#ifndef SV_SPAN_MINB
+#define SV_SPAN_MINB 5
+#endif
+#ifndef SV_STREAM_CTAS
+#define SV_STREAM_CTAS 2
+#endif
+#ifndef SV_STREAM_STAGES
+#define SV_STREAM_STAGES 5
+#endif
+#ifndef SV_STREAM_RANGES
+#define SV_STREAM_RANGES 1
+#endif
+#ifndef SV_LAYOUT
+#define SV_LAYOUT 0
+#endif
+constexpr int kSpanBytes = SV_SPAN_BYTES;      // span kernel: bytes of a row one CTA reduces
+constexpr int kGroup = SV_GROUP;               // 16-byte loads per thread per group
+constexpr int kSpanMinBlocks = SV_SPAN_MINB;   // span kernel: resident CTAs per SM it is built for
+constexpr int kStreamMaxB = 2048;              // stream kernel keeps per-request row counts in smem
+constexpr int kStreamCtasPerSm = SV_STREAM_CTAS;   // stream kernel: resident CTAs per SM
+constexpr int kStreamStages = SV_STREAM_STAGES;    // stream kernel: cp.async groups per warp
+constexpr int kStreamRanges = SV_STREAM_RANGES;    // stream kernel: byte ranges per warp
+constexpr int kLayoutChoice = SV_LAYOUT;       // 0 automatic, 1 span only, 2 stream when possible
 constexpr int kLevel1 = 8192;           // tokens per level-1 block of the grouped inverse CDF
 constexpr int kLevel2 = 256;            // tokens per level-2 block
 constexpr int kLevel3 = 16;             // tokens per level-3 block
@@ -89,14 +115,16 @@ struct Workspace {
 // every valid request, draft rows 0..N-1 of sampled ones; request-major) are
 // concatenated into one byte stream of total = rows * row_bytes bytes, cut
 // into ranges of range_bytes (a multiple of 16, at most one row) so that
-// every warp of the launch gets one range (or a few when rows are small).
+// every warp of the launch gets kStreamRanges ranges, spread over the stream
+// (warp w takes ranges w, w + warps, ...), or more when rows are small.
 // Range rho covers [rho * range_bytes, ...) and touches at most two rows;
 // its partial for the first row it touches is partials[2 rho], for the
 // second partials[2 rho + 1].
 __host__ __device__ inline unsigned long long stream_range_bytes(unsigned long long total,
                                                                  unsigned long long row_bytes,
                                                                  unsigned long long warps) {
-  unsigned long long r = ((total + warps - 1) / warps + 15) / 16 * 16;
+  const unsigned long long parts = warps * static_cast<unsigned long long>(kStreamRanges);
+  unsigned long long r = ((total + parts - 1) / parts + 15) / 16 * 16;
   if (r > row_bytes) r = row_bytes;
   return r < 16 ? 16 : r;
 }

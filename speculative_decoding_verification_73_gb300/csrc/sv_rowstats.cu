@@ -206,7 +206,7 @@ __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int e
 }
 
 template <typename T, bool kVecPath>
-__global__ void __launch_bounds__(kThreads, 5) rowstats_kernel(Problem p, Workspace w) {
+__global__ void __launch_bounds__(kThreads, kSpanMinBlocks) rowstats_kernel(Problem p, Workspace w) {
   const int S1 = w.S1;
   const int per = 2 * p.N + 1;
   const int row = blockIdx.x / S1;
