@@ -15,7 +15,6 @@
 struct spec_verify_ctx {
   int max_B, max_N, max_V, dtype;
   int device;
-  int stream_warps;  // warps of the stream row-statistics launch
   cudaStream_t stream;
   void* ws;  // one cudaMalloc holding the whole workspace
   sv::Workspace w;
@@ -100,27 +99,16 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   ctx->max_V = max_V;
   ctx->dtype = dtype;
   ctx->stream = static_cast<cudaStream_t>(cuda_stream);
-  int sms = 0;
-  if (cudaGetDevice(&ctx->device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess ||
-      sv::prepare_rowstats() != cudaSuccess) {
+  if (cudaGetDevice(&ctx->device) != cudaSuccess) {
     delete ctx;
     return SV_ECUDA;
   }
-  ctx->stream_warps = sms * sv::kStreamCtasPerSm * (sv::kThreads / 32);
   const int s1 = ceil_div(max_V, sv::row_chunk_elems(dtype));
   const int s3 = ceil_div(max_V, sv::sample_chunk_elems(dtype));
   const size_t rows = static_cast<size_t>(max_B) * (2 * static_cast<size_t>(max_N) + 1);
   size_t off = 0;
-  // partials: span layout rows * s1, stream layout 2 per byte range (at most
-  // max(warps, rows) + 1 ranges)
-  const size_t stream_ranges = static_cast<size_t>(ctx->stream_warps) * sv::kStreamRanges;
-  const size_t stream_parts = 2 * ((rows > stream_ranges ? rows : stream_ranges) + 1);
-  const size_t n_parts = rows * s1 > stream_parts ? rows * s1 : stream_parts;
   const size_t o_part = off;
-  off = align_up(off + n_parts * sizeof(sv::Partial), 256);
-  const size_t o_pref = off;
-  off = align_up(off + (static_cast<size_t>(max_B) + 1) * sizeof(unsigned), 256);
+  off = align_up(off + rows * s1 * sizeof(sv::Partial), 256);
   const size_t o_tok = off;
   off = align_up(off + rows * sizeof(float), 256);
   const size_t o_sums = off;
@@ -138,7 +126,6 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   }
   char* base = static_cast<char*>(ctx->ws);
   ctx->w.partials = reinterpret_cast<sv::Partial*>(base + o_part);
-  ctx->w.row_prefix = reinterpret_cast<unsigned*>(base + o_pref);
   ctx->w.tok_logit = reinterpret_cast<float*>(base + o_tok);
   ctx->w.chunk_sums = reinterpret_cast<float*>(base + o_sums);
   ctx->w.err = reinterpret_cast<unsigned*>(base + o_err);
@@ -184,9 +171,6 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
   p.out_kv = out_kv_len;
   sv::Workspace w = ctx->w;
   w.S1 = ceil_div(V, sv::row_chunk_elems(ctx->dtype));
-  w.layout = (sv::kLayoutChoice != 1 && vec && B <= sv::kStreamMaxB) ? sv::kLayoutStream
-                                                                     : sv::kLayoutSpan;
-  w.stream_warps = ctx->stream_warps;
   w.S3 = ceil_div(V, sv::sample_chunk_elems(ctx->dtype));
 
   cudaEvent_t* ev = nullptr;

@@ -15,17 +15,19 @@
 // rounding leaves none).  The law is exactly r / sum(r), and every decision
 // compares a uniform against at most a few dozen float32 edges.
 //
-// Grid: one cluster of kSampleCluster CTAs per request.  Every CTA first runs
-// the request's accept/reject walk itself from the row-statistics partials
-// (cheap, and no CTA waits for another to get it); rank 0 writes the walk's
-// outputs.  For a sampled request each CTA then sums r over its share of the
-// level-1 blocks (blocks rank, rank + cluster, ...), the cluster meets at one
-// hardware cluster barrier, and rank 0 picks the level-1 block, rescans only
-// that block for levels 2-4 and writes the token.
-
-// r_t is evaluated as q_t * (1 - 2^-d_t) with d_t = log2(q_t / p_t) taken from
-// the logit difference, so that it keeps its relative precision when q_t and
-// p_t nearly cancel.
+// Grid: one cluster of kSampleCluster CTAs of kSampleThreads threads per
+// request.  Every CTA first runs the request's accept/reject walk itself from
+// the row-statistics partials (cheap, and no CTA waits for another to get
+// it); rank 0 writes the walk's outputs.  For a sampled request each CTA then
+// sums r over its share of the level-1 blocks (blocks rank, rank + cluster,
+// ...), the cluster meets at one hardware cluster barrier, and rank 0 picks
+// the level-1 block, rescans only that block for levels 2-4 (thread t holds
+// the 16 tokens of level-3 block t) and writes the token.
+//
+// r_t = max(q_t - p_t, 0) with q_t = 2^(z_t k - c_q) / s_q and likewise p_t,
+// evaluated two tokens at a time with the paired float instructions.  Its
+// rounding (a few float32 ulps of q_t per token) moves the level edges by
+// ~1e-7 of the level mass, well inside the 1e-5 near-threshold window.
 
 #include <climits>
 #include <cuda_bf16.h>
@@ -36,31 +38,58 @@
 namespace sv {
 namespace {
 
-// 1 - 2^-d for d > 0, to full float precision: for d >= 1/2 directly (no
-// cancellation), below that from the Taylor series of 1 - e^-x at x = d ln 2
-// (x < 0.35; the first omitted term is below 1.6e-8 of the value).
-__device__ __forceinline__ float one_minus_exp2_neg(float d) {
-  const float x = d * 0.693147180559945309f;
-  float poly = 1.f / 5040.f;
-  poly = fmaf(poly, x, -1.f / 720.f);
-  poly = fmaf(poly, x, 1.f / 120.f);
-  poly = fmaf(poly, x, -1.f / 24.f);
-  poly = fmaf(poly, x, 1.f / 6.f);
-  poly = fmaf(poly, x, -0.5f);
-  poly = fmaf(poly, x, 1.f);
-  const float small = poly * x;
-  return d < 0.5f ? small : 1.f - ex2(-d);
+constexpr int kST = kSampleThreads;        // threads per sampler CTA
+constexpr int kSegTok = kLevel1 / kST;      // tokens per thread in a level-1 block (16)
+static_assert(kSegTok == kLevel3, "one thread per level-3 block in the rescan");
+
+__device__ __forceinline__ float cta_sum(float v, float* scratch) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = 0.f;
+#pragma unroll
+  for (int w = 0; w < kST / 32; ++w) v += scratch[w];
+  __syncthreads();
+  return v;
 }
 
-// r_t from one target value (and one draft value when has_p).  The block
-// masses and the rescan evaluate exactly this expression.
-__device__ __forceinline__ float resid(float zt, float yt, const Job& job, bool has_p) {
+// r for the (up to) 8 tokens of one 16-byte vector of each row; rv[e] gets
+// token e of the vector.
+template <typename T>
+__device__ __forceinline__ void resid_vec(const uint4& zv, const uint4& yv, const Job& job, bool has_p,
+                                          float (&rv)[Elem<T>::kVec]) {
+  using E = Elem<T>;
+  const uint64_t k2 = f2pack(job.k, job.k);
+  const uint64_t nq2 = f2pack(-job.cq, -job.cq), iq2 = f2pack(job.inv_sq, job.inv_sq);
+  const uint64_t np2 = f2pack(-job.cp, -job.cp), ip2 = f2pack(job.inv_sp, job.inv_sp);
+#pragma unroll
+  for (int e = 0; e < E::kPairs; ++e) {
+    float a0, a1;
+    f2unpack(f2fma(E::pair(zv, e), k2, nq2), a0, a1);
+    float q0, q1;
+    f2unpack(f2mul(f2pack(ex2(a0), ex2(a1)), iq2), q0, q1);
+    if (has_p) {
+      float b0, b1;
+      f2unpack(f2fma(E::pair(yv, e), k2, np2), b0, b1);
+      float p0, p1;
+      f2unpack(f2mul(f2pack(ex2(b0), ex2(b1)), ip2), p0, p1);
+      q0 = fmaxf(q0 - p0, 0.f);
+      q1 = fmaxf(q1 - p1, 0.f);
+    }
+    rv[2 * e] = q0;
+    rv[2 * e + 1] = q1;
+  }
+}
+
+// Scalar form for rows that are not 16-byte aligned (same arithmetic).
+__device__ __forceinline__ float resid1(float zt, float yt, const Job& job, bool has_p) {
   const float q = ex2(fmaf(zt, job.k, -job.cq)) * job.inv_sq;
   if (!has_p) return q;
-  const float d = fmaf(zt - yt, job.k, -job.dhi) - job.dlo;  // log2(q_t / p_t)
-  return d > 0.f ? q * one_minus_exp2_neg(d) : 0.f;
+  return fmaxf(q - ex2(fmaf(yt, job.k, -job.cp)) * job.inv_sp, 0.f);
 }
 
+// Residual mass of level-1 block [beg, end) (all threads; result in all).
 template <typename T, bool kVecPath>
 __device__ float block_mass(const T* z, const T* y, int beg, int end, const Job& job, bool has_p,
                             float* scratch) {
@@ -68,32 +97,31 @@ __device__ float block_mass(const T* z, const T* y, int beg, int end, const Job&
   float s = 0.f;
   if (kVecPath) {
     constexpr int kVec = E::kVec;
-    constexpr int kPer = kLevel1 / kVec / kThreads;
+    constexpr int kPer = kLevel1 / kVec / kST;
     const uint4* zp = reinterpret_cast<const uint4*>(z + beg);
     const uint4* yp = reinterpret_cast<const uint4*>(y + beg);
     const int nv = (end - beg) / kVec;
+    const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
     uint4 zr[kPer], yr[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-      const int v = threadIdx.x + i * kThreads;
+      const int v = threadIdx.x + i * kST;
       const bool in = v < nv;
-      zr[i] = in ? __ldg(zp + v)
-                 : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
-      yr[i] = (in && has_p) ? __ldg(yp + v) : zr[i];
+      zr[i] = in ? __ldg(zp + v) : pad;
+      yr[i] = (in && has_p) ? __ldg(yp + v) : pad;
     }
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
+      float rv[kVec];
+      resid_vec<T>(zr[i], yr[i], job, has_p, rv);
 #pragma unroll
-      for (int e = 0; e < kVec; ++e) s += resid(E::get(zr[i], e), E::get(yr[i], e), job, has_p);
+      for (int e = 0; e < kVec; ++e) s += rv[e];
     }
   } else {
-    for (int t = beg + threadIdx.x; t < end; t += kThreads) {
-      const float zt = E::load1(z + t);
-      const float yt = has_p ? E::load1(y + t) : 0.f;
-      s += resid(zt, yt, job, has_p);
-    }
+    for (int t = beg + threadIdx.x; t < end; t += kST)
+      s += resid1(E::load1(z + t), has_p ? E::load1(y + t) : 0.f, job, has_p);
   }
-  return block_sum(s, scratch);
+  return cta_sum(s, scratch);
 }
 
 // Inverse CDF over n masses, evaluated by one whole warp (all lanes get the
@@ -152,11 +180,10 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 template <typename T, bool kVecPath>
-__global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kThreads)
+__global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kST)
     sample_kernel(Problem p, Workspace w) {
   using E = Elem<T>;
-  constexpr int kSeg = kLevel1 / kThreads;  // 32 contiguous tokens per thread in the rescan
-  __shared__ float red[kThreads / 32];
+  __shared__ float red[kST / 32];
   __shared__ float s_l2[kLevel1 / kLevel2];         // 32 level-2 masses
   __shared__ float s_l3[kLevel1 / kLevel3];         // 512 level-3 masses
   __shared__ float s_l4[kLevel3];                   // 16 token masses
@@ -192,7 +219,6 @@ __global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kThread
   if (rank != 0) return;
 
   // ---- rank 0 of request b.  Level 1: pick the block.
-  // ---- last CTA of request b.  Level 1: pick the block.
   for (int pass = 0; pass < 2; ++pass) {
     if (threadIdx.x < 32) {
       const int sel = warp_pick([&](int i) { return __ldcg(sums + i); }, S3, job.u[0]);
@@ -206,52 +232,47 @@ __global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kThread
       const int bi = i * kLevel1;
       const float v = block_mass<T, kVecPath>(z, y, bi, min(V, bi + kLevel1), job, false, red);
       if (threadIdx.x == 0) sums[i] = v;
-      __syncthreads();
     }
     __threadfence_block();
   }
   const int sel = s_sel;
   int token = 0;
   if (sel >= 0) {
-    // Rescan the chosen block: thread t holds tokens [32t, 32t + 32) of it.
+    // Rescan the chosen block: thread t holds tokens [16t, 16t + 16) of it,
+    // i.e. level-3 block t; 16 threads make a level-2 block.
     const int cbeg = sel * kLevel1;
     const int cend = min(V, cbeg + kLevel1);
-    const int t0 = cbeg + threadIdx.x * kSeg;
-    float r[kSeg];
+    const int t0 = cbeg + threadIdx.x * kSegTok;
+    float r[kSegTok];
     if (kVecPath) {
       constexpr int kVec = E::kVec;
+      const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
 #pragma unroll
-      for (int i = 0; i < kSeg / kVec; ++i) {
+      for (int i = 0; i < kSegTok / kVec; ++i) {
         const int e0 = t0 + i * kVec;
         const bool in = e0 < cend;
-        const uint4 zv = in ? __ldg(reinterpret_cast<const uint4*>(z + e0))
-                            : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord,
-                                         E::kNegInfWord);
-        const uint4 yv = (in && has_p) ? __ldg(reinterpret_cast<const uint4*>(y + e0)) : zv;
+        const uint4 zv = in ? __ldg(reinterpret_cast<const uint4*>(z + e0)) : pad;
+        const uint4 yv = (in && has_p) ? __ldg(reinterpret_cast<const uint4*>(y + e0)) : pad;
+        float rv[kVec];
+        resid_vec<T>(zv, yv, job, has_p, rv);
 #pragma unroll
-        for (int e = 0; e < kVec; ++e) r[i * kVec + e] = resid(E::get(zv, e), E::get(yv, e), job, has_p);
+        for (int e = 0; e < kVec; ++e) r[i * kVec + e] = rv[e];
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < kSeg; ++i) {
+      for (int i = 0; i < kSegTok; ++i) {
         const int t = t0 + i;
-        r[i] = t < cend ? resid(E::load1(z + t), has_p ? E::load1(y + t) : 0.f, job, has_p) : 0.f;
+        r[i] = t < cend ? resid1(E::load1(z + t), has_p ? E::load1(y + t) : 0.f, job, has_p) : 0.f;
       }
     }
-    float h0 = 0.f, h1 = 0.f;
+    float h = 0.f;
 #pragma unroll
-    for (int i = 0; i < kLevel3; ++i) {
-      h0 += r[i];
-      h1 += r[kLevel3 + i];
-    }
-    s_l3[2 * threadIdx.x] = h0;
-    s_l3[2 * threadIdx.x + 1] = h1;
-    // level-2 mass: the 8 consecutive threads of one 256-token block
-    float m2 = h0 + h1;
-    m2 += __shfl_xor_sync(kFull, m2, 1);
-    m2 += __shfl_xor_sync(kFull, m2, 2);
-    m2 += __shfl_xor_sync(kFull, m2, 4);
-    if ((threadIdx.x & 7) == 0) s_l2[threadIdx.x >> 3] = m2;
+    for (int i = 0; i < kSegTok; ++i) h += r[i];
+    s_l3[threadIdx.x] = h;
+    float m2 = h;  // level-2 mass: the 16 consecutive threads of one 256-token block
+#pragma unroll
+    for (int o = 1; o < kLevel2 / kLevel3; o <<= 1) m2 += __shfl_xor_sync(kFull, m2, o);
+    if ((threadIdx.x & (kLevel2 / kLevel3 - 1)) == 0) s_l2[threadIdx.x / (kLevel2 / kLevel3)] = m2;
     __syncthreads();
     if (threadIdx.x < 32) {
       // a chosen block has mass > 0, so each level below finds a sub-block
@@ -266,11 +287,10 @@ __global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kThread
       }
     }
     __syncthreads();
-    // the 16 token masses of the chosen level-3 block live in one thread
-    const int blk3 = s_g2 * (kLevel2 / kLevel3) + s_g3;   // level-3 block within the level-1 block
-    if (threadIdx.x == (blk3 >> 1)) {
+    const int blk3 = s_g2 * (kLevel2 / kLevel3) + s_g3;  // level-3 block = thread index
+    if (threadIdx.x == blk3) {
 #pragma unroll
-      for (int i = 0; i < kLevel3; ++i) s_l4[i] = (blk3 & 1) ? r[kLevel3 + i] : r[i];
+      for (int i = 0; i < kLevel3; ++i) s_l4[i] = r[i];
     }
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -293,14 +313,14 @@ cudaError_t launch_sample(int dtype, bool vec, const Problem& p, const Workspace
   const dim3 grid(static_cast<unsigned>(blocks));
   if (dtype == 1) {
     if (vec)
-      sample_kernel<__nv_bfloat16, true><<<grid, kThreads, 0, s>>>(p, w);
+      sample_kernel<__nv_bfloat16, true><<<grid, kST, 0, s>>>(p, w);
     else
-      sample_kernel<__nv_bfloat16, false><<<grid, kThreads, 0, s>>>(p, w);
+      sample_kernel<__nv_bfloat16, false><<<grid, kST, 0, s>>>(p, w);
   } else {
     if (vec)
-      sample_kernel<float, true><<<grid, kThreads, 0, s>>>(p, w);
+      sample_kernel<float, true><<<grid, kST, 0, s>>>(p, w);
     else
-      sample_kernel<float, false><<<grid, kThreads, 0, s>>>(p, w);
+      sample_kernel<float, false><<<grid, kST, 0, s>>>(p, w);
   }
   return cudaGetLastError();
 }

@@ -108,49 +108,6 @@ __device__ __forceinline__ RowMax merge_greedy(At at, int n) {
   return r;
 }
 
-// Where the partials of row `slot` of request b live, for either layout.
-struct RowParts {
-  const Partial* base;  // span layout: partials of the row, contiguous
-  int n;                // number of partials
-  unsigned long long first, rq;  // stream layout: first range, row start / range bytes
-  unsigned long long rb;
-  bool stream;
-  __device__ __forceinline__ const Partial* operator()(int i) const {
-    if (!stream) return base + i;
-    const unsigned long long rho = first + static_cast<unsigned long long>(i);
-    return base + 2 * rho + (rho * rb < rq ? 1 : 0);
-  }
-};
-
-template <typename T>
-__device__ __forceinline__ RowParts row_parts(const Problem& p, const Workspace& w, int b, int slot) {
-  RowParts r;
-  if (w.layout == kLayoutSpan) {
-    r.stream = false;
-    r.base = w.partials + (static_cast<size_t>(b) * (2 * p.N + 1) + slot) * w.S1;
-    r.n = w.S1;
-    return r;
-  }
-  r.stream = true;
-  r.base = w.partials;
-  const unsigned long long row_bytes = static_cast<unsigned long long>(p.V) * sizeof(T);
-  const unsigned long long total = static_cast<unsigned long long>(__ldcg(w.row_prefix + p.B)) * row_bytes;
-  r.rb = stream_range_bytes(total, row_bytes, static_cast<unsigned long long>(w.stream_warps));
-  const unsigned long long q = static_cast<unsigned long long>(__ldcg(w.row_prefix + b)) + slot;
-  r.rq = q * row_bytes;
-  r.first = r.rq / r.rb;
-  const unsigned long long last = (r.rq + row_bytes - 1) / r.rb;
-  r.n = static_cast<int>(last - r.first + 1);
-  return r;
-}
-
-// Error-free sum: s + e == a + b exactly.
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = a + b;
-  const float bb = s - a;
-  e = (a - (s - bb)) + (b - bb);
-}
-
 template <typename T>
 __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& w, int b,
                                              bool write_outputs, Job* job_out) {
@@ -169,7 +126,6 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
 
   const float t = p.temperature[b];
   const int mode = temp_mode(t);
-  const size_t trow = static_cast<size_t>(b) * (N + 1) + j;  // target row in its tensor
   int d = -1;
   float zd = 0.f, yd = 0.f;
   if (pos_thread) {
@@ -177,30 +133,26 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
     if (d < 0 || d >= V) {
       atomicOr(&s_bad_token, 1);
     } else if (mode == kModeSampled) {
-      if (w.layout == kLayoutStream) {
-        // the row-statistics pass stored the logits at the draft token
-        const float* tl = w.tok_logit + static_cast<size_t>(b) * (2 * N + 1);
-        zd = __ldcg(tl + j);
-        yd = __ldcg(tl + N + 1 + j);
-      } else {
-        zd = Elem<T>::load1(static_cast<const T*>(p.target) + trow * V + d);
-        yd = Elem<T>::load1(static_cast<const T*>(p.draft) + (static_cast<size_t>(b) * N + j) * V + d);
-      }
+      // the row-statistics pass stored the logits at the draft token
+      const float* tl = w.tok_logit + static_cast<size_t>(b) * (2 * N + 1);
+      zd = __ldcg(tl + j);
+      yd = __ldcg(tl + N + 1 + j);
     }
   }
   RowNorm q{}, pn{};
   RowMax g{};
+  const int S1 = w.S1;
+  const Partial* req_parts = w.partials + static_cast<size_t>(b) * (2 * N + 1) * S1;
+  const Partial* tparts = req_parts + static_cast<size_t>(j) * S1;
+  const Partial* dparts = req_parts + static_cast<size_t>(N + 1 + j) * S1;
   if (mode == kModeGreedy && row_thread) {
-    const RowParts tp = row_parts<T>(p, w, b, j);
-    g = merge_greedy(tp, tp.n);
+    g = merge_greedy([&](int i) { return tparts + i; }, S1);
     if (!g.ok) atomicOr(&s_bad_logit, 1);
   } else if (mode == kModeSampled && row_thread) {
-    const RowParts tp = row_parts<T>(p, w, b, j);
-    q = merge_sampled(tp, tp.n);
+    q = merge_sampled([&](int i) { return tparts + i; }, S1);
     if (!q.ok) atomicOr(&s_bad_logit, 1);
     if (pos_thread) {
-      const RowParts dp = row_parts<T>(p, w, b, N + 1 + j);
-      pn = merge_sampled(dp, dp.n);
+      pn = merge_sampled([&](int i) { return dparts + i; }, S1);
       if (!pn.ok) atomicOr(&s_bad_logit, 1);
     }
   }
@@ -274,17 +226,8 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
     job.k = k;
     job.cq = q.c;
     job.inv_sq = 1.f / q.s;
-    // log2 Z_q - log2 Z_p = (c_q - c_p) + log2(s_q / s_p) as a float pair,
-    // so that log2(q_t / p_t) keeps its precision when q_t and p_t are close
-    float hi = 0.f, lo = 0.f;
-    if (a < N) {
-      float d1, e1, e2;
-      two_sum(q.c, -pn.c, d1, e1);
-      two_sum(d1, log2f(q.s / pn.s), hi, e2);
-      lo = e1 + e2;
-    }
-    job.dhi = hi;
-    job.dlo = lo;
+    job.cp = a < N ? pn.c : 0.f;
+    job.inv_sp = a < N ? 1.f / pn.s : 0.f;
     *job_out = job;
     if (write_outputs) {
       p.out_accept[b] = a;
