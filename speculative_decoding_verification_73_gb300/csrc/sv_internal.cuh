@@ -26,7 +26,7 @@ constexpr int kLevel1 = 8192;           // tokens per level-1 block of the group
 constexpr int kLevel2 = 256;            // tokens per level-2 block
 constexpr int kLevel3 = 16;             // tokens per level-3 block
 constexpr int kSampleCluster = 8;       // sampler: CTAs (one cluster) per request
-constexpr int kSampleThreads = 512;     // sampler: threads per CTA
+constexpr int kSampleThreads = 256;     // sampler: threads per CTA
 // The walk runs on a sampler CTA, one thread per row of a request, so
 // N + 1 <= kSampleThreads (the API caps N at 255).
 

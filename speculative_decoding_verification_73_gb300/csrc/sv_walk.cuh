@@ -126,18 +126,18 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
 
   const float t = p.temperature[b];
   const int mode = temp_mode(t);
+  // Every load the walk needs is issued here, before any of them is used:
+  // the draft token, the logits at it that the row-statistics pass stored
+  // (meaningful only for a sampled request with a valid token), and, in the
+  // merges below, the rows' partials.
   int d = -1;
   float zd = 0.f, yd = 0.f;
   if (pos_thread) {
+    const float* tl = w.tok_logit + static_cast<size_t>(b) * (2 * N + 1);
     d = p.tokens[static_cast<size_t>(b) * N + j];
-    if (d < 0 || d >= V) {
-      atomicOr(&s_bad_token, 1);
-    } else if (mode == kModeSampled) {
-      // the row-statistics pass stored the logits at the draft token
-      const float* tl = w.tok_logit + static_cast<size_t>(b) * (2 * N + 1);
-      zd = __ldcg(tl + j);
-      yd = __ldcg(tl + N + 1 + j);
-    }
+    zd = __ldcg(tl + j);
+    yd = __ldcg(tl + N + 1 + j);
+    if (d < 0 || d >= V) atomicOr(&s_bad_token, 1);
   }
   RowNorm q{}, pn{};
   RowMax g{};
