@@ -55,6 +55,8 @@ extern "C" {
 #define SV_EBADLOGIT   4  /* device check: a row that is read holds NaN or +inf,
                              or all of its entries are -inf                    */
 #define SV_ECUDA       5  /* a CUDA runtime call failed                        */
+#define SV_ESCRATCH    6  /* spec_verify_noalloc: the problem's working memory
+                             exceeds SV_NOALLOC_SCRATCH_BYTES                  */
 
 /* Bits of the device error word (spec_verify_get_error).  A request that
  * fails a device check gets out_tokens = -1 everywhere, out_accept_len = -1
@@ -120,6 +122,51 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V,
                 const int32_t* draft_tokens, const float* temperature,
                 uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len,
                 int32_t* out_kv_len);
+
+/*
+ * spec_verify_noalloc -- the same verify step as spec_verify, for callers
+ * that may not allocate device memory while they run (for instance a
+ * serving runtime that has handed all of HBM to its own KV-cache and
+ * activation pools, or that cannot afford the device-wide synchronisation
+ * of a cudaMalloc / cudaFree inside its decode loop).  The method itself
+ * has no counterpart to this entry point: it exists only for that kind of
+ * caller.
+ *
+ * No context: the call takes B, N, V, dtype (SV_F32 or SV_BF16) and the
+ * stream directly; the tensors, seed and outputs are exactly those of
+ * spec_verify and the results are identical to a spec_verify call with the
+ * same inputs.  The library allocates nothing: the working memory comes
+ * from one static device array of SV_NOALLOC_SCRATCH_BYTES bytes in the
+ * library, and the call makes no cudaMalloc, cudaFree or other allocating
+ * call.  The working memory is about
+ *     B (2N+1) (16 ceil(V / C) + 8) + B (4 ceil(V / 8192) + 4 N)  bytes,
+ * C = 32768 elements for bfloat16 and 16384 for float32 logits (plus
+ * 256-byte alignment of each part); problems that need more are refused
+ * with SV_ESCRATCH before anything is enqueued.  B = 64 requests with
+ * N = 7 drafts over V = 128256 bfloat16 logits need about 75 KB.
+ *
+ * Set-up: the first call on a device (with that device current) looks up
+ * the array's device address with cudaGetSymbolAddress and caches it for
+ * that device; make that first call before any stream capture starts.
+ *
+ * Sharing: all calls on a device use the same array.  Calls must be ordered
+ * (one stream, or streams ordered by events): two calls whose kernels
+ * overlap corrupt each other's results.  Each call clears its device error
+ * word before its kernels run; device-detected input errors are reported in
+ * the request's outputs only (out_tokens -1, out_accept_len -1,
+ * out_kv_len 0; see SV_ERRBIT_*), since there is no context to read them
+ * from.
+ *
+ * Returns SV_OK, SV_EINVAL (nothing enqueued), SV_ESCRATCH (nothing
+ * enqueued) or SV_ECUDA.
+ */
+#define SV_NOALLOC_SCRATCH_BYTES (1u << 20)
+int spec_verify_noalloc(int B, int N, int V, int dtype,
+                        const void* target_logits, const void* draft_logits,
+                        const int32_t* draft_tokens, const float* temperature,
+                        uint64_t seed, int32_t* out_tokens,
+                        int32_t* out_accept_len, int32_t* out_kv_len,
+                        void* cuda_stream);
 
 /*
  * spec_verify_get_error -- wait for the context's stream, then return the

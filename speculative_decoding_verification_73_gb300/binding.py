@@ -14,11 +14,12 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 
-SV_OK, SV_EINVAL, SV_EBADTEMP, SV_EBADTOKEN, SV_EBADLOGIT, SV_ECUDA = range(6)
+SV_OK, SV_EINVAL, SV_EBADTEMP, SV_EBADTOKEN, SV_EBADLOGIT, SV_ECUDA, SV_ESCRATCH = range(7)
 SV_ERRBIT_TEMP, SV_ERRBIT_TOKEN, SV_ERRBIT_LOGIT = 1, 2, 4
 SV_F32, SV_BF16 = 0, 1
 SV_NUM_KERNELS = 2
 SV_MAX_N = 255
+SV_NOALLOC_SCRATCH_BYTES = 1 << 20
 KERNEL_NAMES = ("rowstats_walk", "sample")
 
 _DTYPE_CODE = {torch.float32: SV_F32, torch.bfloat16: SV_BF16}
@@ -28,6 +29,7 @@ EXPORTS = (
     "spec_verify_init", "spec_verify", "spec_verify_get_error", "spec_verify_debug_stats",
     "spec_verify_profile", "spec_verify_profile_read", "spec_verify_launches_per_call",
     "spec_verify_debug_philox", "spec_verify_destroy", "spec_verify_strerror",
+    "spec_verify_noalloc",
 )
 
 _lib = None
@@ -61,6 +63,8 @@ def load():
     lib.spec_verify_launches_per_call.argtypes = []
     lib.spec_verify_debug_philox.argtypes = [c_u64, c_void, c_void, c_int, c_void]
     lib.spec_verify_destroy.argtypes = [c_void]
+    lib.spec_verify_noalloc.argtypes = [c_int, c_int, c_int, c_int, c_void, c_void, c_void, c_void,
+                                        c_u64, c_void, c_void, c_void, c_void]
     lib.spec_verify_strerror.argtypes = [c_int]
     lib.spec_verify_strerror.restype = ctypes.c_char_p
     for name in EXPORTS:
@@ -134,6 +138,31 @@ def spec_verify(ctx, target_logits, draft_logits, draft_tokens, temperature, see
                               _ptr(draft_logits), _ptr(draft_tokens), _ptr(temperature),
                               ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF), _ptr(out_tokens),
                               _ptr(out_accept_len), _ptr(out_kv_len)), "spec_verify")
+
+
+def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, temperature, seed,
+                        out_tokens, out_accept_len, out_kv_len, stream=None):
+    """The verify step through the library's static scratch array: no context
+    and no device allocation by the library (the caller owns every tensor).
+    Enqueued on ``stream`` (default: torch's current stream).  Raises
+    SpecVerifyError with code SV_ESCRATCH when the problem's working memory
+    exceeds SV_NOALLOC_SCRATCH_BYTES."""
+    B, n1, V = target_logits.shape
+    logit_dt = (torch.float32, torch.bfloat16)
+    _require(target_logits, "target_logits", (B, n1, V), logit_dt)
+    if n1 > 1:
+        _require(draft_logits, "draft_logits", (B, n1 - 1, V), (target_logits.dtype,))
+        _require(draft_tokens, "draft_tokens", (B, n1 - 1), (torch.int32,))
+    _require(temperature, "temperature", (B,), (torch.float32,))
+    _require(out_tokens, "out_tokens", (B, n1), (torch.int32,))
+    _require(out_accept_len, "out_accept_len", (B,), (torch.int32,))
+    _require(out_kv_len, "out_kv_len", (B,), (torch.int32,))
+    _check(load().spec_verify_noalloc(int(B), int(n1 - 1), int(V), _DTYPE_CODE[target_logits.dtype],
+                                      _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens),
+                                      _ptr(temperature),
+                                      ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF),
+                                      _ptr(out_tokens), _ptr(out_accept_len), _ptr(out_kv_len),
+                                      _stream_handle(stream)), "spec_verify_noalloc")
 
 
 def spec_verify_get_error(ctx):

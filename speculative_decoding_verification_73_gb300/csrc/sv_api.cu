@@ -79,6 +79,9 @@ const char* spec_verify_strerror(int code) {
     case SV_EBADTOKEN: return "a draft token is outside [0, V)";
     case SV_EBADLOGIT: return "a logit row holds NaN or +inf, or has no finite entry";
     case SV_ECUDA: return "a CUDA runtime call failed";
+    case SV_ESCRATCH:
+      return "the problem needs more working memory than spec_verify_noalloc's static array "
+             "(SV_NOALLOC_SCRATCH_BYTES) holds";
     default: return "unknown error code";
   }
 }
