@@ -196,9 +196,9 @@ int spec_verify_debug_stats(spec_verify_ctx* ctx, int B, int N,
  * stream.  spec_verify_profile_read waits for the stream and returns, for
  * the calls since the last read, the summed device time in milliseconds of
  * each of the SV_NUM_KERNELS kernels and the number of calls; it then
- * clears the sums.  Kernel 0 streams every logit row once (row statistics)
- * and runs each request's accept/reject walk as its last chunk finishes;
- * kernel 1 samples the correction / bonus tokens.
+ * clears the sums.  Kernel 0 streams every logit row once (row statistics
+ * and the draft tokens' logits); kernel 1 runs each request's accept/reject
+ * walk and samples its correction or bonus token.
  */
 #define SV_NUM_KERNELS 2
 int spec_verify_profile(spec_verify_ctx* ctx, int enable);

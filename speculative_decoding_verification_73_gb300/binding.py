@@ -20,7 +20,7 @@ SV_F32, SV_BF16 = 0, 1
 SV_NUM_KERNELS = 2
 SV_MAX_N = 255
 SV_NOALLOC_SCRATCH_BYTES = 1 << 20
-KERNEL_NAMES = ("rowstats_walk", "sample")
+KERNEL_NAMES = ("rowstats", "sample")
 
 _DTYPE_CODE = {torch.float32: SV_F32, torch.bfloat16: SV_BF16}
 
