@@ -139,11 +139,11 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V,
  * from one static device array of SV_NOALLOC_SCRATCH_BYTES bytes in the
  * library, and the call makes no cudaMalloc, cudaFree or other allocating
  * call.  The working memory is about
- *     B (2N+1) (16 ceil(V / C) + 8) + B (4 ceil(V / 8192) + 4 N)  bytes,
+ *     B (2N+1) (16 ceil(V / C) + 8) + B (8 ceil(V / 8192) + 4 N + 4)  bytes,
  * C = 32768 elements for bfloat16 and 16384 for float32 logits (plus
  * 256-byte alignment of each part); problems that need more are refused
  * with SV_ESCRATCH before anything is enqueued.  B = 64 requests with
- * N = 7 drafts over V = 128256 bfloat16 logits need about 75 KB.
+ * N = 7 drafts over V = 128256 bfloat16 logits need about 80 KB.
  *
  * Set-up: the first call on a device (with that device current) looks up
  * the array's device address with cudaGetSymbolAddress and caches it for
@@ -152,7 +152,7 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V,
  * Sharing: all calls on a device use the same array.  Calls must be ordered
  * (one stream, or streams ordered by events): two calls whose kernels
  * overlap corrupt each other's results.  Each call clears its device error
- * word before its kernels run; device-detected input errors are reported in
+ * word and its sampling counters before its kernels run; device-detected input errors are reported in
  * the request's outputs only (out_tokens -1, out_accept_len -1,
  * out_kv_len 0; see SV_ERRBIT_*), since there is no context to read them
  * from.
@@ -191,17 +191,21 @@ int spec_verify_debug_stats(spec_verify_ctx* ctx, int B, int N,
                             float* accept_prob, float* log_z);
 
 /*
- * Kernel timing for benchmarks.  With profiling on, every spec_verify call
- * records CUDA events around each kernel it launches on the context's
- * stream.  spec_verify_profile_read waits for the stream and returns, for
- * the calls since the last read, the summed device time in milliseconds of
- * each of the SV_NUM_KERNELS kernels and the number of calls; it then
- * clears the sums.  Kernel 0 streams every logit row once (row statistics
+ * Kernel timing for benchmarks.  spec_verify_profile(ctx, every) with
+ * every > 0 makes every every-th spec_verify call (the first, then each
+ * every-th after it; 1 = all calls) record CUDA events around each kernel
+ * it launches on the context's stream; every == 0 turns this off, and a
+ * negative value is SV_EINVAL.  Events between the two kernels keep them
+ * from overlapping, so recording a sample of the calls disturbs a timed
+ * loop less.  spec_verify_profile_read waits for the stream and returns, for
+ * the recorded calls since the last read, the summed device time in
+ * milliseconds of each of the SV_NUM_KERNELS kernels and the number of
+ * recorded calls; it then clears the sums.  Kernel 0 streams every logit row once (row statistics
  * and the draft tokens' logits); kernel 1 runs each request's accept/reject
  * walk and samples its correction or bonus token.
  */
 #define SV_NUM_KERNELS 2
-int spec_verify_profile(spec_verify_ctx* ctx, int enable);
+int spec_verify_profile(spec_verify_ctx* ctx, int every);
 int spec_verify_profile_read(spec_verify_ctx* ctx, double* ms_per_kernel,
                              int* calls);
 

@@ -183,12 +183,14 @@ def spec_verify_debug_stats(ctx, B, N, device=None):
     return acc, lz
 
 
-def spec_verify_profile(ctx, enable):
-    _check(load().spec_verify_profile(ctx, int(bool(enable))), "spec_verify_profile")
+def spec_verify_profile(ctx, every):
+    """Record kernel events on every ``every``-th call (True = 1 = all calls;
+    0 or False = off)."""
+    _check(load().spec_verify_profile(ctx, int(every)), "spec_verify_profile")
 
 
 def spec_verify_profile_read(ctx):
-    """({kernel name: summed ms}, calls) since the last read."""
+    """({kernel name: summed ms}, recorded calls) since the last read."""
     ms = (ctypes.c_double * SV_NUM_KERNELS)()
     calls = ctypes.c_int(0)
     _check(load().spec_verify_profile_read(ctx, ms, ctypes.byref(calls)), "spec_verify_profile_read")

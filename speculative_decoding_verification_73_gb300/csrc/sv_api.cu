@@ -19,7 +19,8 @@ struct spec_verify_ctx {
   void* ws;  // one cudaMalloc holding the whole workspace
   sv::Workspace w;
   // profiling
-  bool profile;
+  int profile_every;                // record every n-th call (0 = off)
+  long long profile_seen;           // calls since profiling was turned on
   std::vector<cudaEvent_t> events;  // SV_NUM_KERNELS + 1 per recorded call
   int recorded;                     // calls whose events are in `events`
   double ms[SV_NUM_KERNELS];
@@ -116,9 +117,13 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   off = align_up(off + rows * sizeof(float), 256);
   const size_t o_sums = off;
   off = align_up(off + static_cast<size_t>(max_B) * s3 * sizeof(float), 256);
+  const size_t o_btok = off;
+  off = align_up(off + static_cast<size_t>(max_B) * s3 * sizeof(int), 256);
   const size_t o_err = off;
   off = align_up(off + sizeof(unsigned), 256);
-  const size_t zero_bytes = off - o_err;  // the error word starts at zero
+  const size_t o_arr = off;
+  off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
+  const size_t zero_bytes = off - o_err;  // the error word and arrival counters start at zero
   const size_t o_acc = off;
   off = align_up(off + static_cast<size_t>(max_B) * (max_N > 0 ? max_N : 1) * sizeof(float), 256);
   const size_t o_lz = off;
@@ -131,7 +136,9 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   ctx->w.partials = reinterpret_cast<sv::Partial*>(base + o_part);
   ctx->w.tok_logit = reinterpret_cast<float*>(base + o_tok);
   ctx->w.chunk_sums = reinterpret_cast<float*>(base + o_sums);
+  ctx->w.blk_tok = reinterpret_cast<int*>(base + o_btok);
   ctx->w.err = reinterpret_cast<unsigned*>(base + o_err);
+  ctx->w.arrivals = reinterpret_cast<unsigned*>(base + o_arr);
   ctx->w.dbg_accept = reinterpret_cast<float*>(base + o_acc);
   ctx->w.dbg_logz = reinterpret_cast<float*>(base + o_lz);
   if (cudaMemsetAsync(base + o_err, 0, zero_bytes, ctx->stream) != cudaSuccess ||
@@ -177,7 +184,7 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
   w.S3 = ceil_div(V, sv::sample_chunk_elems(ctx->dtype));
 
   cudaEvent_t* ev = nullptr;
-  if (ctx->profile) {
+  if (ctx->profile_every > 0 && (ctx->profile_seen++ % ctx->profile_every) == 0) {
     ev = profile_slot(ctx);
     if (ev == nullptr) return SV_ECUDA;
     if (cudaEventRecord(ev[0], ctx->stream) != cudaSuccess) return SV_ECUDA;
@@ -222,10 +229,11 @@ int spec_verify_debug_stats(spec_verify_ctx* ctx, int B, int N, float* accept_pr
   return SV_OK;
 }
 
-int spec_verify_profile(spec_verify_ctx* ctx, int enable) {
-  if (ctx == nullptr) return SV_EINVAL;
-  if (!enable && ctx->profile && flush_profile(ctx) != SV_OK) return SV_ECUDA;
-  ctx->profile = enable != 0;
+int spec_verify_profile(spec_verify_ctx* ctx, int every) {
+  if (ctx == nullptr || every < 0) return SV_EINVAL;
+  if (every == 0 && ctx->profile_every > 0 && flush_profile(ctx) != SV_OK) return SV_ECUDA;
+  ctx->profile_every = every;
+  ctx->profile_seen = 0;
   return SV_OK;
 }
 

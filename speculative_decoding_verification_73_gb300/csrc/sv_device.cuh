@@ -12,6 +12,20 @@ namespace sv {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// ------------------------------------------------- dependent launches
+// Programmatic dependent launch (PTX griddepcontrol).  A kernel launched
+// with the programmatic-serialisation attribute may start while the kernel
+// before it in the stream is still running; it must call
+// wait_for_prerequisite() before touching anything that kernel writes (the
+// call returns once that grid has completed and its writes are visible, and
+// at once when there is no such dependency).  allow_dependents() lets the
+// dependent grid be scheduled as soon as every CTA of this grid has made
+// the call or exited.
+__device__ __forceinline__ void wait_for_prerequisite() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ---------------------------------------------------------------- numbers
 
 // 2^x on the SFU (PTX ex2.approx.ftz.f32): results below 2^-126 flush to 0,

@@ -25,8 +25,7 @@ constexpr int kSpanMinBlocks = SV_SPAN_MINB;   // resident CTAs per SM the kerne
 constexpr int kLevel1 = 8192;           // tokens per level-1 block of the grouped inverse CDF
 constexpr int kLevel2 = 256;            // tokens per level-2 block
 constexpr int kLevel3 = 16;             // tokens per level-3 block
-constexpr int kSampleCluster = 8;       // sampler: CTAs (one cluster) per request
-constexpr int kSampleThreads = 256;     // sampler: threads per CTA
+constexpr int kSampleThreads = 256;     // sampler: threads per CTA (one CTA per level-1 block)
 // The walk runs on a sampler CTA, one thread per row of a request, so
 // N + 1 <= kSampleThreads (the API caps N at 255).
 
@@ -81,7 +80,9 @@ struct Workspace {
   Partial* partials;     // [B][2N+1][S1]: target rows 0..N, then draft rows 0..N-1
   float* tok_logit;      // [B][2N+1]: logit at the row's draft token (sampled rows)
   float* chunk_sums;     // [B, S3]: residual mass of each level-1 block
-  unsigned* err;         // [1], OR of kErr* bits
+  int* blk_tok;          // [B, S3]: the token each level-1 block would give
+  unsigned* err;         // [1], OR of kErr* bits (starts at zero)
+  unsigned* arrivals;    // [B]: sampler CTAs done per request (zero between calls)
   float* dbg_accept;     // [B, N]
   float* dbg_logz;       // [B, 2N+1]
   int S1;                // spans per row for this call's V

@@ -9,20 +9,20 @@
 // whose creation allocates the workspace.
 //
 // How: the working memory of one call (row-statistics partials, token
-// logits, level-1 masses of the sampler, the error word and the debug
-// statistics) lives in g_scratch, a file-scope device array of
-// SV_NOALLOC_SCRATCH_BYTES that exists in every device's copy of the
-// module.  Host code cannot use the array's name as a device pointer, so
+// logits, the sampler's per-block masses, candidates and arrival counters,
+// the error word and the debug statistics) lives in g_scratch, a file-scope
+// device array of SV_NOALLOC_SCRATCH_BYTES that exists in every device's
+// copy of the module.  Host code cannot use the array's name as a device pointer, so
 // the first call on each device (with that device current) asks the runtime
 // for its address with cudaGetSymbolAddress and caches it; later calls on
 // that device reuse the cached pointer.  Problems whose working memory does
 // not fit are refused with SV_ESCRATCH before anything is enqueued.
 //
 // Sharing: every call on a device uses the same array.  Only the error word
-// has to start at zero; each call clears it on its stream before its
-// kernels run.  Two calls whose kernels overlap in time (different streams
-// without ordering between them, or host threads racing on one stream)
-// corrupt each other's scratch and results.
+// and the arrival counters have to start at zero; each call clears them on
+// its stream before its kernels run.  Two calls whose kernels overlap in
+// time (different streams without ordering between them, or host threads
+// racing on one stream) corrupt each other's scratch and results.
 
 #include <cstdint>
 #include <mutex>
@@ -51,7 +51,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // Byte offsets of the workspace parts inside g_scratch for one problem; the
 // same order and 256-byte alignment as the context workspace.
 struct Carve {
-  size_t part, tok, sums, err, acc, logz, end;
+  size_t part, tok, sums, btok, err, arr, acc, logz, end;
 };
 
 Carve carve(size_t B, size_t N, int s1, int s3) {
@@ -64,8 +64,12 @@ Carve carve(size_t B, size_t N, int s1, int s3) {
   off = align_up(off + rows * sizeof(float), 256);
   c.sums = off;
   off = align_up(off + B * s3 * sizeof(float), 256);
+  c.btok = off;
+  off = align_up(off + B * s3 * sizeof(int), 256);
   c.err = off;
   off = align_up(off + sizeof(unsigned), 256);
+  c.arr = off;
+  off = align_up(off + B * sizeof(unsigned), 256);
   c.acc = off;
   off = align_up(off + B * (N > 0 ? N : 1) * sizeof(float), 256);
   c.logz = off;
@@ -115,7 +119,9 @@ int spec_verify_noalloc(int B, int N, int V, int dtype, const void* target_logit
   w.partials = reinterpret_cast<sv::Partial*>(base + c.part);
   w.tok_logit = reinterpret_cast<float*>(base + c.tok);
   w.chunk_sums = reinterpret_cast<float*>(base + c.sums);
+  w.blk_tok = reinterpret_cast<int*>(base + c.btok);
   w.err = reinterpret_cast<unsigned*>(base + c.err);
+  w.arrivals = reinterpret_cast<unsigned*>(base + c.arr);
   w.dbg_accept = reinterpret_cast<float*>(base + c.acc);
   w.dbg_logz = reinterpret_cast<float*>(base + c.logz);
 
@@ -135,7 +141,8 @@ int spec_verify_noalloc(int B, int N, int V, int dtype, const void* target_logit
   const bool vec = (static_cast<size_t>(V) * esize) % 16 == 0 && aligned16(target_logits) &&
                    (N == 0 || aligned16(draft_logits));
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  if (cudaMemsetAsync(w.err, 0, sizeof(unsigned), s) != cudaSuccess) return SV_ECUDA;
+  // the error word and the sampler's arrival counters start at zero
+  if (cudaMemsetAsync(base + c.err, 0, c.acc - c.err, s) != cudaSuccess) return SV_ECUDA;
   if (sv::launch_rowstats(dtype, vec, p, w, s) != cudaSuccess) return SV_ECUDA;
   if (sv::launch_sample(dtype, vec, p, w, s) != cudaSuccess) return SV_ECUDA;
   return SV_OK;

@@ -222,6 +222,7 @@ __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int e
 
 template <typename T, bool kVecPath>
 __global__ void __launch_bounds__(kThreads, kSpanMinBlocks) rowstats_kernel(Problem p, Workspace w) {
+  allow_dependents();  // the sampler may be scheduled behind the last wave
   const int S1 = w.S1;
   const int per = 2 * p.N + 1;
   const int row = blockIdx.x / S1;
@@ -255,26 +256,23 @@ __global__ void __launch_bounds__(kThreads, kSpanMinBlocks) rowstats_kernel(Prob
   if (threadIdx.x == 0) w.partials[static_cast<size_t>(row) * S1 + span] = out;
 }
 
+template <typename T, bool kVecPath>
+cudaError_t launch_rowstats_t(const Problem& p, const Workspace& w, cudaStream_t s) {
+  const long long blocks = static_cast<long long>(p.B) * (2 * p.N + 1) * w.S1;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  rowstats_kernel<T, kVecPath><<<dim3(static_cast<unsigned>(blocks)), kThreads, 0, s>>>(p, w);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_rowstats(int dtype, bool vec, const Problem& p, const Workspace& w,
                             cudaStream_t s) {
-  const long long blocks = static_cast<long long>(p.B) * (2 * p.N + 1) * w.S1;
-  if (blocks <= 0) return cudaSuccess;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const dim3 grid(static_cast<unsigned>(blocks));
-  if (dtype == 1) {
-    if (vec)
-      rowstats_kernel<__nv_bfloat16, true><<<grid, kThreads, 0, s>>>(p, w);
-    else
-      rowstats_kernel<__nv_bfloat16, false><<<grid, kThreads, 0, s>>>(p, w);
-  } else {
-    if (vec)
-      rowstats_kernel<float, true><<<grid, kThreads, 0, s>>>(p, w);
-    else
-      rowstats_kernel<float, false><<<grid, kThreads, 0, s>>>(p, w);
-  }
-  return cudaGetLastError();
+  if (dtype == 1)
+    return vec ? launch_rowstats_t<__nv_bfloat16, true>(p, w, s)
+               : launch_rowstats_t<__nv_bfloat16, false>(p, w, s);
+  return vec ? launch_rowstats_t<float, true>(p, w, s) : launch_rowstats_t<float, false>(p, w, s);
 }
 
 }  // namespace sv

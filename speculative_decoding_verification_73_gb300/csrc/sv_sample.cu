@@ -1,5 +1,5 @@
-// The accept/reject walk and the correction / bonus sampling, touching only
-// the one row (or row pair) per request that the walk selected.
+// The correction / bonus sampling, touching only the one row (or row pair)
+// per request that the accept/reject walk selected.
 //
 // "Speculative Decoding and EAGLE-3" lesson, "Invariant: Leviathan rejection
 // sampling" and "Build it" step 2: after a rejection at position j the token
@@ -15,21 +15,18 @@
 // rounding leaves none).  The law is exactly r / sum(r), and every decision
 // compares a uniform against at most a few dozen float32 edges.
 //
-// Grid: one cluster of kSampleCluster CTAs of kSampleThreads threads per
-// request.  Every CTA first runs the request's accept/reject walk itself from
-// the row-statistics partials (cheap, and no CTA waits for another to get
-// it); rank 0 writes the walk's outputs.  For a sampled request each CTA then
-// takes level-1 blocks rank, rank + cluster, ...: thread t evaluates tokens
-// [32t, 32t + 32) of a block, which gives the block's level-3 masses (two per
-// thread), level-2 masses (eight threads) and level-1 mass (the CTA) in one
-// pass, kept in the CTA's shared memory.  After a cluster barrier rank 0 reads
-// the masses it needs from the owners' shared memory (distributed shared
-// memory), picks levels 1-3, re-evaluates only the 16 tokens of the chosen
-// level-3 block for level 4, and writes the token; a second cluster barrier
-// keeps the owners alive until then.  When a CTA owns more blocks than it can
-// keep (V > kSampleCluster * kKeepBlocks * 8192) or the residual has no mass,
-// rank 0 instead picks level 1 from masses in global memory and rescans the
-// chosen block itself.
+// Grid: one CTA per (request, level-1 block), request-major.  Every CTA runs
+// the request's accept/reject walk itself from the row-statistics partials
+// (one L2 round trip; CTA 0 of the request writes the walk's outputs).  For
+// a sampled request each CTA then evaluates r over its block (thread t takes
+// tokens [32t, 32t + 32): two level-3 masses per thread, a level-2 mass per
+// eight threads, the level-1 mass per CTA) and picks the block's candidate
+// token at levels 2-4 with u_2..u_4, as if level 1 had chosen this block.
+// It stores (level-1 mass, candidate) and counts itself in the request's
+// arrival counter; the CTA that arrives last picks level 1 over the blocks'
+// masses with u_1, writes the chosen block's candidate, and resets the
+// counter for the next call.  No CTA waits for another.  If the residual
+// has no mass anywhere, that last CTA redoes every block with q alone.
 //
 // r_t = max(q_t - p_t, 0) with q_t = 2^(z_t k - c_q) / s_q and likewise p_t,
 // evaluated two tokens at a time with the paired float instructions.  Its
@@ -50,32 +47,17 @@ constexpr int kSegTok = kLevel1 / kST;   // tokens per thread in a level-1 block
 constexpr int kL2 = kLevel1 / kLevel2;   // level-2 blocks per level-1 block (32)
 constexpr int kL3 = kLevel1 / kLevel3;   // level-3 blocks per level-1 block (512)
 constexpr int kL3PerL2 = kLevel2 / kLevel3;  // 16
-constexpr int kKeepBlocks = 4;           // level-1 blocks whose masses a CTA keeps
 static_assert(kSegTok == 2 * kLevel3, "two level-3 blocks per thread");
 
-__device__ __forceinline__ unsigned cluster_rank() {
-  unsigned r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
+// Level-1 blocks one CTA takes: their row pair is staged in shared memory
+// (64 KB either way), all of it requested at once.
+template <typename T>
+constexpr int blocks_per_cta() {
+  return sizeof(T) == 2 ? 2 : 1;
 }
-
-// Hardware barrier over all threads of all CTAs of the cluster; orders the
-// memory accesses before it (release) with those after it (acquire).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-
-// Load a float from the shared memory of CTA `rank` of this cluster, at the
-// place where `local` lives in this CTA's shared memory.
-__device__ __forceinline__ float ld_dsmem(const float* local, unsigned rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(remote)
-               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
+template <typename T>
+constexpr int stage_bytes() {
+  return 2 * blocks_per_cta<T>() * kLevel1 * static_cast<int>(sizeof(T));
 }
 
 __device__ __forceinline__ float cta_sum(float v, float* scratch) {
@@ -117,44 +99,12 @@ __device__ __forceinline__ void resid_vec(const uint4& zv, const uint4& yv, cons
   }
 }
 
-// Scalar form for rows that are not 16-byte aligned (same arithmetic).
+// Scalar form (rows that are not 16-byte aligned, and level 4): bit for bit
+// the value resid_vec gives the token.
 __device__ __forceinline__ float resid1(float zt, float yt, const Job& job, bool has_p) {
   const float q = ex2(fmaf(zt, job.k, -job.cq)) * job.inv_sq;
   if (!has_p) return q;
   return fmaxf(q - ex2(fmaf(yt, job.k, -job.cp)) * job.inv_sp, 0.f);
-}
-
-// r at tokens [t0, t0 + kSegTok) of the row pair (0 past cend): one thread's
-// contiguous share of a level-1 block.
-template <typename T, bool kVecPath>
-__device__ __forceinline__ void resid_seg(const T* z, const T* y, int t0, int cend, const Job& job,
-                                          bool has_p, float (&r)[kSegTok]) {
-  using E = Elem<T>;
-  if (kVecPath) {
-    constexpr int kVec = E::kVec;
-    const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
-    uint4 zv[kSegTok / kVec], yv[kSegTok / kVec];
-#pragma unroll
-    for (int i = 0; i < kSegTok / kVec; ++i) {
-      const int e0 = t0 + i * kVec;
-      const bool in = e0 < cend;
-      zv[i] = in ? __ldg(reinterpret_cast<const uint4*>(z + e0)) : pad;
-      yv[i] = (in && has_p) ? __ldg(reinterpret_cast<const uint4*>(y + e0)) : pad;
-    }
-#pragma unroll
-    for (int i = 0; i < kSegTok / kVec; ++i) {
-      float rv[kVec];
-      resid_vec<T>(zv[i], yv[i], job, has_p, rv);
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) r[i * kVec + e] = rv[e];
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < kSegTok; ++i) {
-      const int t = t0 + i;
-      r[i] = t < cend ? resid1(E::load1(z + t), has_p ? E::load1(y + t) : 0.f, job, has_p) : 0.f;
-    }
-  }
 }
 
 // The two level-3 masses of one thread's 32 tokens [t0, t0 + 32) (0 past
@@ -257,195 +207,280 @@ __device__ int warp_pick(Get get, int n, float u) {
   return last_pos;
 }
 
-template <typename T, bool kVecPath>
-__global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kST, 3)
-    sample_kernel(Problem p, Workspace w) {
+// 16-byte copy global -> shared that holds no register while in flight
+// (cached in L2 only); the issuing thread waits for its own copies with
+// cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// One element of a staged row (shared memory), as float.
+__device__ __forceinline__ float staged1(const float* p) { return *p; }
+__device__ __forceinline__ float staged1(const __nv_bfloat16* p) {
+  return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
+}
+
+// Stage this thread's tokens [32t, 32t + 32) of the level-1 block starting at
+// cbeg into sz / sy (block-relative); vectors at or past cend get -inf.
+template <typename T>
+__device__ __forceinline__ void stage_block(const T* z, const T* y, int cbeg, int cend, bool has_p,
+                                            T* sz, T* sy) {
   using E = Elem<T>;
-  __shared__ float red[kST / 32];
-  __shared__ float s_l1[kKeepBlocks];        // level-1 masses of the kept own blocks
-  __shared__ float s_l2[kKeepBlocks][kL2];   // their level-2 masses
-  __shared__ float s_l3[kKeepBlocks][kL3];   // their level-3 masses
-  __shared__ float s_l4[kLevel3];            // the chosen level-3 block's token masses
-  __shared__ int s_sel, s_g2, s_g3, s_tok;
+  constexpr int kVec = E::kVec;
+  const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+#pragma unroll
+  for (int i = 0; i < kSegTok / kVec; ++i) {
+    const int e = threadIdx.x * kSegTok + i * kVec;
+    if (cbeg + e < cend) {
+      cp_async16(sz + e, z + cbeg + e);
+      if (has_p) cp_async16(sy + e, y + cbeg + e);
+    } else {
+      *reinterpret_cast<uint4*>(sz + e) = pad;
+      if (has_p) *reinterpret_cast<uint4*>(sy + e) = pad;
+    }
+  }
+}
+
+// The two level-3 masses of this thread's 32 staged tokens.
+template <typename T>
+__device__ __forceinline__ void staged_halves(const T* sz, const T* sy, const Job& job, bool has_p,
+                                              float& h0, float& h1) {
+  using E = Elem<T>;
+  constexpr int kVec = E::kVec;
+  constexpr int kVecs = kSegTok / kVec;
+  h0 = 0.f;
+  h1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < kVecs; ++i) {
+    const int e = threadIdx.x * kSegTok + i * kVec;
+    const uint4 zv = *reinterpret_cast<const uint4*>(sz + e);
+    const uint4 yv = has_p ? *reinterpret_cast<const uint4*>(sy + e) : zv;
+    float rv[kVec];
+    resid_vec<T>(zv, yv, job, has_p, rv);
+    float part = 0.f;
+#pragma unroll
+    for (int q = 0; q < kVec; ++q) part += rv[q];
+    if (i < kVecs / 2)
+      h0 += part;
+    else
+      h1 += part;
+  }
+}
+
+struct BlockScratch {
+  float red[kST / 32];
+  float l2[kL2];      // level-2 masses of the block
+  float l3[kL3];      // level-3 masses of the block
+  float l4[kLevel3];  // token masses of the chosen level-3 block
+  int pick;
+  int tok;
+};
+
+// From each thread's two level-3 masses of the level-1 block
+// [cbeg, cbeg + kLevel1): the level-2 and level-1 masses (*mass), and the
+// token the grouped inverse CDF picks inside the block at levels 2-4
+// (u[1..3]), or -1 when the block has no mass.  r_at(t) re-evaluates r at
+// token t (cbeg <= t < cend) for level 4 with the same arithmetic.  Called
+// by the whole CTA.
+template <typename RAt>
+__device__ int block_pick(float h0, float h1, int cbeg, int cend, const Job& job, RAt r_at,
+                          BlockScratch& sc, float* mass) {
+  sc.l3[2 * threadIdx.x] = h0;
+  sc.l3[2 * threadIdx.x + 1] = h1;
+  float m2 = h0 + h1;  // level-2 mass: the 8 consecutive threads of a 256-token block
+#pragma unroll
+  for (int o = 1; o < kL3PerL2 / 2; o <<= 1) m2 += __shfl_xor_sync(kFull, m2, o);
+  if ((threadIdx.x & (kL3PerL2 / 2 - 1)) == 0) sc.l2[threadIdx.x / (kL3PerL2 / 2)] = m2;
+  *mass = cta_sum(h0 + h1, sc.red);  // its barriers also publish l2 and l3
+  if (threadIdx.x < 32) {
+    const int g2 = warp_pick([&](int i) { return sc.l2[i]; }, kL2, job.u[1]);
+    int pick = -1;
+    if (g2 >= 0) {
+      const int g3 = warp_pick([&](int i) { return sc.l3[g2 * kL3PerL2 + i]; }, kL3PerL2, job.u[2]);
+      pick = g2 * kL3PerL2 + max(g3, 0);
+    }
+    if (threadIdx.x == 0) sc.pick = pick;
+  }
+  __syncthreads();
+  const int blk3 = sc.pick;
+  if (blk3 < 0) return -1;  // CTA-uniform
+  const int t0 = cbeg + blk3 * kLevel3;
+  if (threadIdx.x < kLevel3) {
+    const int t = t0 + threadIdx.x;
+    sc.l4[threadIdx.x] = t < cend ? r_at(t) : 0.f;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int g4 = max(warp_pick([&](int i) { return sc.l4[i]; }, kLevel3, job.u[3]), 0);
+    if (threadIdx.x == 0) sc.tok = t0 + g4;
+  }
+  __syncthreads();
+  return sc.tok;
+}
+
+// Masses and candidate of one level-1 block read straight from global memory
+// (rows that are not 16-byte aligned, and the q-only redo).
+template <typename T, bool kVecPath>
+__device__ int block_candidate_global(const T* z, const T* y, int cbeg, int V, const Job& job,
+                                      bool has_p, BlockScratch& sc, float* mass) {
+  using E = Elem<T>;
+  const int cend = min(V, cbeg + kLevel1);
+  float h0, h1;
+  resid_halves<T, kVecPath>(z, y, cbeg + threadIdx.x * kSegTok, cend, job, has_p, h0, h1);
+  return block_pick(
+      h0, h1, cbeg, cend, job,
+      [&](int t) { return resid1(E::load1(z + t), has_p ? E::load1(y + t) : 0.f, job, has_p); }, sc,
+      mass);
+}
+
+template <typename T, bool kVecPath>
+__global__ void __launch_bounds__(kST, 3) sample_kernel(Problem p, Workspace w) {
+  constexpr int kB = blocks_per_cta<T>();
+  extern __shared__ __align__(16) unsigned char s_rows[];  // staged rows (vector path)
+  __shared__ BlockScratch sc;
   __shared__ Job s_job;
+  __shared__ int s_last;
   const int S3 = w.S3;
-  const int b = blockIdx.x / kSampleCluster;
-  const unsigned rank = cluster_rank();
-  // Only sampled requests need the other CTAs of the cluster (the choice is
-  // the same in every CTA of a cluster, so either all of them reach the
-  // cluster barriers below or none does); rank 0 writes the outputs.
-  if (rank != 0 && temp_mode(p.temperature[b]) != kModeSampled) return;
-  walk_request<T>(p, w, b, rank == 0, &s_job);
+  const int G = (S3 + kB - 1) / kB;  // CTAs per request
+  const int b = blockIdx.x / G;
+  const int g = blockIdx.x - b * G;
+  walk_request<T>(p, w, b, g == 0, &s_job);
   __syncthreads();
   const Job job = s_job;
-  if (job.kind == kJobNone) return;  // identical in every CTA of the cluster
+  if (job.kind == kJobNone) return;  // identical in every CTA of the request
   const int N = p.N, V = p.V;
   const T* z = static_cast<const T*>(p.target) + (static_cast<size_t>(b) * (N + 1) + job.row) * V;
   const T* y = job.kind == kJobResidual
                    ? static_cast<const T*>(p.draft) + (static_cast<size_t>(b) * N + job.row) * V
                    : z;
-  bool has_p = job.kind == kJobResidual;
-  float* sums = w.chunk_sums + static_cast<size_t>(b) * S3;
-  const bool keep_all = S3 <= kSampleCluster * kKeepBlocks;
+  const bool has_p = job.kind == kJobResidual;
+  float* masses = w.chunk_sums + static_cast<size_t>(b) * S3;
+  int* cands = w.blk_tok + static_cast<size_t>(b) * S3;
+  const int c0 = g * kB;
+  const int nb = min(kB, S3 - c0);
 
-  // One pass over this CTA's level-1 blocks: masses at all three levels.
-  int kept = 0;
-  for (int c = static_cast<int>(rank); c < S3; c += kSampleCluster, ++kept) {
-    const int cbeg = c * kLevel1;
-    float h0, h1;
-    resid_halves<T, kVecPath>(z, y, cbeg + threadIdx.x * kSegTok, min(V, cbeg + kLevel1), job, has_p,
-                              h0, h1);
-    float m2 = h0 + h1;  // level-2 mass: the 8 consecutive threads of a 256-token block
-#pragma unroll
-    for (int o = 1; o < kL3PerL2 / 2; o <<= 1) m2 += __shfl_xor_sync(kFull, m2, o);
-    const float m1 = cta_sum(h0 + h1, red);
-    if (keep_all) {
-      s_l3[kept][2 * threadIdx.x] = h0;
-      s_l3[kept][2 * threadIdx.x + 1] = h1;
-      if ((threadIdx.x & (kL3PerL2 / 2 - 1)) == 0) s_l2[kept][threadIdx.x / (kL3PerL2 / 2)] = m2;
-      if (threadIdx.x == 0) s_l1[kept] = m1;
-    } else if (threadIdx.x == 0) {
-      sums[c] = m1;
-    }
-  }
-  if (!keep_all) __threadfence();
-  cluster_sync();  // every owner's masses are in place
-  if (rank != 0) {
-    cluster_sync();  // stay resident until rank 0 has read them
-    return;
-  }
-
-  // ---- rank 0 of request b.
-  int sel = -1;
-  if (keep_all) {
-    if (threadIdx.x < 32) {
-      const int c1 = warp_pick(
-          [&](int c) { return ld_dsmem(&s_l1[c / kSampleCluster], c % kSampleCluster); }, S3, job.u[0]);
-      int g2 = -1, g3 = -1;
-      if (c1 >= 0) {
-        const unsigned own = c1 % kSampleCluster;
-        const int li = c1 / kSampleCluster;
-        g2 = max(warp_pick([&](int i) { return ld_dsmem(&s_l2[li][i], own); }, kL2, job.u[1]), 0);
-        g3 = max(warp_pick([&](int i) { return ld_dsmem(&s_l3[li][g2 * kL3PerL2 + i], own); }, kL3PerL2,
-                           job.u[2]),
-                 0);
-      }
+  if (kVecPath) {
+    T* sz = reinterpret_cast<T*>(s_rows);
+    T* sy = sz + kB * kLevel1;
+    for (int i = 0; i < nb; ++i)
+      stage_block<T>(z, y, (c0 + i) * kLevel1, V, has_p, sz + i * kLevel1, sy + i * kLevel1);
+    cp_async_wait_all();  // this thread's copies; it alone reads them before the barriers
+    for (int i = 0; i < nb; ++i) {
+      const int cbeg = (c0 + i) * kLevel1;
+      const T* bz = sz + i * kLevel1;
+      const T* by = sy + i * kLevel1;
+      float h0, h1, mass;
+      staged_halves<T>(bz, by, job, has_p, h0, h1);
+      const int cand = block_pick(
+          h0, h1, cbeg, min(V, cbeg + kLevel1), job,
+          [&](int t) {
+            return resid1(staged1(bz + (t - cbeg)), has_p ? staged1(by + (t - cbeg)) : 0.f, job, has_p);
+          },
+          sc, &mass);
       if (threadIdx.x == 0) {
-        s_sel = c1;
-        s_g2 = g2;
-        s_g3 = g3;
+        masses[c0 + i] = mass;
+        cands[c0 + i] = cand;
       }
     }
-    __syncthreads();
-    sel = s_sel;
+  } else {
+    for (int i = 0; i < nb; ++i) {
+      float mass;
+      const int cand = block_candidate_global<T, false>(z, y, (c0 + i) * kLevel1, V, job, has_p, sc, &mass);
+      if (threadIdx.x == 0) {
+        masses[c0 + i] = mass;
+        cands[c0 + i] = cand;
+      }
+    }
   }
-  cluster_sync();  // the owners may leave now
-  int token = 0;
-  if (keep_all && sel >= 0) {
-    // Level 4: the 16 tokens of the chosen level-3 block.
-    const int t0 = sel * kLevel1 + (s_g2 * kL3PerL2 + s_g3) * kLevel3;
-    if (threadIdx.x < kLevel3) {
-      const int t = t0 + threadIdx.x;
-      s_l4[threadIdx.x] = t < V ? resid1(E::load1(z + t), has_p ? E::load1(y + t) : 0.f, job, has_p) : 0.f;
+  if (threadIdx.x == 0) {
+    __threadfence();  // publish before counting in
+    const unsigned before = atomicAdd(w.arrivals + b, 1u);
+    s_last = before == static_cast<unsigned>(G - 1);
+    if (s_last) w.arrivals[b] = 0u;  // every CTA of the request has counted in
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();  // see the other CTAs' masses and candidates
+
+  // Level 1 over the blocks' masses; with at most 32 blocks lane i fetches
+  // block i's candidate together with its mass.
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int mine = (S3 <= 32 && lane < S3) ? __ldcg(cands + lane) : -1;
+    const int c1 = warp_pick([&](int i) { return __ldcg(masses + i); }, S3, job.u[0]);
+    const int tok = S3 <= 32 ? __shfl_sync(kFull, mine, c1 & 31) : (c1 >= 0 ? __ldcg(cands + c1) : 0);
+    if (lane == 0) {
+      sc.pick = c1;
+      sc.tok = tok;
+    }
+  }
+  __syncthreads();
+  int c1 = sc.pick;
+  if (c1 < 0 && has_p) {
+    // The residual has no mass anywhere: draw from q (same levels, same
+    // uniforms), every block redone by this CTA.
+    for (int cc = 0; cc < S3; ++cc) {
+      float mq;
+      const int cq = block_candidate_global<T, kVecPath>(z, z, cc * kLevel1, V, job, false, sc, &mq);
+      if (threadIdx.x == 0) {
+        masses[cc] = mq;
+        cands[cc] = cq;
+      }
     }
     __syncthreads();
     if (threadIdx.x < 32) {
-      const int g4 = max(warp_pick([&](int i) { return s_l4[i]; }, kLevel3, job.u[3]), 0);
-      if (threadIdx.x == 0) s_tok = t0 + g4;
+      const int cq1 = warp_pick([&](int i) { return __ldcg(masses + i); }, S3, job.u[0]);
+      if (threadIdx.x == 0) sc.tok = cq1 >= 0 ? __ldcg(cands + cq1) : 0;
     }
     __syncthreads();
-    token = s_tok;
-  } else {
-    // Level 1 from global masses (many blocks, or a residual without mass,
-    // which falls back to q), then a rescan of the chosen block.
-    if (keep_all) has_p = false;  // the residual had no mass
-    for (int pass = 0; pass < 2; ++pass) {
-      if (!keep_all || pass == 1) {
-        if (threadIdx.x < 32) {
-          const int s1 = warp_pick([&](int i) { return __ldcg(sums + i); }, S3, job.u[0]);
-          if (threadIdx.x == 0) s_sel = s1;
-        }
-        __syncthreads();
-        if (s_sel >= 0 || !has_p || pass == 1) break;
-      }
-      // q-only masses of every block (the residual had no mass)
-      has_p = false;
-      for (int c = 0; c < S3; ++c) {
-        const int cbeg = c * kLevel1;
-        float h0, h1;
-        resid_halves<T, kVecPath>(z, y, cbeg + threadIdx.x * kSegTok, min(V, cbeg + kLevel1), job,
-                                  false, h0, h1);
-        const float m1 = cta_sum(h0 + h1, red);
-        if (threadIdx.x == 0) sums[c] = m1;
-      }
-      __threadfence_block();
-    }
-    sel = s_sel;
-    if (sel >= 0) {
-      const int cbeg = sel * kLevel1;
-      float r[kSegTok];
-      resid_seg<T, kVecPath>(z, y, cbeg + threadIdx.x * kSegTok, min(V, cbeg + kLevel1), job, has_p, r);
-      float h0 = 0.f, h1 = 0.f;
-#pragma unroll
-      for (int i = 0; i < kLevel3; ++i) {
-        h0 += r[i];
-        h1 += r[kLevel3 + i];
-      }
-      s_l3[0][2 * threadIdx.x] = h0;
-      s_l3[0][2 * threadIdx.x + 1] = h1;
-      float m2 = h0 + h1;
-#pragma unroll
-      for (int o = 1; o < kL3PerL2 / 2; o <<= 1) m2 += __shfl_xor_sync(kFull, m2, o);
-      if ((threadIdx.x & (kL3PerL2 / 2 - 1)) == 0) s_l2[0][threadIdx.x / (kL3PerL2 / 2)] = m2;
-      __syncthreads();
-      if (threadIdx.x < 32) {
-        const int g2 = max(warp_pick([&](int i) { return s_l2[0][i]; }, kL2, job.u[1]), 0);
-        const int g3 = max(warp_pick([&](int i) { return s_l3[0][g2 * kL3PerL2 + i]; }, kL3PerL2,
-                                     job.u[2]),
-                           0);
-        if (threadIdx.x == 0) {
-          s_g2 = g2;
-          s_g3 = g3;
-        }
-      }
-      __syncthreads();
-      const int blk3 = s_g2 * kL3PerL2 + s_g3;  // thread blk3 / 2 holds its tokens
-      if (threadIdx.x == (blk3 >> 1)) {
-#pragma unroll
-        for (int i = 0; i < kLevel3; ++i) s_l4[i] = (blk3 & 1) ? r[kLevel3 + i] : r[i];
-      }
-      __syncthreads();
-      if (threadIdx.x < 32) {
-        const int g4 = max(warp_pick([&](int i) { return s_l4[i]; }, kLevel3, job.u[3]), 0);
-        if (threadIdx.x == 0) s_tok = cbeg + blk3 * kLevel3 + g4;
-      }
-      __syncthreads();
-      token = s_tok;
-    }
+  } else if (c1 < 0) {
+    if (threadIdx.x == 0) sc.tok = 0;  // no mass at all (cannot happen for q)
+    __syncthreads();
   }
-  if (threadIdx.x == 0) p.out_tokens[static_cast<size_t>(b) * (N + 1) + job.row] = token;
+  if (threadIdx.x == 0) p.out_tokens[static_cast<size_t>(b) * (N + 1) + job.row] = sc.tok;
+}
+
+template <typename T, bool kVecPath>
+cudaError_t launch_sample_t(const Problem& p, const Workspace& w, cudaStream_t s) {
+  constexpr int kB = blocks_per_cta<T>();
+  const long long blocks = static_cast<long long>(p.B) * ((w.S3 + kB - 1) / kB);
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const int smem = kVecPath ? stage_bytes<T>() : 0;
+  if (kVecPath) {
+    // above the default 48 KB of dynamic shared memory: opt in (cheap, idempotent)
+    const cudaError_t e =
+        cudaFuncSetAttribute(sample_kernel<T, kVecPath>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+  }
+  // Programmatic dependent launch: the grid may be scheduled while the
+  // row-statistics kernel drains; the walk waits for it before reading its
+  // results.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kST);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, sample_kernel<T, kVecPath>, p, w);
 }
 
 }  // namespace
 
 cudaError_t launch_sample(int dtype, bool vec, const Problem& p, const Workspace& w,
                           cudaStream_t s) {
-  const long long blocks = static_cast<long long>(p.B) * kSampleCluster;
-  if (blocks <= 0) return cudaSuccess;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const dim3 grid(static_cast<unsigned>(blocks));
-  if (dtype == 1) {
-    if (vec)
-      sample_kernel<__nv_bfloat16, true><<<grid, kST, 0, s>>>(p, w);
-    else
-      sample_kernel<__nv_bfloat16, false><<<grid, kST, 0, s>>>(p, w);
-  } else {
-    if (vec)
-      sample_kernel<float, true><<<grid, kST, 0, s>>>(p, w);
-    else
-      sample_kernel<float, false><<<grid, kST, 0, s>>>(p, w);
-  }
-  return cudaGetLastError();
+  if (dtype == 1)
+    return vec ? launch_sample_t<__nv_bfloat16, true>(p, w, s)
+               : launch_sample_t<__nv_bfloat16, false>(p, w, s);
+  return vec ? launch_sample_t<float, true>(p, w, s) : launch_sample_t<float, false>(p, w, s);
 }
 
 }  // namespace sv

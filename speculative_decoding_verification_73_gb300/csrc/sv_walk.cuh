@@ -37,35 +37,47 @@ struct RowNorm {
   bool ok;
 };
 
-// Partials are loaded kBatch at a time with every load issued before any is
-// used, so a row costs ceil(n / kBatch) L2 round trips, not n.  `at(i)` gives
-// the address of the row's i-th partial.
+// The first kPre partials of every row are loaded together with the walk's
+// other inputs (one L2 round trip for V up to kPre spans); any further ones
+// kBatch at a time, every load of a batch issued before any is used.
+constexpr int kPre = 4;
 constexpr int kBatch = 8;
 
-template <typename At>
-__device__ __forceinline__ RowNorm merge_sampled(At at, int n) {
+// A partial, or an empty one (maximum -inf, nothing summed) when !take.
+__device__ __forceinline__ float4 partial_or_empty(const Partial* at, bool take) {
+  return take ? __ldcg(reinterpret_cast<const float4*>(at))
+              : make_float4(-INFINITY, 0.f, __int_as_float(INT_MAX), 0.f);
+}
+
+template <int kN>
+__device__ __forceinline__ void absorb_sampled(const float4 (&pt)[kN], float& c, float& s, bool& bad) {
+  float cb = c;
+#pragma unroll
+  for (int i = 0; i < kN; ++i) {
+    if (pt[i].y != pt[i].y || pt[i].x != pt[i].x) bad = true;
+    cb = fmaxf(cb, pt[i].x);
+  }
+  if (cb > -INFINITY) {
+    float sb = c > -INFINITY ? s * exp2f(c - cb) : 0.f;
+#pragma unroll
+    for (int i = 0; i < kN; ++i)
+      if (pt[i].x > -INFINITY) sb += pt[i].y * exp2f(pt[i].x - cb);
+    s = sb;
+    c = cb;
+  }
+}
+
+// Merge the n partials of a sampled row; `pre` holds the first kPre.
+__device__ __forceinline__ RowNorm merge_sampled(const float4 (&pre)[kPre], const Partial* parts,
+                                                 int n) {
   float c = -INFINITY, s = 0.f;
   bool bad = false;
-  for (int i0 = 0; i0 < n; i0 += kBatch) {
+  absorb_sampled(pre, c, s, bad);
+  for (int i0 = kPre; i0 < n; i0 += kBatch) {
     float4 pt[kBatch];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i)
-      pt[i] = i0 + i < n ? __ldcg(reinterpret_cast<const float4*>(at(i0 + i)))
-                         : make_float4(-INFINITY, 0.f, 0.f, 0.f);
-    float cb = c;
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      if (pt[i].y != pt[i].y || pt[i].x != pt[i].x) bad = true;
-      cb = fmaxf(cb, pt[i].x);
-    }
-    if (cb > -INFINITY) {
-      float sb = c > -INFINITY ? s * exp2f(c - cb) : 0.f;
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i)
-        if (pt[i].x > -INFINITY) sb += pt[i].y * exp2f(pt[i].x - cb);
-      s = sb;
-      c = cb;
-    }
+    for (int i = 0; i < kBatch; ++i) pt[i] = partial_or_empty(parts + i0 + i, i0 + i < n);
+    absorb_sampled(pt, c, s, bad);
   }
   RowNorm r;
   r.c = c;
@@ -79,28 +91,31 @@ struct RowMax {
   bool ok;
 };
 
+template <int kN>
+__device__ __forceinline__ void absorb_greedy(const float4 (&pt)[kN], float& best, int& idx,
+                                              bool& bad) {
+#pragma unroll
+  for (int i = 0; i < kN; ++i) {
+    if (pt[i].y != pt[i].y || pt[i].x != pt[i].x) bad = true;
+    if (pt[i].x > best) {
+      best = pt[i].x;
+      idx = __float_as_int(pt[i].z);
+    }
+  }
+}
+
 // Greedy rows: partials come in increasing index order, so strict > keeps
 // the lowest index among equal maxima.
-template <typename At>
-__device__ __forceinline__ RowMax merge_greedy(At at, int n) {
+__device__ __forceinline__ RowMax merge_greedy(const float4 (&pre)[kPre], const Partial* parts, int n) {
   float best = -INFINITY;
   int idx = INT_MAX;
   bool bad = false;
-  for (int i0 = 0; i0 < n; i0 += kBatch) {
-    int4 pt[kBatch];
+  absorb_greedy(pre, best, idx, bad);
+  for (int i0 = kPre; i0 < n; i0 += kBatch) {
+    float4 pt[kBatch];
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i)
-      pt[i] = i0 + i < n ? __ldcg(reinterpret_cast<const int4*>(at(i0 + i)))
-                         : make_int4(__float_as_int(-INFINITY), 0, INT_MAX, 0);
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const float a = __int_as_float(pt[i].x), sv = __int_as_float(pt[i].y);
-      if (sv != sv || a != a) bad = true;
-      if (a > best) {
-        best = a;
-        idx = pt[i].z;
-      }
-    }
+    for (int i = 0; i < kBatch; ++i) pt[i] = partial_or_empty(parts + i0 + i, i0 + i < n);
+    absorb_greedy(pt, best, idx, bad);
   }
   RowMax r;
   r.idx = idx;
@@ -117,42 +132,53 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
   const bool pos_thread = j < N;
 
   __shared__ int s_bad_token, s_bad_logit, s_first;
+
+  // Every load the walk needs is issued here, before any of them is used:
+  // the temperature and the draft token (inputs, fetched while the
+  // row-statistics kernel may still be finishing), then the logits at the
+  // token that the row-statistics pass stored (meaningful only for a sampled
+  // request with a valid token) and the first partials of the row pair.
+  const float t = p.temperature[b];
+  const int d = pos_thread ? p.tokens[static_cast<size_t>(b) * N + j] : -1;
+  wait_for_prerequisite();
+  float zd = 0.f, yd = 0.f;
+  if (pos_thread) {
+    const float* tl = w.tok_logit + static_cast<size_t>(b) * (2 * N + 1);
+    zd = __ldcg(tl + j);
+    yd = __ldcg(tl + N + 1 + j);
+  }
+  const int S1 = w.S1;
+  const Partial* req_parts = w.partials + static_cast<size_t>(b) * (2 * N + 1) * S1;
+  const Partial* tparts = req_parts + static_cast<size_t>(j) * S1;
+  const Partial* dparts = req_parts + static_cast<size_t>(N + 1 + j) * S1;
+  float4 tpre[kPre], dpre[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) {
+    tpre[i] = partial_or_empty(tparts + i, row_thread && i < S1);
+    dpre[i] = partial_or_empty(dparts + i, pos_thread && i < S1);
+  }
   if (j == 0) {
     s_bad_token = 0;
     s_bad_logit = 0;
     s_first = N;
   }
-  __syncthreads();
-
-  const float t = p.temperature[b];
   const int mode = temp_mode(t);
-  // Every load the walk needs is issued here, before any of them is used:
-  // the draft token, the logits at it that the row-statistics pass stored
-  // (meaningful only for a sampled request with a valid token), and, in the
-  // merges below, the rows' partials.
-  int d = -1;
-  float zd = 0.f, yd = 0.f;
-  if (pos_thread) {
-    const float* tl = w.tok_logit + static_cast<size_t>(b) * (2 * N + 1);
-    d = p.tokens[static_cast<size_t>(b) * N + j];
-    zd = __ldcg(tl + j);
-    yd = __ldcg(tl + N + 1 + j);
-    if (d < 0 || d >= V) atomicOr(&s_bad_token, 1);
+  if (!write_outputs && mode != kModeSampled) {  // CTA-uniform: nothing to sample
+    if (j == 0) job_out->kind = kJobNone;
+    return;
   }
+  __syncthreads();
+  if (pos_thread && (d < 0 || d >= V)) atomicOr(&s_bad_token, 1);
   RowNorm q{}, pn{};
   RowMax g{};
-  const int S1 = w.S1;
-  const Partial* req_parts = w.partials + static_cast<size_t>(b) * (2 * N + 1) * S1;
-  const Partial* tparts = req_parts + static_cast<size_t>(j) * S1;
-  const Partial* dparts = req_parts + static_cast<size_t>(N + 1 + j) * S1;
   if (mode == kModeGreedy && row_thread) {
-    g = merge_greedy([&](int i) { return tparts + i; }, S1);
+    g = merge_greedy(tpre, tparts, S1);
     if (!g.ok) atomicOr(&s_bad_logit, 1);
   } else if (mode == kModeSampled && row_thread) {
-    q = merge_sampled([&](int i) { return tparts + i; }, S1);
+    q = merge_sampled(tpre, tparts, S1);
     if (!q.ok) atomicOr(&s_bad_logit, 1);
     if (pos_thread) {
-      pn = merge_sampled([&](int i) { return dparts + i; }, S1);
+      pn = merge_sampled(dpre, dparts, S1);
       if (!pn.ok) atomicOr(&s_bad_logit, 1);
     }
   }
