@@ -12,10 +12,10 @@
 // logits, the sampler's per-block masses, candidates and arrival counters,
 // the error word and the debug statistics) lives in g_scratch, a file-scope
 // device array of SV_NOALLOC_SCRATCH_BYTES that exists in every device's
-// copy of the module.  Host code cannot use the array's name as a device pointer, so
-// the first call on each device (with that device current) asks the runtime
-// for its address with cudaGetSymbolAddress and caches it; later calls on
-// that device reuse the cached pointer.  Problems whose working memory does
+// copy of the module.  Host code cannot use the array's name as a device
+// pointer, so the first call on each device (with that device current) asks
+// the runtime for its address with cudaGetSymbolAddress and caches it; later
+// calls on that device reuse the cached pointer.  Problems whose working memory does
 // not fit are refused with SV_ESCRATCH before anything is enqueued.
 //
 // Sharing: every call on a device uses the same array.  Only the error word

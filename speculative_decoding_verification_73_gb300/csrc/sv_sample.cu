@@ -15,18 +15,23 @@
 // rounding leaves none).  The law is exactly r / sum(r), and every decision
 // compares a uniform against at most a few dozen float32 edges.
 //
-// Grid: one CTA per (request, level-1 block), request-major.  Every CTA runs
-// the request's accept/reject walk itself from the row-statistics partials
-// (one L2 round trip; CTA 0 of the request writes the walk's outputs).  For
-// a sampled request each CTA then evaluates r over its block (thread t takes
-// tokens [32t, 32t + 32): two level-3 masses per thread, a level-2 mass per
-// eight threads, the level-1 mass per CTA) and picks the block's candidate
-// token at levels 2-4 with u_2..u_4, as if level 1 had chosen this block.
-// It stores (level-1 mass, candidate) and counts itself in the request's
-// arrival counter; the CTA that arrives last picks level 1 over the blocks'
-// masses with u_1, writes the chosen block's candidate, and resets the
-// counter for the next call.  No CTA waits for another.  If the residual
-// has no mass anywhere, that last CTA redoes every block with q alone.
+// Grid: one CTA per request and group of blocks_per_cta() level-1 blocks,
+// request-major, launched with programmatic dependent launch (it may become
+// resident while the row-statistics kernel drains; the walk waits for that
+// kernel before reading its results).  Every CTA runs the request's
+// accept/reject walk itself from the row-statistics partials (one L2 round
+// trip; CTA 0 of the request writes the walk's outputs).  For a sampled
+// request each CTA then stages its blocks' row pair in shared memory
+// (cp.async, all of it in flight at once), evaluates r over each block
+// (thread t takes tokens [32t, 32t + 32): two level-3 masses per thread, a
+// level-2 mass per eight threads, the level-1 mass per CTA) and picks the
+// block's candidate token at levels 2-4 with u_2..u_4, as if level 1 had
+// chosen this block.  It stores (level-1 mass, candidate) and counts itself
+// in the request's arrival counter; the CTA that arrives last picks level 1
+// over the blocks' masses with u_1, writes the chosen block's candidate, and
+// resets the counter for the next call.  No CTA waits for another.  If the
+// residual has no mass anywhere, that last CTA redoes every block with q
+// alone.
 //
 // r_t = max(q_t - p_t, 0) with q_t = 2^(z_t k - c_q) / s_q and likewise p_t,
 // evaluated two tokens at a time with the paired float instructions.  Its
