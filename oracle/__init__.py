@@ -19,6 +19,12 @@ What it computes (plain float64, in the order the pages state it):
   the committed KV length ("Speculative Decoding and EAGLE-3" lesson,
   sections "Invariant: Leviathan rejection sampling", "Build it" steps
   1-4 and "KV cache rollback").
+* ``tree``    -- verification of a draft tree (EAGLE-2's dynamic draft tree
+  in the same lesson's "Key terms", its tree-mask remark and exercise 3):
+  the per-node Leviathan test of each child in turn against the residual
+  left by its rejected elder siblings, descent on acceptance, a drawn
+  token where every child is rejected or at a leaf, and the argmax path at
+  temperature 0.
 
 Pins (see tests/test_oracle_*.py): exact Fraction enumeration of the
 output law on tiny vocabularies, the acceptance identity sum_t min(p, q),
@@ -26,4 +32,4 @@ the E[accepted] closed form, brute-force greedy chains, textbook softmax
 special cases, Philox known-answer vectors and a library Philox.
 """
 
-from . import philox, verify  # noqa: F401
+from . import philox, tree, verify  # noqa: F401

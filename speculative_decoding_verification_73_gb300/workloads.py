@@ -296,3 +296,133 @@ NAMED = {
     "batch64-bf16": batch64_bf16,
     "mixture-bf16": mixture_bf16,
 }
+
+
+# --------------------------------------------------------------------------
+# Draft trees
+# --------------------------------------------------------------------------
+
+TREE_SAMPLED = 0   # children are independent draws from the parent's draft row
+TREE_TOPK = 1      # children are the parent's top draft tokens, most probable first
+
+
+@dataclasses.dataclass
+class TreeWorkload:
+    """One batch of tree-verify inputs on the host (torch CPU tensors).
+    Node 0 is the root, nodes 1..M the drafts; row r of both logit tensors
+    belongs to node r."""
+
+    name: str
+    dtype: str
+    mode: int                   # TREE_SAMPLED | TREE_TOPK
+    target: torch.Tensor        # [B, M+1, V]
+    draft: torch.Tensor         # [B, M+1, V]
+    parents: torch.Tensor       # [B, M] int32, parent of node i+1 in [0, i]
+    tokens: torch.Tensor        # [B, M] int32
+    temperature: torch.Tensor   # [B] float32
+    seed: int
+
+    @property
+    def shape(self):
+        b, m1, v = self.target.shape
+        return b, m1 - 1, v
+
+    def raw(self):
+        if self.dtype == "bf16":
+            return (self.target.view(torch.int16).numpy().view(np.uint16),
+                    self.draft.view(torch.int16).numpy().view(np.uint16))
+        return self.target.numpy(), self.draft.numpy()
+
+    def inner_rows(self):
+        """Number of nodes with children, per request."""
+        b, m, _ = self.shape
+        out = np.zeros(b, dtype=np.int64)
+        par = self.parents.numpy()
+        for i in range(b):
+            out[i] = len(set(int(x) for x in par[i]))
+        return out
+
+    def bytes_read(self):
+        """Logit bytes of one tree verify: every target row, plus (SAMPLED
+        mode, T > 0) the draft rows of nodes with children."""
+        b, m, v = self.shape
+        esize = self.target.element_size()
+        rows = b * (m + 1)
+        if self.mode == TREE_SAMPLED:
+            inner = self.inner_rows()
+            rows += int(sum(inner[i] for i in range(b) if float(self.temperature[i]) > 0))
+        return rows * v * esize
+
+
+def full_tree_parents(widths):
+    """Parents (breadth-first ids) of the tree with widths[d] children under
+    every node of depth d: (2, 2, 2) gives 14 draft nodes and 8 leaves."""
+    parents, level, nxt = [], [0], 1
+    for w in widths:
+        new = []
+        for node in level:
+            for _ in range(w):
+                parents.append(node)
+                new.append(nxt)
+                nxt += 1
+        level = new
+    return np.array(parents, dtype=np.int32)
+
+
+def random_tree_parents(gen, m, max_children=4):
+    """A random topology with m draft nodes: node i+1 hangs under a uniformly
+    chosen earlier node that still has fewer than max_children children."""
+    parents, kids = [], [0] * (m + 1)
+    for i in range(m):
+        while True:
+            p = int(torch.randint(0, i + 1, (1,), generator=gen))
+            if kids[p] < max_children:
+                break
+        kids[p] += 1
+        parents.append(p)
+    return np.array(parents, dtype=np.int32)
+
+
+def make_tree(batch, vocab, dtype, *, gen_seed, widths=None, m=None, mode=TREE_SAMPLED,
+              verify_seed=0, temps=(0.0, 0.7, 1.0), sigma=(0.2, 1.5), s=1.1,
+              target_noise=0.3, name=None):
+    """Tree workload: a full tree of ``widths`` for every request, or (with
+    ``m``) a random topology of m draft nodes per request.  Target rows are
+    Zipf-shaped; draft row r = target row r + N(0, sigma_b).  Children of a
+    node take tokens from the node's draft row at the request's temperature:
+    independent Gumbel-max draws (SAMPLED) or its largest logits in
+    decreasing order (TOPK, and every request with T = 0)."""
+    gen = _gen(gen_seed + 4409)
+    lo, hi = sigma
+    sig = (lo + (hi - lo) * torch.rand(batch, generator=gen, dtype=torch.float64)).numpy()
+    pick = torch.randint(0, len(temps), (batch,), generator=gen).numpy()
+    tv = np.asarray(temps, dtype=np.float32)[pick]
+    if widths is not None:
+        par = np.tile(full_tree_parents(widths), (batch, 1))
+    else:
+        par = np.stack([random_tree_parents(gen, m) for _ in range(batch)])
+    mm = par.shape[1]
+    tdt = DTYPES[dtype]
+    target = torch.empty(batch, mm + 1, vocab, dtype=tdt)
+    draft = torch.empty(batch, mm + 1, vocab, dtype=tdt)
+    tokens = np.zeros((batch, mm), dtype=np.int32)
+    for b in range(batch):
+        z = _zipf_rows(gen, mm + 1, vocab, s, target_noise)
+        target[b] = z.to(tdt)
+        y = z + float(sig[b]) * torch.randn(mm + 1, vocab, generator=gen, dtype=torch.float64)
+        draft[b] = y.to(tdt)
+        yw = _widen(draft[b])
+        for node in range(mm + 1):
+            kids = [i for i in range(mm) if par[b, i] == node]
+            if not kids:
+                continue
+            if mode == TREE_TOPK or tv[b] == 0:
+                order = np.argsort(-yw[node], kind="stable")
+                for k, i in enumerate(kids):
+                    tokens[b, i] = int(order[k])
+            else:
+                rows = np.repeat(yw[node:node + 1], len(kids), axis=0)
+                tokens[b, kids] = _gumbel_argmax(gen, rows, float(tv[b]))
+    label = name or f"tree-{'topk' if mode == TREE_TOPK else 'sampled'}-{dtype}-B{batch}-M{mm}-V{vocab}"
+    return TreeWorkload(label, dtype, mode, target, draft, torch.from_numpy(par),
+                        torch.from_numpy(tokens), torch.from_numpy(tv), int(verify_seed))
