@@ -57,6 +57,8 @@ extern "C" {
 #define SV_ECUDA       5  /* a CUDA runtime call failed                        */
 #define SV_ESCRATCH    6  /* spec_verify_noalloc: the problem's working memory
                              exceeds SV_NOALLOC_SCRATCH_BYTES                  */
+#define SV_EBADTREE    7  /* device check (spec_verify_tree): a node's parent is
+                             outside [0, node - 1]                             */
 
 /* Bits of the device error word (spec_verify_get_error).  A request that
  * fails a device check gets out_tokens = -1 everywhere, out_accept_len = -1
@@ -65,6 +67,8 @@ extern "C" {
 #define SV_ERRBIT_TEMP   1u
 #define SV_ERRBIT_TOKEN  2u
 #define SV_ERRBIT_LOGIT  4u
+#define SV_ERRBIT_TREE   8u   /* spec_verify_tree only; checked after the
+                                 temperature, before tokens and logits */
 
 /* ---- logit element types ---------------------------------------------- */
 #define SV_F32   0
@@ -89,7 +93,8 @@ typedef struct spec_verify_ctx spec_verify_ctx;   /* opaque, library-owned */
  *
  * Allocates the whole device workspace once (per-row partial statistics,
  * per-request walk results and sampling sums; a few MB at most) and zeroes
- * the parts that must start at zero.  Returns SV_OK, SV_EINVAL or SV_ECUDA.
+ * the parts that must start at zero.  The same context serves
+ * spec_verify_tree with up to max_N draft nodes per tree.  Returns SV_OK, SV_EINVAL or SV_ECUDA.
  */
 int spec_verify_init(spec_verify_ctx** ctx, int max_B, int max_N, int max_V,
                      int dtype, void* cuda_stream);
@@ -169,9 +174,65 @@ int spec_verify_noalloc(int B, int N, int V, int dtype,
                         void* cuda_stream);
 
 /*
+ * spec_verify_tree -- one batched verify step over a draft TREE instead of
+ * a chain (the lesson's "Key terms" entry on EAGLE-2's dynamic draft tree,
+ * its tree-mask remark in "KV cache rollback", and exercise 3's [2, 2, 2]
+ * tree of eight candidate paths scored by one verifier pass).
+ *
+ * Layout per request: node 0 is the root (the last verified token), draft
+ * nodes are 1..M in topological order.
+ *   parents          [B, M] int32: parent of node i+1, in [0, i]
+ *   draft_tokens     [B, M] int32: token of node i+1, in [0, V)
+ *   target_logits    [B, M+1, V] dtype: row r = the verifier's next-token
+ *                    logits after node r (the tree-masked forward pass)
+ *   draft_logits     [B, M+1, V] dtype: row r = the drafter's logits from
+ *                    which node r's children were drawn (read only in
+ *                    SV_TREE_SAMPLED mode, and only rows of nodes that have
+ *                    children); may be NULL in SV_TREE_TOPK mode
+ *   temperature      [B] float32, seed: as for spec_verify
+ *   mode             SV_TREE_SAMPLED: the children of a node are independent
+ *                    draws from its draft row; SV_TREE_TOPK: they are fixed
+ *                    candidates (e.g. the drafter's top-k), tested as draws
+ *                    from a point mass on their own token
+ * The walk starts at the root; the children of the current node are tried
+ * in increasing node index (list siblings most probable first).  Child x is
+ * accepted iff p(x) = 0 or u < min(1, r(x) / p(x)), r the node's current
+ * distribution (q at first, after a rejection (r - p)_+ renormalised; in
+ * TOPK mode p is the point mass, so r(x) decides and the residual drops x).
+ * Accepting descends into the child; when every child is rejected a token
+ * is drawn from the final r, and at a leaf a bonus token from its q.  Both
+ * modes keep the verifier's law exactly.  Uniforms: the i-th child tried at
+ * depth j uses Philox counter (b, j, i == 0 ? 0 : i + 1, 0); the token drawn
+ * at depth j uses draw 1 and the grouped inverse CDF of spec_verify, so a
+ * tree with one child per node gives exactly spec_verify's results.  T = 0
+ * descends into the first child whose token is the node's target argmax.
+ *
+ * Outputs:
+ *   out_tokens       [B, M+1] int32: the accepted path's tokens, then the
+ *                    drawn token, then -1
+ *   out_path         [B, M] int32: the accepted node indices (1..M), then -1
+ *                    (the tree positions whose KV entries to keep)
+ *   out_accept_len   [B] int32: path length a; out_kv_len [B]: a + 1
+ * Limits: 0 <= M <= max_N of the context, B <= max_B, V <= max_V.  Device
+ * errors mark the request (-1 / -1 / 0) and set SV_ERRBIT_* (temperature,
+ * tree, token, logit, in that order).  Each rejection in SAMPLED mode costs
+ * one extra pass over that node's two rows.  Returns SV_OK, SV_EINVAL
+ * (nothing enqueued) or SV_ECUDA.  Two kernel launches per call.
+ */
+#define SV_TREE_SAMPLED 0
+#define SV_TREE_TOPK    1
+int spec_verify_tree(spec_verify_ctx* ctx, int B, int M, int V, int mode,
+                     const void* target_logits, const void* draft_logits,
+                     const int32_t* parents, const int32_t* draft_tokens,
+                     const float* temperature, uint64_t seed,
+                     int32_t* out_tokens, int32_t* out_path,
+                     int32_t* out_accept_len, int32_t* out_kv_len);
+
+/*
  * spec_verify_get_error -- wait for the context's stream, then return the
  * first device-detected error since the last read (SV_EBADTEMP,
- * SV_EBADTOKEN, SV_EBADLOGIT in that priority) or SV_OK, and clear it.
+ * SV_EBADTREE, SV_EBADTOKEN, SV_EBADLOGIT in that priority) or SV_OK, and
+ * clear it.
  * bits (may be NULL) receives the OR of SV_ERRBIT_* flags.
  */
 int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits);

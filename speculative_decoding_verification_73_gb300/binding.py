@@ -14,8 +14,9 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 
-SV_OK, SV_EINVAL, SV_EBADTEMP, SV_EBADTOKEN, SV_EBADLOGIT, SV_ECUDA, SV_ESCRATCH = range(7)
-SV_ERRBIT_TEMP, SV_ERRBIT_TOKEN, SV_ERRBIT_LOGIT = 1, 2, 4
+SV_OK, SV_EINVAL, SV_EBADTEMP, SV_EBADTOKEN, SV_EBADLOGIT, SV_ECUDA, SV_ESCRATCH, SV_EBADTREE = range(8)
+SV_ERRBIT_TEMP, SV_ERRBIT_TOKEN, SV_ERRBIT_LOGIT, SV_ERRBIT_TREE = 1, 2, 4, 8
+SV_TREE_SAMPLED, SV_TREE_TOPK = 0, 1
 SV_F32, SV_BF16 = 0, 1
 SV_NUM_KERNELS = 2
 SV_MAX_N = 255
@@ -29,7 +30,7 @@ EXPORTS = (
     "spec_verify_init", "spec_verify", "spec_verify_get_error", "spec_verify_debug_stats",
     "spec_verify_profile", "spec_verify_profile_read", "spec_verify_launches_per_call",
     "spec_verify_debug_philox", "spec_verify_destroy", "spec_verify_strerror",
-    "spec_verify_noalloc",
+    "spec_verify_noalloc", "spec_verify_tree",
 )
 
 _lib = None
@@ -63,6 +64,8 @@ def load():
     lib.spec_verify_launches_per_call.argtypes = []
     lib.spec_verify_debug_philox.argtypes = [c_u64, c_void, c_void, c_int, c_void]
     lib.spec_verify_destroy.argtypes = [c_void]
+    lib.spec_verify_tree.argtypes = [c_void, c_int, c_int, c_int, c_int, c_void, c_void, c_void,
+                                     c_void, c_void, c_u64, c_void, c_void, c_void, c_void]
     lib.spec_verify_noalloc.argtypes = [c_int, c_int, c_int, c_int, c_void, c_void, c_void, c_void,
                                         c_u64, c_void, c_void, c_void, c_void]
     lib.spec_verify_strerror.argtypes = [c_int]
@@ -165,6 +168,31 @@ def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, temperature, 
                                       _stream_handle(stream)), "spec_verify_noalloc")
 
 
+def spec_verify_tree(ctx, mode, target_logits, draft_logits, parents, draft_tokens, temperature,
+                     seed, out_tokens, out_path, out_accept_len, out_kv_len):
+    """Enqueue one tree verify step; B, M, V are taken from ``target_logits``
+    [B, M+1, V].  ``draft_logits`` [B, M+1, V] may be None in TOPK mode."""
+    B, m1, V = target_logits.shape
+    M = m1 - 1
+    logit_dt = (torch.float32, torch.bfloat16)
+    _require(target_logits, "target_logits", (B, m1, V), logit_dt)
+    if mode == SV_TREE_SAMPLED and M > 0:
+        _require(draft_logits, "draft_logits", (B, m1, V), (target_logits.dtype,))
+    if M > 0:
+        _require(parents, "parents", (B, M), (torch.int32,))
+        _require(draft_tokens, "draft_tokens", (B, M), (torch.int32,))
+        _require(out_path, "out_path", (B, M), (torch.int32,))
+    _require(temperature, "temperature", (B,), (torch.float32,))
+    _require(out_tokens, "out_tokens", (B, m1), (torch.int32,))
+    _require(out_accept_len, "out_accept_len", (B,), (torch.int32,))
+    _require(out_kv_len, "out_kv_len", (B,), (torch.int32,))
+    _check(load().spec_verify_tree(ctx, int(B), int(M), int(V), int(mode), _ptr(target_logits),
+                                   _ptr(draft_logits), _ptr(parents), _ptr(draft_tokens),
+                                   _ptr(temperature), ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF),
+                                   _ptr(out_tokens), _ptr(out_path), _ptr(out_accept_len),
+                                   _ptr(out_kv_len)), "spec_verify_tree")
+
+
 def spec_verify_get_error(ctx):
     """(code, bits) of the device-detected input errors since the last read."""
     bits = ctypes.c_uint32(0)
@@ -229,6 +257,7 @@ class SpecVerify:
         self.out_tokens = torch.empty(max_B * (max_N + 1), dtype=torch.int32, device=self.device)
         self.out_accept = torch.empty(max_B, dtype=torch.int32, device=self.device)
         self.out_kv = torch.empty(max_B, dtype=torch.int32, device=self.device)
+        self.out_path = torch.empty(max_B * max(max_N, 1), dtype=torch.int32, device=self.device)
 
     def __call__(self, target, draft, tokens, temperature, seed):
         B, n1, _ = target.shape
@@ -236,6 +265,17 @@ class SpecVerify:
         acc, kv = self.out_accept[:B], self.out_kv[:B]
         spec_verify(self.ctx, target, draft, tokens, temperature, seed, toks, acc, kv)
         return toks, acc, kv
+
+    def tree(self, target, draft, parents, tokens, temperature, seed, mode=SV_TREE_SAMPLED):
+        """Tree verify; returns (out_tokens [B, M+1], out_path [B, M],
+        out_accept_len [B], out_kv_len [B]) as CUDA tensors."""
+        B, m1, _ = target.shape
+        toks = self.out_tokens[: B * m1].view(B, m1)
+        path = self.out_path[: B * (m1 - 1)].view(B, m1 - 1)
+        acc, kv = self.out_accept[:B], self.out_kv[:B]
+        spec_verify_tree(self.ctx, mode, target, draft, parents, tokens, temperature, seed,
+                         toks, path, acc, kv)
+        return toks, path, acc, kv
 
     def get_error(self):
         return spec_verify_get_error(self.ctx)

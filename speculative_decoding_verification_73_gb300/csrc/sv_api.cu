@@ -80,6 +80,7 @@ const char* spec_verify_strerror(int code) {
     case SV_EBADTOKEN: return "a draft token is outside [0, V)";
     case SV_EBADLOGIT: return "a logit row holds NaN or +inf, or has no finite entry";
     case SV_ECUDA: return "a CUDA runtime call failed";
+    case SV_EBADTREE: return "a draft-tree node's parent is outside [0, node - 1]";
     case SV_ESCRATCH:
       return "the problem needs more working memory than spec_verify_noalloc's static array "
              "(SV_NOALLOC_SCRATCH_BYTES) holds";
@@ -110,9 +111,11 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   const int s1 = ceil_div(max_V, sv::row_chunk_elems(dtype));
   const int s3 = ceil_div(max_V, sv::sample_chunk_elems(dtype));
   const size_t rows = static_cast<size_t>(max_B) * (2 * static_cast<size_t>(max_N) + 1);
+  // partials also serve a tree of up to max_N draft nodes: 2 (max_N + 1) rows
+  const size_t part_rows = static_cast<size_t>(max_B) * (2 * static_cast<size_t>(max_N) + 2);
   size_t off = 0;
   const size_t o_part = off;
-  off = align_up(off + rows * s1 * sizeof(sv::Partial), 256);
+  off = align_up(off + part_rows * s1 * sizeof(sv::Partial), 256);
   const size_t o_tok = off;
   off = align_up(off + rows * sizeof(float), 256);
   const size_t o_sums = off;
@@ -200,6 +203,62 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
   return SV_OK;
 }
 
+int spec_verify_tree(spec_verify_ctx* ctx, int B, int M, int V, int mode,
+                     const void* target_logits, const void* draft_logits, const int32_t* parents,
+                     const int32_t* draft_tokens, const float* temperature, uint64_t seed,
+                     int32_t* out_tokens, int32_t* out_path, int32_t* out_accept_len,
+                     int32_t* out_kv_len) {
+  if (ctx == nullptr) return SV_EINVAL;
+  if (B < 0 || B > ctx->max_B || M < 0 || M > ctx->max_N || V < 1 || V > ctx->max_V ||
+      (mode != SV_TREE_SAMPLED && mode != SV_TREE_TOPK))
+    return SV_EINVAL;
+  if (B == 0) return SV_OK;
+  if (target_logits == nullptr || temperature == nullptr || out_tokens == nullptr ||
+      out_accept_len == nullptr || out_kv_len == nullptr)
+    return SV_EINVAL;
+  if (M > 0 && (parents == nullptr || draft_tokens == nullptr || out_path == nullptr))
+    return SV_EINVAL;
+  const bool use_draft = mode == SV_TREE_SAMPLED && M > 0;
+  if (use_draft && draft_logits == nullptr) return SV_EINVAL;
+
+  const size_t esize = ctx->dtype == SV_BF16 ? 2 : 4;
+  const bool vec = (static_cast<size_t>(V) * esize) % 16 == 0 && aligned16(target_logits) &&
+                   (!use_draft || aligned16(draft_logits));
+  sv::TreeProblem p;
+  p.B = B;
+  p.M = M;
+  p.V = V;
+  p.mode = mode;
+  p.target = target_logits;
+  p.draft = use_draft ? draft_logits : target_logits;
+  p.parents = parents;
+  p.tokens = draft_tokens;
+  p.temperature = temperature;
+  p.seed = seed;
+  p.out_tokens = out_tokens;
+  p.out_path = out_path;
+  p.out_accept = out_accept_len;
+  p.out_kv = out_kv_len;
+  sv::Workspace w = ctx->w;
+  w.S1 = ceil_div(V, sv::row_chunk_elems(ctx->dtype));
+  w.S3 = ceil_div(V, sv::sample_chunk_elems(ctx->dtype));
+
+  cudaEvent_t* ev = nullptr;
+  if (ctx->profile_every > 0 && (ctx->profile_seen++ % ctx->profile_every) == 0) {
+    ev = profile_slot(ctx);
+    if (ev == nullptr) return SV_ECUDA;
+    if (cudaEventRecord(ev[0], ctx->stream) != cudaSuccess) return SV_ECUDA;
+  }
+  if (sv::launch_tree_rowstats(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
+  if (ev && cudaEventRecord(ev[1], ctx->stream) != cudaSuccess) return SV_ECUDA;
+  if (sv::launch_tree_walk(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
+  if (ev) {
+    if (cudaEventRecord(ev[2], ctx->stream) != cudaSuccess) return SV_ECUDA;
+    ctx->recorded += 1;
+  }
+  return SV_OK;
+}
+
 int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits) {
   if (ctx == nullptr) return SV_EINVAL;
   unsigned word = 0;
@@ -210,6 +269,7 @@ int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits) {
     return SV_ECUDA;
   if (bits) *bits = word;
   if (word & SV_ERRBIT_TEMP) return SV_EBADTEMP;
+  if (word & SV_ERRBIT_TREE) return SV_EBADTREE;
   if (word & SV_ERRBIT_TOKEN) return SV_EBADTOKEN;
   if (word & SV_ERRBIT_LOGIT) return SV_EBADLOGIT;
   return SV_OK;

@@ -36,6 +36,11 @@ constexpr int kModeSampled = 2;
 constexpr unsigned kErrTemp = 1u;
 constexpr unsigned kErrToken = 2u;
 constexpr unsigned kErrLogit = 4u;
+constexpr unsigned kErrTree = 8u;
+
+// How the children of a draft-tree node were drafted.
+constexpr int kTreeSampled = 0;  // independent draws from the node's draft row
+constexpr int kTreeTopk = 1;     // fixed candidates (point masses)
 
 // Statistics of one chunk of one logit row (16 bytes).
 //   sampled row: a = c = fl(M * k) with M the chunk maximum and k = log2(e)/T,
@@ -76,8 +81,23 @@ struct Problem {
   int32_t* out_kv;           // [B]
 };
 
+struct TreeProblem {
+  int B, M, V, mode;         // mode: kTreeSampled | kTreeTopk
+  const void* target;        // [B, M+1, V]: row r after node r
+  const void* draft;         // [B, M+1, V]: row r drafted node r's children
+  const int32_t* parents;    // [B, M]: parent of node i+1, in [0, i]
+  const int32_t* tokens;     // [B, M]
+  const float* temperature;  // [B]
+  unsigned long long seed;
+  int32_t* out_tokens;       // [B, M+1]
+  int32_t* out_path;         // [B, M]
+  int32_t* out_accept;       // [B]
+  int32_t* out_kv;           // [B]
+};
+
 struct Workspace {
   Partial* partials;     // [B][2N+1][S1]: target rows 0..N, then draft rows 0..N-1
+                         // (tree: [B][2(M+1)][S1], target rows then draft rows 0..M)
   float* tok_logit;      // [B][2N+1]: logit at the row's draft token (sampled rows)
   float* chunk_sums;     // [B, S3]: residual mass of each level-1 block
   int* blk_tok;          // [B, S3]: the token each level-1 block would give
@@ -94,6 +114,10 @@ cudaError_t launch_rowstats(int dtype, bool vec, const Problem& p, const Workspa
                             cudaStream_t s);
 cudaError_t launch_sample(int dtype, bool vec, const Problem& p, const Workspace& w,
                           cudaStream_t s);
+cudaError_t launch_tree_rowstats(int dtype, bool vec, const TreeProblem& p, const Workspace& w,
+                                 cudaStream_t s);
+cudaError_t launch_tree_walk(int dtype, bool vec, const TreeProblem& p, const Workspace& w,
+                             cudaStream_t s);
 cudaError_t launch_philox_probe(unsigned long long seed, const uint32_t* ctr3, uint32_t* out4,
                                 int n, cudaStream_t s);
 

@@ -42,17 +42,11 @@
 #include <cuda_bf16.h>
 
 #include "sv_device.cuh"
+#include "sv_pick.cuh"
 #include "sv_walk.cuh"
 
 namespace sv {
 namespace {
-
-constexpr int kST = kSampleThreads;      // threads per sampler CTA
-constexpr int kSegTok = kLevel1 / kST;   // tokens per thread in a level-1 block (32)
-constexpr int kL2 = kLevel1 / kLevel2;   // level-2 blocks per level-1 block (32)
-constexpr int kL3 = kLevel1 / kLevel3;   // level-3 blocks per level-1 block (512)
-constexpr int kL3PerL2 = kLevel2 / kLevel3;  // 16
-static_assert(kSegTok == 2 * kLevel3, "two level-3 blocks per thread");
 
 // Level-1 blocks one CTA takes: their row pair is staged in shared memory
 // (64 KB either way), all of it requested at once.
@@ -63,18 +57,6 @@ constexpr int blocks_per_cta() {
 template <typename T>
 constexpr int stage_bytes() {
   return 2 * blocks_per_cta<T>() * kLevel1 * static_cast<int>(sizeof(T));
-}
-
-__device__ __forceinline__ float cta_sum(float v, float* scratch) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-  __syncthreads();
-  v = 0.f;
-#pragma unroll
-  for (int w = 0; w < kST / 32; ++w) v += scratch[w];
-  __syncthreads();
-  return v;
 }
 
 // r for the tokens of one 16-byte vector of each row; rv[e] gets token e.
@@ -156,62 +138,6 @@ __device__ __forceinline__ void resid_halves(const T* z, const T* y, int t0, int
   }
 }
 
-// Inverse CDF over n masses, evaluated by one whole warp (all lanes get the
-// result): the smallest c with running sum C_c > u * C_{n-1}; if none, the
-// last c with mass > 0; -1 if every mass is 0.  Masses are read through
-// `get(i)`, once each when n <= 32; longer lists are scanned in tiles of 32
-// twice (total, then the crossing) with identical arithmetic.
-template <typename Get>
-__device__ int warp_pick(Get get, int n, float u) {
-  const int lane = threadIdx.x & 31;
-  if (n <= 32) {
-    const float m = lane < n ? get(lane) : 0.f;
-    float incl = m;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const unsigned pos = __ballot_sync(kFull, m > 0.f);
-    if (!pos) return -1;
-    const float target = u * __shfl_sync(kFull, incl, 31);
-    const unsigned hit = __ballot_sync(kFull, lane < n && incl > target);
-    return hit ? __ffs(hit) - 1 : 31 - __clz(pos);
-  }
-  float carry = 0.f;
-  int last_pos = -1;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
-    const float m = i < n ? get(i) : 0.f;
-    float incl = m;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const unsigned pos = __ballot_sync(kFull, m > 0.f);
-    if (pos) last_pos = base + 31 - __clz(pos);
-    carry += __shfl_sync(kFull, incl, 31);
-  }
-  if (last_pos < 0) return -1;
-  const float target = u * carry;
-  carry = 0.f;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
-    const float m = i < n ? get(i) : 0.f;
-    float incl = m;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float t = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const unsigned hit = __ballot_sync(kFull, i < n && carry + incl > target);
-    if (hit) return base + __ffs(hit) - 1;
-    carry += __shfl_sync(kFull, incl, 31);
-  }
-  return last_pos;
-}
-
 // 16-byte copy global -> shared that holds no register while in flight
 // (cached in L2 only); the issuing thread waits for its own copies with
 // cp_async_wait_all.
@@ -274,57 +200,6 @@ __device__ __forceinline__ void staged_halves(const T* sz, const T* sy, const Jo
     else
       h1 += part;
   }
-}
-
-struct BlockScratch {
-  float red[kST / 32];
-  float l2[kL2];      // level-2 masses of the block
-  float l3[kL3];      // level-3 masses of the block
-  float l4[kLevel3];  // token masses of the chosen level-3 block
-  int pick;
-  int tok;
-};
-
-// From each thread's two level-3 masses of the level-1 block
-// [cbeg, cbeg + kLevel1): the level-2 and level-1 masses (*mass), and the
-// token the grouped inverse CDF picks inside the block at levels 2-4
-// (u[1..3]), or -1 when the block has no mass.  r_at(t) re-evaluates r at
-// token t (cbeg <= t < cend) for level 4 with the same arithmetic.  Called
-// by the whole CTA.
-template <typename RAt>
-__device__ int block_pick(float h0, float h1, int cbeg, int cend, const Job& job, RAt r_at,
-                          BlockScratch& sc, float* mass) {
-  sc.l3[2 * threadIdx.x] = h0;
-  sc.l3[2 * threadIdx.x + 1] = h1;
-  float m2 = h0 + h1;  // level-2 mass: the 8 consecutive threads of a 256-token block
-#pragma unroll
-  for (int o = 1; o < kL3PerL2 / 2; o <<= 1) m2 += __shfl_xor_sync(kFull, m2, o);
-  if ((threadIdx.x & (kL3PerL2 / 2 - 1)) == 0) sc.l2[threadIdx.x / (kL3PerL2 / 2)] = m2;
-  *mass = cta_sum(h0 + h1, sc.red);  // its barriers also publish l2 and l3
-  if (threadIdx.x < 32) {
-    const int g2 = warp_pick([&](int i) { return sc.l2[i]; }, kL2, job.u[1]);
-    int pick = -1;
-    if (g2 >= 0) {
-      const int g3 = warp_pick([&](int i) { return sc.l3[g2 * kL3PerL2 + i]; }, kL3PerL2, job.u[2]);
-      pick = g2 * kL3PerL2 + max(g3, 0);
-    }
-    if (threadIdx.x == 0) sc.pick = pick;
-  }
-  __syncthreads();
-  const int blk3 = sc.pick;
-  if (blk3 < 0) return -1;  // CTA-uniform
-  const int t0 = cbeg + blk3 * kLevel3;
-  if (threadIdx.x < kLevel3) {
-    const int t = t0 + threadIdx.x;
-    sc.l4[threadIdx.x] = t < cend ? r_at(t) : 0.f;
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    const int g4 = max(warp_pick([&](int i) { return sc.l4[i]; }, kLevel3, job.u[3]), 0);
-    if (threadIdx.x == 0) sc.tok = t0 + g4;
-  }
-  __syncthreads();
-  return sc.tok;
 }
 
 // Masses and candidate of one level-1 block read straight from global memory

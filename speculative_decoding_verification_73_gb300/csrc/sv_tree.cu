@@ -1,0 +1,542 @@
+// Verification of a draft tree (EAGLE-2's dynamic draft tree).
+//
+// "Speculative Decoding and EAGLE-3" lesson: the "Key terms" entry on
+// EAGLE-2 (a small candidate tree scored by one verifier pass, the walk
+// following the most probable path), its tree-mask remark in "KV cache
+// rollback", exercise 3 (the [2, 2, 2] tree), and "Invariant: Leviathan
+// rejection sampling" for the test at each node.
+//
+// Node 0 is the root, draft nodes 1..M (parent of node i in [0, i-1], token
+// tokens[i-1]); target row r and draft row r belong to node r.  From the
+// root, the children of the current node are tried in increasing index: a
+// child with token x is accepted iff p(x) = 0 or u < min(1, r(x) / p(x)),
+// r the node's current distribution (q at first).  Accepting descends;
+// rejecting turns r into (r - p)_+ normalised (r itself if that is all 0).
+// When every child is rejected a token is drawn from the final r; at a leaf
+// a bonus token is drawn from its q.  SAMPLED mode: the children were drawn
+// independently from the node's draft row.  TOPK mode: they are fixed
+// candidates, whose drafting law is a point mass on their own token, so
+// accept iff u < r(x) and the residual is r with x removed; draft logits are
+// not read.  Uniforms: the i-th child tried at depth j uses Philox counter
+// (b, j, i == 0 ? 0 : i + 1, 0); the token drawn at depth j uses draw 1 and
+// the grouped inverse CDF (levels of 8192 / 256 / 16 / 1 tokens).  T = 0
+// descends into the first child whose token is the node's target argmax and
+// emits the argmax where there is none.
+//
+// Two kernels.  tree_rowstats_kernel streams every target row and, for a
+// sampled request in SAMPLED mode, the draft rows of nodes that have
+// children, one CTA per 64 KB span (the chain's span reduction).
+// tree_walk_kernel gives each request a cluster of kTreeCluster CTAs.  Every
+// CTA merges the partials of all rows and fetches the logits of every child
+// at its token (thread i holds node i), then all of them run the same walk:
+// one thread decides, and each rejection in SAMPLED mode triggers a pass in
+// which every CTA sums max(r(t) - p(t), 0) over its share of the vocabulary
+// and the eight partial sums are exchanged through distributed shared
+// memory after a cluster barrier, so every CTA holds the same normaliser.
+// The final draw computes, per level-1 block, the block's mass and the token
+// levels 2-4 would pick in it (each CTA its own blocks), then rank 0 picks
+// level 1.  All arithmetic is float32; each CTA takes the same decisions
+// from the same numbers, so the cluster stays in step.
+
+#include <climits>
+#include <cuda_bf16.h>
+
+#include "sv_device.cuh"
+#include "sv_pick.cuh"
+#include "sv_span.cuh"
+#include "sv_walk.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kTreeCluster = 8;
+constexpr int kMaxNodes = kST;  // root + up to 255 draft nodes, one thread each
+constexpr int kNoNode = INT_MAX;
+
+// ------------------------------------------------------------ row statistics
+
+template <typename T, bool kVecPath>
+__global__ void __launch_bounds__(kThreads, kSpanMinBlocks) tree_rowstats_kernel(TreeProblem p,
+                                                                                   Workspace w) {
+  const int S1 = w.S1;
+  const int per = 2 * (p.M + 1);
+  const int row = blockIdx.x / S1;
+  const int span = blockIdx.x - row * S1;
+  const int b = row / per;
+  const int slot = row - b * per;
+  const bool draft = slot > p.M;
+  const int node = draft ? slot - p.M - 1 : slot;
+  const int mode = temp_mode(p.temperature[b]);
+  if (mode == kModeInvalid) return;  // CTA-uniform
+  if (draft) {
+    if (mode == kModeGreedy || p.mode != kTreeSampled) return;
+    int has_children = 0;  // only draft rows of inner nodes are read
+    const int32_t* par = p.parents + static_cast<size_t>(b) * p.M;
+    for (int i = threadIdx.x; i < p.M; i += kThreads) has_children |= par[i] == node;
+    if (!__syncthreads_or(has_children)) return;
+  }
+  const T* base = static_cast<const T*>(draft ? p.draft : p.target) +
+                  (static_cast<size_t>(b) * (p.M + 1) + node) * p.V;
+  constexpr int kSpan = kSpanBytes / static_cast<int>(sizeof(T));
+  const int beg = span * kSpan;
+  const int end = min(p.V, beg + kSpan);
+  const bool greedy = mode == kModeGreedy;
+  const float k = greedy ? 0.f : scale_of(p.temperature[b]);
+  Partial out;
+  if (!kVecPath) {
+    out = chunk_partial_scalar<T>(base, beg, end, greedy, k, -1, nullptr);
+  } else if (end - beg == kSpan) {
+    out = greedy ? span_partial_vec<T, true, true>(base, beg, end, k, -1, nullptr)
+                 : span_partial_vec<T, false, true>(base, beg, end, k, -1, nullptr);
+  } else {
+    out = greedy ? span_partial_vec<T, true, false>(base, beg, end, k, -1, nullptr)
+                 : span_partial_vec<T, false, false>(base, beg, end, k, -1, nullptr);
+  }
+  if (threadIdx.x == 0) w.partials[static_cast<size_t>(row) * S1 + span] = out;
+}
+
+// ------------------------------------------------------------ cluster helpers
+
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Barrier over every thread of every CTA of the cluster; orders the memory
+// accesses before it (release) with those after it (acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// The float at `local`'s place in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ float ld_dsmem(const float* local, unsigned rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// ------------------------------------------------------------ distributions
+
+// The distribution a node's token is drawn from, or that its next child is
+// tested against, as a per-token function of the two logits.
+//   kQ:       q_t = 2^(z_t k - cq) / sq
+//   kSampled: r_m after m rejections: r_0 = q, r_j = (r_{j-1} - p)_+ * inv[j-1]
+//             (inv = 1 / sum of the positive part; 0 marks a step that left r
+//             unchanged because that sum was 0)
+//   kTopk:    q with the rejected tokens removed (unnormalised)
+// For a draw (scale-free) the last residual step is left unnormalised, so a
+// one-child chain computes exactly the values of the chain sampler.
+struct NodeLaw {
+  static constexpr int kQ = 0, kSampled = 1, kTopk = 2;
+  int kind;
+  float k, cq, inv_sq, cp, inv_sp;
+  int m;
+  const float* inv;
+  const int* rej;
+  bool draw;
+  __device__ __forceinline__ float q(float zt) const { return ex2(fmaf(zt, k, -cq)) * inv_sq; }
+  __device__ __forceinline__ float p(float yt) const { return ex2(fmaf(yt, k, -cp)) * inv_sp; }
+  __device__ __forceinline__ float r(float zt, float yt, int t) const {
+    float v = q(zt);
+    if (kind == kSampled) {
+      const float pt = p(yt);
+      for (int j = 0; j < m; ++j) {
+        if (inv[j] > 0.f) {
+          v = fmaxf(v - pt, 0.f);
+          if (!(draw && j == m - 1)) v *= inv[j];
+        }
+      }
+    } else if (kind == kTopk) {
+      for (int j = 0; j < m; ++j)
+        if (rej[j] == t) v = 0.f;
+    }
+    return v;
+  }
+  // the positive part of r - p (a residual step's mass at t)
+  __device__ __forceinline__ float excess(float zt, float yt, int t) const {
+    return fmaxf(r(zt, yt, t) - p(yt), 0.f);
+  }
+};
+
+// Sums of f(z_t, y_t, t) over this thread's 32 tokens [t0, t0 + 32) of a
+// level-1 block (0 past cend): h0 over the first 16, h1 over the last 16.
+template <typename T, bool kVecPath, typename F>
+__device__ __forceinline__ void seg_sums(const T* z, const T* y, bool need_y, int t0, int cend, F f,
+                                         float& h0, float& h1) {
+  using E = Elem<T>;
+  h0 = 0.f;
+  h1 = 0.f;
+  if (kVecPath) {
+    constexpr int kVec = E::kVec;
+    constexpr int kVecs = kSegTok / kVec;
+    uint4 zv[kVecs], yv[kVecs];
+#pragma unroll
+    for (int i = 0; i < kVecs; ++i) {
+      const int e0 = t0 + i * kVec;
+      const bool in = e0 < cend;
+      zv[i] = in ? __ldg(reinterpret_cast<const uint4*>(z + e0)) : make_uint4(0, 0, 0, 0);
+      yv[i] = (in && need_y) ? __ldg(reinterpret_cast<const uint4*>(y + e0)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < kVecs; ++i) {
+      float part = 0.f;
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) {
+        const int t = t0 + i * kVec + e;
+        if (t < cend) part += f(E::get(zv[i], e), need_y ? E::get(yv[i], e) : 0.f, t);
+      }
+      if (i < kVecs / 2)
+        h0 += part;
+      else
+        h1 += part;
+    }
+  } else {
+    for (int i = 0; i < kSegTok; ++i) {
+      const int t = t0 + i;
+      const float v = t < cend ? f(E::load1(z + t), need_y ? E::load1(y + t) : 0.f, t) : 0.f;
+      if (i < kLevel3)
+        h0 += v;
+      else
+        h1 += v;
+    }
+  }
+}
+
+// ------------------------------------------------------------ the walk
+
+constexpr int kActContinue = 0, kActPass = 1, kActBonus = 2, kActResidual = 3;
+
+template <typename T, bool kVecPath>
+__global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, 2)
+    tree_walk_kernel(TreeProblem p, Workspace w) {
+  using E = Elem<T>;
+  __shared__ int s_par[kMaxNodes], s_tok[kMaxNodes], s_first[kMaxNodes], s_next[kMaxNodes];
+  __shared__ int s_gidx[kMaxNodes], s_path[kMaxNodes], s_rej[kMaxNodes];
+  __shared__ float s_cq[kMaxNodes], s_sq[kMaxNodes], s_cp[kMaxNodes], s_sp[kMaxNodes];
+  __shared__ float s_zc[kMaxNodes], s_yc[kMaxNodes], s_inv[kMaxNodes];
+  __shared__ float s_part[2];
+  __shared__ BlockScratch sc;
+  __shared__ Job s_job;
+  __shared__ unsigned s_err;
+  __shared__ int s_node, s_depth, s_child, s_m, s_plen, s_act;
+  __shared__ float s_rej_mass;
+
+  const int b = blockIdx.x / kTreeCluster;
+  const unsigned rank = cluster_rank();
+  const int M = p.M, V = p.V;
+  const int i = threadIdx.x;  // node id
+  const bool is_node = i <= M;
+  const float temp = p.temperature[b];
+  const int mode = temp_mode(temp);
+  const bool sampled = mode == kModeSampled;
+  const bool use_draft = sampled && p.mode == kTreeSampled;
+  const float k = sampled ? scale_of(temp) : 0.f;
+
+  // ---- per node: topology, token, row statistics, child logits
+  int par = -1, tok = -1;
+  if (i >= 1 && is_node) {
+    par = p.parents[static_cast<size_t>(b) * M + i - 1];
+    tok = p.tokens[static_cast<size_t>(b) * M + i - 1];
+  }
+  const int S1 = w.S1;
+  const Partial* req_parts = w.partials + static_cast<size_t>(b) * 2 * (M + 1) * S1;
+  const Partial* tparts = req_parts + static_cast<size_t>(i) * S1;
+  const Partial* dparts = req_parts + static_cast<size_t>(M + 1 + i) * S1;
+  float4 tpre[kPre], dpre[kPre];
+#pragma unroll
+  for (int j = 0; j < kPre; ++j) {
+    tpre[j] = partial_or_empty(tparts + j, is_node && mode != kModeInvalid && j < S1);
+    dpre[j] = partial_or_empty(dparts + j, is_node && use_draft && j < S1);
+  }
+  if (i == 0) s_err = mode == kModeInvalid ? kErrTemp : 0u;
+  s_first[i] = kNoNode;
+  s_next[i] = kNoNode;
+  s_par[i] = par;
+  s_tok[i] = tok;
+  __syncthreads();
+  const bool par_ok = i >= 1 && is_node && par >= 0 && par < i;
+  const bool tok_ok = tok >= 0 && tok < V;
+  if (i >= 1 && is_node) {
+    if (!par_ok) atomicOr(&s_err, kErrTree);
+    if (!tok_ok) atomicOr(&s_err, kErrToken);
+  }
+  if (par_ok) atomicMin(&s_first[par], i);
+  __syncthreads();
+  if (par_ok) {
+    for (int j = i + 1; j <= M; ++j)
+      if (s_par[j] == par) {
+        s_next[i] = j;
+        break;
+      }
+  }
+  // child logits at the child's token, in its parent's rows
+  float zc = 0.f, yc = 0.f;
+  if (sampled && par_ok && tok_ok) {
+    const size_t off = (static_cast<size_t>(b) * (M + 1) + par) * V + tok;
+    zc = E::load1(static_cast<const T*>(p.target) + off);
+    if (use_draft) yc = E::load1(static_cast<const T*>(p.draft) + off);
+  }
+  if (is_node && mode == kModeGreedy) {
+    const RowMax g = merge_greedy(tpre, tparts, S1);
+    s_gidx[i] = g.idx;
+    if (!g.ok) atomicOr(&s_err, kErrLogit);
+  } else if (is_node && sampled) {
+    const RowNorm q = merge_sampled(tpre, tparts, S1);
+    s_cq[i] = q.c;
+    s_sq[i] = q.s;
+    if (!q.ok) atomicOr(&s_err, kErrLogit);
+    if (use_draft && s_first[i] != kNoNode) {
+      const RowNorm pn = merge_sampled(dpre, dparts, S1);
+      s_cp[i] = pn.c;
+      s_sp[i] = pn.s;
+      if (!pn.ok) atomicOr(&s_err, kErrLogit);
+    } else {
+      s_cp[i] = 0.f;
+      s_sp[i] = 1.f;
+    }
+  }
+  s_zc[i] = zc;
+  s_yc[i] = yc;
+  __syncthreads();
+
+  int32_t* out_tok = p.out_tokens + static_cast<size_t>(b) * (M + 1);
+  int32_t* out_path = p.out_path + static_cast<size_t>(b) * M;
+  const unsigned bits = s_err;
+  if (bits) {
+    // report the first failing check in the order temperature, topology,
+    // tokens, logits
+    const unsigned err = (bits & kErrTemp)    ? kErrTemp
+                         : (bits & kErrTree)  ? kErrTree
+                         : (bits & kErrToken) ? kErrToken
+                                              : kErrLogit;
+    if (rank == 0) {
+      if (is_node) out_tok[i] = -1;
+      if (i < M) out_path[i] = -1;
+      if (i == 0) {
+        p.out_accept[b] = -1;
+        p.out_kv[b] = 0;
+        atomicOr(w.err, err);
+      }
+    }
+    return;  // identical in every CTA of the cluster
+  }
+
+  if (mode == kModeGreedy) {
+    if (rank != 0) return;
+    if (i == 0) {
+      int node = 0, plen = 0;
+      while (true) {
+        const int g = s_gidx[node];
+        int c = s_first[node];
+        while (c != kNoNode && s_tok[c] != g) c = s_next[c];
+        if (c == kNoNode) {
+          out_tok[plen] = g;
+          break;
+        }
+        out_tok[plen] = g;
+        out_path[plen] = c;
+        s_path[plen++] = c;
+        node = c;
+      }
+      s_plen = plen;
+      p.out_accept[b] = plen;
+      p.out_kv[b] = plen + 1;
+    }
+    __syncthreads();
+    const int plen = s_plen;
+    if (is_node && i > plen) out_tok[i] = -1;
+    if (i < M && i >= plen) out_path[i] = -1;
+    return;
+  }
+
+  // ---- sampled walk: every CTA runs it; thread 0 decides
+  if (i == 0) {
+    s_node = 0;
+    s_depth = 1;
+    s_child = s_first[0];
+    s_m = 0;
+    s_plen = 0;
+    s_rej_mass = 0.f;
+  }
+  __syncthreads();
+  const bool topk = p.mode == kTreeTopk;
+  const T* zbase = static_cast<const T*>(p.target) + static_cast<size_t>(b) * (M + 1) * V;
+  const T* ybase = use_draft ? static_cast<const T*>(p.draft) + static_cast<size_t>(b) * (M + 1) * V
+                             : zbase;
+  const int S3 = w.S3;
+  int pass = 0;
+  while (true) {
+    if (i == 0) {
+      const int node = s_node, c = s_child, m = s_m;
+      int act = kActContinue;
+      if (c == kNoNode) {
+        act = s_first[node] == kNoNode ? kActBonus : kActResidual;
+      } else {
+        const float zx = s_zc[c], yx = s_yc[c];
+        const float cq = s_cq[node], sq = s_sq[node];
+        const float u = philox_uniform(p.seed, b, s_depth, m == 0 ? 0u : static_cast<uint32_t>(m + 1));
+        bool ok;
+        if (!topk) {
+          const float cp = s_cp[node], sp = s_sp[node];
+          if (yx == -INFINITY) {
+            ok = true;  // the drafter gives the child no mass
+          } else if (m == 0) {
+            // log2 q(x)/p(x), every term small when q and p are close
+            const float lr = fmaf(zx - yx, k, -(cq - cp)) + log2f(sp / sq);
+            ok = u < fminf(1.f, exp2f(lr));
+          } else {
+            float v = exp2f(fmaf(zx, k, -cq)) / sq;
+            const float px = exp2f(fmaf(yx, k, -cp)) / sp;
+            for (int j = 0; j < m; ++j)
+              if (s_inv[j] > 0.f) v = fmaxf(v - px, 0.f) * s_inv[j];
+            ok = u < fminf(1.f, v / px);
+          }
+        } else {
+          const int x = s_tok[c];
+          bool seen = false;
+          for (int j = 0; j < m; ++j) seen |= s_rej[j] == x;
+          const float qx = exp2f(fmaf(zx, k, -cq)) / sq;
+          const float rest = 1.f - s_rej_mass;  // q's mass left after the rejected tokens
+          const float rx = seen ? 0.f : (rest > 0.f ? qx / rest : 1.f);
+          ok = u < fminf(1.f, rx);
+          if (!ok) {
+            s_rej[m] = x;
+            if (!seen) s_rej_mass += qx;
+            s_m = m + 1;
+            s_child = s_next[c];
+          }
+        }
+        if (ok) {
+          s_path[s_plen++] = c;
+          s_node = c;
+          s_depth += 1;
+          s_child = s_first[c];
+          s_m = 0;
+          s_rej_mass = 0.f;
+        } else if (!topk) {
+          act = kActPass;
+        }
+      }
+      s_act = act;
+    }
+    __syncthreads();
+    const int act = s_act;
+    if (act == kActContinue) continue;
+    if (act != kActPass) break;
+    // Residual pass: every CTA sums (r_m - p)_+ over its level-1 blocks.
+    const int node = s_node;
+    NodeLaw law{NodeLaw::kSampled, k, s_cq[node], 1.f / s_sq[node], s_cp[node], 1.f / s_sp[node],
+                s_m, s_inv, s_rej, false};
+    const T* z = zbase + static_cast<size_t>(node) * V;
+    const T* y = ybase + static_cast<size_t>(node) * V;
+    float acc = 0.f;
+    for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster) {
+      float h0, h1;
+      seg_sums<T, kVecPath>(z, y, true, c * kLevel1 + i * kSegTok, min(V, (c + 1) * kLevel1),
+                            [&](float zt, float yt, int t) { return law.excess(zt, yt, t); }, h0, h1);
+      acc += h0 + h1;
+    }
+    acc = cta_sum(acc, sc.red);
+    if (i == 0) s_part[pass & 1] = acc;
+    cluster_sync();
+    if (i == 0) {
+      float total = 0.f;
+      for (unsigned r = 0; r < kTreeCluster; ++r) total += ld_dsmem(&s_part[pass & 1], r);
+      s_inv[s_m] = total > 0.f ? 1.f / total : 0.f;
+      s_m += 1;
+      s_child = s_next[s_child];
+    }
+    ++pass;
+    __syncthreads();
+  }
+
+  // ---- the drawn token: bonus from q at a leaf, else from the final r
+  const int node = s_node;
+  const int depth = s_depth;
+  const bool bonus = s_act == kActBonus;
+  NodeLaw law{bonus ? NodeLaw::kQ : (topk ? NodeLaw::kTopk : NodeLaw::kSampled), k, s_cq[node],
+              1.f / s_sq[node], s_cp[node], 1.f / s_sp[node], s_m, s_inv, s_rej, true};
+  const bool need_y = law.kind == NodeLaw::kSampled;
+  const T* z = zbase + static_cast<size_t>(node) * V;
+  const T* y = ybase + static_cast<size_t>(node) * V;
+  if (i == 0) philox_uniforms4(p.seed, b, depth, 1, s_job.u);
+  __syncthreads();
+  const Job job = s_job;
+  float* masses = w.chunk_sums + static_cast<size_t>(b) * S3;
+  int* cands = w.blk_tok + static_cast<size_t>(b) * S3;
+  auto rf = [&](float zt, float yt, int t) { return law.r(zt, yt, t); };
+  for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster) {
+    const int cbeg = c * kLevel1, cend = min(V, cbeg + kLevel1);
+    float h0, h1, mass;
+    seg_sums<T, kVecPath>(z, y, need_y, cbeg + i * kSegTok, cend, rf, h0, h1);
+    const int cand = block_pick(
+        h0, h1, cbeg, cend, job,
+        [&](int t) { return law.r(E::load1(z + t), need_y ? E::load1(y + t) : 0.f, t); }, sc, &mass);
+    if (i == 0) {
+      masses[c] = mass;
+      cands[c] = cand;
+    }
+  }
+  __threadfence();
+  cluster_sync();  // every block's mass and candidate are stored
+  if (rank != 0) return;
+  if (i < 32) {
+    const int c1 = warp_pick([&](int j) { return __ldcg(masses + j); }, S3, job.u[0]);
+    if (i == 0) s_child = c1 >= 0 ? __ldcg(cands + c1) : 0;
+  }
+  __syncthreads();
+  const int plen = s_plen;
+  if (is_node) {
+    if (i < plen)
+      out_tok[i] = s_tok[s_path[i]];
+    else
+      out_tok[i] = i == plen ? s_child : -1;
+  }
+  if (i < M) out_path[i] = i < plen ? s_path[i] : -1;
+  if (i == 0) {
+    p.out_accept[b] = plen;
+    p.out_kv[b] = plen + 1;
+  }
+}
+
+template <typename T, bool kVecPath>
+cudaError_t launch_tree_t(const TreeProblem& p, const Workspace& w, cudaStream_t s, bool walk) {
+  if (!walk) {
+    const long long blocks = static_cast<long long>(p.B) * 2 * (p.M + 1) * w.S1;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    tree_rowstats_kernel<T, kVecPath><<<dim3(static_cast<unsigned>(blocks)), kThreads, 0, s>>>(p, w);
+  } else {
+    const long long blocks = static_cast<long long>(p.B) * kTreeCluster;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    tree_walk_kernel<T, kVecPath><<<dim3(static_cast<unsigned>(blocks)), kST, 0, s>>>(p, w);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_tree_rowstats(int dtype, bool vec, const TreeProblem& p, const Workspace& w,
+                                 cudaStream_t s) {
+  if (dtype == 1)
+    return vec ? launch_tree_t<__nv_bfloat16, true>(p, w, s, false)
+               : launch_tree_t<__nv_bfloat16, false>(p, w, s, false);
+  return vec ? launch_tree_t<float, true>(p, w, s, false) : launch_tree_t<float, false>(p, w, s, false);
+}
+
+cudaError_t launch_tree_walk(int dtype, bool vec, const TreeProblem& p, const Workspace& w,
+                             cudaStream_t s) {
+  if (dtype == 1)
+    return vec ? launch_tree_t<__nv_bfloat16, true>(p, w, s, true)
+               : launch_tree_t<__nv_bfloat16, false>(p, w, s, true);
+  return vec ? launch_tree_t<float, true>(p, w, s, true) : launch_tree_t<float, false>(p, w, s, true);
+}
+
+}  // namespace sv

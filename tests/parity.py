@@ -101,3 +101,57 @@ def max_rel(gpu, ref):
     if not m.any():
         return 0.0
     return float(np.max(np.abs(gpu[m] - ref[m]) / np.maximum(np.abs(ref[m]), 1.0)))
+
+
+def run_tree_oracle(wl, seed=None):
+    from oracle import tree as ot
+    z, y = wl.raw()
+    return ot.verify_tree(z, y, wl.parents.numpy(), wl.tokens.numpy(), wl.temperature.numpy(),
+                          wl.seed if seed is None else seed, wl.dtype, wl.mode)
+
+
+def compare_tree(res, tokens, path, accept, kv, temperature, label=""):
+    """Tree outputs against an oracle TreeResult, with the same rules as
+    ``compare``: greedy and error requests exact; a sampled request may
+    differ only where the oracle's decision at the depth where the two walks
+    part had its uniform within WINDOW of its threshold (any child test at
+    that depth when the paths part there, else the drawn token's level)."""
+    tokens = np.asarray(tokens).reshape(res.tokens.shape)
+    path = np.asarray(path).reshape(res.path.shape)
+    accept = np.asarray(accept).reshape(-1)
+    kv = np.asarray(kv).reshape(-1)
+    temperature = np.asarray(temperature).reshape(-1)
+    logged = []
+    for b in range(res.tokens.shape[0]):
+        same = (np.array_equal(tokens[b], res.tokens[b]) and np.array_equal(path[b], res.path[b])
+                and accept[b] == res.accept_len[b] and kv[b] == res.kv_len[b])
+        if same:
+            continue
+        where = f"{label} request {b}: gpu a={accept[b]} path={path[b].tolist()} tok={tokens[b].tolist()} " \
+                f"oracle a={res.accept_len[b]} path={res.path[b].tolist()} tok={res.tokens[b].tolist()}"
+        assert res.request_errors[b] == 0, "error request differs: " + where
+        assert float(temperature[b]) != 0.0, "greedy request differs: " + where
+        assert kv[b] == accept[b] + 1, where
+        a_g, a_o = int(accept[b]), int(res.accept_len[b])
+        common = 0
+        while common < min(a_g, a_o) and path[b, common] == res.path[b, common]:
+            common += 1
+        decs = res.decisions[b]
+        depth = common + 1
+        if common < a_g or common < a_o:
+            cand = [x for x in decs if x.kind == "accept" and x.j == depth]
+            assert cand, "no oracle decision at the divergence: " + where
+            dist = min(x.distance() for x in cand)
+            kind = "accept"
+        else:
+            cand = [x for x in decs if x.kind in ("residual", "bonus") and x.j == depth]
+            assert cand, "no oracle decision at the divergence: " + where
+            t_gpu, t_ref = int(tokens[b, a_g]), int(res.tokens[b, a_o])
+            level = next(lv for lv, sh in enumerate(LEVEL_SHIFTS) if (t_gpu >> sh) != (t_ref >> sh))
+            accept_cands = [x for x in decs if x.kind == "accept" and x.j == depth]
+            dist = min([cand[0].distance(level)] + [x.distance() for x in accept_cands])
+            kind = cand[0].kind
+        assert dist < WINDOW, f"mismatch outside the 1e-5 window (distance {dist:.3g}): " + where
+        logged.append((label, b, kind, depth, dist))
+        print("near-threshold mismatch:", where, f"distance={dist:.3g}")
+    return logged

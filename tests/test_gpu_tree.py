@@ -1,0 +1,115 @@
+"""GPU parity of tree verification through the C ABI against the tree
+oracle, and bit-for-bit agreement with spec_verify on one-child-per-node
+trees.  Every input is a seeded synthetic tree from ``workloads``."""
+
+import numpy as np
+import pytest
+import torch
+
+from speculative_decoding_verification_73_gb300 import binding, build, workloads
+
+from parity import compare_tree, run_tree_oracle
+
+pytestmark = pytest.mark.gpu
+
+TORCH_DT = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    return binding.load()
+
+
+def run_tree(wl, seed=None, ctx=None):
+    B, M, V = wl.shape
+    own = ctx is None
+    if own:
+        ctx = binding.SpecVerify(max(B, 1), max(M, 1), V, TORCH_DT[wl.dtype])
+    draft = wl.draft.cuda() if wl.mode == binding.SV_TREE_SAMPLED else None
+    toks, path, acc, kv = ctx.tree(wl.target.cuda(), draft, wl.parents.cuda(), wl.tokens.cuda(),
+                                   wl.temperature.cuda(), wl.seed if seed is None else seed, wl.mode)
+    code, bits = ctx.get_error()
+    out = (toks.cpu().numpy().copy(), path.cpu().numpy().copy(), acc.cpu().numpy().copy(),
+           kv.cpu().numpy().copy(), code, bits)
+    if own:
+        ctx.close()
+    return out
+
+
+def check_tree(wl, seed=None, label=""):
+    res = run_tree_oracle(wl, seed)
+    toks, path, acc, kv, code, bits = run_tree(wl, seed)
+    assert bits == res.errors, (bits, res.errors)
+    return res, compare_tree(res, toks, path, acc, kv, wl.temperature.numpy(), label or wl.name)
+
+
+def test_one_child_per_node_is_spec_verify_bit_for_bit():
+    for wl in (workloads.make_random(16, 6, 5000, "bf16", gen_seed=61, verify_seed=3),
+               workloads.make_random(9, 4, 3001, "f32", gen_seed=62, verify_seed=4)):
+        B, N, V = wl.shape
+        ctx = binding.SpecVerify(B, N, V, TORCH_DT[wl.dtype])
+        z, y = wl.target.cuda(), wl.draft.cuda()
+        d, t = wl.tokens.cuda(), wl.temperature.cuda()
+        par = torch.arange(N, dtype=torch.int32).repeat(B, 1).cuda()
+        y_tree = torch.cat([y, torch.zeros_like(z[:, :1])], dim=1)
+        for seed in (0, 1, 77):
+            ct, ca, ck = (x.cpu().clone() for x in ctx(z, y, d, t, seed))
+            tt, tp, ta, tk = (x.cpu().clone() for x in ctx.tree(z, y_tree, par, d, t, seed))
+            assert torch.equal(tt, ct) and torch.equal(ta, ca) and torch.equal(tk, ck)
+            for b in range(B):
+                a = int(ca[b])
+                assert tp[b, :a].tolist() == list(range(1, a + 1)) and (tp[b, a:] == -1).all()
+        ctx.close()
+
+
+CASES = {
+    "222-sampled-bf16": lambda: workloads.make_tree(24, 32000, "bf16", gen_seed=71, widths=(2, 2, 2),
+                                                    verify_seed=5),
+    "222-topk-bf16": lambda: workloads.make_tree(24, 32000, "bf16", gen_seed=72, widths=(2, 2, 2),
+                                                 mode=workloads.TREE_TOPK, verify_seed=6),
+    "random-sampled-f32-ragged": lambda: workloads.make_tree(12, 3001, "f32", gen_seed=73, m=40,
+                                                             verify_seed=7),
+    "random-topk-f32-ragged": lambda: workloads.make_tree(12, 3001, "f32", gen_seed=74, m=40,
+                                                          mode=workloads.TREE_TOPK, verify_seed=8),
+    "wide-sampled-bf16": lambda: workloads.make_tree(8, 50000, "bf16", gen_seed=75, widths=(4, 3),
+                                                     verify_seed=9),
+    "root-only": lambda: workloads.make_tree(5, 4096, "f32", gen_seed=76, widths=(), verify_seed=1),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_tree_parity(name):
+    wl = CASES[name]()
+    logged = []
+    for seed in (wl.seed, wl.seed + 1000, 2 ** 64 - 3):
+        res, lg = check_tree(wl, seed, f"{name} seed {seed}")
+        logged += lg
+        assert res.errors == 0
+    B, M, _ = wl.shape
+    assert len(logged) == 0 or len(logged) < 1e-5 * 3 * B * max(M, 1)
+
+
+def test_tree_222_full_vocabulary():
+    """The pages' [2, 2, 2] tree over V = 128256 bf16 logits, 32 requests."""
+    wl = workloads.make_tree(32, 128256, "bf16", gen_seed=77, widths=(2, 2, 2), verify_seed=11)
+    for seed in (11, 12):
+        check_tree(wl, seed, "222-full")
+
+
+def test_tree_errors_are_flagged_per_request():
+    wl = workloads.make_tree(6, 2048, "f32", gen_seed=78, widths=(2, 2), temps=(1.0,), verify_seed=2)
+    wl.temperature[0] = float("nan")
+    wl.parents[1, 3] = 5            # node 4 under node 5
+    wl.tokens[2, 0] = 2048          # out of range
+    wl.target[3, 2, 7] = float("inf")
+    wl.parents[4, 0] = -1
+    res, _ = check_tree(wl, label="errors")
+    toks, path, acc, kv, code, bits = run_tree(wl)
+    assert code == binding.SV_EBADTEMP and bits == 1 | 2 | 4 | 8
+    for b, bit in ((0, 1), (1, 8), (2, 2), (3, 4), (4, 8)):
+        assert res.request_errors[b] == bit
+        assert acc[b] == -1 and kv[b] == 0 and (toks[b] == -1).all() and (path[b] == -1).all()
+    assert acc[5] >= 0
