@@ -15,6 +15,12 @@ bracketed by barriers and the slowest rank's time is used.
 
 --impl reference times the CPU oracle (float64, one host thread) on the same
 metric, a bounded sample of requests per step.
+
+--path tree measures spec_verify_tree instead, on tree222-bf16: B=64
+requests, each a full [2, 2, 2] draft tree (14 nodes, 8 leaves) whose
+children are independent draws from the drafter, V=128256 bf16; one step is
+one tree verify of the batch, the metric counts the B*14 verified draft
+nodes per step.
 """
 
 import argparse
@@ -51,6 +57,9 @@ def parse():
     ap.add_argument("--copies", type=int, default=3, help="rotating input copies in HBM")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="chain", choices=["chain", "tree"],
+                    help="chain: spec_verify on batch64-bf16 (the headline); tree: "
+                         "spec_verify_tree on tree222-bf16")
     return ap.parse_args()
 
 
@@ -333,6 +342,161 @@ def run_ours(args):
         print(json.dumps(line))
 
 
+# --------------------------------------------------------------------------- tree
+
+TREE_WORKLOAD = "tree222-bf16"
+
+
+def tree222(verify_seed=0):
+    from speculative_decoding_verification_73_gb300 import workloads
+    return workloads.make_tree(64, 128256, "bf16", gen_seed=1006, widths=(2, 2, 2),
+                               verify_seed=verify_seed, name=TREE_WORKLOAD)
+
+
+def run_tree(args):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_verification_73_gb300 import binding, build
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    wl = tree222(verify_seed=rank)
+    B, M, V = wl.shape
+    copies = max(1, args.copies)
+    target = [wl.target.to(dev) for _ in range(copies)]
+    draft = [wl.draft.to(dev) for _ in range(copies)]
+    parents, tokens = wl.parents.to(dev), wl.tokens.to(dev)
+    temperature = wl.temperature.to(dev)
+    sv = binding.SpecVerify(B, M, V, torch.bfloat16, stream=stream, device=dev)
+    out_t = sv.out_tokens[: B * (M + 1)].view(B, M + 1)
+    out_p = sv.out_path[: B * M].view(B, M)
+    out_a, out_k = sv.out_accept[:B], sv.out_kv[:B]
+
+    def step(i, c=None):
+        c = i % copies if c is None else c
+        binding.spec_verify_tree(sv.ctx, wl.mode, target[c], draft[c], parents, tokens, temperature,
+                                 i, out_t, out_p, out_a, out_k)
+
+    for i in range(args.warmup):
+        step(i)
+    code, _ = sv.get_error()
+    assert code == 0, binding.strerror(code)
+    binding.spec_verify_profile_read(sv.ctx)
+    binding.spec_verify_profile(sv.ctx, PROFILE_EVERY)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t_begin = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_end = time.time()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = ranks_max(ev0.elapsed_time(ev1), dev)
+    kernel_ms, calls = binding.spec_verify_profile_read(sv.ctx)
+    binding.spec_verify_profile(sv.ctx, False)
+    time.sleep(0.2)
+    clk = clocks.stop(t_begin, t_end)
+    value = whole_job_rate(B * M, args.steps, world, elapsed_ms)
+    bytes_per_launch = wl.bytes_read()
+    rs_ms = kernel_ms["rowstats"] / max(calls, 1)
+    achieved = bytes_per_launch / (rs_ms / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    # end to end with pinned host buffers, through the Python binding
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 200))
+    hs = [t.pin_memory() for t in (wl.target, wl.draft, wl.parents, wl.tokens, wl.temperature)]
+    ds = [target[0], draft[0], parents, tokens, temperature]
+    hout = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (out_t, out_p, out_a, out_k)]
+    h2d = sum(t.numel() * t.element_size() for t in hs)
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def e2e_step(i):
+        for h, d in zip(hs, ds):
+            d.copy_(h, non_blocking=True)
+        step(i, 0)
+        for h, d in zip(hout, (out_t, out_p, out_a, out_k)):
+            h.copy_(d, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_value = whole_job_rate(B * M, e2e_steps, world, ranks_max(ev0.elapsed_time(ev1), dev))
+    code, _ = sv.get_error()
+    assert code == 0, binding.strerror(code)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 logits, f32 accumulate",
+        "data": "synthetic (seeded Zipf logits, Gaussian draft noise, children drawn from the drafter)",
+        "config": {
+            "workload": TREE_WORKLOAD, "B": B, "tree": "[2, 2, 2] (14 draft nodes, 8 leaves)",
+            "M": M, "V": V, "logits": "bf16", "drafting": "independent draws (SV_TREE_SAMPLED)",
+            "temperatures": "per request from {0, 0.7, 1.0}",
+            "bytes_read_per_step": bytes_per_launch,
+            "l2": f"inputs larger than L2: {bytes_per_launch / 1e6:.0f} MB read per step, "
+                  f"{copies} rotating copies",
+            "parallelism": f"replicas x{world} (requests shard, no collective)",
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "tree_rowstats", "achieved": achieved, "peak": peak,
+            "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s", "frac": achieved / peak,
+            "traffic": None, "algorithmic_bytes_per_launch": bytes_per_launch,
+            "avg_launch_us": rs_ms * 1e3,
+            "timed_launches": f"{calls} of {args.steps} calls (every {PROFILE_EVERY}th)",
+        },
+        "kernel_us_per_step": {("tree_rowstats" if k == "rowstats" else "tree_walk"): v / max(calls, 1) * 1e3
+                               for k, v in kernel_ms.items()},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps * 2,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = tree_cpu_baseline(wl, budget_s=12.0)
+    sv.close()
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def tree_cpu_baseline(wl, budget_s):
+    from oracle import tree as ot
+    B, M, _ = wl.shape
+    z, y = wl.raw()
+    par, tok, t = wl.parents.numpy(), wl.tokens.numpy(), wl.temperature.numpy()
+    done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        b = done % B
+        ot.verify_request(z[b], y[b], par[b], tok[b], t[b], wl.seed, b, wl.dtype, wl.mode)
+        done += 1
+    el = time.perf_counter() - t0
+    return {"value": done * M / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} requests of {TREE_WORKLOAD} (request i = i mod {B}), {el:.1f} s, "
+                      f"float64 numpy on 1 host thread"}
+
+
 # --------------------------------------------------------------------------- oracle
 
 def oracle_requests(wl, idx):
@@ -395,6 +559,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.path == "tree":
+        run_tree(args)
     else:
         run_ours(args)
 

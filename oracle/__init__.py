@@ -25,6 +25,10 @@ What it computes (plain float64, in the order the pages state it):
   left by its rejected elder siblings, descent on acceptance, a drawn
   token where every child is rejected or at a leaf, and the argmax path at
   temperature 0.
+* ``kv``      -- the KV-cache commit driven by out_kv_len (and a tree's
+  out_path): copy the kept window entries from a scratch buffer, or move
+  them together in place, and advance the logical length (section "KV
+  cache rollback" and exercise 4).
 
 Pins (see tests/test_oracle_*.py): exact Fraction enumeration of the
 output law on tiny vocabularies, the acceptance identity sum_t min(p, q),
@@ -32,4 +36,4 @@ the E[accepted] closed form, brute-force greedy chains, textbook softmax
 special cases, Philox known-answer vectors and a library Philox.
 """
 
-from . import philox, tree, verify  # noqa: F401
+from . import kv, philox, tree, verify  # noqa: F401
