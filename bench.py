@@ -21,6 +21,11 @@ requests, each a full [2, 2, 2] draft tree (14 nodes, 8 leaves) whose
 children are independent draws from the drafter, V=128256 bf16; one step is
 one tree verify of the batch, the metric counts the B*14 verified draft
 nodes per step.
+
+--path kv measures spec_verify_kv_commit (scratch mode): 32 layers x 64
+sequences, 4 KB entries (8 KV heads x 128 dims x K and V in bf16), an
+8-position window, the KV lengths of one batch64-bf16 verify; the metric is
+the bytes the commit reads plus writes per second.
 """
 
 import argparse
@@ -57,9 +62,9 @@ def parse():
     ap.add_argument("--copies", type=int, default=3, help="rotating input copies in HBM")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", default="chain", choices=["chain", "tree"],
+    ap.add_argument("--path", default="chain", choices=["chain", "tree", "kv"],
                     help="chain: spec_verify on batch64-bf16 (the headline); tree: "
-                         "spec_verify_tree on tree222-bf16")
+                         "spec_verify_tree on tree222-bf16; kv: spec_verify_kv_commit")
     return ap.parse_args()
 
 
@@ -497,6 +502,105 @@ def tree_cpu_baseline(wl, budget_s):
                       f"float64 numpy on 1 host thread"}
 
 
+# --------------------------------------------------------------------------- kv commit
+
+KV_WORKLOAD = "kvcommit-32L-64seq-4KB"
+
+
+def run_kv(args):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_verification_73_gb300 import binding, build, workloads
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    wl = workloads.batch64_bf16(verify_seed=rank)
+    B, N, V = wl.shape
+    sv = binding.SpecVerify(B, N, V, torch.bfloat16, stream=stream, device=dev)
+    _, _, kv = sv(wl.target.to(dev), wl.draft.to(dev), wl.tokens.to(dev), wl.temperature.to(dev), 0)
+    kv = kv.clone()
+    L, E, W, S = 32, 4096, N + 1, 1024
+    copies = max(1, args.copies)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+    scratch = [torch.randint(0, 256, (L, B, W, E), generator=gen, dtype=torch.uint8, device=dev)
+               for _ in range(copies)]
+    cache = [torch.zeros(L, B, S, E, dtype=torch.uint8, device=dev) for _ in range(copies)]
+    # lengths start below 200 and grow by at most W per commit: reset every 100 commits
+    seq0 = torch.randint(0, 200, (B,), generator=gen, dtype=torch.int32, device=dev)
+    seq = seq0.clone()
+    kv_host = kv.cpu().numpy()
+    moved = int(sum(2 * max(int(n), 0) for n in kv_host)) * E * L
+
+    def step(i):
+        if i % 100 == 0:
+            seq.copy_(seq0)
+        binding.spec_verify_kv_commit(sv.ctx, binding.SV_KV_SCRATCH, cache[i % copies], seq, kv,
+                                      scratch=scratch[i % copies])
+
+    for i in range(args.warmup):
+        step(i)
+    code, _ = sv.get_error()
+    assert code == 0, binding.strerror(code)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t_begin = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_end = time.time()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = ranks_max(ev0.elapsed_time(ev1), dev)
+    k_ms = elapsed_ms / args.steps  # the commit's two launches are the whole step
+    time.sleep(0.2)
+    clk = clocks.stop(t_begin, t_end)
+    code, _ = sv.get_error()
+    assert code == 0, binding.strerror(code)
+    peak, peak_kind = hbm_peak()
+    value = moved * args.steps * world / (elapsed_ms / 1e3) / 1e9
+    achieved = moved / (k_ms / 1e3) / 1e9
+    line = {
+        "metric": "KV commit bytes moved/sec", "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (random KV bytes; KV lengths from one batch64-bf16 verify)",
+        "config": {"workload": KV_WORKLOAD, "layers": L, "B": B, "entry_bytes": E, "window": W,
+                   "cache_positions": S, "mode": "scratch", "kv_len_sum": int(sum(max(int(n), 0) for n in kv_host)),
+                   "bytes_moved_per_step": moved,
+                   "l2": f"{copies} rotating scratch windows of {L * B * W * E / 1e6:.0f} MB",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "kv_commit", "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": moved, "avg_launch_us": k_ms * 1e3,
+                     "timed_launches": f"all {args.steps} commits of the timed loop (copy + length "
+                                       f"update launches, one length reset per 100 commits)"},
+        "e2e": None,
+        "gpu_launches": args.steps * 2,
+        "clocks": clk,
+    }
+    sv.close()
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
 # --------------------------------------------------------------------------- oracle
 
 def oracle_requests(wl, idx):
@@ -561,6 +665,8 @@ def main():
         run_reference(args)
     elif args.path == "tree":
         run_tree(args)
+    elif args.path == "kv":
+        run_kv(args)
     else:
         run_ours(args)
 

@@ -59,6 +59,8 @@ extern "C" {
                              exceeds SV_NOALLOC_SCRATCH_BYTES                  */
 #define SV_EBADTREE    7  /* device check (spec_verify_tree): a node's parent is
                              outside [0, node - 1]                             */
+#define SV_EBADKV      8  /* device check (spec_verify_kv_commit): a sequence's
+                             commit was refused                                */
 
 /* Bits of the device error word (spec_verify_get_error).  A request that
  * fails a device check gets out_tokens = -1 everywhere, out_accept_len = -1
@@ -69,6 +71,7 @@ extern "C" {
 #define SV_ERRBIT_LOGIT  4u
 #define SV_ERRBIT_TREE   8u   /* spec_verify_tree only; checked after the
                                  temperature, before tokens and logits */
+#define SV_ERRBIT_KV     16u  /* spec_verify_kv_commit only */
 
 /* ---- logit element types ---------------------------------------------- */
 #define SV_F32   0
@@ -229,10 +232,48 @@ int spec_verify_tree(spec_verify_ctx* ctx, int B, int M, int V, int mode,
                      int32_t* out_accept_len, int32_t* out_kv_len);
 
 /*
+ * spec_verify_kv_commit -- commit the verifier's KV entries of the verify
+ * window after spec_verify / spec_verify_tree (the lesson's "KV cache
+ * rollback": the verify pass extends the cache by the window; entries past
+ * the correction token are wrong; either write the window to a scratch
+ * buffer and commit the accepted entries, or keep the physical cache and cut
+ * the logical length back; exercise 4's two sequences).
+ *
+ *   mode         SV_KV_SCRATCH: the window is in `scratch` [L, B, W,
+ *                entry_bytes]; kept window position i is copied to cache
+ *                position seq_len[b] + i.
+ *                SV_KV_INPLACE: the window was written into the cache at
+ *                positions seq_len[b] + w; kept position i is moved from
+ *                seq_len[b] + pos_i to seq_len[b] + i (a chain moves
+ *                nothing); scratch may be NULL.
+ *   cache        [L, B, S, entry_bytes] device bytes (all heads' K and V of
+ *                one layer and position form one entry), 16-byte aligned;
+ *                entry_bytes a multiple of 16
+ *   seq_len      [B] int32, in/out: the logical length before the commit;
+ *                it is advanced by kv_len[b]
+ *   kv_len       [B] int32: out_kv_len of the verify step (<= 0: nothing
+ *                kept, length unchanged)
+ *   path         NULL for a chain (kept positions 0, 1, ..., kv_len - 1), or
+ *                out_path of spec_verify_tree with row stride path_stride
+ *                (kept positions 0, path[0], ..., path[kv_len - 2])
+ * Entries past the new length are left as they are.  A sequence whose
+ * commit would pass S, read outside the window, or keep positions that do
+ * not rise is left unchanged and sets SV_ERRBIT_KV.  Enqueued on the
+ * context's stream (two kernel launches); returns SV_OK, SV_EINVAL or
+ * SV_ECUDA.  Uses only the context's stream and error word.
+ */
+#define SV_KV_SCRATCH 0
+#define SV_KV_INPLACE 1
+int spec_verify_kv_commit(spec_verify_ctx* ctx, int mode, int L, int B, int S, int W,
+                          size_t entry_bytes, const void* scratch, void* cache,
+                          int32_t* seq_len, const int32_t* kv_len,
+                          const int32_t* path, int path_stride);
+
+/*
  * spec_verify_get_error -- wait for the context's stream, then return the
  * first device-detected error since the last read (SV_EBADTEMP,
- * SV_EBADTREE, SV_EBADTOKEN, SV_EBADLOGIT in that priority) or SV_OK, and
- * clear it.
+ * SV_EBADTREE, SV_EBADTOKEN, SV_EBADLOGIT, SV_EBADKV in that priority) or
+ * SV_OK, and clear it.
  * bits (may be NULL) receives the OR of SV_ERRBIT_* flags.
  */
 int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits);

@@ -28,9 +28,10 @@ Readings of points the pages leave open:
   seq_len + pos_i to seq_len + i (nothing moves for a chain).  Either way
   seq_len becomes seq_len + kv_len; entries past the new length are left as
   they are (the logical length is what hides them).
-* A commit that would pass S (or read a window position outside the
-  window) is refused for that sequence: cache and length unchanged, error
-  bit ERR_KV.
+* A commit that would pass S, read a window position outside the window,
+  or keep positions that do not rise (a walk's path always rises: a child's
+  id exceeds its parent's) is refused for that sequence: cache and length
+  unchanged, error bit ERR_KV.
 """
 
 import numpy as np
@@ -63,7 +64,9 @@ def commit(mode, cache, seq_len, kv_len, scratch=None, path=None):
         pos = kept_positions(n, None if path is None else path[b])
         start = int(seq_len[b])
         width = scratch.shape[2] if mode == SCRATCH else S - start
-        if start < 0 or start + n > S or len(pos) != n or min(pos) < 0 or max(pos) >= width:
+        rising = all(pos[i] > pos[i - 1] for i in range(1, len(pos)))
+        if start < 0 or start + n > S or len(pos) != n or min(pos) < 0 or max(pos) >= width \
+                or not rising:
             errors |= ERR_KV
             continue
         src = scratch[:, b] if mode == SCRATCH else cache[:, b, start:].copy()

@@ -14,8 +14,10 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 
-SV_OK, SV_EINVAL, SV_EBADTEMP, SV_EBADTOKEN, SV_EBADLOGIT, SV_ECUDA, SV_ESCRATCH, SV_EBADTREE = range(8)
-SV_ERRBIT_TEMP, SV_ERRBIT_TOKEN, SV_ERRBIT_LOGIT, SV_ERRBIT_TREE = 1, 2, 4, 8
+(SV_OK, SV_EINVAL, SV_EBADTEMP, SV_EBADTOKEN, SV_EBADLOGIT, SV_ECUDA, SV_ESCRATCH, SV_EBADTREE,
+ SV_EBADKV) = range(9)
+SV_ERRBIT_TEMP, SV_ERRBIT_TOKEN, SV_ERRBIT_LOGIT, SV_ERRBIT_TREE, SV_ERRBIT_KV = 1, 2, 4, 8, 16
+SV_KV_SCRATCH, SV_KV_INPLACE = 0, 1
 SV_TREE_SAMPLED, SV_TREE_TOPK = 0, 1
 SV_F32, SV_BF16 = 0, 1
 SV_NUM_KERNELS = 2
@@ -30,7 +32,7 @@ EXPORTS = (
     "spec_verify_init", "spec_verify", "spec_verify_get_error", "spec_verify_debug_stats",
     "spec_verify_profile", "spec_verify_profile_read", "spec_verify_launches_per_call",
     "spec_verify_debug_philox", "spec_verify_destroy", "spec_verify_strerror",
-    "spec_verify_noalloc", "spec_verify_tree",
+    "spec_verify_noalloc", "spec_verify_tree", "spec_verify_kv_commit",
 )
 
 _lib = None
@@ -64,6 +66,8 @@ def load():
     lib.spec_verify_launches_per_call.argtypes = []
     lib.spec_verify_debug_philox.argtypes = [c_u64, c_void, c_void, c_int, c_void]
     lib.spec_verify_destroy.argtypes = [c_void]
+    lib.spec_verify_kv_commit.argtypes = [c_void, c_int, c_int, c_int, c_int, c_int, ctypes.c_size_t,
+                                          c_void, c_void, c_void, c_void, c_void, c_int]
     lib.spec_verify_tree.argtypes = [c_void, c_int, c_int, c_int, c_int, c_void, c_void, c_void,
                                      c_void, c_void, c_u64, c_void, c_void, c_void, c_void]
     lib.spec_verify_noalloc.argtypes = [c_int, c_int, c_int, c_int, c_void, c_void, c_void, c_void,
@@ -191,6 +195,32 @@ def spec_verify_tree(ctx, mode, target_logits, draft_logits, parents, draft_toke
                                    _ptr(temperature), ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF),
                                    _ptr(out_tokens), _ptr(out_path), _ptr(out_accept_len),
                                    _ptr(out_kv_len)), "spec_verify_tree")
+
+
+def spec_verify_kv_commit(ctx, mode, cache, seq_len, kv_len, scratch=None, path=None):
+    """Commit the kept window entries.  cache [L, B, S, E] and scratch
+    [L, B, W, E] are uint8 CUDA tensors (E bytes per layer and position);
+    seq_len [B] int32 is advanced in place; path [B, P] int32 (a tree's
+    out_path) or None for a chain."""
+    if cache.dim() != 4 or cache.dtype != torch.uint8:
+        raise ValueError("cache must be a uint8 tensor [L, B, S, E]")
+    L, B, S, E = cache.shape
+    _require(cache, "cache", (L, B, S, E), (torch.uint8,))
+    _require(seq_len, "seq_len", (B,), (torch.int32,))
+    _require(kv_len, "kv_len", (B,), (torch.int32,))
+    W = 0
+    if mode == SV_KV_SCRATCH:
+        _require(scratch, "scratch", scratch.shape, (torch.uint8,))
+        if scratch.dim() != 4 or tuple(scratch.shape[:2]) != (L, B) or scratch.shape[3] != E:
+            raise ValueError("scratch must be [L, B, W, E] like the cache")
+        W = scratch.shape[2]
+    stride = 0
+    if path is not None:
+        _require(path, "path", path.shape, (torch.int32,))
+        stride = path.shape[1]
+    _check(load().spec_verify_kv_commit(ctx, int(mode), int(L), int(B), int(S), int(W), int(E),
+                                        _ptr(scratch), _ptr(cache), _ptr(seq_len), _ptr(kv_len),
+                                        _ptr(path), int(stride)), "spec_verify_kv_commit")
 
 
 def spec_verify_get_error(ctx):

@@ -81,6 +81,9 @@ const char* spec_verify_strerror(int code) {
     case SV_EBADLOGIT: return "a logit row holds NaN or +inf, or has no finite entry";
     case SV_ECUDA: return "a CUDA runtime call failed";
     case SV_EBADTREE: return "a draft-tree node's parent is outside [0, node - 1]";
+    case SV_EBADKV:
+      return "a KV commit would pass the cache length, read outside the window, or keep "
+             "positions that do not rise";
     case SV_ESCRATCH:
       return "the problem needs more working memory than spec_verify_noalloc's static array "
              "(SV_NOALLOC_SCRATCH_BYTES) holds";
@@ -259,6 +262,35 @@ int spec_verify_tree(spec_verify_ctx* ctx, int B, int M, int V, int mode,
   return SV_OK;
 }
 
+int spec_verify_kv_commit(spec_verify_ctx* ctx, int mode, int L, int B, int S, int W,
+                          size_t entry_bytes, const void* scratch, void* cache, int32_t* seq_len,
+                          const int32_t* kv_len, const int32_t* path, int path_stride) {
+  if (ctx == nullptr || (mode != SV_KV_SCRATCH && mode != SV_KV_INPLACE) || L < 0 || B < 0 ||
+      S < 1 || entry_bytes == 0 || entry_bytes % 16 != 0)
+    return SV_EINVAL;
+  if (mode == SV_KV_SCRATCH && (W < 1 || scratch == nullptr || !aligned16(scratch)))
+    return SV_EINVAL;
+  if (path != nullptr && path_stride < 0) return SV_EINVAL;
+  if (L == 0 || B == 0) return SV_OK;
+  if (cache == nullptr || !aligned16(cache) || seq_len == nullptr || kv_len == nullptr)
+    return SV_EINVAL;
+  sv::KvProblem p;
+  p.mode = mode;
+  p.L = L;
+  p.B = B;
+  p.S = S;
+  p.W = mode == SV_KV_SCRATCH ? W : 0;
+  p.E = entry_bytes;
+  p.scratch = scratch;
+  p.cache = cache;
+  p.seq_len = seq_len;
+  p.kv_len = kv_len;
+  p.path = path;
+  p.path_stride = path_stride;
+  p.err = ctx->w.err;
+  return sv::launch_kv_commit(p, ctx->stream) == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
 int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits) {
   if (ctx == nullptr) return SV_EINVAL;
   unsigned word = 0;
@@ -272,6 +304,7 @@ int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits) {
   if (word & SV_ERRBIT_TREE) return SV_EBADTREE;
   if (word & SV_ERRBIT_TOKEN) return SV_EBADTOKEN;
   if (word & SV_ERRBIT_LOGIT) return SV_EBADLOGIT;
+  if (word & SV_ERRBIT_KV) return SV_EBADKV;
   return SV_OK;
 }
 

@@ -37,6 +37,11 @@ constexpr unsigned kErrTemp = 1u;
 constexpr unsigned kErrToken = 2u;
 constexpr unsigned kErrLogit = 4u;
 constexpr unsigned kErrTree = 8u;
+constexpr unsigned kErrKv = 16u;
+
+// How the verify window's KV entries were written.
+constexpr int kKvScratch = 0;  // to a scratch window [L, B, W, E]
+constexpr int kKvInplace = 1;  // into the cache right after each sequence's length
 
 // How the children of a draft-tree node were drafted.
 constexpr int kTreeSampled = 0;  // independent draws from the node's draft row
@@ -95,6 +100,18 @@ struct TreeProblem {
   int32_t* out_kv;           // [B]
 };
 
+struct KvProblem {
+  int mode, L, B, S, W;
+  size_t E;                  // bytes per (layer, sequence, position); multiple of 16
+  const void* scratch;       // [L, B, W, E] (scratch mode)
+  void* cache;               // [L, B, S, E]
+  int32_t* seq_len;          // [B], in / out
+  const int32_t* kv_len;     // [B]
+  const int32_t* path;       // [B, path_stride] accepted node ids, or nullptr (chain)
+  int path_stride;
+  unsigned* err;
+};
+
 struct Workspace {
   Partial* partials;     // [B][2N+1][S1]: target rows 0..N, then draft rows 0..N-1
                          // (tree: [B][2(M+1)][S1], target rows then draft rows 0..M)
@@ -118,6 +135,7 @@ cudaError_t launch_tree_rowstats(int dtype, bool vec, const TreeProblem& p, cons
                                  cudaStream_t s);
 cudaError_t launch_tree_walk(int dtype, bool vec, const TreeProblem& p, const Workspace& w,
                              cudaStream_t s);
+cudaError_t launch_kv_commit(const KvProblem& p, cudaStream_t s);
 cudaError_t launch_philox_probe(unsigned long long seed, const uint32_t* ctr3, uint32_t* out4,
                                 int n, cudaStream_t s);
 

@@ -1,0 +1,129 @@
+// KV-cache commit after verification ("Speculative Decoding and EAGLE-3"
+// lesson, section "KV cache rollback", and exercise 4): keep the window
+// entries of the verified input token and the accepted drafts, drop the
+// rest, and advance each sequence's logical length by out_kv_len.
+//
+// Cache [L, B, S, E bytes], window [L, B, W, E].  Kept window positions:
+// 0, then 1, 2, ... (chain) or the accepted node ids out_path[b, :] (tree),
+// out_kv_len[b] of them.  SCRATCH: kept position i is copied from the
+// scratch window to cache position seq_len + i.  IN-PLACE: the window was
+// written at cache positions seq_len + w; kept position i moves from
+// seq_len + pos_i to seq_len + i (pos_i >= i because kept positions rise, so
+// a thread that walks i upwards never reads an entry it has already
+// overwritten); entries already in place are not touched.  A sequence whose
+// commit would pass S, read outside the window, or whose kept positions do
+// not rise is left unchanged and flagged.
+//
+// kv_commit_kernel: one thread per 16-byte column of one (layer, sequence)
+// entry, copying the kept positions eight at a time (eight loads in flight
+// per thread) -- a plain bandwidth-bound copy with coalesced 16-byte
+// accesses (consecutive threads, consecutive columns).  kv_advance_kernel then moves the lengths (a second launch, so
+// no CTA of the copy can read a length another has already advanced).
+
+#include <cstdint>
+
+#include "sv_device.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kKvThreads = 256;
+constexpr int kKvBatch = 8;
+
+// Window position of kept entry i, or -1 past the path.
+__device__ __forceinline__ int kept_pos(const KvProblem& p, int b, int i) {
+  if (i == 0) return 0;
+  if (p.path == nullptr) return i;
+  return p.path[static_cast<size_t>(b) * p.path_stride + (i - 1)];
+}
+
+// Whether sequence b's commit is valid (the same answer in every thread).
+__device__ __forceinline__ bool commit_ok(const KvProblem& p, int b, int n, int start) {
+  if (start < 0 || static_cast<long long>(start) + n > p.S) return false;
+  if (p.path != nullptr && n - 1 > p.path_stride) return false;
+  const int width = p.mode == kKvScratch ? p.W : p.S - start;
+  int prev = -1;
+  for (int i = 0; i < n; ++i) {
+    const int w = kept_pos(p, b, i);
+    if (w <= prev || w >= width) return false;
+    prev = w;
+  }
+  return true;
+}
+
+template <bool kScratch>
+__global__ void __launch_bounds__(kKvThreads) kv_commit_kernel(KvProblem p) {
+  const long long cols = static_cast<long long>(p.E / 16);
+  const long long slices = (cols + kKvThreads - 1) / kKvThreads;
+  const long long lb = blockIdx.x / slices;
+  const long long col = (blockIdx.x - lb * slices) * kKvThreads + threadIdx.x;
+  const int l = static_cast<int>(lb / p.B);
+  const int b = static_cast<int>(lb - static_cast<long long>(l) * p.B);
+  const int n = p.kv_len[b];
+  if (n <= 0) return;
+  const int start = p.seq_len[b];
+  if (!commit_ok(p, b, n, start)) {
+    if (l == 0 && col == 0) atomicOr(p.err, kErrKv);
+    return;
+  }
+  if (col >= cols) return;
+  const size_t E = p.E;
+  unsigned char* cache = static_cast<unsigned char*>(p.cache) +
+                         (static_cast<size_t>(l) * p.B + b) * p.S * E + static_cast<size_t>(start) * E +
+                         static_cast<size_t>(col) * 16;
+  const unsigned char* src = kScratch
+                                 ? static_cast<const unsigned char*>(p.scratch) +
+                                       (static_cast<size_t>(l) * p.B + b) * p.W * E + static_cast<size_t>(col) * 16
+                                 : cache;
+  // kKvBatch kept entries at a time: all their loads in flight before any
+  // store.  In place this is still safe: a batch reads positions
+  // pos_i >= i, above every position written so far or by this batch.
+  for (int i0 = 0; i0 < n; i0 += kKvBatch) {
+    uint4 v[kKvBatch];
+    int w[kKvBatch];
+#pragma unroll
+    for (int k = 0; k < kKvBatch; ++k) {
+      const int i = i0 + k;
+      w[k] = i < n ? kept_pos(p, b, i) : i;
+      if (i < n && (kScratch || w[k] != i))
+        v[k] = kScratch ? ld_stream16(src + static_cast<size_t>(w[k]) * E)
+                        : *reinterpret_cast<const uint4*>(src + static_cast<size_t>(w[k]) * E);
+    }
+#pragma unroll
+    for (int k = 0; k < kKvBatch; ++k) {
+      const int i = i0 + k;
+      if (i < n && (kScratch || w[k] != i))  // entries already in place are not touched
+        *reinterpret_cast<uint4*>(cache + static_cast<size_t>(i) * E) = v[k];
+    }
+  }
+}
+
+__global__ void kv_advance_kernel(KvProblem p) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= p.B) return;
+  const int n = p.kv_len[b];
+  if (n <= 0) return;
+  const int start = p.seq_len[b];
+  if (commit_ok(p, b, n, start)) p.seq_len[b] = start + n;
+}
+
+}  // namespace
+
+cudaError_t launch_kv_commit(const KvProblem& p, cudaStream_t s) {
+  if (p.B <= 0 || p.L <= 0) return cudaSuccess;
+  const long long cols = static_cast<long long>(p.E / 16);
+  const long long blocks = static_cast<long long>(p.L) * p.B * ((cols + kKvThreads - 1) / kKvThreads);
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if (blocks > 0) {
+    if (p.mode == kKvScratch)
+      kv_commit_kernel<true><<<dim3(static_cast<unsigned>(blocks)), kKvThreads, 0, s>>>(p);
+    else
+      kv_commit_kernel<false><<<dim3(static_cast<unsigned>(blocks)), kKvThreads, 0, s>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  kv_advance_kernel<<<(p.B + 255) / 256, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace sv

@@ -31,7 +31,7 @@
 // at its token (thread i holds node i), then all of them run the same walk:
 // one thread decides, and each rejection in SAMPLED mode triggers a pass in
 // which every CTA sums max(r(t) - p(t), 0) over its share of the vocabulary
-// and the eight partial sums are exchanged through distributed shared
+// and the cluster's partial sums are exchanged through distributed shared
 // memory after a cluster barrier, so every CTA holds the same normaliser.
 // The final draw computes, per level-1 block, the block's mass and the token
 // levels 2-4 would pick in it (each CTA its own blocks), then rank 0 picks
@@ -49,7 +49,15 @@
 namespace sv {
 namespace {
 
-constexpr int kTreeCluster = 8;
+// Tuning constants, overridable at build time (-D<name>=<value>): CTAs per
+// request cluster and resident CTAs per SM the walk kernel is built for.
+#ifndef SV_TREE_CLUSTER
+#define SV_TREE_CLUSTER 8
+#endif
+#ifndef SV_TREE_MINB
+#define SV_TREE_MINB 2
+#endif
+constexpr int kTreeCluster = SV_TREE_CLUSTER;
 constexpr int kMaxNodes = kST;  // root + up to 255 draft nodes, one thread each
 constexpr int kNoNode = INT_MAX;
 
@@ -126,41 +134,30 @@ __device__ __forceinline__ float ld_dsmem(const float* local, unsigned rank) {
 // The distribution a node's token is drawn from, or that its next child is
 // tested against, as a per-token function of the two logits.
 //   kQ:       q_t = 2^(z_t k - cq) / sq
-//   kSampled: r_m after m rejections: r_0 = q, r_j = (r_{j-1} - p)_+ * inv[j-1]
-//             (inv = 1 / sum of the positive part; 0 marks a step that left r
-//             unchanged because that sum was 0)
-//   kTopk:    q with the rejected tokens removed (unnormalised)
-// For a draw (scale-free) the last residual step is left unnormalised, so a
-// one-child chain computes exactly the values of the chain sampler.
+//   kSampled: after m rejections the residual r_m is a single clipped line in
+//             (q, p): r_0 = q and r_{m+1} = (r_m - p)_+ / S_{m+1} give
+//             r_m = (q - c_m p)_+ / D_m with c_{m+1} = c_m + D_m, D_{m+1} =
+//             D_m S_{m+1} (c_0 = 0, D_0 = 1; a step whose sum S is 0 leaves r
+//             unchanged).  The law evaluates (q - c p)_+ * scale.
+//   kTopk:    q with the m rejected tokens removed (unnormalised)
 struct NodeLaw {
   static constexpr int kQ = 0, kSampled = 1, kTopk = 2;
   int kind;
   float k, cq, inv_sq, cp, inv_sp;
-  int m;
-  const float* inv;
+  float c, scale;  // kSampled
+  int m;           // kTopk: rejected tokens in rej[0, m)
   const int* rej;
-  bool draw;
   __device__ __forceinline__ float q(float zt) const { return ex2(fmaf(zt, k, -cq)) * inv_sq; }
   __device__ __forceinline__ float p(float yt) const { return ex2(fmaf(yt, k, -cp)) * inv_sp; }
   __device__ __forceinline__ float r(float zt, float yt, int t) const {
     float v = q(zt);
     if (kind == kSampled) {
-      const float pt = p(yt);
-      for (int j = 0; j < m; ++j) {
-        if (inv[j] > 0.f) {
-          v = fmaxf(v - pt, 0.f);
-          if (!(draw && j == m - 1)) v *= inv[j];
-        }
-      }
+      v = fmaxf(fmaf(-c, p(yt), v), 0.f) * scale;
     } else if (kind == kTopk) {
       for (int j = 0; j < m; ++j)
         if (rej[j] == t) v = 0.f;
     }
     return v;
-  }
-  // the positive part of r - p (a residual step's mass at t)
-  __device__ __forceinline__ float excess(float zt, float yt, int t) const {
-    return fmaxf(r(zt, yt, t) - p(yt), 0.f);
   }
 };
 
@@ -213,19 +210,19 @@ __device__ __forceinline__ void seg_sums(const T* z, const T* y, bool need_y, in
 constexpr int kActContinue = 0, kActPass = 1, kActBonus = 2, kActResidual = 3;
 
 template <typename T, bool kVecPath>
-__global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, 2)
+__global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_TREE_MINB)
     tree_walk_kernel(TreeProblem p, Workspace w) {
   using E = Elem<T>;
   __shared__ int s_par[kMaxNodes], s_tok[kMaxNodes], s_first[kMaxNodes], s_next[kMaxNodes];
   __shared__ int s_gidx[kMaxNodes], s_path[kMaxNodes], s_rej[kMaxNodes];
   __shared__ float s_cq[kMaxNodes], s_sq[kMaxNodes], s_cp[kMaxNodes], s_sp[kMaxNodes];
-  __shared__ float s_zc[kMaxNodes], s_yc[kMaxNodes], s_inv[kMaxNodes];
+  __shared__ float s_zc[kMaxNodes], s_yc[kMaxNodes];
   __shared__ float s_part[2];
   __shared__ BlockScratch sc;
   __shared__ Job s_job;
   __shared__ unsigned s_err;
   __shared__ int s_node, s_depth, s_child, s_m, s_plen, s_act;
-  __shared__ float s_rej_mass;
+  __shared__ float s_rej_mass, s_c, s_d;  // s_c, s_d: c_m and D_m of the residual
 
   const int b = blockIdx.x / kTreeCluster;
   const unsigned rank = cluster_rank();
@@ -363,6 +360,8 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, 2)
     s_m = 0;
     s_plen = 0;
     s_rej_mass = 0.f;
+    s_c = 0.f;
+    s_d = 1.f;
   }
   __syncthreads();
   const bool topk = p.mode == kTreeTopk;
@@ -391,10 +390,9 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, 2)
             const float lr = fmaf(zx - yx, k, -(cq - cp)) + log2f(sp / sq);
             ok = u < fminf(1.f, exp2f(lr));
           } else {
-            float v = exp2f(fmaf(zx, k, -cq)) / sq;
+            const float qx = exp2f(fmaf(zx, k, -cq)) / sq;
             const float px = exp2f(fmaf(yx, k, -cp)) / sp;
-            for (int j = 0; j < m; ++j)
-              if (s_inv[j] > 0.f) v = fmaxf(v - px, 0.f) * s_inv[j];
+            const float v = fmaxf(fmaf(-s_c, px, qx), 0.f) / s_d;  // r_m(x)
             ok = u < fminf(1.f, v / px);
           }
         } else {
@@ -419,6 +417,8 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, 2)
           s_child = s_first[c];
           s_m = 0;
           s_rej_mass = 0.f;
+          s_c = 0.f;
+          s_d = 1.f;
         } else if (!topk) {
           act = kActPass;
         }
@@ -431,15 +431,17 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, 2)
     if (act != kActPass) break;
     // Residual pass: every CTA sums (r_m - p)_+ over its level-1 blocks.
     const int node = s_node;
-    NodeLaw law{NodeLaw::kSampled, k, s_cq[node], 1.f / s_sq[node], s_cp[node], 1.f / s_sp[node],
-                s_m, s_inv, s_rej, false};
+    // S_{m+1} = sum_t (q - c_{m+1} p)_+ / D_m, c_{m+1} = c_m + D_m
+    const float c_next = s_c + s_d;
+    const NodeLaw law{NodeLaw::kSampled, k, s_cq[node], 1.f / s_sq[node], s_cp[node],
+                      1.f / s_sp[node], c_next, 1.f / s_d, 0, s_rej};
     const T* z = zbase + static_cast<size_t>(node) * V;
     const T* y = ybase + static_cast<size_t>(node) * V;
     float acc = 0.f;
     for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster) {
       float h0, h1;
       seg_sums<T, kVecPath>(z, y, true, c * kLevel1 + i * kSegTok, min(V, (c + 1) * kLevel1),
-                            [&](float zt, float yt, int t) { return law.excess(zt, yt, t); }, h0, h1);
+                            [&](float zt, float yt, int t) { return law.r(zt, yt, t); }, h0, h1);
       acc += h0 + h1;
     }
     acc = cta_sum(acc, sc.red);
@@ -448,7 +450,10 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, 2)
     if (i == 0) {
       float total = 0.f;
       for (unsigned r = 0; r < kTreeCluster; ++r) total += ld_dsmem(&s_part[pass & 1], r);
-      s_inv[s_m] = total > 0.f ? 1.f / total : 0.f;
+      if (total > 0.f) {  // else the residual step leaves r as it is
+        s_c = c_next;
+        s_d *= total;
+      }
       s_m += 1;
       s_child = s_next[s_child];
     }
@@ -460,9 +465,10 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, 2)
   const int node = s_node;
   const int depth = s_depth;
   const bool bonus = s_act == kActBonus;
-  NodeLaw law{bonus ? NodeLaw::kQ : (topk ? NodeLaw::kTopk : NodeLaw::kSampled), k, s_cq[node],
-              1.f / s_sq[node], s_cp[node], 1.f / s_sp[node], s_m, s_inv, s_rej, true};
-  const bool need_y = law.kind == NodeLaw::kSampled;
+  // a draw is scale-free: r_m is taken as (q - c_m p)_+ without the 1 / D_m
+  const NodeLaw law{bonus ? NodeLaw::kQ : (topk ? NodeLaw::kTopk : NodeLaw::kSampled), k,
+                    s_cq[node], 1.f / s_sq[node], s_cp[node], 1.f / s_sp[node], s_c, 1.f, s_m, s_rej};
+  const bool need_y = law.kind == NodeLaw::kSampled && s_m > 0;
   const T* z = zbase + static_cast<size_t>(node) * V;
   const T* y = ybase + static_cast<size_t>(node) * V;
   if (i == 0) philox_uniforms4(p.seed, b, depth, 1, s_job.u);

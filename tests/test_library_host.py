@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_strerror_and_launch_count(lib):
     assert binding.strerror(0) == "success"
-    for code in range(1, 6):
+    for code in range(1, 9):
         assert binding.strerror(code) != "unknown error code"
     assert binding.strerror(99) == "unknown error code"
     assert binding.spec_verify_launches_per_call() == binding.SV_NUM_KERNELS == 2
@@ -66,6 +66,10 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.spec_verify_destroy(None) == binding.SV_OK
     assert lib.spec_verify_debug_philox(0, None, None, -1, None) == binding.SV_EINVAL
     assert lib.spec_verify_debug_philox(0, None, None, 0, None) == binding.SV_OK
+    assert lib.spec_verify_tree(None, 1, 1, 1, 0, None, None, None, None, None, 0, None, None, None,
+                                None) == binding.SV_EINVAL
+    assert lib.spec_verify_kv_commit(None, 0, 1, 1, 1, 1, 16, None, None, None, None, None, 0) \
+        == binding.SV_EINVAL
 
 
 def test_binding_refuses_to_run_without_library(monkeypatch, tmp_path):

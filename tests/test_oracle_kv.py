@@ -84,3 +84,13 @@ def test_failed_and_overflowing_sequences_are_left_alone():
     got, new_len, err = okv.commit(okv.SCRATCH, cache.copy(), [2, 6, 1], [-1, 3, 0], scratch=scratch)
     assert err == okv.ERR_KV and new_len.tolist() == [2, 6, 1]
     np.testing.assert_array_equal(got, cache)
+
+
+def test_non_rising_path_is_refused():
+    L, B, S, E, W = 1, 1, 10, 16, 7
+    cache = _pattern((L, B, S, E), 4)
+    scratch = _pattern((L, B, W, E), 5)
+    got, new_len, err = okv.commit(okv.SCRATCH, cache.copy(), [1], [3], scratch=scratch,
+                                   path=np.array([[4, 2]]))
+    assert err == okv.ERR_KV and new_len.tolist() == [1]
+    np.testing.assert_array_equal(got, cache)
