@@ -318,6 +318,67 @@ def verify_request(z_raw, y_raw, drafts, temperature, seed, b, dtype):
     return 0, tokens, a, kv, decisions
 
 
+def verify_request_lazy(z_raw, y_raw, drafts, temperature, seed, b, dtype):
+    """The lazy reading of one request: the same walk, but a row is only
+    read (and so only checked) when the walk reaches it -- target and draft
+    row j-1 for the test at position j, target row N for the bonus.  Rows
+    past the point where the walk stops are never looked at, so a bad row
+    there is not an error.  Otherwise identical to ``verify_request``."""
+    z_raw = np.asarray(z_raw)
+    n = z_raw.shape[0] - 1
+    vocab = z_raw.shape[1]
+    t = float(np.float32(temperature))
+    if not temperature_is_valid(t):
+        return ERR_TEMP, None, None, None, []
+    drafts = [int(x) for x in np.asarray(drafts).reshape(-1)[:n]]
+    if any(d < 0 or d >= vocab for d in drafts):
+        return ERR_TOKEN, None, None, None, []
+    z = logits_to_f64(z_raw, dtype)
+    y = logits_to_f64(y_raw, dtype) if (n > 0 and t != 0.0) else None
+
+    class _Bad(Exception):
+        pass
+
+    def target(j):
+        if not row_is_valid(z[j]):
+            raise _Bad
+        return z[j]
+
+    def draft(j):
+        if not row_is_valid(y[j]):
+            raise _Bad
+        return y[j]
+
+    try:
+        if t == 0.0:
+            tokens = []
+            for j in range(1, n + 1):
+                g = argmax_lowest(target(j - 1))
+                tokens.append(g)
+                if drafts[j - 1] != g:
+                    return 0, tokens, j - 1, j, []
+            tokens.append(argmax_lowest(target(n)))
+            return 0, tokens, n, n + 1, []
+        q_rows = _LazyRows(lambda j: softmax(target(j), t))
+        p_rows = _LazyRows(lambda j: softmax(draft(j), t))
+        tokens, a, kv, decisions = walk(q_rows, p_rows, drafts, philox_draws(seed, b))
+        return 0, tokens, a, kv, decisions
+    except _Bad:
+        return ERR_LOGIT, None, None, None, []
+
+
+class _LazyRows:
+    """Rows computed on first use (for the lazy reading)."""
+
+    def __init__(self, make):
+        self.make, self.cache = make, {}
+
+    def __getitem__(self, j):
+        if j not in self.cache:
+            self.cache[j] = self.make(j)
+        return self.cache[j]
+
+
 # --------------------------------------------------------------------------
 # The batch
 # --------------------------------------------------------------------------
@@ -334,9 +395,10 @@ class Result:
         self.decisions = [[] for _ in range(batch)]
 
 
-def verify(target, draft, drafts, temperature, seed, dtype):
+def verify(target, draft, drafts, temperature, seed, dtype, lazy=False):
     """Batched verify: target [B, N+1, V], draft [B, N, V] (may be None when
-    every T is 0), drafts [B, N] int, temperature [B] float32, 64-bit seed.
+    every T is 0), drafts [B, N] int, temperature [B] float32, 64-bit seed;
+    ``lazy`` selects ``verify_request_lazy`` (rows checked only when read).
 
     A request that fails a check gets tokens -1, accept_len -1, kv_len 0,
     and its error bit is OR-ed into ``errors``.
@@ -349,8 +411,8 @@ def verify(target, draft, drafts, temperature, seed, dtype):
     temperature = np.asarray(temperature, dtype=np.float32).reshape(batch)
     for b in range(batch):
         y_b = None if draft is None or n == 0 else np.asarray(draft[b])
-        err, tokens, a, kv, dec = verify_request(
-            target[b], y_b, drafts[b], temperature[b], seed, b, dtype)
+        one = verify_request_lazy if lazy else verify_request
+        err, tokens, a, kv, dec = one(target[b], y_b, drafts[b], temperature[b], seed, b, dtype)
         if err:
             res.errors |= err
             res.request_errors[b] = err
