@@ -16,6 +16,10 @@ bracketed by barriers and the slowest rank's time is used.
 --impl reference times the CPU oracle (float64, one host thread) on the same
 metric, a bounded sample of requests per step.
 
+--path lazy measures spec_verify_lazy on the same batch64-bf16 workload
+(rows read only up to each request's first rejection); its roofline counts
+the rows the walks actually read, averaged over 16 seeds.
+
 --path tree measures spec_verify_tree instead, on tree222-bf16: B=64
 requests, each a full [2, 2, 2] draft tree (14 nodes, 8 leaves) whose
 children are independent draws from the drafter, V=128256 bf16; one step is
@@ -62,9 +66,10 @@ def parse():
     ap.add_argument("--copies", type=int, default=3, help="rotating input copies in HBM")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", default="chain", choices=["chain", "tree", "kv"],
+    ap.add_argument("--path", default="chain", choices=["chain", "lazy", "tree", "kv"],
                     help="chain: spec_verify on batch64-bf16 (the headline); tree: "
-                         "spec_verify_tree on tree222-bf16; kv: spec_verify_kv_commit")
+                         "spec_verify_tree on tree222-bf16; kv: spec_verify_kv_commit; lazy: "
+                         "spec_verify_lazy on batch64-bf16")
     return ap.parse_args()
 
 
@@ -222,9 +227,12 @@ def run_ours(args):
     p_tok, p_temp = P(tokens.data_ptr()), P(temperature.data_ptr())
     p_ot, p_oa, p_ok = P(out_t.data_ptr()), P(out_a.data_ptr()), P(out_k.data_ptr())
 
+    lazy = args.path == "lazy"
+    entry = lib.spec_verify_lazy if lazy else lib.spec_verify
+
     def step(i):
         zt, yt = ptrs[i % copies]
-        rc = lib.spec_verify(sv.ctx, B, N, V, zt, yt, p_tok, p_temp, ctypes.c_uint64(i), p_ot, p_oa, p_ok)
+        rc = entry(sv.ctx, B, N, V, zt, yt, p_tok, p_temp, ctypes.c_uint64(i), p_ot, p_oa, p_ok)
         if rc != 0:
             raise binding.SpecVerifyError(rc, "spec_verify")
 
@@ -259,7 +267,7 @@ def run_ours(args):
     clk = clocks.stop(t_begin, t_end)
     elapsed_ms = ranks_max(elapsed_ms, dev)
     value = whole_job_rate(B * N, args.steps, world, elapsed_ms)
-    bytes_per_launch = wl.bytes_read()
+    bytes_per_launch = lazy_bytes(wl, sv, step, out_a) if lazy else wl.bytes_read()
     rowstats_ms = kernel_ms["rowstats"] / max(calls, 1)
     achieved = bytes_per_launch / (rowstats_ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
@@ -282,7 +290,8 @@ def run_ours(args):
         d_draft.copy_(h_draft, non_blocking=True)
         tokens.copy_(h_tokens, non_blocking=True)
         temperature.copy_(h_temp, non_blocking=True)
-        binding.spec_verify(sv.ctx, d_target, d_draft, tokens, temperature, i, out_t, out_a, out_k)
+        (binding.spec_verify_lazy if lazy else binding.spec_verify)(
+            sv.ctx, d_target, d_draft, tokens, temperature, i, out_t, out_a, out_k)
         h_out_t.copy_(out_t, non_blocking=True)
         h_out_a.copy_(out_a, non_blocking=True)
         h_out_k.copy_(out_k, non_blocking=True)
@@ -317,7 +326,7 @@ def run_ours(args):
         "dtype": "bf16 logits, f32 accumulate",
         "data": "synthetic (seeded Zipf logits, Gaussian draft noise)",
         "config": {
-            "workload": WORKLOAD, "B": B, "N": N, "V": V, "logits": "bf16",
+            "workload": WORKLOAD + ("-lazy" if lazy else ""), "B": B, "N": N, "V": V, "logits": "bf16",
             "temperatures": "per request from {0, 0.7, 1.0}",
             "sampled_requests": int((wl.temperature > 0).sum()),
             "bytes_read_per_step": bytes_per_launch,
@@ -326,16 +335,18 @@ def run_ours(args):
             "parallelism": f"replicas x{world} (requests shard, no collective)",
         },
         "roofline": {
-            "bound": "hbm", "kernel": "rowstats", "achieved": achieved, "peak": peak,
+            "bound": "hbm", "kernel": "lazy" if lazy else "rowstats", "achieved": achieved, "peak": peak,
             "peak_kind": f"{peak_kind} copy bandwidth", "unit": "GB/s", "frac": achieved / peak,
-            "traffic": traffic_per_launch(), "algorithmic_bytes_per_launch": bytes_per_launch,
+            "traffic": None if lazy else traffic_per_launch(),
+            "algorithmic_bytes_per_launch": bytes_per_launch,
             "avg_launch_us": rowstats_ms * 1e3,
             "timed_launches": f"{calls} of {args.steps} calls (every {PROFILE_EVERY}th)",
         },
-        "kernel_us_per_step": {k: v / max(calls, 1) * 1e3 for k, v in kernel_ms.items()},
+        "kernel_us_per_step": ({"lazy": kernel_ms["rowstats"] / max(calls, 1) * 1e3} if lazy else
+                               {k: v / max(calls, 1) * 1e3 for k, v in kernel_ms.items()}),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": args.steps * binding.spec_verify_launches_per_call(),
+        "gpu_launches": args.steps * (1 if lazy else binding.spec_verify_launches_per_call()),
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -345,6 +356,32 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line))
+
+
+def lazy_bytes(wl, sv, step, out_a):
+    """Logit bytes the lazy walks read, averaged over 16 seeds: per request
+    the target rows up to its stop and, when sampled, the draft rows it
+    tested plus the re-read of the row (pair) the final token is drawn from."""
+    import torch
+    B, N, V = wl.shape
+    esize = wl.target.element_size()
+    temps = wl.temperature.numpy()
+    total = 0
+    for s in range(16):
+        step(s)
+        torch.cuda.synchronize()
+        acc = out_a.cpu().numpy()
+        rows = 0
+        for b in range(B):
+            a = int(acc[b])
+            if a < 0:
+                continue
+            rows += a + 1                                   # target rows 0..a
+            if temps[b] > 0:
+                rows += min(a + 1, N)                       # draft rows tested
+                rows += 2 if a < N else 1                   # residual pair / bonus row re-read
+        total += rows * V * esize
+    return total // 16
 
 
 # --------------------------------------------------------------------------- tree

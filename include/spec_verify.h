@@ -232,6 +232,28 @@ int spec_verify_tree(spec_verify_ctx* ctx, int B, int M, int V, int mode,
                      int32_t* out_accept_len, int32_t* out_kv_len);
 
 /*
+ * spec_verify_lazy -- the same step as spec_verify (same arguments, same
+ * outputs bit for bit on valid inputs), reading each request's rows only as
+ * far as its walk goes: position j reads target row j-1 and draft row j-1
+ * (target row j-1 alone at T = 0), the bonus / last greedy argmax reads
+ * target row N, and rows after the first rejection are never read (the
+ * lesson's "Invariant: Leviathan rejection sampling": the walk is left to
+ * right and stops at the first rejection).  Fewer bytes when drafts are
+ * rejected early; one dependent pass per position instead of one pass over
+ * everything.  One kernel launch (a thread-block cluster per request).
+ * Device checks: the temperature and every token first; a row is checked
+ * when the walk reads it, so a bad row past the stop is not an error (the
+ * one way its outputs can differ from spec_verify's).  Does not write the
+ * statistics read by spec_verify_debug_stats.  Returns SV_OK, SV_EINVAL
+ * (nothing enqueued) or SV_ECUDA.
+ */
+int spec_verify_lazy(spec_verify_ctx* ctx, int B, int N, int V,
+                     const void* target_logits, const void* draft_logits,
+                     const int32_t* draft_tokens, const float* temperature,
+                     uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len,
+                     int32_t* out_kv_len);
+
+/*
  * spec_verify_kv_commit -- commit the verifier's KV entries of the verify
  * window after spec_verify / spec_verify_tree (the lesson's "KV cache
  * rollback": the verify pass extends the cache by the window; entries past

@@ -32,7 +32,7 @@ EXPORTS = (
     "spec_verify_init", "spec_verify", "spec_verify_get_error", "spec_verify_debug_stats",
     "spec_verify_profile", "spec_verify_profile_read", "spec_verify_launches_per_call",
     "spec_verify_debug_philox", "spec_verify_destroy", "spec_verify_strerror",
-    "spec_verify_noalloc", "spec_verify_tree", "spec_verify_kv_commit",
+    "spec_verify_noalloc", "spec_verify_tree", "spec_verify_kv_commit", "spec_verify_lazy",
 )
 
 _lib = None
@@ -66,6 +66,7 @@ def load():
     lib.spec_verify_launches_per_call.argtypes = []
     lib.spec_verify_debug_philox.argtypes = [c_u64, c_void, c_void, c_int, c_void]
     lib.spec_verify_destroy.argtypes = [c_void]
+    lib.spec_verify_lazy.argtypes = list(lib.spec_verify.argtypes)
     lib.spec_verify_kv_commit.argtypes = [c_void, c_int, c_int, c_int, c_int, c_int, ctypes.c_size_t,
                                           c_void, c_void, c_void, c_void, c_void, c_int]
     lib.spec_verify_tree.argtypes = [c_void, c_int, c_int, c_int, c_int, c_void, c_void, c_void,
@@ -223,6 +224,26 @@ def spec_verify_kv_commit(ctx, mode, cache, seq_len, kv_len, scratch=None, path=
                                         _ptr(path), int(stride)), "spec_verify_kv_commit")
 
 
+def spec_verify_lazy(ctx, target_logits, draft_logits, draft_tokens, temperature, seed,
+                     out_tokens, out_accept_len, out_kv_len):
+    """spec_verify that reads each request's rows only as far as its walk
+    goes (same arguments and outputs)."""
+    B, n1, V = target_logits.shape
+    logit_dt = (torch.float32, torch.bfloat16)
+    _require(target_logits, "target_logits", (B, n1, V), logit_dt)
+    if n1 > 1:
+        _require(draft_logits, "draft_logits", (B, n1 - 1, V), (target_logits.dtype,))
+        _require(draft_tokens, "draft_tokens", (B, n1 - 1), (torch.int32,))
+    _require(temperature, "temperature", (B,), (torch.float32,))
+    _require(out_tokens, "out_tokens", (B, n1), (torch.int32,))
+    _require(out_accept_len, "out_accept_len", (B,), (torch.int32,))
+    _require(out_kv_len, "out_kv_len", (B,), (torch.int32,))
+    _check(load().spec_verify_lazy(ctx, int(B), int(n1 - 1), int(V), _ptr(target_logits),
+                                   _ptr(draft_logits), _ptr(draft_tokens), _ptr(temperature),
+                                   ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF), _ptr(out_tokens),
+                                   _ptr(out_accept_len), _ptr(out_kv_len)), "spec_verify_lazy")
+
+
 def spec_verify_get_error(ctx):
     """(code, bits) of the device-detected input errors since the last read."""
     bits = ctypes.c_uint32(0)
@@ -294,6 +315,14 @@ class SpecVerify:
         toks = self.out_tokens[: B * n1].view(B, n1)
         acc, kv = self.out_accept[:B], self.out_kv[:B]
         spec_verify(self.ctx, target, draft, tokens, temperature, seed, toks, acc, kv)
+        return toks, acc, kv
+
+    def lazy(self, target, draft, tokens, temperature, seed):
+        """spec_verify_lazy into this context's output buffers."""
+        B, n1, _ = target.shape
+        toks = self.out_tokens[: B * n1].view(B, n1)
+        acc, kv = self.out_accept[:B], self.out_kv[:B]
+        spec_verify_lazy(self.ctx, target, draft, tokens, temperature, seed, toks, acc, kv)
         return toks, acc, kv
 
     def tree(self, target, draft, parents, tokens, temperature, seed, mode=SV_TREE_SAMPLED):

@@ -88,6 +88,18 @@ __device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
 
 // ---------------------------------------------------------------- loads
 
+// 16-byte copy global -> shared that holds no register while in flight
+// (cached in L2 only); the issuing thread waits for its own copies with
+// cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+
 // 16-byte read-only load that does not allocate in L1 (each byte of a row
 // is read once by the row-statistics pass).
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {

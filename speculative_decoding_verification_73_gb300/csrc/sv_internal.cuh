@@ -136,6 +136,7 @@ cudaError_t launch_tree_rowstats(int dtype, bool vec, const TreeProblem& p, cons
 cudaError_t launch_tree_walk(int dtype, bool vec, const TreeProblem& p, const Workspace& w,
                              cudaStream_t s);
 cudaError_t launch_kv_commit(const KvProblem& p, cudaStream_t s);
+cudaError_t launch_lazy(int dtype, bool vec, const Problem& p, const Workspace& w, cudaStream_t s);
 cudaError_t launch_philox_probe(unsigned long long seed, const uint32_t* ctr3, uint32_t* out4,
                                 int n, cudaStream_t s);
 

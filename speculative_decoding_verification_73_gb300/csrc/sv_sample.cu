@@ -138,17 +138,6 @@ __device__ __forceinline__ void resid_halves(const T* z, const T* y, int t0, int
   }
 }
 
-// 16-byte copy global -> shared that holds no register while in flight
-// (cached in L2 only); the issuing thread waits for its own copies with
-// cp_async_wait_all.
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
-               "l"(gmem_src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
 // One element of a staged row (shared memory), as float.
 __device__ __forceinline__ float staged1(const float* p) { return *p; }
 __device__ __forceinline__ float staged1(const __nv_bfloat16* p) {

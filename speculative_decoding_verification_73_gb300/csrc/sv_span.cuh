@@ -83,7 +83,10 @@ __device__ Partial chunk_partial_scalar(const T* row, int beg, int end, bool gre
 // threads' states are merged once at the end.  kFull: the span is complete,
 // so no vector needs a bounds check.  Exponent arguments and sums use the
 // paired float instructions, two elements per instruction.
-template <typename T, bool kGreedy, bool kFull>
+// kSmem: `row` + beg points to a copy of the span staged in shared memory
+// (plain loads) instead of global memory (streaming loads); the arithmetic
+// is the same either way.
+template <typename T, bool kGreedy, bool kFull, bool kSmem = false>
 __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int end, float k, int d,
                                                     float* tok_out) {
   using E = Elem<T>;
@@ -101,7 +104,7 @@ __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int e
 #pragma unroll
   for (int u = 0; u < kGroup; ++u) {
     const int v = threadIdx.x + u * kThreads;
-    buf[0][u] = (kFull || v < nv) ? ld_stream16(vp + v) : pad;
+    buf[0][u] = (kFull || v < nv) ? (kSmem ? vp[v] : ld_stream16(vp + v)) : pad;
   }
   float m = -INFINITY;      // running maximum (raw logits)
   float c = -INFINITY;      // fl(m k), the exponent reference of the sum
@@ -116,7 +119,7 @@ __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int e
 #pragma unroll
       for (int u = 0; u < kGroup; ++u) {
         const int v = threadIdx.x + ((gi + 1) * kGroup + u) * kThreads;
-        buf[cur ^ 1][u] = (kFull || v < nv) ? ld_stream16(vp + v) : pad;
+        buf[cur ^ 1][u] = (kFull || v < nv) ? (kSmem ? vp[v] : ld_stream16(vp + v)) : pad;
       }
     }
     if (!kGreedy) {

@@ -42,6 +42,7 @@
 #include <cuda_bf16.h>
 
 #include "sv_device.cuh"
+#include "sv_law.cuh"
 #include "sv_pick.cuh"
 #include "sv_span.cuh"
 #include "sv_walk.cuh"
@@ -101,108 +102,6 @@ __global__ void __launch_bounds__(kThreads, kSpanMinBlocks) tree_rowstats_kernel
                  : span_partial_vec<T, false, false>(base, beg, end, k, -1, nullptr);
   }
   if (threadIdx.x == 0) w.partials[static_cast<size_t>(row) * S1 + span] = out;
-}
-
-// ------------------------------------------------------------ cluster helpers
-
-__device__ __forceinline__ unsigned cluster_rank() {
-  unsigned r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// Barrier over every thread of every CTA of the cluster; orders the memory
-// accesses before it (release) with those after it (acquire).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-
-// The float at `local`'s place in the shared memory of cluster CTA `rank`.
-__device__ __forceinline__ float ld_dsmem(const float* local, unsigned rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(remote)
-               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
-}
-
-// ------------------------------------------------------------ distributions
-
-// The distribution a node's token is drawn from, or that its next child is
-// tested against, as a per-token function of the two logits.
-//   kQ:       q_t = 2^(z_t k - cq) / sq
-//   kSampled: after m rejections the residual r_m is a single clipped line in
-//             (q, p): r_0 = q and r_{m+1} = (r_m - p)_+ / S_{m+1} give
-//             r_m = (q - c_m p)_+ / D_m with c_{m+1} = c_m + D_m, D_{m+1} =
-//             D_m S_{m+1} (c_0 = 0, D_0 = 1; a step whose sum S is 0 leaves r
-//             unchanged).  The law evaluates (q - c p)_+ * scale.
-//   kTopk:    q with the m rejected tokens removed (unnormalised)
-struct NodeLaw {
-  static constexpr int kQ = 0, kSampled = 1, kTopk = 2;
-  int kind;
-  float k, cq, inv_sq, cp, inv_sp;
-  float c, scale;  // kSampled
-  int m;           // kTopk: rejected tokens in rej[0, m)
-  const int* rej;
-  __device__ __forceinline__ float q(float zt) const { return ex2(fmaf(zt, k, -cq)) * inv_sq; }
-  __device__ __forceinline__ float p(float yt) const { return ex2(fmaf(yt, k, -cp)) * inv_sp; }
-  __device__ __forceinline__ float r(float zt, float yt, int t) const {
-    float v = q(zt);
-    if (kind == kSampled) {
-      v = fmaxf(fmaf(-c, p(yt), v), 0.f) * scale;
-    } else if (kind == kTopk) {
-      for (int j = 0; j < m; ++j)
-        if (rej[j] == t) v = 0.f;
-    }
-    return v;
-  }
-};
-
-// Sums of f(z_t, y_t, t) over this thread's 32 tokens [t0, t0 + 32) of a
-// level-1 block (0 past cend): h0 over the first 16, h1 over the last 16.
-template <typename T, bool kVecPath, typename F>
-__device__ __forceinline__ void seg_sums(const T* z, const T* y, bool need_y, int t0, int cend, F f,
-                                         float& h0, float& h1) {
-  using E = Elem<T>;
-  h0 = 0.f;
-  h1 = 0.f;
-  if (kVecPath) {
-    constexpr int kVec = E::kVec;
-    constexpr int kVecs = kSegTok / kVec;
-    uint4 zv[kVecs], yv[kVecs];
-#pragma unroll
-    for (int i = 0; i < kVecs; ++i) {
-      const int e0 = t0 + i * kVec;
-      const bool in = e0 < cend;
-      zv[i] = in ? __ldg(reinterpret_cast<const uint4*>(z + e0)) : make_uint4(0, 0, 0, 0);
-      yv[i] = (in && need_y) ? __ldg(reinterpret_cast<const uint4*>(y + e0)) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int i = 0; i < kVecs; ++i) {
-      float part = 0.f;
-#pragma unroll
-      for (int e = 0; e < kVec; ++e) {
-        const int t = t0 + i * kVec + e;
-        if (t < cend) part += f(E::get(zv[i], e), need_y ? E::get(yv[i], e) : 0.f, t);
-      }
-      if (i < kVecs / 2)
-        h0 += part;
-      else
-        h1 += part;
-    }
-  } else {
-    for (int i = 0; i < kSegTok; ++i) {
-      const int t = t0 + i;
-      const float v = t < cend ? f(E::load1(z + t), need_y ? E::load1(y + t) : 0.f, t) : 0.f;
-      if (i < kLevel3)
-        h0 += v;
-      else
-        h1 += v;
-    }
-  }
 }
 
 // ------------------------------------------------------------ the walk
