@@ -25,6 +25,9 @@ What it computes (plain float64, in the order the pages state it):
   left by its rejected elder siblings, descent on acceptance, a drawn
   token where every child is rejected or at a leaf, and the argmax path at
   temperature 0.
+* ``fcnorm``  -- the drafter's input fusion of EAGLE-3 / EAGLE 3.1: the
+  three target hidden states, each LayerNorm- or RMSNorm-normalised (or
+  not), concatenated and projected by one FC layer.
 * ``kv``      -- the KV-cache commit driven by out_kv_len (and a tree's
   out_path): copy the kept window entries from a scratch buffer, or move
   them together in place, and advance the logical length (section "KV
@@ -36,4 +39,4 @@ the E[accepted] closed form, brute-force greedy chains, textbook softmax
 special cases, Philox known-answer vectors and a library Philox.
 """
 
-from . import kv, philox, tree, verify  # noqa: F401
+from . import fcnorm, kv, philox, tree, verify  # noqa: F401
