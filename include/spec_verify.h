@@ -61,6 +61,8 @@ extern "C" {
                              outside [0, node - 1]                             */
 #define SV_EBADKV      8  /* device check (spec_verify_kv_commit): a sequence's
                              commit was refused                                */
+#define SV_ETIMEOUT    9  /* a bounded device wait ran out and the kernel stopped
+                             early (never expected; the context stays usable) */
 
 /* Bits of the device error word (spec_verify_get_error).  A request that
  * fails a device check gets out_tokens = -1 everywhere, out_accept_len = -1
@@ -72,6 +74,7 @@ extern "C" {
 #define SV_ERRBIT_TREE   8u   /* spec_verify_tree only; checked after the
                                  temperature, before tokens and logits */
 #define SV_ERRBIT_KV     16u  /* spec_verify_kv_commit only */
+#define SV_ERRBIT_WAIT   32u  /* a bounded device wait ran out */
 
 /* ---- logit element types ---------------------------------------------- */
 #define SV_F32   0
@@ -292,10 +295,44 @@ int spec_verify_kv_commit(spec_verify_ctx* ctx, int mode, int L, int B, int S, i
                           const int32_t* path, int path_stride);
 
 /*
+ * spec_verify_fc_norm -- the drafter's input fusion of EAGLE-3 / EAGLE 3.1
+ * (the EAGLE-3 page's "FC normalisation: the key change of EAGLE 3.1"):
+ *     out = [norm(h_early); norm(h_mid); norm(h_late)] . W^T + bias
+ * with the three target hidden states of an early, a middle and a late
+ * layer.  norm: SV_NORM_NONE (EAGLE-3: plain concatenation), SV_NORM_LAYER
+ * (LayerNorm: (h - mean) / sqrt(var + eps) * gamma + beta, the page's
+ * formula) or SV_NORM_RMS (h / sqrt(mean(h^2) + eps) * gamma, the wording of
+ * the EAGLE 3.1 news page); each segment has its own gamma / beta.
+ *
+ *   T, d, d_out   tokens, hidden width (a multiple of 64), output width
+ *   h_early/mid/late  [T, d] bfloat16 device, 16-byte aligned
+ *   gamma         [3, d] float32 (ignored for SV_NORM_NONE)
+ *   beta          [3, d] float32 or NULL (LayerNorm only)
+ *   weight        [d_out, 3 d] bfloat16, row-major, 16-byte aligned
+ *   bias          [d_out] float32 or NULL
+ *   out           [T, d_out] bfloat16 (caller-owned)
+ *   stats         [T, 3, 2] float32 scratch (caller-owned): per token and
+ *                 segment the mean and 1/sqrt(var + eps)
+ * Statistics in float32; the normalised inputs are rounded to bfloat16 and
+ * multiplied on the tensor cores (tcgen05, fp32 accumulation in tensor
+ * memory); the output is rounded to bfloat16.  Two kernel launches on the
+ * context's stream.  Returns SV_OK, SV_EINVAL (nothing enqueued) or
+ * SV_ECUDA; a device wait that ran out is reported by spec_verify_get_error
+ * as SV_ETIMEOUT.
+ */
+#define SV_NORM_NONE  0
+#define SV_NORM_LAYER 1
+#define SV_NORM_RMS   2
+int spec_verify_fc_norm(spec_verify_ctx* ctx, int T, int d, int d_out, int norm, float eps,
+                        const void* h_early, const void* h_mid, const void* h_late,
+                        const float* gamma, const float* beta, const void* weight,
+                        const float* bias, void* out, float* stats);
+
+/*
  * spec_verify_get_error -- wait for the context's stream, then return the
  * first device-detected error since the last read (SV_EBADTEMP,
- * SV_EBADTREE, SV_EBADTOKEN, SV_EBADLOGIT, SV_EBADKV in that priority) or
- * SV_OK, and clear it.
+ * SV_EBADTREE, SV_EBADTOKEN, SV_EBADLOGIT, SV_EBADKV, SV_ETIMEOUT in that
+ * priority) or SV_OK, and clear it.
  * bits (may be NULL) receives the OR of SV_ERRBIT_* flags.
  */
 int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits);

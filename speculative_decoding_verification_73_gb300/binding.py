@@ -15,9 +15,10 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 
 (SV_OK, SV_EINVAL, SV_EBADTEMP, SV_EBADTOKEN, SV_EBADLOGIT, SV_ECUDA, SV_ESCRATCH, SV_EBADTREE,
- SV_EBADKV) = range(9)
+ SV_EBADKV, SV_ETIMEOUT) = range(10)
 SV_ERRBIT_TEMP, SV_ERRBIT_TOKEN, SV_ERRBIT_LOGIT, SV_ERRBIT_TREE, SV_ERRBIT_KV = 1, 2, 4, 8, 16
 SV_KV_SCRATCH, SV_KV_INPLACE = 0, 1
+SV_NORM_NONE, SV_NORM_LAYER, SV_NORM_RMS = 0, 1, 2
 SV_TREE_SAMPLED, SV_TREE_TOPK = 0, 1
 SV_F32, SV_BF16 = 0, 1
 SV_NUM_KERNELS = 2
@@ -33,6 +34,7 @@ EXPORTS = (
     "spec_verify_profile", "spec_verify_profile_read", "spec_verify_launches_per_call",
     "spec_verify_debug_philox", "spec_verify_destroy", "spec_verify_strerror",
     "spec_verify_noalloc", "spec_verify_tree", "spec_verify_kv_commit", "spec_verify_lazy",
+    "spec_verify_fc_norm",
 )
 
 _lib = None
@@ -67,6 +69,8 @@ def load():
     lib.spec_verify_debug_philox.argtypes = [c_u64, c_void, c_void, c_int, c_void]
     lib.spec_verify_destroy.argtypes = [c_void]
     lib.spec_verify_lazy.argtypes = list(lib.spec_verify.argtypes)
+    lib.spec_verify_fc_norm.argtypes = [c_void, c_int, c_int, c_int, c_int, ctypes.c_float, c_void,
+                                        c_void, c_void, c_void, c_void, c_void, c_void, c_void, c_void]
     lib.spec_verify_kv_commit.argtypes = [c_void, c_int, c_int, c_int, c_int, c_int, ctypes.c_size_t,
                                           c_void, c_void, c_void, c_void, c_void, c_int]
     lib.spec_verify_tree.argtypes = [c_void, c_int, c_int, c_int, c_int, c_void, c_void, c_void,
@@ -242,6 +246,35 @@ def spec_verify_lazy(ctx, target_logits, draft_logits, draft_tokens, temperature
                                    _ptr(draft_logits), _ptr(draft_tokens), _ptr(temperature),
                                    ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF), _ptr(out_tokens),
                                    _ptr(out_accept_len), _ptr(out_kv_len)), "spec_verify_lazy")
+
+
+def spec_verify_fc_norm(ctx, norm, h_early, h_mid, h_late, weight, gamma=None, beta=None,
+                        bias=None, eps=1e-5, out=None, stats=None):
+    """out [T, d_out] bf16 = [norm(h_early); norm(h_mid); norm(h_late)] . W^T
+    + bias.  h_*: [T, d] bf16 CUDA tensors; weight [d_out, 3d] bf16; gamma /
+    beta [3, d] and bias [d_out] float32.  Returns out."""
+    T, d = h_early.shape
+    d_out = weight.shape[0]
+    for name, h in (("h_early", h_early), ("h_mid", h_mid), ("h_late", h_late)):
+        _require(h, name, (T, d), (torch.bfloat16,))
+    _require(weight, "weight", (d_out, 3 * d), (torch.bfloat16,))
+    if gamma is not None:
+        _require(gamma, "gamma", (3, d), (torch.float32,))
+    if beta is not None:
+        _require(beta, "beta", (3, d), (torch.float32,))
+    if bias is not None:
+        _require(bias, "bias", (d_out,), (torch.float32,))
+    if out is None:
+        out = torch.empty(T, d_out, dtype=torch.bfloat16, device=h_early.device)
+    _require(out, "out", (T, d_out), (torch.bfloat16,))
+    if stats is None:
+        stats = torch.empty(T, 3, 2, dtype=torch.float32, device=h_early.device)
+    _require(stats, "stats", (T, 3, 2), (torch.float32,))
+    _check(load().spec_verify_fc_norm(ctx, int(T), int(d), int(d_out), int(norm), float(eps),
+                                      _ptr(h_early), _ptr(h_mid), _ptr(h_late), _ptr(gamma), _ptr(beta),
+                                      _ptr(weight), _ptr(bias), _ptr(out), _ptr(stats)),
+           "spec_verify_fc_norm")
+    return out
 
 
 def spec_verify_get_error(ctx):

@@ -84,6 +84,7 @@ const char* spec_verify_strerror(int code) {
     case SV_EBADKV:
       return "a KV commit would pass the cache length, read outside the window, or keep "
              "positions that do not rise";
+    case SV_ETIMEOUT: return "a bounded device wait ran out (a kernel stopped early)";
     case SV_ESCRATCH:
       return "the problem needs more working memory than spec_verify_noalloc's static array "
              "(SV_NOALLOC_SCRATCH_BYTES) holds";
@@ -337,6 +338,41 @@ int spec_verify_lazy(spec_verify_ctx* ctx, int B, int N, int V, const void* targ
   return SV_OK;
 }
 
+int spec_verify_fc_norm(spec_verify_ctx* ctx, int T, int d, int d_out, int norm, float eps,
+                        const void* h_early, const void* h_mid, const void* h_late,
+                        const float* gamma, const float* beta, const void* weight,
+                        const float* bias, void* out, float* stats) {
+  if (ctx == nullptr || T < 0 || d < 64 || d % 64 != 0 || d_out < 1 ||
+      (norm != SV_NORM_NONE && norm != SV_NORM_LAYER && norm != SV_NORM_RMS) || !(eps >= 0.f) ||
+      eps > 3.0e38f)
+    return SV_EINVAL;
+  if (static_cast<long long>(d) * 3 > (1LL << 30) || d_out > (1 << 28)) return SV_EINVAL;
+  if (T == 0) return SV_OK;
+  if (h_early == nullptr || h_mid == nullptr || h_late == nullptr || weight == nullptr ||
+      out == nullptr || stats == nullptr || !aligned16(h_early) || !aligned16(h_mid) ||
+      !aligned16(h_late) || !aligned16(weight))
+    return SV_EINVAL;
+  if (norm != SV_NORM_NONE && gamma == nullptr) return SV_EINVAL;
+  sv::FcNormProblem p;
+  p.T = T;
+  p.d = d;
+  p.d_out = d_out;
+  p.norm = norm;
+  p.eps = eps;
+  p.h[0] = static_cast<const __nv_bfloat16*>(h_early);
+  p.h[1] = static_cast<const __nv_bfloat16*>(h_mid);
+  p.h[2] = static_cast<const __nv_bfloat16*>(h_late);
+  p.gamma = gamma;
+  p.beta = norm == SV_NORM_LAYER ? beta : nullptr;
+  p.w = static_cast<const __nv_bfloat16*>(weight);
+  p.bias = bias;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.out_vec = aligned16(out) && d_out % 8 == 0;
+  p.stats = stats;
+  p.err = ctx->w.err;
+  return sv::launch_fcnorm(p, ctx->stream) == cudaSuccess ? SV_OK : SV_ECUDA;
+}
+
 int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits) {
   if (ctx == nullptr) return SV_EINVAL;
   unsigned word = 0;
@@ -351,6 +387,7 @@ int spec_verify_get_error(spec_verify_ctx* ctx, uint32_t* bits) {
   if (word & SV_ERRBIT_TOKEN) return SV_EBADTOKEN;
   if (word & SV_ERRBIT_LOGIT) return SV_EBADLOGIT;
   if (word & SV_ERRBIT_KV) return SV_EBADKV;
+  if (word & SV_ERRBIT_WAIT) return SV_ETIMEOUT;
   return SV_OK;
 }
 

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace sv {
@@ -38,6 +39,12 @@ constexpr unsigned kErrToken = 2u;
 constexpr unsigned kErrLogit = 4u;
 constexpr unsigned kErrTree = 8u;
 constexpr unsigned kErrKv = 16u;
+constexpr unsigned kErrWait = 32u;
+
+// FC-norm: how each target hidden state is normalised before the FC.
+constexpr int kNormNone = 0;   // EAGLE-3
+constexpr int kNormLayer = 1;  // LayerNorm (EAGLE 3.1)
+constexpr int kNormRms = 2;    // RMSNorm
 
 // How the verify window's KV entries were written.
 constexpr int kKvScratch = 0;  // to a scratch window [L, B, W, E]
@@ -112,6 +119,20 @@ struct KvProblem {
   unsigned* err;
 };
 
+struct FcNormProblem {
+  int T, d, d_out, norm;
+  float eps;
+  const __nv_bfloat16* h[3];   // [T, d] each: early, middle, late layer
+  const float* gamma;          // [3, d]
+  const float* beta;           // [3, d] or nullptr
+  const __nv_bfloat16* w;      // [d_out, 3d]
+  const float* bias;           // [d_out] or nullptr
+  __nv_bfloat16* out;          // [T, d_out]
+  bool out_vec;                // rows of out 16-byte aligned
+  float* stats;                // [T, 3, 2]: mean, 1 / sqrt(var + eps)
+  unsigned* err;
+};
+
 struct Workspace {
   Partial* partials;     // [B][2N+1][S1]: target rows 0..N, then draft rows 0..N-1
                          // (tree: [B][2(M+1)][S1], target rows then draft rows 0..M)
@@ -136,6 +157,7 @@ cudaError_t launch_tree_rowstats(int dtype, bool vec, const TreeProblem& p, cons
 cudaError_t launch_tree_walk(int dtype, bool vec, const TreeProblem& p, const Workspace& w,
                              cudaStream_t s);
 cudaError_t launch_kv_commit(const KvProblem& p, cudaStream_t s);
+cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s);
 cudaError_t launch_lazy(int dtype, bool vec, const Problem& p, const Workspace& w, cudaStream_t s);
 cudaError_t launch_philox_probe(unsigned long long seed, const uint32_t* ctr3, uint32_t* out4,
                                 int n, cudaStream_t s);

@@ -426,3 +426,36 @@ def make_tree(batch, vocab, dtype, *, gen_seed, widths=None, m=None, mode=TREE_S
     label = name or f"tree-{'topk' if mode == TREE_TOPK else 'sampled'}-{dtype}-B{batch}-M{mm}-V{vocab}"
     return TreeWorkload(label, dtype, mode, target, draft, torch.from_numpy(par),
                         torch.from_numpy(tokens), torch.from_numpy(tv), int(verify_seed))
+
+
+# --------------------------------------------------------------------------
+# FC-norm inputs
+# --------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class FcNormWorkload:
+    """Hidden states of three target layers and the FC weights (CPU tensors).
+    The later layers' states are larger, as the EAGLE 3.1 page describes
+    (residual accumulation): standard deviations 1, 4 and 16, means 0, 0.5
+    and 2."""
+
+    name: str
+    h: list                     # 3 x [T, d] bf16
+    weight: torch.Tensor        # [d_out, 3d] bf16
+    gamma: torch.Tensor         # [3, d] float32
+    beta: torch.Tensor          # [3, d] float32
+    bias: torch.Tensor          # [d_out] float32
+
+
+def make_fcnorm(T, d, d_out, *, gen_seed, name=None):
+    gen = _gen(gen_seed + 313)
+    h = []
+    for scale, mean in ((1.0, 0.0), (4.0, 0.5), (16.0, 2.0)):
+        x = mean + scale * torch.randn(T, d, generator=gen, dtype=torch.float64)
+        h.append(x.to(torch.bfloat16))
+    w = torch.randn(d_out, 3 * d, generator=gen, dtype=torch.float64) / math.sqrt(3 * d)
+    gamma = 1.0 + 0.1 * torch.randn(3, d, generator=gen, dtype=torch.float64)
+    beta = 0.1 * torch.randn(3, d, generator=gen, dtype=torch.float64)
+    bias = 0.1 * torch.randn(d_out, generator=gen, dtype=torch.float64)
+    return FcNormWorkload(name or f"fcnorm-T{T}-d{d}-o{d_out}", h, w.to(torch.bfloat16),
+                          gamma.to(torch.float32), beta.to(torch.float32), bias.to(torch.float32))

@@ -1,0 +1,75 @@
+"""FC-norm on the GPU (stats kernel + tcgen05 GEMM) through the C ABI against
+the float64 oracle, within the bound that bf16 rounding of the normalised
+inputs and of the output implies: |gpu - ref| <= 2^-8 (sum_k |x_k||w_k| +
+|ref|)."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import fcnorm as ofc
+from speculative_decoding_verification_73_gb300 import binding, build, workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    return binding.load()
+
+
+def _f64(t):
+    return t.to(torch.float64).numpy()
+
+
+def run_case(wl, norm, with_bias=True, with_beta=True, eps=1e-5):
+    ctx = binding.SpecVerify(1, 1, 16, torch.float32)
+    h = [x.cuda() for x in wl.h]
+    gamma = wl.gamma.cuda() if norm != binding.SV_NORM_NONE else None
+    beta = wl.beta.cuda() if (norm == binding.SV_NORM_LAYER and with_beta) else None
+    bias = wl.bias.cuda() if with_bias else None
+    out = binding.spec_verify_fc_norm(ctx.ctx, norm, *h, wl.weight.cuda(), gamma=gamma, beta=beta,
+                                      bias=bias, eps=eps)
+    code, bits = ctx.get_error()
+    assert code == 0 and bits == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    hs = [_f64(x) for x in wl.h]
+    g = _f64(wl.gamma) if gamma is not None else None
+    b = _f64(wl.beta) if beta is not None else None
+    ref = ofc.fc_norm(*hs, _f64(wl.weight), norm, g, b, _f64(wl.bias) if with_bias else None, eps)
+    bound = ofc.abs_bound(*hs, _f64(wl.weight), norm, g, b, eps)
+    err = np.abs(got - ref)
+    tol = 2.0 ** -8 * (bound + np.abs(ref)) + 1e-6
+    worst = float((err / tol).max())
+    assert (err <= tol).all(), f"worst error / tolerance {worst:.3g}"
+    ctx.close()
+    return worst
+
+
+CASES = [
+    ("layer-bias", 200, 256, 384, binding.SV_NORM_LAYER, True, True),
+    ("rms-ragged-out", 130, 64, 100, binding.SV_NORM_RMS, False, False),
+    ("none-one-token", 1, 128, 256, binding.SV_NORM_NONE, True, False),
+    ("layer-no-beta", 129, 192, 264, binding.SV_NORM_LAYER, False, False),
+    ("layer-medium", 512, 1024, 1024, binding.SV_NORM_LAYER, True, True),
+]
+
+
+@pytest.mark.parametrize("name,T,d,d_out,norm,bias,beta", CASES)
+def test_fc_norm_matches_oracle(name, T, d, d_out, norm, bias, beta):
+    wl = workloads.make_fcnorm(T, d, d_out, gen_seed=sum(map(ord, name)))
+    worst = run_case(wl, norm, bias, beta)
+    print(f"{name}: worst error / tolerance {worst:.3f}")
+
+
+def test_selector_weights_return_the_normalised_segment():
+    """W = [0 I 0]: the output is the middle segment's LayerNorm, rounded."""
+    T, d = 64, 128
+    wl = workloads.make_fcnorm(T, d, d, gen_seed=7)
+    w = torch.zeros(d, 3 * d, dtype=torch.float64)
+    w[:, d:2 * d] = torch.eye(d, dtype=torch.float64)
+    wl.weight = w.to(torch.bfloat16)
+    run_case(wl, binding.SV_NORM_LAYER, with_bias=False, with_beta=True)
