@@ -26,6 +26,11 @@ children are independent draws from the drafter, V=128256 bf16; one step is
 one tree verify of the batch, the metric counts the B*14 verified draft
 nodes per step.
 
+--path fcnorm measures spec_verify_fc_norm (EAGLE 3.1 LayerNorm fusion):
+T=4096 tokens, three 4096-wide hidden states, a 4096 x 12288 bf16 FC weight
+and bias; the metric is TFLOP/s of the FC (2 T 3d d_out per call), against
+the measured bf16 tensor peak.
+
 --path kv measures spec_verify_kv_commit (scratch mode): 32 layers x 64
 sequences, 4 KB entries (8 KV heads x 128 dims x K and V in bf16), an
 8-position window, the KV lengths of one batch64-bf16 verify; the metric is
@@ -66,10 +71,10 @@ def parse():
     ap.add_argument("--copies", type=int, default=3, help="rotating input copies in HBM")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", default="chain", choices=["chain", "lazy", "tree", "kv"],
+    ap.add_argument("--path", default="chain", choices=["chain", "lazy", "tree", "kv", "fcnorm"],
                     help="chain: spec_verify on batch64-bf16 (the headline); tree: "
                          "spec_verify_tree on tree222-bf16; kv: spec_verify_kv_commit; lazy: "
-                         "spec_verify_lazy on batch64-bf16")
+                         "spec_verify_lazy on batch64-bf16; fcnorm: spec_verify_fc_norm")
     return ap.parse_args()
 
 
@@ -638,6 +643,95 @@ def run_kv(args):
         print(json.dumps(line))
 
 
+# --------------------------------------------------------------------------- fc norm
+
+FC_WORKLOAD = "fcnorm-T4096-d4096-o4096-layernorm"
+
+
+def bf16_peak():
+    try:
+        with open(PEAKS) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def run_fcnorm(args):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decoding_verification_73_gb300 import binding, build, workloads
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build.build()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    T, d, d_out = 4096, 4096, 4096
+    wl = workloads.make_fcnorm(T, d, d_out, gen_seed=2026 + rank, name=FC_WORKLOAD)
+    h = [x.to(dev) for x in wl.h]
+    w, g, b, bias = wl.weight.to(dev), wl.gamma.to(dev), wl.beta.to(dev), wl.bias.to(dev)
+    out = torch.empty(T, d_out, dtype=torch.bfloat16, device=dev)
+    stats = torch.empty(T, 3, 2, dtype=torch.float32, device=dev)
+    sv = binding.SpecVerify(1, 1, 16, torch.float32, stream=stream, device=dev)
+
+    def step():
+        binding.spec_verify_fc_norm(sv.ctx, binding.SV_NORM_LAYER, *h, w, gamma=g, beta=b, bias=bias,
+                                    out=out, stats=stats)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    code, _ = sv.get_error()
+    assert code == 0, binding.strerror(code)
+    steps = min(args.steps, 500)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t_begin = time.time()
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_end = time.time()
+    elapsed_ms = ranks_max(ev0.elapsed_time(ev1), dev)
+    time.sleep(0.2)
+    clk = clocks.stop(t_begin, t_end)
+    code, _ = sv.get_error()
+    assert code == 0, binding.strerror(code)
+    flops = 2.0 * T * 3 * d * d_out
+    per_ms = elapsed_ms / steps
+    value = flops * steps * world / (elapsed_ms / 1e3) / 1e12
+    peak, kind = bf16_peak()
+    achieved = flops / (per_ms / 1e3) / 1e12
+    line = {
+        "metric": "FC-norm TFLOP/s", "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": per_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate",
+        "data": "synthetic (Gaussian hidden states of three magnitudes, random weights)",
+        "config": {"workload": FC_WORKLOAD, "T": T, "d": d, "d_out": d_out, "norm": "layernorm",
+                   "flops_per_call": flops, "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "fcnorm_gemm (+ fcnorm_stats)", "achieved": achieved,
+                     "peak": peak, "peak_kind": f"{kind} cuBLAS bf16 burst", "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "algorithmic_flops_per_launch": flops, "avg_launch_us": per_ms * 1e3,
+                     "timed_launches": f"{steps} calls of two launches each"},
+        "e2e": None, "gpu_launches": steps * 2, "clocks": clk,
+    }
+    sv.close()
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line))
+
+
 # --------------------------------------------------------------------------- oracle
 
 def oracle_requests(wl, idx):
@@ -704,6 +798,8 @@ def main():
         run_tree(args)
     elif args.path == "kv":
         run_kv(args)
+    elif args.path == "fcnorm":
+        run_fcnorm(args)
     else:
         run_ours(args)
 
