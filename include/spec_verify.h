@@ -311,8 +311,8 @@ int spec_verify_kv_commit(spec_verify_ctx* ctx, int mode, int L, int B, int S, i
  *   weight        [d_out, 3 d] bfloat16, row-major, 16-byte aligned
  *   bias          [d_out] float32 or NULL
  *   out           [T, d_out] bfloat16 (caller-owned)
- *   stats         [T, 3, 2] float32 scratch (caller-owned): per token and
- *                 segment the mean and 1/sqrt(var + eps)
+ *   xbuf          [T, 3 d] bfloat16 scratch (caller-owned, 16-byte aligned):
+ *                 receives the normalised, concatenated input
  * Statistics in float32; the normalised inputs are rounded to bfloat16 and
  * multiplied on the tensor cores (tcgen05, fp32 accumulation in tensor
  * memory); the output is rounded to bfloat16.  Two kernel launches on the
@@ -326,7 +326,7 @@ int spec_verify_kv_commit(spec_verify_ctx* ctx, int mode, int L, int B, int S, i
 int spec_verify_fc_norm(spec_verify_ctx* ctx, int T, int d, int d_out, int norm, float eps,
                         const void* h_early, const void* h_mid, const void* h_late,
                         const float* gamma, const float* beta, const void* weight,
-                        const float* bias, void* out, float* stats);
+                        const float* bias, void* out, void* xbuf);
 
 /*
  * spec_verify_get_error -- wait for the context's stream, then return the

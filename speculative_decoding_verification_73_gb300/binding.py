@@ -249,7 +249,7 @@ def spec_verify_lazy(ctx, target_logits, draft_logits, draft_tokens, temperature
 
 
 def spec_verify_fc_norm(ctx, norm, h_early, h_mid, h_late, weight, gamma=None, beta=None,
-                        bias=None, eps=1e-5, out=None, stats=None):
+                        bias=None, eps=1e-5, out=None, xbuf=None):
     """out [T, d_out] bf16 = [norm(h_early); norm(h_mid); norm(h_late)] . W^T
     + bias.  h_*: [T, d] bf16 CUDA tensors; weight [d_out, 3d] bf16; gamma /
     beta [3, d] and bias [d_out] float32.  Returns out."""
@@ -267,12 +267,12 @@ def spec_verify_fc_norm(ctx, norm, h_early, h_mid, h_late, weight, gamma=None, b
     if out is None:
         out = torch.empty(T, d_out, dtype=torch.bfloat16, device=h_early.device)
     _require(out, "out", (T, d_out), (torch.bfloat16,))
-    if stats is None:
-        stats = torch.empty(T, 3, 2, dtype=torch.float32, device=h_early.device)
-    _require(stats, "stats", (T, 3, 2), (torch.float32,))
+    if xbuf is None:
+        xbuf = torch.empty(T, 3 * d, dtype=torch.bfloat16, device=h_early.device)
+    _require(xbuf, "xbuf", (T, 3 * d), (torch.bfloat16,))
     _check(load().spec_verify_fc_norm(ctx, int(T), int(d), int(d_out), int(norm), float(eps),
                                       _ptr(h_early), _ptr(h_mid), _ptr(h_late), _ptr(gamma), _ptr(beta),
-                                      _ptr(weight), _ptr(bias), _ptr(out), _ptr(stats)),
+                                      _ptr(weight), _ptr(bias), _ptr(out), _ptr(xbuf)),
            "spec_verify_fc_norm")
     return out
 

@@ -341,7 +341,7 @@ int spec_verify_lazy(spec_verify_ctx* ctx, int B, int N, int V, const void* targ
 int spec_verify_fc_norm(spec_verify_ctx* ctx, int T, int d, int d_out, int norm, float eps,
                         const void* h_early, const void* h_mid, const void* h_late,
                         const float* gamma, const float* beta, const void* weight,
-                        const float* bias, void* out, float* stats) {
+                        const float* bias, void* out, void* xbuf) {
   if (ctx == nullptr || T < 0 || d < 64 || d % 64 != 0 || d_out < 1 ||
       (norm != SV_NORM_NONE && norm != SV_NORM_LAYER && norm != SV_NORM_RMS) || !(eps >= 0.f) ||
       eps > 3.0e38f)
@@ -349,8 +349,8 @@ int spec_verify_fc_norm(spec_verify_ctx* ctx, int T, int d, int d_out, int norm,
   if (static_cast<long long>(d) * 3 > (1LL << 30) || d_out > (1 << 28)) return SV_EINVAL;
   if (T == 0) return SV_OK;
   if (h_early == nullptr || h_mid == nullptr || h_late == nullptr || weight == nullptr ||
-      out == nullptr || stats == nullptr || !aligned16(h_early) || !aligned16(h_mid) ||
-      !aligned16(h_late) || !aligned16(weight))
+      out == nullptr || xbuf == nullptr || !aligned16(h_early) || !aligned16(h_mid) ||
+      !aligned16(h_late) || !aligned16(weight) || !aligned16(xbuf))
     return SV_EINVAL;
   if (norm != SV_NORM_NONE && gamma == nullptr) return SV_EINVAL;
   sv::FcNormProblem p;
@@ -368,7 +368,7 @@ int spec_verify_fc_norm(spec_verify_ctx* ctx, int T, int d, int d_out, int norm,
   p.bias = bias;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.out_vec = aligned16(out) && d_out % 8 == 0;
-  p.stats = stats;
+  p.x = static_cast<__nv_bfloat16*>(xbuf);
   p.err = ctx->w.err;
   return sv::launch_fcnorm(p, ctx->stream) == cudaSuccess ? SV_OK : SV_ECUDA;
 }

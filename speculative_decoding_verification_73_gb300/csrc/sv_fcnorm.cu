@@ -4,21 +4,23 @@
 // 3.1": LayerNorm on each of the three target hidden states before the FC;
 // the EAGLE 3.1 news page speaks of RMSNorm; no norm is EAGLE-3).
 //
-// Two kernels.  fcnorm_stats: one warp per (token, segment) computes the
+// Two kernels.  fcnorm_prep: one warp per (token, segment) computes the
 // row's mean and 1/sqrt(var + eps) (LayerNorm; mean 0 and 1/sqrt(mean
-// square + eps) for RMSNorm) in fp32, two passes over the row.
-// fcnorm_gemm: a tcgen05 GEMM.  Each CTA owns a 128 x 256 output tile; per
-// 64-wide K step its 256 threads build the A tile (128 tokens x 64 inputs)
-// by normalising h on the fly -- (h - mean) * rstd * gamma + beta, rounded
-// to bf16 -- straight into shared memory in the canonical K-major layout
-// (8 x 16-byte core matrices, no swizzle), while the W tile (256 outputs x
-// 64 inputs) arrives with cp.async.  One thread issues four
-// tcgen05.mma.kind::f16 (K = 16 each) into an fp32 accumulator of 256 TMEM
-// columns and commits them to the stage's mbarrier; three stages let the
-// loads of the next steps overlap the tensor core.  The epilogue reads the
-// accumulator with tcgen05.ld, adds the bias and stores bf16.  Every wait on
-// an mbarrier is bounded; a wait that runs out sets an error bit and the
-// kernel still frees its TMEM.
+// square + eps) for RMSNorm) in fp32 and writes the normalised row, rounded
+// to bf16, into its third of the concatenated input X [T, 3d] (three passes
+// over a row that stays in L1/L2).  fc_gemm: a tcgen05 GEMM out = X W^T +
+// bias.  Each CTA owns a 128 x 256 output tile and walks K in steps of 64
+// through four shared-memory stages filled by cp.async in the canonical
+// K-major layout (8 x 16-byte core matrices, no swizzle), loads issued two
+// steps ahead; one thread issues four tcgen05.mma.kind::f16 (K = 16 each)
+// per step into an fp32 accumulator of 256 TMEM columns and commits them to
+// the stage's mbarrier, which frees the stage two steps later.  The
+// epilogue reads the accumulator with tcgen05.ld, adds the bias and stores
+// bf16.  Every mbarrier wait is bounded; one that runs out sets an error bit
+// and the kernel still frees its TMEM.  (A first version normalised the A
+// tile on the fly inside the GEMM, with each step's loads issued only after
+// the previous step's MMAs: 150 TFLOP/s on T = d = d_out = 4096; writing X
+// costs one more pass over the hidden states and lets the GEMM pipeline.)
 
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -30,12 +32,14 @@ namespace {
 
 constexpr int kBM = 128, kBN = 256, kBK = 64;
 constexpr int kKG = kBK / 8;                       // core matrices along K per tile
-constexpr int kStages = 3;
+constexpr int kStages = 4;
+constexpr int kAhead = 2;                          // steps of loads in flight ahead of the MMAs
 constexpr int kFcThreads = 256;
 constexpr int kABytes = kBM * kBK * 2;             // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;             // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;     // 48 KB
 constexpr int kTmemCols = kBN;                     // fp32 accumulator 128 lanes x 256 columns
+static_assert(kAhead + 2 <= kStages, "a stage is refilled only after the MMAs two steps back");
 constexpr uint32_t kWaitLimit = 1u << 26;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -74,69 +78,119 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return false;
 }
 
-// --------------------------------------------------------------- statistics
-
-__global__ void fcnorm_stats_kernel(FcNormProblem p) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= p.T * 3) return;
-  const int t = warp / 3, s = warp - t * 3;
-  const __nv_bfloat16* h = (s == 0 ? p.h[0] : s == 1 ? p.h[1] : p.h[2]) + static_cast<size_t>(t) * p.d;
-  float mu = 0.f, rstd = 1.f;
-  if (p.norm != kNormNone) {
-    float sum = 0.f;
-    if (p.norm == kNormLayer) {
-      for (int f = lane * 8; f < p.d; f += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(h + f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sum += Elem<__nv_bfloat16>::get(v, e);
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-      mu = sum / static_cast<float>(p.d);
-    }
-    float sq = 0.f;
-    for (int f = lane * 8; f < p.d; f += 256) {
-      const uint4 v = *reinterpret_cast<const uint4*>(h + f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float x = Elem<__nv_bfloat16>::get(v, e) - mu;
-        sq = fmaf(x, x, sq);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(kFull, sq, o);
-    rstd = rsqrtf(sq / static_cast<float>(p.d) + p.eps);
-  }
-  if (lane == 0) {
-    p.stats[(static_cast<size_t>(t) * 3 + s) * 2] = mu;
-    p.stats[(static_cast<size_t>(t) * 3 + s) * 2 + 1] = rstd;
-  }
-}
-
-// --------------------------------------------------------------- the GEMM
+// --------------------------------------------------------------- normalisation
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__global__ void __launch_bounds__(kFcThreads, 1) fcnorm_gemm_kernel(FcNormProblem p) {
+__global__ void fcnorm_prep_kernel(FcNormProblem p) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= p.T * 3) return;
+  const int t = warp / 3, s = warp - t * 3;
+  const int d = p.d;
+  const __nv_bfloat16* h = (s == 0 ? p.h[0] : s == 1 ? p.h[1] : p.h[2]) + static_cast<size_t>(t) * d;
+  __nv_bfloat16* x = p.x + static_cast<size_t>(t) * 3 * d + static_cast<size_t>(s) * d;
+  float mu = 0.f, rstd = 1.f;
+  if (p.norm != kNormNone) {
+    if (p.norm == kNormLayer) {
+      float sum = 0.f;
+      for (int f = lane * 8; f < d; f += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(h + f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sum += Elem<__nv_bfloat16>::get(v, e);
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+      mu = sum / static_cast<float>(d);
+    }
+    float sq = 0.f;
+    for (int f = lane * 8; f < d; f += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(h + f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float y = Elem<__nv_bfloat16>::get(v, e) - mu;
+        sq = fmaf(y, y, sq);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(kFull, sq, o);
+    rstd = rsqrtf(sq / static_cast<float>(d) + p.eps);
+  }
+  const float* g = p.gamma + static_cast<size_t>(s) * d;
+  const float* bt = p.beta != nullptr ? p.beta + static_cast<size_t>(s) * d : nullptr;
+  for (int f = lane * 8; f < d; f += 256) {
+    const uint4 v = *reinterpret_cast<const uint4*>(h + f);
+    uint4 o = v;
+    if (p.norm != kNormNone) {
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float z = (Elem<__nv_bfloat16>::get(v, e) - mu) * rstd * __ldg(g + f + e);
+        if (bt != nullptr) z += __ldg(bt + f + e);
+        y[e] = z;
+      }
+      o = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                     pack_bf16(y[6], y[7]));
+    }
+    *reinterpret_cast<uint4*>(x + f) = o;
+  }
+}
+
+// --------------------------------------------------------------- the GEMM
+
+// 16-byte cp.async that writes zeros instead of reading when !valid.
+__device__ __forceinline__ void cp_async16_or_zero(void* smem_dst, const void* gmem_src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+               "l"(gmem_src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kN>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(kN) : "memory");
+}
+
+// Loads of K step kt into a stage: X rows m0.., W rows n0.., 8 chunks of 16
+// bytes each.  Chunk q goes to row (q / 64) * 8 + q % 8 and column chunk
+// (q / 8) % 8: eight consecutive threads fill one 16-byte column of eight
+// rows (eight distinct bank groups of a core matrix: no shared-memory bank
+// conflict), and a warp reads 64 contiguous bytes from each of eight rows.
+__device__ __forceinline__ int chunk_row(int q) { return (q >> 6) * 8 + (q & 7); }
+__device__ __forceinline__ int chunk_col(int q) { return (q >> 3) & 7; }
+
+__device__ __forceinline__ void load_stage(const FcNormProblem& p, unsigned char* stage, int m0, int n0,
+                                           int kt) {
+  const int K = 3 * p.d;
+  const int k0 = kt * kBK;
+  unsigned char* sA = stage;
+  unsigned char* sB = stage + kABytes;
+  for (int q = threadIdx.x; q < kBM * kKG; q += kFcThreads) {
+    const int m = chunk_row(q), c = chunk_col(q);
+    const bool in = m0 + m < p.T;
+    const __nv_bfloat16* src = p.x + static_cast<size_t>(in ? m0 + m : 0) * K + k0 + c * 8;
+    cp_async16_or_zero(sA + (m >> 3) * (kKG * 128) + c * 128 + (m & 7) * 16, src, in);
+  }
+  for (int q = threadIdx.x; q < kBN * kKG; q += kFcThreads) {
+    const int n = chunk_row(q), c = chunk_col(q);
+    const bool in = n0 + n < p.d_out;
+    const __nv_bfloat16* src = p.w + static_cast<size_t>(in ? n0 + n : 0) * K + k0 + c * 8;
+    cp_async16_or_zero(sB + (n >> 3) * (kKG * 128) + c * 128 + (n & 7) * 16, src, in);
+  }
+}
+
+__global__ void __launch_bounds__(kFcThreads, 1) fc_gemm_kernel(FcNormProblem p) {
   extern __shared__ __align__(1024) unsigned char smem[];
-  __shared__ float s_mu[3][kBM], s_rs[3][kBM];
   __shared__ __align__(8) uint64_t s_bar[kStages];
   __shared__ uint32_t s_tmem;
   __shared__ int s_fail;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM;
-  const int d = p.d, K = 3 * d, nk = K / kBK;
+  const int nk = 3 * p.d / kBK;
 
-  for (int i = tid; i < 3 * kBM; i += kFcThreads) {
-    const int s = i / kBM, r = i - s * kBM;
-    const int t = m0 + r;
-    s_mu[s][r] = t < p.T ? p.stats[(static_cast<size_t>(t) * 3 + s) * 2] : 0.f;
-    s_rs[s][r] = t < p.T ? p.stats[(static_cast<size_t>(t) * 3 + s) * 2 + 1] : 0.f;
-  }
   if (tid == 0) {
     s_fail = 0;
     for (int s = 0; s < kStages; ++s)
@@ -150,6 +204,11 @@ __global__ void __launch_bounds__(kFcThreads, 1) fcnorm_gemm_kernel(FcNormProble
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+#pragma unroll
+  for (int a = 0; a < kAhead; ++a) {
+    if (a < nk) load_stage(p, smem + a * kStageBytes, m0, n0, a);
+    cp_async_commit();
+  }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -158,65 +217,28 @@ __global__ void __launch_bounds__(kFcThreads, 1) fcnorm_gemm_kernel(FcNormProble
 
   bool ok = true;
   int committed = -1;  // last k step whose MMAs were committed
-  for (int kt = 0; kt < nk && ok; ++kt) {
-    const int st = kt % kStages;
-    unsigned char* sA = smem + st * kStageBytes;
-    unsigned char* sB = sA + kABytes;
-    if (kt >= kStages) {  // the MMAs that read this stage kStages steps ago are done
-      if (!mbar_wait(smem_u32(&s_bar[st]), static_cast<uint32_t>((kt / kStages - 1) & 1))) {
-        if (tid == 0) s_fail = 1;
-      }
-      __syncthreads();
-      if (s_fail) {
-        ok = false;
-        break;
-      }
+  for (int kt = 0; kt < nk; ++kt) {
+    // refill the stage of step kt + kAhead, last read by the MMAs of step
+    // kt + kAhead - kStages (<= kt - 2): wait for them first
+    const int nxt = kt + kAhead;
+    const int prev = nxt - kStages;
+    if (prev >= 0 && nxt < nk) {
+      if (!mbar_wait(smem_u32(&s_bar[prev % kStages]), static_cast<uint32_t>((prev / kStages) & 1)))
+        s_fail = 1;
     }
-    const int k0 = kt * kBK;
-    // W tile: 256 rows x 8 chunks of 16 bytes, rows past d_out zero
-    for (int q = tid; q < kBN * kKG; q += kFcThreads) {
-      const int n = q % kBN, c = q / kBN;
-      unsigned char* dst = sB + (n >> 3) * (kKG * 128) + c * 128 + (n & 7) * 16;
-      if (n0 + n < p.d_out)
-        cp_async16(dst, p.w + static_cast<size_t>(n0 + n) * K + k0 + c * 8);
-      else
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-    }
-    // A tile: normalised hidden states, 128 tokens x 8 chunks
-    const int seg = k0 / d, f0 = k0 - seg * d;
-    const __nv_bfloat16* hs = seg == 0 ? p.h[0] : seg == 1 ? p.h[1] : p.h[2];
-    for (int q = tid; q < kBM * kKG; q += kFcThreads) {
-      const int m = q % kBM, c = q / kBM;
-      unsigned char* dst = sA + (m >> 3) * (kKG * 128) + c * 128 + (m & 7) * 16;
-      const int t = m0 + m;
-      uint4 out = make_uint4(0, 0, 0, 0);
-      if (t < p.T) {
-        const int f = f0 + c * 8;
-        const uint4 v = *reinterpret_cast<const uint4*>(hs + static_cast<size_t>(t) * d + f);
-        if (p.norm == kNormNone) {
-          out = v;
-        } else {
-          const float mu = s_mu[seg][m], rs = s_rs[seg][m];
-          const float* g = p.gamma + seg * d + f;
-          const float* bt = p.beta != nullptr ? p.beta + seg * d + f : nullptr;
-          float x[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float y = (Elem<__nv_bfloat16>::get(v, e) - mu) * rs * __ldg(g + e);
-            if (bt != nullptr) y += __ldg(bt + e);
-            x[e] = y;
-          }
-          out = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-                           pack_bf16(x[6], x[7]));
-        }
-      }
-      *reinterpret_cast<uint4*>(dst) = out;
-    }
-    cp_async_wait_all();
+    if (nxt < nk) load_stage(p, smem + (nxt % kStages) * kStageBytes, m0, n0, nxt);
+    cp_async_commit();
+    cp_async_wait_group<kAhead>();  // this thread's loads of step kt have landed
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
     __syncthreads();
+    if (s_fail) {
+      ok = false;
+      break;
+    }
     if (tid == 0) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const unsigned char* sA = smem + (kt % kStages) * kStageBytes;
+      const unsigned char* sB = sA + kABytes;
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
         const uint64_t da = smem_desc(smem_u32(sA) + kk * 256, 128, kKG * 128);
@@ -230,11 +252,12 @@ __global__ void __launch_bounds__(kFcThreads, 1) fcnorm_gemm_kernel(FcNormProble
       }
       asm volatile(
           "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-              smem_u32(&s_bar[st]))
+              smem_u32(&s_bar[kt % kStages]))
           : "memory");
     }
     committed = kt;
   }
+  cp_async_wait_group<0>();
 
   // the last commit covers every MMA issued before it
   if (ok && nk > 0) {
@@ -299,19 +322,17 @@ __global__ void __launch_bounds__(kFcThreads, 1) fcnorm_gemm_kernel(FcNormProble
 
 }  // namespace
 
-int fcnorm_smem_bytes() { return kStages * kStageBytes; }
-
 cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s) {
   if (p.T <= 0 || p.d_out <= 0) return cudaSuccess;
   const int warps = p.T * 3;
-  fcnorm_stats_kernel<<<(warps * 32 + 255) / 256, 256, 0, s>>>(p);
+  fcnorm_prep_kernel<<<(warps * 32 + 255) / 256, 256, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int smem = kStages * kStageBytes;
-  e = cudaFuncSetAttribute(fcnorm_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(fc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((p.d_out + kBN - 1) / kBN, (p.T + kBM - 1) / kBM);
-  fcnorm_gemm_kernel<<<grid, kFcThreads, smem, s>>>(p);
+  fc_gemm_kernel<<<grid, kFcThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -129,7 +129,7 @@ struct FcNormProblem {
   const float* bias;           // [d_out] or nullptr
   __nv_bfloat16* out;          // [T, d_out]
   bool out_vec;                // rows of out 16-byte aligned
-  float* stats;                // [T, 3, 2]: mean, 1 / sqrt(var + eps)
+  __nv_bfloat16* x;            // [T, 3d]: the normalised, concatenated input (scratch)
   unsigned* err;
 };
 
