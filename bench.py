@@ -102,7 +102,7 @@ def whole_job_rate(units_per_rank_step, steps, world, max_ms):
     return units_per_rank_step * steps * world / (max_ms / 1e3)
 
 
-def csrc_hash(files=("sv_device.cuh", "sv_internal.cuh", "sv_rowstats.cu")):
+def csrc_hash(files=("sv_device.cuh", "sv_internal.cuh", "sv_rowstats.cu", "sv_span.cuh")):
     """Hash of the row-statistics kernel's sources: the committed traffic
     figure is used only while these are unchanged."""
     h = hashlib.sha256()
