@@ -3,6 +3,8 @@
 // draft-tree walk and the lazy chain).
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "sv_device.cuh"
 #include "sv_pick.cuh"
 
@@ -69,7 +71,14 @@ struct NodeLaw {
 
 // Sums of f(z_t, y_t, t) over this thread's 32 tokens [t0, t0 + 32) of a
 // level-1 block (0 past cend): h0 over the first 16, h1 over the last 16.
-template <typename T, bool kVecPath, typename F>
+// One element of a row staged in shared memory, as float.
+__device__ __forceinline__ float staged_elem(const float* p) { return *p; }
+__device__ __forceinline__ float staged_elem(const __nv_bfloat16* p) {
+  return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
+}
+
+// kSmem: z and y point into rows staged in shared memory (plain loads).
+template <typename T, bool kVecPath, typename F, bool kSmem = false>
 __device__ __forceinline__ void seg_sums(const T* z, const T* y, bool need_y, int t0, int cend, F f,
                                          float& h0, float& h1) {
   using E = Elem<T>;
@@ -83,8 +92,10 @@ __device__ __forceinline__ void seg_sums(const T* z, const T* y, bool need_y, in
     for (int i = 0; i < kVecs; ++i) {
       const int e0 = t0 + i * kVec;
       const bool in = e0 < cend;
-      zv[i] = in ? __ldg(reinterpret_cast<const uint4*>(z + e0)) : make_uint4(0, 0, 0, 0);
-      yv[i] = (in && need_y) ? __ldg(reinterpret_cast<const uint4*>(y + e0)) : make_uint4(0, 0, 0, 0);
+      const uint4* zp = reinterpret_cast<const uint4*>(z + e0);
+      const uint4* yp = reinterpret_cast<const uint4*>(y + e0);
+      zv[i] = in ? (kSmem ? *zp : __ldg(zp)) : make_uint4(0, 0, 0, 0);
+      yv[i] = (in && need_y) ? (kSmem ? *yp : __ldg(yp)) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < kVecs; ++i) {

@@ -108,10 +108,26 @@ __global__ void __launch_bounds__(kThreads, kSpanMinBlocks) tree_rowstats_kernel
 
 constexpr int kActContinue = 0, kActPass = 1, kActBonus = 2, kActResidual = 3;
 
+// Level-1 blocks a CTA can keep staged in shared memory (both rows of the
+// node under test): a residual pass or a draw at the same node then reads
+// no global memory.  Staging is used for 16-bit rows with at most
+// kStageBlocks blocks per CTA; other cases read the rows from global memory.
+constexpr int kStageBlocks = 2;
+template <typename T>
+constexpr int tree_stage_bytes() {
+  return 2 * kStageBlocks * kLevel1 * static_cast<int>(sizeof(T));
+}
+template <typename T, bool kVecPath>
+constexpr bool tree_stages() {
+  return kVecPath && sizeof(T) == 2;
+}
+
 template <typename T, bool kVecPath>
 __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_TREE_MINB)
     tree_walk_kernel(TreeProblem p, Workspace w) {
   using E = Elem<T>;
+  extern __shared__ __align__(16) unsigned char s_stage_raw[];
+  __shared__ int s_staged;  // node whose rows are staged, -1 for none
   __shared__ int s_par[kMaxNodes], s_tok[kMaxNodes], s_first[kMaxNodes], s_next[kMaxNodes];
   __shared__ int s_gidx[kMaxNodes], s_path[kMaxNodes], s_rej[kMaxNodes];
   __shared__ float s_cq[kMaxNodes], s_sq[kMaxNodes], s_cp[kMaxNodes], s_sp[kMaxNodes];
@@ -268,6 +284,33 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   const T* ybase = use_draft ? static_cast<const T*>(p.draft) + static_cast<size_t>(b) * (M + 1) * V
                              : zbase;
   const int S3 = w.S3;
+  const bool staging = tree_stages<T, kVecPath>() && S3 <= kStageBlocks * kTreeCluster;
+  T* sz = reinterpret_cast<T*>(s_stage_raw);        // [kStageBlocks][kLevel1] of z
+  T* sy = sz + kStageBlocks * kLevel1;              // the same for y
+  if (i == 0) s_staged = -1;
+  __syncthreads();
+  // Stage this CTA's blocks of the node's rows (z, and y when read) unless
+  // they are staged already; every thread copies the vectors it will sum.
+  auto stage_node = [&](int node, bool with_y) {
+    if (s_staged == node) return;
+    const T* z = zbase + static_cast<size_t>(node) * V;
+    const T* y = ybase + static_cast<size_t>(node) * V;
+    int bi = 0;
+    for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster, ++bi) {
+      const int cbeg = c * kLevel1, cend = min(V, cbeg + kLevel1);
+      constexpr int kVec = Elem<T>::kVec;
+      for (int e = i * kSegTok; e < i * kSegTok + kSegTok; e += kVec) {
+        if (cbeg + e < cend) {
+          cp_async16(sz + bi * kLevel1 + e, z + cbeg + e);
+          if (with_y) cp_async16(sy + bi * kLevel1 + e, y + cbeg + e);
+        }
+      }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    if (i == 0) s_staged = node;
+    __syncthreads();
+  };
   int pass = 0;
   while (true) {
     if (i == 0) {
@@ -337,11 +380,24 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
     const T* z = zbase + static_cast<size_t>(node) * V;
     const T* y = ybase + static_cast<size_t>(node) * V;
     float acc = 0.f;
-    for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster) {
-      float h0, h1;
-      seg_sums<T, kVecPath>(z, y, true, c * kLevel1 + i * kSegTok, min(V, (c + 1) * kLevel1),
-                            [&](float zt, float yt, int t) { return law.r(zt, yt, t); }, h0, h1);
-      acc += h0 + h1;
+    auto lf = [&](float zt, float yt, int t) { return law.r(zt, yt, t); };
+    if (staging) {
+      stage_node(node, true);
+      int bi = 0;
+      for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster, ++bi) {
+        float h0, h1;
+        const int cbeg = c * kLevel1;
+        seg_sums<T, kVecPath, decltype(lf), true>(sz + bi * kLevel1 - cbeg, sy + bi * kLevel1 - cbeg, true,
+                                                  cbeg + i * kSegTok, min(V, cbeg + kLevel1), lf, h0, h1);
+        acc += h0 + h1;
+      }
+    } else {
+      for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster) {
+        float h0, h1;
+        seg_sums<T, kVecPath>(z, y, true, c * kLevel1 + i * kSegTok, min(V, (c + 1) * kLevel1), lf, h0,
+                              h1);
+        acc += h0 + h1;
+      }
     }
     acc = cta_sum(acc, sc.red);
     if (i == 0) s_part[pass & 1] = acc;
@@ -376,13 +432,26 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   float* masses = w.chunk_sums + static_cast<size_t>(b) * S3;
   int* cands = w.blk_tok + static_cast<size_t>(b) * S3;
   auto rf = [&](float zt, float yt, int t) { return law.r(zt, yt, t); };
-  for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster) {
+  if (staging) stage_node(node, need_y);
+  int bi = 0;
+  for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster, ++bi) {
     const int cbeg = c * kLevel1, cend = min(V, cbeg + kLevel1);
     float h0, h1, mass;
-    seg_sums<T, kVecPath>(z, y, need_y, cbeg + i * kSegTok, cend, rf, h0, h1);
-    const int cand = block_pick(
-        h0, h1, cbeg, cend, job,
-        [&](int t) { return law.r(E::load1(z + t), need_y ? E::load1(y + t) : 0.f, t); }, sc, &mass);
+    int cand;
+    if (staging) {
+      const T* bz = sz + bi * kLevel1 - cbeg;
+      const T* by = sy + bi * kLevel1 - cbeg;
+      seg_sums<T, kVecPath, decltype(rf), true>(bz, by, need_y, cbeg + i * kSegTok, cend, rf, h0, h1);
+      cand = block_pick(
+          h0, h1, cbeg, cend, job,
+          [&](int t) { return law.r(staged_elem(bz + t), need_y ? staged_elem(by + t) : 0.f, t); }, sc,
+          &mass);
+    } else {
+      seg_sums<T, kVecPath>(z, y, need_y, cbeg + i * kSegTok, cend, rf, h0, h1);
+      cand = block_pick(
+          h0, h1, cbeg, cend, job,
+          [&](int t) { return law.r(E::load1(z + t), need_y ? E::load1(y + t) : 0.f, t); }, sc, &mass);
+    }
     if (i == 0) {
       masses[c] = mass;
       cands[c] = cand;
@@ -421,7 +490,13 @@ cudaError_t launch_tree_t(const TreeProblem& p, const Workspace& w, cudaStream_t
     const long long blocks = static_cast<long long>(p.B) * kTreeCluster;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    tree_walk_kernel<T, kVecPath><<<dim3(static_cast<unsigned>(blocks)), kST, 0, s>>>(p, w);
+    const int smem = tree_stages<T, kVecPath>() ? tree_stage_bytes<T>() : 0;
+    if (smem > 0) {
+      const cudaError_t e = cudaFuncSetAttribute(tree_walk_kernel<T, kVecPath>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+    }
+    tree_walk_kernel<T, kVecPath><<<dim3(static_cast<unsigned>(blocks)), kST, smem, s>>>(p, w);
   }
   return cudaGetLastError();
 }
