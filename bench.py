@@ -759,6 +759,27 @@ def cpu_baseline(wl, budget_s):
                       f"{el:.1f} s, float64 numpy on 1 host thread"}
 
 
+def oracle_position(wl, z, y, b, j, seed):
+    """The oracle's work for draft position j (1-based) of request b, as it
+    stands: widen the rows, then the argmax (T = 0) or both softmaxes, the
+    Philox uniform and the accept test; at the last position also the
+    residual of that row pair and its grouped draw (one draw per request)."""
+    from oracle import philox as oph
+    from oracle import verify as ov
+    _, N, _ = wl.shape
+    t = float(wl.temperature[b])
+    zr = ov.logits_to_f64(z[b, j - 1], wl.dtype)
+    if t == 0.0:
+        ov.argmax_lowest(zr)
+        return
+    d = int(wl.tokens[b, j - 1])
+    q = ov.softmax(zr, t)
+    p = ov.softmax(ov.logits_to_f64(y[b, j - 1], wl.dtype), t)
+    ov.accept(q[d], p[d], oph.uniform(seed, b, j, oph.ACCEPT_DRAW))
+    if j == N:
+        ov.sample_grouped(ov.residual(q, p), oph.uniforms4(seed, b, j, oph.SAMPLE_DRAW))
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -766,19 +787,24 @@ def run_reference(args):
     from speculative_decoding_verification_73_gb300 import workloads
     wl = workloads.batch64_bf16()
     B, N, V = wl.shape
-    # time one request to size the per-step sample so the run stays within ~3 minutes
-    t0 = time.perf_counter()
-    oracle_requests(wl, [0])
-    per_req = time.perf_counter() - t0
-    per_step = max(1, min(B, int(150.0 / max(args.steps + args.warmup, 1) / max(per_req, 1e-3))))
+    z, y = wl.raw()
+    # one step = the oracle's work for one draft position (request-major
+    # order over all B x N positions, rotating), so any --steps stays bounded
+    def step(i):
+        k = i % (B * N)
+        oracle_position(wl, z, y, k // N, k % N + 1, wl.seed)
+
     for i in range(args.warmup):
-        oracle_requests(wl, [(i * per_step + k) % B for k in range(per_step)])
+        step(i)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        oracle_requests(wl, [(i * per_step + k) % B for k in range(per_step)])
+        step(args.warmup + i)
     el = time.perf_counter() - t0
-    value = per_step * N * args.steps / el
-    sample = f"{per_step} request(s) of {WORKLOAD} per step (rotating), float64 numpy, 1 host thread"
+    value = args.steps / el
+    sample = (f"one draft position of {WORKLOAD} per step (positions taken request-major, "
+              f"rotating over all {B * N}; greedy positions cost an argmax, sampled ones two "
+              f"softmaxes, the accept test and, at a request's last position, the residual draw), "
+              f"float64 numpy, 1 host thread")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
