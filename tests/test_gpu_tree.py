@@ -113,3 +113,53 @@ def test_tree_errors_are_flagged_per_request():
         assert res.request_errors[b] == bit
         assert acc[b] == -1 and kv[b] == 0 and (toks[b] == -1).all() and (path[b] == -1).all()
     assert acc[5] >= 0
+
+
+MAX_CASES = {
+    # 255 draft nodes per tree: the largest M a context accepts
+    "random-255-sampled-f32": lambda: workloads.make_tree(3, 3001, "f32", gen_seed=81, m=binding.SV_MAX_N,
+                                                          verify_seed=21),
+    "random-255-topk-bf16": lambda: workloads.make_tree(3, 4099, "bf16", gen_seed=82, m=binding.SV_MAX_N,
+                                                        mode=workloads.TREE_TOPK, verify_seed=22),
+    "star-255-sampled-bf16": lambda: workloads.make_tree(3, 4099, "bf16", gen_seed=83, widths=(255,),
+                                                         verify_seed=23),
+    "star-255-topk-f32": lambda: workloads.make_tree(3, 3001, "f32", gen_seed=84, widths=(255,),
+                                                     mode=workloads.TREE_TOPK, verify_seed=24),
+    "line-255-sampled-f32": lambda: workloads.make_tree(3, 3001, "f32", gen_seed=85, widths=(1,) * 255,
+                                                        sigma=(0.0, 0.05), verify_seed=25),
+}
+
+
+@pytest.mark.parametrize("name", list(MAX_CASES))
+def test_tree_max_size(name):
+    wl = MAX_CASES[name]()
+    assert wl.shape[1] == binding.SV_MAX_N
+    for seed in (wl.seed, wl.seed + 7):
+        res, _ = check_tree(wl, seed, f"{name} seed {seed}")
+        assert res.errors == 0
+
+
+def _repeat_first_sibling(wl):
+    """Give the second child of every node the token of its first child."""
+    B, M, _ = wl.shape
+    par = wl.parents.numpy()
+    for b in range(B):
+        kids = {}
+        for i in range(M):
+            kids.setdefault(int(par[b, i]), []).append(i)
+        for ks in kids.values():
+            if len(ks) > 1:
+                wl.tokens[b, ks[1]] = wl.tokens[b, ks[0]]
+    return wl
+
+
+@pytest.mark.parametrize("mode", [workloads.TREE_SAMPLED, workloads.TREE_TOPK])
+def test_repeated_sibling_tokens(mode):
+    """A token tried twice at one node: in TOPK mode the residual has already
+    removed it, so the second try is always rejected and the removed mass is
+    counted once; in SAMPLED mode the second try faces the residual."""
+    wl = _repeat_first_sibling(workloads.make_tree(16, 32000, "bf16", gen_seed=86, widths=(3, 2, 2),
+                                                   mode=mode, verify_seed=26))
+    for seed in (26, 27, 28):
+        res, _ = check_tree(wl, seed, f"repeat mode {mode} seed {seed}")
+        assert res.errors == 0
