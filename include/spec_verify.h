@@ -126,7 +126,12 @@ int spec_verify_init(spec_verify_ctx** ctx, int max_B, int max_N, int max_V,
  * B == 0 is a no-op.  Returns SV_OK, SV_EINVAL (nothing enqueued) or
  * SV_ECUDA.  Device-detected input errors do not change the return value:
  * they mark the request's outputs (see SV_ERRBIT_*) and are read with
- * spec_verify_get_error.
+ * spec_verify_get_error.  The sampling kernel starts on a request as soon
+ * as that request's rows are reduced, by polling tags on the partial
+ * statistics; the tag is a per-call sequence number the context keeps on
+ * the host, so every call is enqueued by the host (a replay of one captured
+ * call would reuse its number).  A poll that runs out (about a second, only
+ * if the row kernel stalls) marks the request with SV_ERRBIT_WAIT.
  */
 int spec_verify(spec_verify_ctx* ctx, int B, int N, int V,
                 const void* target_logits, const void* draft_logits,
@@ -163,7 +168,8 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V,
  * Sharing: all calls on a device use the same array.  Calls must be ordered
  * (one stream, or streams ordered by events): two calls whose kernels
  * overlap corrupt each other's results.  Each call clears its device error
- * word and its sampling counters before its kernels run; device-detected input errors are reported in
+ * word, its sampling counters and the tags of its partial statistics (one
+ * memset) before its kernels run; device-detected input errors are reported in
  * the request's outputs only (out_tokens -1, out_accept_len -1,
  * out_kv_len 0; see SV_ERRBIT_*), since there is no context to read them
  * from.

@@ -25,6 +25,10 @@ struct spec_verify_ctx {
   int recorded;                     // calls whose events are in `events`
   double ms[SV_NUM_KERNELS];
   int calls;
+  // sequence number of the last chain call: the tag of its row-statistics
+  // partials (1, 2, ...; the partials are cleared again when it wraps)
+  unsigned epoch;
+  size_t part_bytes;  // bytes of the partials region
 };
 
 namespace {
@@ -148,7 +152,11 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   ctx->w.arrivals = reinterpret_cast<unsigned*>(base + o_arr);
   ctx->w.dbg_accept = reinterpret_cast<float*>(base + o_acc);
   ctx->w.dbg_logz = reinterpret_cast<float*>(base + o_lz);
+  // tags start at 0, which no chain call uses
+  ctx->part_bytes = part_rows * s1 * sizeof(sv::Partial);
+  ctx->epoch = 0;
   if (cudaMemsetAsync(base + o_err, 0, zero_bytes, ctx->stream) != cudaSuccess ||
+      cudaMemsetAsync(base + o_part, 0, ctx->part_bytes, ctx->stream) != cudaSuccess ||
       cudaStreamSynchronize(ctx->stream) != cudaSuccess) {
     cudaFree(ctx->ws);
     delete ctx;
@@ -189,6 +197,14 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
   sv::Workspace w = ctx->w;
   w.S1 = ceil_div(V, sv::row_chunk_elems(ctx->dtype));
   w.S3 = ceil_div(V, sv::sample_chunk_elems(ctx->dtype));
+  // A fresh tag per call: the sampler of this call takes a partial only once
+  // it carries this tag, never one left by an earlier call.
+  if (++ctx->epoch == 0) {
+    if (cudaMemsetAsync(ctx->w.partials, 0, ctx->part_bytes, ctx->stream) != cudaSuccess)
+      return SV_ECUDA;
+    ctx->epoch = 1;
+  }
+  p.epoch = ctx->epoch;
 
   cudaEvent_t* ev = nullptr;
   if (ctx->profile_every > 0 && (ctx->profile_seen++ % ctx->profile_every) == 0) {
@@ -319,6 +335,7 @@ int spec_verify_lazy(spec_verify_ctx* ctx, int B, int N, int V, const void* targ
   p.out_tokens = out_tokens;
   p.out_accept = out_accept_len;
   p.out_kv = out_kv_len;
+  p.epoch = 0;  // the lazy kernel reads its own partials after a CTA barrier
   sv::Workspace w = ctx->w;
   w.S1 = ceil_div(V, sv::row_chunk_elems(ctx->dtype));
   w.S3 = ceil_div(V, sv::sample_chunk_elems(ctx->dtype));

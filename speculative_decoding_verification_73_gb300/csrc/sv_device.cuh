@@ -15,16 +15,35 @@ constexpr unsigned kFull = 0xffffffffu;
 // ------------------------------------------------- dependent launches
 // Programmatic dependent launch (PTX griddepcontrol).  A kernel launched
 // with the programmatic-serialisation attribute may start while the kernel
-// before it in the stream is still running; it must call
-// wait_for_prerequisite() before touching anything that kernel writes (the
-// call returns once that grid has completed and its writes are visible, and
-// at once when there is no such dependency).  allow_dependents() lets the
+// before it in the stream is still running; allow_dependents() lets such a
 // dependent grid be scheduled as soon as every CTA of this grid has made
-// the call or exited.
-__device__ __forceinline__ void wait_for_prerequisite() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
+// the call or exited.  The dependent then synchronises with this grid by
+// itself (the chain sampler polls the tags of the partials it reads).
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// A Partial moved as one 128-bit scalar at gpu scope (PTX .b128 with
+// .relaxed.gpu): a reader in another grid that is running at the same time
+// sees either the whole old or the whole new 16 bytes, never a mix, so the
+// tag in the last word vouches for the three words before it.  Returned as
+// float4 (a, s, idx bits, tag bits).
+__device__ __forceinline__ void st_partial_relaxed(Partial* at, const Partial& v) {
+  const uint64_t lo = static_cast<uint64_t>(__float_as_uint(v.s)) << 32 | __float_as_uint(v.a);
+  const uint64_t hi = static_cast<uint64_t>(v.tag) << 32 | static_cast<uint32_t>(v.idx);
+  asm volatile(
+      "{\n\t.reg .b128 t;\n\tmov.b128 t, {%1, %2};\n\tst.relaxed.gpu.global.b128 [%0], t;\n\t}" ::"l"(at),
+      "l"(lo), "l"(hi)
+      : "memory");
+}
+__device__ __forceinline__ float4 ld_partial_relaxed(const Partial* at) {
+  uint64_t lo, hi;
+  asm volatile(
+      "{\n\t.reg .b128 t;\n\tld.relaxed.gpu.global.b128 t, [%2];\n\tmov.b128 {%0, %1}, t;\n\t}"
+      : "=l"(lo), "=l"(hi)
+      : "l"(at)
+      : "memory");
+  return make_float4(__uint_as_float(static_cast<uint32_t>(lo)), __uint_as_float(static_cast<uint32_t>(lo >> 32)),
+                     __uint_as_float(static_cast<uint32_t>(hi)), __uint_as_float(static_cast<uint32_t>(hi >> 32)));
+}
 
 // ---------------------------------------------------------------- numbers
 
@@ -98,6 +117,18 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Groups of copies: commit closes the group of this thread's copies issued
+// since the last commit; wait_pending(n) returns once at most n of this
+// thread's groups are still in flight (n a constant after unrolling).
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+  switch (n) {
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+  }
+}
 
 
 // 16-byte read-only load that does not allocate in L1 (each byte of a row

@@ -54,16 +54,23 @@ constexpr int kKvInplace = 1;  // into the cache right after each sequence's len
 constexpr int kTreeSampled = 0;  // independent draws from the node's draft row
 constexpr int kTreeTopk = 1;     // fixed candidates (point masses)
 
-// Statistics of one chunk of one logit row (16 bytes).
+// Statistics of one chunk of one logit row (16 bytes, 16-byte aligned).
 //   sampled row: a = c = fl(M * k) with M the chunk maximum and k = log2(e)/T,
 //                s = sum over the chunk of 2^(x*k - c)   (NaN marks a bad chunk)
+//                idx = bits of the float logit at the row's draft token when
+//                the chunk holds it (chain kernel), else 0
 //   greedy row : a = chunk maximum M, s = 0 (NaN if a NaN was seen),
 //                idx = lowest index holding M
+//   tag        : the chain call's sequence number (never 0); every other
+//                kernel writes 0.  The chain row-statistics kernel stores the
+//                whole partial with one 128-bit access and the chain sampler
+//                polls for its tag, so it can start on a request whose rows
+//                are done while the rest of the grid still runs.
 struct Partial {
   float a;
   float s;
   int idx;
-  int pad;
+  unsigned tag;
 };
 
 constexpr int kJobNone = 0;
@@ -91,6 +98,7 @@ struct Problem {
   int32_t* out_tokens;       // [B, N+1]
   int32_t* out_accept;       // [B]
   int32_t* out_kv;           // [B]
+  unsigned epoch;            // tag of this call's row-statistics partials (never 0)
 };
 
 struct TreeProblem {
@@ -163,6 +171,7 @@ cudaError_t launch_philox_probe(unsigned long long seed, const uint32_t* ctr3, u
                                 int n, cudaStream_t s);
 
 inline int row_chunk_elems(int dtype) { return kSpanBytes / (dtype == 1 ? 2 : 4); }
+
 inline int sample_chunk_elems(int) { return kLevel1; }
 
 }  // namespace sv

@@ -18,9 +18,10 @@
 // calls on that device reuse the cached pointer.  Problems whose working memory does
 // not fit are refused with SV_ESCRATCH before anything is enqueued.
 //
-// Sharing: every call on a device uses the same array.  Only the error word
-// and the arrival counters have to start at zero; each call clears them on
-// its stream before its kernels run.  Two calls whose kernels overlap in
+// Sharing: every call on a device uses the same array.  The row-statistics
+// partials (whose tags the sampler polls), the error word and the arrival
+// counters have to start at zero; each call clears that front part of the
+// array on its stream before its kernels run, in one memset.  Two calls whose kernels overlap in
 // time (different streams without ordering between them, or host threads
 // racing on one stream) corrupt each other's scratch and results.
 
@@ -137,12 +138,16 @@ int spec_verify_noalloc(int B, int N, int V, int dtype, const void* target_logit
   p.out_tokens = out_tokens;
   p.out_accept = out_accept_len;
   p.out_kv = out_kv_len;
+  p.epoch = 1;  // the partials were cleared just before (below)
   const size_t esize = dtype == SV_BF16 ? 2 : 4;
   const bool vec = (static_cast<size_t>(V) * esize) % 16 == 0 && aligned16(target_logits) &&
                    (N == 0 || aligned16(draft_logits));
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-  // the error word and the sampler's arrival counters start at zero
-  if (cudaMemsetAsync(base + c.err, 0, c.acc - c.err, s) != cudaSuccess) return SV_ECUDA;
+  // The partials (tags 0: not yet written by this call), token logits,
+  // block sums, the error word and the arrival counters start at zero.  The
+  // parts move with the problem's shape, so whatever an earlier call left
+  // there could otherwise pass for a tag of this call.
+  if (cudaMemsetAsync(base, 0, c.acc, s) != cudaSuccess) return SV_ECUDA;
   if (sv::launch_rowstats(dtype, vec, p, w, s) != cudaSuccess) return SV_ECUDA;
   if (sv::launch_sample(dtype, vec, p, w, s) != cudaSuccess) return SV_ECUDA;
   return SV_OK;

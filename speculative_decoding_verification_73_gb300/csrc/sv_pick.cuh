@@ -134,5 +134,78 @@ __device__ int block_pick(float h0, float h1, int cbeg, int cend, const Job& job
   return sc.tok;
 }
 
+// block_pick for the kNB consecutive level-1 blocks starting at token c0
+// (the first nb of them real, the last one cut at V): the same masses and
+// tokens, bit for bit, as kNB calls of block_pick, with one set of CTA
+// barriers for all the blocks.  Warp b picks levels 2-4 of block b, so kNB
+// <= kST / 32.  r_at(b, t) re-evaluates r at token t of block b.
+template <int kNB, typename RAt>
+__device__ void blocks_pick(const float (&h0)[kNB], const float (&h1)[kNB], int c0, int V, int nb,
+                            const Job& job, RAt r_at, BlockScratch (&sc)[kNB], float (&mass)[kNB],
+                            int (&tok)[kNB]) {
+  static_assert(kNB <= kST / 32, "one warp per block");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float tot[kNB];
+#pragma unroll
+  for (int b = 0; b < kNB; ++b) {
+    sc[b].l3[2 * threadIdx.x] = h0[b];
+    sc[b].l3[2 * threadIdx.x + 1] = h1[b];
+    float m2 = h0[b] + h1[b];
+#pragma unroll
+    for (int o = 1; o < kL3PerL2 / 2; o <<= 1) m2 += __shfl_xor_sync(kFull, m2, o);
+    if ((threadIdx.x & (kL3PerL2 / 2 - 1)) == 0) sc[b].l2[threadIdx.x / (kL3PerL2 / 2)] = m2;
+    // CTA sum of h0 + h1 in cta_sum's order
+    float v = h0[b] + h1[b];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    if (lane == 0) sc[b].red[warp] = v;
+  }
+  __syncthreads();  // publishes l2, l3 and the warp sums
+#pragma unroll
+  for (int b = 0; b < kNB; ++b) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kST / 32; ++w) v += sc[b].red[w];
+    tot[b] = v;
+  }
+  if (warp < nb) {  // warp-uniform
+    const int b = warp;
+    const int g2 = warp_pick([&](int i) { return sc[b].l2[i]; }, kL2, job.u[1]);
+    int pick = -1;
+    if (g2 >= 0) {
+      const int g3 = warp_pick([&](int i) { return sc[b].l3[g2 * kL3PerL2 + i]; }, kL3PerL2, job.u[2]);
+      pick = g2 * kL3PerL2 + max(g3, 0);
+    }
+    if (lane == 0) sc[b].pick = pick;
+  }
+  __syncthreads();
+  if (warp < nb && lane < kLevel3) {
+    const int b = warp;
+    const int blk3 = sc[b].pick;
+    if (blk3 >= 0) {
+      const int cbeg = c0 + b * kLevel1;
+      const int t = cbeg + blk3 * kLevel3 + lane;
+      sc[b].l4[lane] = t < min(V, cbeg + kLevel1) ? r_at(b, t) : 0.f;
+    }
+  }
+  __syncthreads();
+  if (warp < nb) {
+    const int b = warp;
+    const int blk3 = sc[b].pick;
+    int tk = -1;
+    if (blk3 >= 0) {
+      const int g4 = max(warp_pick([&](int i) { return sc[b].l4[i]; }, kLevel3, job.u[3]), 0);
+      tk = c0 + b * kLevel1 + blk3 * kLevel3 + g4;
+    }
+    if (lane == 0) sc[b].tok = tk;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int b = 0; b < kNB; ++b) {
+    mass[b] = tot[b];
+    tok[b] = b < nb ? sc[b].tok : -1;
+  }
+}
+
 }  // namespace
 }  // namespace sv

@@ -15,9 +15,12 @@
 // spans of kSpanBytes; one CTA reduces one span in a single streaming pass
 // (16-byte non-allocating loads, the next group of loads in flight while the
 // current one is reduced, a running maximum with a rescaled sum per thread,
-// one CTA-wide merge per span) and writes partials[row][span].  The CTA
-// whose span holds the row's draft token also stores that token's logit, so
-// the walk never reads the logits again.  Rows that are not 16-byte aligned
+// one CTA-wide merge per span) and writes partials[row][span] tagged with
+// the call's sequence number, in one 128-bit store: the sampler polls the
+// tags of its own request, so it can start on a request whose rows are done
+// while later rows are still streaming.  The CTA whose span holds the row's
+// draft token puts that token's logit in the same partial, so the walk
+// never reads the logits again.  Rows that are not 16-byte aligned
 // take a scalar two-pass path over the same spans.  Small per-thread state
 // and groups of two loads keep eight CTAs resident per SM, which measured
 // best (more warps in flight, fewer registers per byte in flight).
@@ -66,7 +69,8 @@ __global__ void __launch_bounds__(kThreads, kSpanMinBlocks) rowstats_kernel(Prob
   // is captured in the same pass for the walk
   const int j = slot <= p.N ? slot : slot - p.N - 1;
   const int d = (!greedy && slot != p.N) ? p.tokens[static_cast<size_t>(b) * p.N + j] : -1;
-  float* tok = w.tok_logit + row;
+  __shared__ float s_tok;  // the logit at d, set by the thread whose vector holds it
+  float* tok = &s_tok;
   Partial out;
   if (!kVecPath) {
     out = chunk_partial_scalar<T>(base, beg, end, greedy, k, d, tok);
@@ -77,7 +81,12 @@ __global__ void __launch_bounds__(kThreads, kSpanMinBlocks) rowstats_kernel(Prob
     out = greedy ? span_partial_vec<T, true, false>(base, beg, end, k, -1, tok)
                  : span_partial_vec<T, false, false>(base, beg, end, k, d, tok);
   }
-  if (threadIdx.x == 0) w.partials[static_cast<size_t>(row) * S1 + span] = out;
+  if (threadIdx.x == 0) {
+    // the reductions above end in CTA barriers, so s_tok is visible here
+    if (!greedy) out.idx = (d >= beg && d < end) ? __float_as_int(s_tok) : 0;
+    out.tag = p.epoch;
+    st_partial_relaxed(w.partials + static_cast<size_t>(row) * S1 + span, out);
+  }
 }
 
 template <typename T, bool kVecPath>

@@ -16,9 +16,11 @@
 // compares a uniform against at most a few dozen float32 edges.
 //
 // Grid: one CTA per request and group of blocks_per_cta() level-1 blocks,
-// request-major, launched with programmatic dependent launch (it may become
-// resident while the row-statistics kernel drains; the walk waits for that
-// kernel before reading its results).  Every CTA runs the request's
+// request-major, launched with programmatic dependent launch: it becomes
+// resident once every row-statistics CTA has started, while that grid
+// drains, and never waits for the grid as a whole.  The walk polls the tags
+// of its own request's partials instead, so the requests whose rows were
+// reduced first are sampled while later rows still stream.  Every CTA runs the request's
 // accept/reject walk itself from the row-statistics partials (one L2 round
 // trip; CTA 0 of the request writes the walk's outputs).  For a sampled
 // request each CTA then stages its blocks' row pair in shared memory
@@ -49,10 +51,15 @@ namespace sv {
 namespace {
 
 // Level-1 blocks one CTA takes: their row pair is staged in shared memory
-// (64 KB either way), all of it requested at once.
+// (64 KB for two bf16 blocks or one fp32 block), all of it requested at
+// once.  Build-time override: -DSV_SAMPLE_BF16_BLOCKS=1 (one bf16 block per
+// CTA, twice the CTAs per request, 32 KB each).
+#ifndef SV_SAMPLE_BF16_BLOCKS
+#define SV_SAMPLE_BF16_BLOCKS 2
+#endif
 template <typename T>
 constexpr int blocks_per_cta() {
-  return sizeof(T) == 2 ? 2 : 1;
+  return sizeof(T) == 2 ? SV_SAMPLE_BF16_BLOCKS : 1;
 }
 template <typename T>
 constexpr int stage_bytes() {
@@ -210,7 +217,8 @@ template <typename T, bool kVecPath>
 __global__ void __launch_bounds__(kST, 3) sample_kernel(Problem p, Workspace w) {
   constexpr int kB = blocks_per_cta<T>();
   extern __shared__ __align__(16) unsigned char s_rows[];  // staged rows (vector path)
-  __shared__ BlockScratch sc;
+  __shared__ BlockScratch scs[kB];
+  BlockScratch& sc = scs[0];
   __shared__ Job s_job;
   __shared__ int s_last;
   const int S3 = w.S3;
@@ -235,24 +243,39 @@ __global__ void __launch_bounds__(kST, 3) sample_kernel(Problem p, Workspace w) 
   if (kVecPath) {
     T* sz = reinterpret_cast<T*>(s_rows);
     T* sy = sz + kB * kLevel1;
-    for (int i = 0; i < nb; ++i)
-      stage_block<T>(z, y, (c0 + i) * kLevel1, V, has_p, sz + i * kLevel1, sy + i * kLevel1);
-    cp_async_wait_all();  // this thread's copies; it alone reads them before the barriers
-    for (int i = 0; i < nb; ++i) {
-      const int cbeg = (c0 + i) * kLevel1;
-      const T* bz = sz + i * kLevel1;
-      const T* by = sy + i * kLevel1;
-      float h0, h1, mass;
-      staged_halves<T>(bz, by, job, has_p, h0, h1);
-      const int cand = block_pick(
-          h0, h1, cbeg, min(V, cbeg + kLevel1), job,
-          [&](int t) {
-            return resid1(staged1(bz + (t - cbeg)), has_p ? staged1(by + (t - cbeg)) : 0.f, job, has_p);
-          },
-          sc, &mass);
-      if (threadIdx.x == 0) {
-        masses[c0 + i] = mass;
-        cands[c0 + i] = cand;
+    // one group of copies per block, so block i is reduced while the
+    // blocks after it are still arriving
+#pragma unroll
+    for (int i = 0; i < kB; ++i) {
+      if (i < nb) stage_block<T>(z, y, (c0 + i) * kLevel1, V, has_p, sz + i * kLevel1, sy + i * kLevel1);
+      cp_async_commit();
+    }
+    // every block's level-3 masses first, then the picks of all blocks
+    // together (warp i picks inside block i)
+    float h0[kB], h1[kB], mass[kB];
+    int cand[kB];
+#pragma unroll
+    for (int i = 0; i < kB; ++i) {
+      h0[i] = 0.f;
+      h1[i] = 0.f;
+      cp_async_wait_pending(kB - 1 - i);  // this thread's copies of block i; it alone reads them here
+      if (i < nb) staged_halves<T>(sz + i * kLevel1, sy + i * kLevel1, job, has_p, h0[i], h1[i]);
+    }
+    blocks_pick<kB>(
+        h0, h1, c0 * kLevel1, V, nb, job,
+        [&](int i, int t) {
+          const int e = t - (c0 + i) * kLevel1;
+          return resid1(staged1(sz + i * kLevel1 + e), has_p ? staged1(sy + i * kLevel1 + e) : 0.f, job,
+                        has_p);
+        },
+        scs, mass, cand);
+    if (threadIdx.x == 0) {
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        if (i < nb) {
+          masses[c0 + i] = mass[i];
+          cands[c0 + i] = cand[i];
+        }
       }
     }
   } else {
@@ -326,9 +349,9 @@ cudaError_t launch_sample_t(const Problem& p, const Workspace& w, cudaStream_t s
         cudaFuncSetAttribute(sample_kernel<T, kVecPath>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
-  // Programmatic dependent launch: the grid may be scheduled while the
-  // row-statistics kernel drains; the walk waits for it before reading its
-  // results.
+  // Programmatic dependent launch: the grid may be scheduled once every
+  // row-statistics CTA has started (they are all resident or done, so CTAs
+  // of this grid that poll for partials never hold back a CTA they wait for).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kST);

@@ -36,7 +36,7 @@ __device__ Partial chunk_partial_scalar(const T* row, int beg, int end, bool gre
   for (int t = beg + threadIdx.x; t < end; t += kThreads) m = fmax_nan(m, E::load1(row + t));
   const float cmax = block_max_nan(m, red_f);
   Partial out;
-  out.pad = 0;
+  out.tag = 0;
   if (greedy) {
     int idx = INT_MAX;
     if (m == cmax) {
@@ -171,7 +171,7 @@ __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int e
     }
   }
   Partial out;
-  out.pad = 0;
+  out.tag = 0;
   if (kGreedy) {
     const float best = block_max_nan(bad ? __int_as_float(0x7fc00000) : m, red_f);
     out.idx = block_min_int(m == best ? idx : INT_MAX, red_i);

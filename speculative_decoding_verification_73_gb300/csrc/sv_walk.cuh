@@ -5,7 +5,8 @@
 //
 // Thread j merges the row-statistics partials of target row j (and, for a
 // sampled request, draft row j), checks the inputs, and evaluates position
-// j+1 of the chain.  "Speculative Decoding and EAGLE-3" lesson:
+// j+1 of the chain.  The partials are polled by their tags (below), so a
+// request's walk starts as soon as its own rows are reduced.  "Speculative Decoding and EAGLE-3" lesson:
 //   * "Build it", step 1: a draft with p(d) = 0 is accepted; otherwise it is
 //     accepted iff u < min(1, q(d) / p(d));
 //   * "Invariant: Leviathan rejection sampling": the walk goes left to right
@@ -67,16 +68,16 @@ __device__ __forceinline__ void absorb_sampled(const float4 (&pt)[kN], float& c,
   }
 }
 
-// Merge the n partials of a sampled row; `pre` holds the first kPre.
-__device__ __forceinline__ RowNorm merge_sampled(const float4 (&pre)[kPre], const Partial* parts,
-                                                 int n) {
+// Merge the n partials of a sampled row; `pre` holds the first kPre and
+// load(i0, pt) fetches the kBatch partials from index i0 on (empty past n).
+template <class Load>
+__device__ __forceinline__ RowNorm merge_sampled_by(const float4 (&pre)[kPre], int n, Load load) {
   float c = -INFINITY, s = 0.f;
   bool bad = false;
   absorb_sampled(pre, c, s, bad);
   for (int i0 = kPre; i0 < n; i0 += kBatch) {
     float4 pt[kBatch];
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) pt[i] = partial_or_empty(parts + i0 + i, i0 + i < n);
+    load(i0, pt);
     absorb_sampled(pt, c, s, bad);
   }
   RowNorm r;
@@ -84,6 +85,15 @@ __device__ __forceinline__ RowNorm merge_sampled(const float4 (&pre)[kPre], cons
   r.s = s;
   r.ok = !bad && c > -INFINITY && c < INFINITY && s > 0.f && s < INFINITY;
   return r;
+}
+
+// The same with plain loads (partials written by a kernel that has ended).
+__device__ __forceinline__ RowNorm merge_sampled(const float4 (&pre)[kPre], const Partial* parts,
+                                                 int n) {
+  return merge_sampled_by(pre, n, [&](int i0, float4(&pt)[kBatch]) {
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) pt[i] = partial_or_empty(parts + i0 + i, i0 + i < n);
+  });
 }
 
 struct RowMax {
@@ -106,15 +116,15 @@ __device__ __forceinline__ void absorb_greedy(const float4 (&pt)[kN], float& bes
 
 // Greedy rows: partials come in increasing index order, so strict > keeps
 // the lowest index among equal maxima.
-__device__ __forceinline__ RowMax merge_greedy(const float4 (&pre)[kPre], const Partial* parts, int n) {
+template <class Load>
+__device__ __forceinline__ RowMax merge_greedy_by(const float4 (&pre)[kPre], int n, Load load) {
   float best = -INFINITY;
   int idx = INT_MAX;
   bool bad = false;
   absorb_greedy(pre, best, idx, bad);
   for (int i0 = kPre; i0 < n; i0 += kBatch) {
     float4 pt[kBatch];
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) pt[i] = partial_or_empty(parts + i0 + i, i0 + i < n);
+    load(i0, pt);
     absorb_greedy(pt, best, idx, bad);
   }
   RowMax r;
@@ -122,6 +132,73 @@ __device__ __forceinline__ RowMax merge_greedy(const float4 (&pre)[kPre], const 
   r.ok = !bad && best > -INFINITY && best < INFINITY;
   return r;
 }
+
+__device__ __forceinline__ RowMax merge_greedy(const float4 (&pre)[kPre], const Partial* parts, int n) {
+  return merge_greedy_by(pre, n, [&](int i0, float4(&pt)[kBatch]) {
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) pt[i] = partial_or_empty(parts + i0 + i, i0 + i < n);
+  });
+}
+
+// ------------------------------------------------------- tagged partials
+// The chain sampler does not wait for the row-statistics grid to end: each
+// partial it needs is read with a relaxed 128-bit load and used once its tag
+// is this call's sequence number.  A partial not yet written is polled again
+// after a short sleep; a thread gives up after kPollLimit polls (about a
+// second), which only a stalled row-statistics grid could cause, and its
+// request is then reported with kErrWait.
+constexpr int kPollLimit = 1 << 20;
+
+struct Poll {
+  unsigned epoch;
+  int budget;
+  bool late;  // a partial never showed this call's tag
+};
+
+__device__ __forceinline__ bool tagged(const float4& v, unsigned epoch) { return __float_as_uint(v.w) == epoch; }
+
+// Settle the partials a[i] (from pa + i) for i < na and b[i] (from pb + i)
+// for i < nb, whose first loads are already issued: every round sleeps
+// briefly and re-issues the loads of all those still untagged before it
+// looks at any of them, so a row's spans are waited for together, not one
+// after another.
+template <int kN>
+__device__ __forceinline__ void settle(float4 (&a)[kN], const Partial* pa, int na, float4 (&b)[kN],
+                                       const Partial* pb, int nb, Poll& pl) {
+  auto pending = [&]() {
+    bool any = false;
+#pragma unroll
+    for (int i = 0; i < kN; ++i) {
+      any |= i < na && !tagged(a[i], pl.epoch);
+      any |= i < nb && !tagged(b[i], pl.epoch);
+    }
+    return any;
+  };
+  while (pending() && pl.budget > 0) {
+    --pl.budget;
+    __nanosleep(100);
+#pragma unroll
+    for (int i = 0; i < kN; ++i) {
+      if (i < na && !tagged(a[i], pl.epoch)) a[i] = ld_partial_relaxed(pa + i);
+      if (i < nb && !tagged(b[i], pl.epoch)) b[i] = ld_partial_relaxed(pb + i);
+    }
+  }
+  if (pending()) pl.late = true;
+}
+
+// Batch loader for merge_*_by: every load issued, then the batch settled.
+struct TaggedLoad {
+  const Partial* parts;
+  int n;
+  Poll* pl;
+  __device__ __forceinline__ void operator()(int i0, float4 (&pt)[kBatch]) const {
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      pt[i] = i0 + i < n ? ld_partial_relaxed(parts + i0 + i)
+                         : make_float4(-INFINITY, 0.f, __int_as_float(INT_MAX), 0.f);
+    settle(pt, parts + i0, n - i0, pt, parts + i0, 0, *pl);
+  }
+};
 
 template <typename T>
 __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& w, int b,
@@ -131,62 +208,83 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
   const bool row_thread = j <= N;
   const bool pos_thread = j < N;
 
-  __shared__ int s_bad_token, s_bad_logit, s_first;
+  __shared__ int s_bad_token, s_bad_logit, s_first, s_late;
 
-  // Every load the walk needs is issued here, before any of them is used:
-  // the temperature and the draft token (inputs, fetched while the
-  // row-statistics kernel may still be finishing), then the logits at the
-  // token that the row-statistics pass stored (meaningful only for a sampled
-  // request with a valid token) and the first partials of the row pair.
+  // The inputs first (temperature, draft token), then every partial of the
+  // request's rows that this thread merges, all loads issued before any is
+  // used; a partial whose tag is not yet this call's is polled until it is.
   const float t = p.temperature[b];
   const int d = pos_thread ? p.tokens[static_cast<size_t>(b) * N + j] : -1;
-  wait_for_prerequisite();
-  float zd = 0.f, yd = 0.f;
-  if (pos_thread) {
-    const float* tl = w.tok_logit + static_cast<size_t>(b) * (2 * N + 1);
-    zd = __ldcg(tl + j);
-    yd = __ldcg(tl + N + 1 + j);
+  const int mode = temp_mode(t);
+  if (!write_outputs && mode != kModeSampled) {  // CTA-uniform: nothing to sample
+    if (j == 0) job_out->kind = kJobNone;
+    return;
   }
+  const bool take_t = row_thread && mode != kModeInvalid;
+  const bool take_d = pos_thread && mode == kModeSampled;
   const int S1 = w.S1;
   const Partial* req_parts = w.partials + static_cast<size_t>(b) * (2 * N + 1) * S1;
   const Partial* tparts = req_parts + static_cast<size_t>(j) * S1;
   const Partial* dparts = req_parts + static_cast<size_t>(N + 1 + j) * S1;
+  const float4 empty = make_float4(-INFINITY, 0.f, __int_as_float(INT_MAX), 0.f);
   float4 tpre[kPre], dpre[kPre];
 #pragma unroll
   for (int i = 0; i < kPre; ++i) {
-    tpre[i] = partial_or_empty(tparts + i, row_thread && i < S1);
-    dpre[i] = partial_or_empty(dparts + i, pos_thread && i < S1);
+    tpre[i] = (take_t && i < S1) ? ld_partial_relaxed(tparts + i) : empty;
+    dpre[i] = (take_d && i < S1) ? ld_partial_relaxed(dparts + i) : empty;
   }
   if (j == 0) {
     s_bad_token = 0;
     s_bad_logit = 0;
     s_first = N;
+    s_late = 0;
   }
-  const int mode = temp_mode(t);
-  if (!write_outputs && mode != kModeSampled) {  // CTA-uniform: nothing to sample
-    if (j == 0) job_out->kind = kJobNone;
-    return;
+  Poll pl{p.epoch, kPollLimit, false};
+  settle(tpre, tparts, take_t ? S1 : 0, dpre, dparts, take_d ? S1 : 0, pl);
+  // The logits at d_j in target row j and draft row j: the row-statistics
+  // CTA of the span holding d_j put them in that span's partial.
+  float zd = 0.f, yd = 0.f;
+  if (take_d && d >= 0 && d < V) {
+    constexpr int kSpanElems = kSpanBytes / static_cast<int>(sizeof(T));
+    const int sp = d / kSpanElems;
+    if (sp < kPre) {
+#pragma unroll
+      for (int i = 0; i < kPre; ++i) {
+        if (i == sp) {
+          zd = tpre[i].z;
+          yd = dpre[i].z;
+        }
+      }
+    } else {
+      float4 zt[1] = {ld_partial_relaxed(tparts + sp)}, yt[1] = {ld_partial_relaxed(dparts + sp)};
+      settle(zt, tparts + sp, 1, yt, dparts + sp, 1, pl);
+      zd = zt[0].z;
+      yd = yt[0].z;
+    }
   }
   __syncthreads();
   if (pos_thread && (d < 0 || d >= V)) atomicOr(&s_bad_token, 1);
   RowNorm q{}, pn{};
   RowMax g{};
   if (mode == kModeGreedy && row_thread) {
-    g = merge_greedy(tpre, tparts, S1);
+    g = merge_greedy_by(tpre, S1, TaggedLoad{tparts, S1, &pl});
     if (!g.ok) atomicOr(&s_bad_logit, 1);
   } else if (mode == kModeSampled && row_thread) {
-    q = merge_sampled(tpre, tparts, S1);
+    q = merge_sampled_by(tpre, S1, TaggedLoad{tparts, S1, &pl});
     if (!q.ok) atomicOr(&s_bad_logit, 1);
     if (pos_thread) {
-      pn = merge_sampled(dpre, dparts, S1);
+      pn = merge_sampled_by(dpre, S1, TaggedLoad{dparts, S1, &pl});
       if (!pn.ok) atomicOr(&s_bad_logit, 1);
     }
   }
+  if (pl.late) atomicOr(&s_late, 1);
   __syncthreads();
 
   unsigned err = 0;
   if (mode == kModeInvalid)
     err = kErrTemp;
+  else if (s_late)
+    err = kErrWait;
   else if (s_bad_token)
     err = kErrToken;
   else if (s_bad_logit)
