@@ -151,8 +151,20 @@ __device__ __forceinline__ float staged1(const __nv_bfloat16* p) {
   return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
 }
 
+// Staged layout of a level-1 block: thread t owns tokens [32t, 32t + 32),
+// and its i-th 16-byte vector sits at element (i * kST + t) * kVec, so the
+// vector accesses of a warp (copies in, reads out) cover 512 consecutive
+// bytes and meet no bank conflict.  staged_at maps a token offset in the
+// block to its element.
+template <typename T>
+__device__ __forceinline__ int staged_at(int e) {
+  constexpr int kVec = Elem<T>::kVec;
+  const int th = e / kSegTok, r = e - th * kSegTok;
+  return ((r / kVec) * kST + th) * kVec + (r % kVec);
+}
+
 // Stage this thread's tokens [32t, 32t + 32) of the level-1 block starting at
-// cbeg into sz / sy (block-relative); vectors at or past cend get -inf.
+// cbeg into sz / sy; vectors at or past cend get -inf.
 template <typename T>
 __device__ __forceinline__ void stage_block(const T* z, const T* y, int cbeg, int cend, bool has_p,
                                             T* sz, T* sy) {
@@ -162,12 +174,13 @@ __device__ __forceinline__ void stage_block(const T* z, const T* y, int cbeg, in
 #pragma unroll
   for (int i = 0; i < kSegTok / kVec; ++i) {
     const int e = threadIdx.x * kSegTok + i * kVec;
+    const int at = (i * kST + threadIdx.x) * kVec;
     if (cbeg + e < cend) {
-      cp_async16(sz + e, z + cbeg + e);
-      if (has_p) cp_async16(sy + e, y + cbeg + e);
+      cp_async16(sz + at, z + cbeg + e);
+      if (has_p) cp_async16(sy + at, y + cbeg + e);
     } else {
-      *reinterpret_cast<uint4*>(sz + e) = pad;
-      if (has_p) *reinterpret_cast<uint4*>(sy + e) = pad;
+      *reinterpret_cast<uint4*>(sz + at) = pad;
+      if (has_p) *reinterpret_cast<uint4*>(sy + at) = pad;
     }
   }
 }
@@ -183,7 +196,7 @@ __device__ __forceinline__ void staged_halves(const T* sz, const T* sy, const Jo
   h1 = 0.f;
 #pragma unroll
   for (int i = 0; i < kVecs; ++i) {
-    const int e = threadIdx.x * kSegTok + i * kVec;
+    const int e = (i * kST + threadIdx.x) * kVec;
     const uint4 zv = *reinterpret_cast<const uint4*>(sz + e);
     const uint4 yv = has_p ? *reinterpret_cast<const uint4*>(sy + e) : zv;
     float rv[kVec];
@@ -264,9 +277,8 @@ __global__ void __launch_bounds__(kST, 3) sample_kernel(Problem p, Workspace w) 
     blocks_pick<kB>(
         h0, h1, c0 * kLevel1, V, nb, job,
         [&](int i, int t) {
-          const int e = t - (c0 + i) * kLevel1;
-          return resid1(staged1(sz + i * kLevel1 + e), has_p ? staged1(sy + i * kLevel1 + e) : 0.f, job,
-                        has_p);
+          const int e = i * kLevel1 + staged_at<T>(t - (c0 + i) * kLevel1);
+          return resid1(staged1(sz + e), has_p ? staged1(sy + e) : 0.f, job, has_p);
         },
         scs, mass, cand);
     if (threadIdx.x == 0) {

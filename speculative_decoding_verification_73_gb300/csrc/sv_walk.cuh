@@ -213,15 +213,11 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
   // The inputs first (temperature, draft token), then every partial of the
   // request's rows that this thread merges, all loads issued before any is
   // used; a partial whose tag is not yet this call's is polled until it is.
+  // (the partial loads go out before the temperature is back, so the
+  // request's mode costs no extra round trip; loads a mode does not need
+  // are never settled or used)
   const float t = p.temperature[b];
   const int d = pos_thread ? p.tokens[static_cast<size_t>(b) * N + j] : -1;
-  const int mode = temp_mode(t);
-  if (!write_outputs && mode != kModeSampled) {  // CTA-uniform: nothing to sample
-    if (j == 0) job_out->kind = kJobNone;
-    return;
-  }
-  const bool take_t = row_thread && mode != kModeInvalid;
-  const bool take_d = pos_thread && mode == kModeSampled;
   const int S1 = w.S1;
   const Partial* req_parts = w.partials + static_cast<size_t>(b) * (2 * N + 1) * S1;
   const Partial* tparts = req_parts + static_cast<size_t>(j) * S1;
@@ -230,9 +226,16 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
   float4 tpre[kPre], dpre[kPre];
 #pragma unroll
   for (int i = 0; i < kPre; ++i) {
-    tpre[i] = (take_t && i < S1) ? ld_partial_relaxed(tparts + i) : empty;
-    dpre[i] = (take_d && i < S1) ? ld_partial_relaxed(dparts + i) : empty;
+    tpre[i] = (row_thread && i < S1) ? ld_partial_relaxed(tparts + i) : empty;
+    dpre[i] = (pos_thread && i < S1) ? ld_partial_relaxed(dparts + i) : empty;
   }
+  const int mode = temp_mode(t);
+  if (!write_outputs && mode != kModeSampled) {  // CTA-uniform: nothing to sample
+    if (j == 0) job_out->kind = kJobNone;
+    return;
+  }
+  const bool take_t = row_thread && mode != kModeInvalid;
+  const bool take_d = pos_thread && mode == kModeSampled;
   if (j == 0) {
     s_bad_token = 0;
     s_bad_logit = 0;
