@@ -389,6 +389,15 @@ int spec_verify_launches_per_call(void);
 int spec_verify_debug_philox(uint64_t seed, const uint32_t* ctr3, uint32_t* out4, int n,
                              void* cuda_stream);
 
+/*
+ * spec_verify_debug_seek_calls -- test hook.  Sets the context's count of
+ * spec_verify calls (the tag the next call's partial statistics carry is
+ * calls + 1, wrapping past 2^32 - 1 to 1 after clearing every tag), so a
+ * test can cross the wrap without 2^32 calls.  Host-side only: enqueues
+ * nothing.  Returns SV_OK or SV_EINVAL.
+ */
+int spec_verify_debug_seek_calls(spec_verify_ctx* ctx, uint32_t calls);
+
 /* Release the context and its workspace (waits for its stream first).
  * NULL is accepted.  Returns SV_OK or SV_ECUDA. */
 int spec_verify_destroy(spec_verify_ctx* ctx);

@@ -34,7 +34,7 @@ EXPORTS = (
     "spec_verify_profile", "spec_verify_profile_read", "spec_verify_launches_per_call",
     "spec_verify_debug_philox", "spec_verify_destroy", "spec_verify_strerror",
     "spec_verify_noalloc", "spec_verify_tree", "spec_verify_kv_commit", "spec_verify_lazy",
-    "spec_verify_fc_norm",
+    "spec_verify_fc_norm", "spec_verify_debug_seek_calls",
 )
 
 _lib = None
@@ -67,6 +67,7 @@ def load():
                                              ctypes.POINTER(c_int)]
     lib.spec_verify_launches_per_call.argtypes = []
     lib.spec_verify_debug_philox.argtypes = [c_u64, c_void, c_void, c_int, c_void]
+    lib.spec_verify_debug_seek_calls.argtypes = [c_void, ctypes.c_uint32]
     lib.spec_verify_destroy.argtypes = [c_void]
     lib.spec_verify_lazy.argtypes = list(lib.spec_verify.argtypes)
     lib.spec_verify_fc_norm.argtypes = [c_void, c_int, c_int, c_int, c_int, ctypes.c_float, c_void,
@@ -371,6 +372,11 @@ class SpecVerify:
 
     def get_error(self):
         return spec_verify_get_error(self.ctx)
+
+    def debug_seek_calls(self, calls):
+        """Test hook: set the context's call count (see spec_verify_debug_seek_calls)."""
+        _check(load().spec_verify_debug_seek_calls(self.ctx, int(calls) & 0xFFFFFFFF),
+               "spec_verify_debug_seek_calls")
 
     def debug_stats(self, B, N):
         return spec_verify_debug_stats(self.ctx, B, N, self.device)

@@ -455,6 +455,12 @@ int spec_verify_destroy(spec_verify_ctx* ctx) {
 /* Test hook: Philox4x32-10 words for n counters (c0, c1, c2, 0) under a
  * 64-bit seed, computed by the same device function the walk uses.
  * ctr3: device [n, 3] uint32; out4: device [n, 4] uint32. */
+int spec_verify_debug_seek_calls(spec_verify_ctx* ctx, uint32_t calls) {
+  if (ctx == nullptr) return SV_EINVAL;
+  ctx->epoch = calls;
+  return SV_OK;
+}
+
 int spec_verify_debug_philox(uint64_t seed, const uint32_t* ctr3, uint32_t* out4, int n,
                              void* cuda_stream) {
   if (n < 0 || (n > 0 && (ctr3 == nullptr || out4 == nullptr))) return SV_EINVAL;

@@ -18,8 +18,11 @@ constexpr unsigned kFull = 0xffffffffu;
 // before it in the stream is still running; allow_dependents() lets such a
 // dependent grid be scheduled as soon as every CTA of this grid has made
 // the call or exited.  The dependent then synchronises with this grid by
-// itself (the chain sampler polls the tags of the partials it reads).
+// itself: the chain sampler polls the tags of the partials it reads, and
+// the KV length update calls wait_for_prerequisite(), which returns once
+// the grid before it has completed and its writes are visible.
 __device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void wait_for_prerequisite() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // A Partial moved as one 128-bit scalar at gpu scope (PTX .b128 with
 // .relaxed.gpu): a reader in another grid that is running at the same time

@@ -17,8 +17,15 @@
 // kv_commit_kernel: one thread per 16-byte column of one (layer, sequence)
 // entry, copying the kept positions eight at a time (eight loads in flight
 // per thread) -- a plain bandwidth-bound copy with coalesced 16-byte
-// accesses (consecutive threads, consecutive columns).  kv_advance_kernel then moves the lengths (a second launch, so
-// no CTA of the copy can read a length another has already advanced).
+// accesses (consecutive threads, consecutive columns).  kv_advance_kernel
+// then moves the lengths: a second grid, launched with programmatic
+// dependent launch so that it is resident while the copy drains, whose
+// griddepcontrol.wait returns only once the copy grid has completed and its
+// writes are visible -- so no CTA of the copy can read a length already
+// advanced.  The copy is itself a programmatic dependent of the grid before
+// it and waits for that grid the same way.  (A CTA per sequence and group
+// of four layers, reading the lengths once for the group, measured slower:
+// 18.1 against 14.9 us per commit.)
 
 #include <cstdint>
 
@@ -53,6 +60,11 @@ __device__ __forceinline__ bool commit_ok(const KvProblem& p, int b, int n, int 
 
 template <bool kScratch>
 __global__ void __launch_bounds__(kKvThreads) kv_commit_kernel(KvProblem p) {
+  // Launched as a programmatic dependent of whatever precedes it: wait for
+  // that grid (it may be the verify step writing kv_len, or the previous
+  // commit's length update) before reading anything.
+  wait_for_prerequisite();
+  allow_dependents();  // the length update may be scheduled behind the last wave
   const long long cols = static_cast<long long>(p.E / 16);
   const long long slices = (cols + kKvThreads - 1) / kKvThreads;
   const long long lb = blockIdx.x / slices;
@@ -99,6 +111,8 @@ __global__ void __launch_bounds__(kKvThreads) kv_commit_kernel(KvProblem p) {
 }
 
 __global__ void kv_advance_kernel(KvProblem p) {
+  allow_dependents();       // a following commit may be scheduled early (it waits too)
+  wait_for_prerequisite();  // the copy grid has completed
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= p.B) return;
   const int n = p.kv_len[b];
@@ -114,16 +128,24 @@ cudaError_t launch_kv_commit(const KvProblem& p, cudaStream_t s) {
   const long long cols = static_cast<long long>(p.E / 16);
   const long long blocks = static_cast<long long>(p.L) * p.B * ((cols + kKvThreads - 1) / kKvThreads);
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  // Both launches are programmatic dependents of the grid before them; each
+  // kernel waits for that grid before it reads what the grid writes.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kKvThreads);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (blocks > 0) {
-    if (p.mode == kKvScratch)
-      kv_commit_kernel<true><<<dim3(static_cast<unsigned>(blocks)), kKvThreads, 0, s>>>(p);
-    else
-      kv_commit_kernel<false><<<dim3(static_cast<unsigned>(blocks)), kKvThreads, 0, s>>>(p);
-    const cudaError_t e = cudaGetLastError();
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    const cudaError_t e = p.mode == kKvScratch ? cudaLaunchKernelEx(&cfg, kv_commit_kernel<true>, p)
+                                               : cudaLaunchKernelEx(&cfg, kv_commit_kernel<false>, p);
     if (e != cudaSuccess) return e;
   }
-  kv_advance_kernel<<<(p.B + 255) / 256, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  cfg.gridDim = dim3(static_cast<unsigned>((p.B + kKvThreads - 1) / kKvThreads));
+  return cudaLaunchKernelEx(&cfg, kv_advance_kernel, p);
 }
 
 }  // namespace sv

@@ -1,0 +1,98 @@
+"""The chain's tagged row statistics across calls on one context.
+
+The sampler takes a partial once it carries the call's sequence number, so
+whatever earlier calls left in the workspace must never pass for this
+call's: calls of other shapes, tree and lazy calls (which write their own
+partials) and the counter's wrap past 2^32 - 1 all have to give exactly the
+results of a fresh context on the same inputs.
+"""
+
+import pytest
+import torch
+
+from speculative_decoding_verification_73_gb300 import binding, build, workloads
+
+pytestmark = pytest.mark.gpu
+
+MAX_B, MAX_N, MAX_V = 24, 14, 32000
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    return binding.load()
+
+
+def _inputs(wl):
+    B, N, V = wl.shape
+    return (wl.target.cuda(), wl.draft.cuda() if N > 0 else None, wl.tokens.cuda(),
+            wl.temperature.cuda())
+
+
+def _host(outs):
+    return [x.cpu().clone() for x in outs]
+
+
+def _fresh(wl, seed):
+    B, N, V = wl.shape
+    ctx = binding.SpecVerify(B, max(N, 1), V, torch.bfloat16)
+    out = _host(ctx(*_inputs(wl), seed))
+    err = ctx.get_error()
+    ctx.close()
+    return out, err
+
+
+CHAINS = {
+    "a": lambda: workloads.make_random(16, 6, 5000, "bf16", gen_seed=301, verify_seed=1),
+    "b": lambda: workloads.make_random(24, 14, 32000, "bf16", gen_seed=302, verify_seed=2),
+    "c": lambda: workloads.make_random(9, 3, 3001, "bf16", gen_seed=303, verify_seed=3),
+    "d": lambda: workloads.make_random(20, 7, 24576, "bf16", gen_seed=304, verify_seed=4),
+}
+
+
+def test_chain_calls_between_other_shapes_tree_and_lazy_calls():
+    chains = {k: f() for k, f in CHAINS.items()}
+    tree = workloads.make_tree(12, 5000, "bf16", gen_seed=305, widths=(2, 2, 2), verify_seed=5)
+    want = {(k, s): _fresh(wl, s) for k, wl in chains.items() for s in (11, 12)}
+    ctx = binding.SpecVerify(MAX_B, MAX_N, MAX_V, torch.bfloat16)
+    order = ["a", "tree", "b", "lazy-c", "c", "a", "d", "tree", "b", "lazy-d", "d", "c"]
+    for i, step in enumerate(order):
+        seed = 11 + (i % 2)
+        if step == "tree":
+            draft = tree.draft.cuda()
+            ctx.tree(tree.target.cuda(), draft, tree.parents.cuda(), tree.tokens.cuda(),
+                     tree.temperature.cuda(), seed, tree.mode)
+            torch.cuda.synchronize()
+            continue
+        if step.startswith("lazy-"):
+            ctx.lazy(*_inputs(chains[step[5:]]), seed)
+            torch.cuda.synchronize()
+            continue
+        got = _host(ctx(*_inputs(chains[step]), seed))
+        err = ctx.get_error()
+        ref, ref_err = want[(step, seed)]
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b), (i, step)
+        assert err == ref_err == (0, 0), (i, step)
+    ctx.close()
+
+
+def test_call_counter_wrap():
+    first = workloads.make_random(16, 6, 5000, "bf16", gen_seed=311, verify_seed=1)
+    other = workloads.make_random(24, 14, 32000, "bf16", gen_seed=312, verify_seed=2)
+    again = workloads.make_random(16, 6, 5000, "bf16", gen_seed=313, verify_seed=3)
+    ctx = binding.SpecVerify(MAX_B, MAX_N, MAX_V, torch.bfloat16)
+    # tags of call 1 left in the slots of `first`'s shape ...
+    ctx(*_inputs(first), 7)
+    torch.cuda.synchronize()
+    # ... then calls 2^32 - 1, (wrap: every tag cleared) 1, 2, 3
+    ctx.debug_seek_calls(0xFFFFFFFE)
+    for i, wl in enumerate((other, again, first, again)):
+        got = _host(ctx(*_inputs(wl), 20 + i))
+        ref, ref_err = _fresh(wl, 20 + i)
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b), i
+        assert ctx.get_error() == ref_err == (0, 0)
+    ctx.close()
