@@ -29,6 +29,7 @@ struct spec_verify_ctx {
   // partials (1, 2, ...; the partials are cleared again when it wraps)
   unsigned epoch;
   size_t part_bytes;  // bytes of the partials region
+  size_t late_bytes;  // bytes of the tree walk's timeout tags
 };
 
 namespace {
@@ -70,6 +71,20 @@ cudaEvent_t* profile_slot(spec_verify_ctx* ctx) {
     ctx->events.push_back(e);
   }
   return ctx->events.data() + static_cast<size_t>(ctx->recorded) * per;
+}
+
+// The next call's sequence number: the tag its row statistics carry.  When
+// the count wraps, every tag in the workspace is cleared first, so no tag
+// left by an earlier call can equal a later call's.
+int next_epoch(spec_verify_ctx* ctx, unsigned* epoch) {
+  if (++ctx->epoch == 0) {
+    if (cudaMemsetAsync(ctx->w.partials, 0, ctx->part_bytes, ctx->stream) != cudaSuccess ||
+        cudaMemsetAsync(ctx->w.late, 0, ctx->late_bytes, ctx->stream) != cudaSuccess)
+      return SV_ECUDA;
+    ctx->epoch = 1;
+  }
+  *epoch = ctx->epoch;
+  return SV_OK;
 }
 
 }  // namespace
@@ -134,7 +149,10 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   off = align_up(off + sizeof(unsigned), 256);
   const size_t o_arr = off;
   off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
-  const size_t zero_bytes = off - o_err;  // the error word and arrival counters start at zero
+  const size_t o_late = off;
+  off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
+  // the error word, arrival counters and tree-walk timeout tags start at zero
+  const size_t zero_bytes = off - o_err;
   const size_t o_acc = off;
   off = align_up(off + static_cast<size_t>(max_B) * (max_N > 0 ? max_N : 1) * sizeof(float), 256);
   const size_t o_lz = off;
@@ -150,6 +168,8 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   ctx->w.blk_tok = reinterpret_cast<int*>(base + o_btok);
   ctx->w.err = reinterpret_cast<unsigned*>(base + o_err);
   ctx->w.arrivals = reinterpret_cast<unsigned*>(base + o_arr);
+  ctx->w.late = reinterpret_cast<unsigned*>(base + o_late);
+  ctx->late_bytes = static_cast<size_t>(max_B) * sizeof(unsigned);
   ctx->w.dbg_accept = reinterpret_cast<float*>(base + o_acc);
   ctx->w.dbg_logz = reinterpret_cast<float*>(base + o_lz);
   // tags start at 0, which no chain call uses
@@ -199,12 +219,7 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
   w.S3 = ceil_div(V, sv::sample_chunk_elems(ctx->dtype));
   // A fresh tag per call: the sampler of this call takes a partial only once
   // it carries this tag, never one left by an earlier call.
-  if (++ctx->epoch == 0) {
-    if (cudaMemsetAsync(ctx->w.partials, 0, ctx->part_bytes, ctx->stream) != cudaSuccess)
-      return SV_ECUDA;
-    ctx->epoch = 1;
-  }
-  p.epoch = ctx->epoch;
+  if (next_epoch(ctx, &p.epoch) != SV_OK) return SV_ECUDA;
 
   cudaEvent_t* ev = nullptr;
   if (ctx->profile_every > 0 && (ctx->profile_seen++ % ctx->profile_every) == 0) {
@@ -262,6 +277,8 @@ int spec_verify_tree(spec_verify_ctx* ctx, int B, int M, int V, int mode,
   sv::Workspace w = ctx->w;
   w.S1 = ceil_div(V, sv::row_chunk_elems(ctx->dtype));
   w.S3 = ceil_div(V, sv::sample_chunk_elems(ctx->dtype));
+  // the walk polls the tags of this call's partials
+  if (next_epoch(ctx, &p.epoch) != SV_OK) return SV_ECUDA;
 
   cudaEvent_t* ev = nullptr;
   if (ctx->profile_every > 0 && (ctx->profile_seen++ % ctx->profile_every) == 0) {

@@ -61,11 +61,12 @@ constexpr int kTreeTopk = 1;     // fixed candidates (point masses)
 //                the chunk holds it (chain kernel), else 0
 //   greedy row : a = chunk maximum M, s = 0 (NaN if a NaN was seen),
 //                idx = lowest index holding M
-//   tag        : the chain call's sequence number (never 0); every other
-//                kernel writes 0.  The chain row-statistics kernel stores the
-//                whole partial with one 128-bit access and the chain sampler
-//                polls for its tag, so it can start on a request whose rows
-//                are done while the rest of the grid still runs.
+//   tag        : the call's sequence number (never 0) in the chain's and the
+//                tree's row statistics; the lazy kernel writes 0.  The whole
+//                partial is stored with one 128-bit access and the chain
+//                sampler / tree walk polls for its tag, so it can start on a
+//                request whose rows are done while the rest of the grid
+//                still runs.
 struct Partial {
   float a;
   float s;
@@ -113,6 +114,7 @@ struct TreeProblem {
   int32_t* out_path;         // [B, M]
   int32_t* out_accept;       // [B]
   int32_t* out_kv;           // [B]
+  unsigned epoch;            // tag of this call's row-statistics partials (never 0)
 };
 
 struct KvProblem {
@@ -149,6 +151,7 @@ struct Workspace {
   int* blk_tok;          // [B, S3]: the token each level-1 block would give
   unsigned* err;         // [1], OR of kErr* bits (starts at zero)
   unsigned* arrivals;    // [B]: sampler CTAs done per request (zero between calls)
+  unsigned* late;        // [B]: tree walk: the call's tag once a wait of the request ran out
   float* dbg_accept;     // [B, N]
   float* dbg_logz;       // [B, 2N+1]
   int S1;                // spans per row for this call's V

@@ -123,6 +123,7 @@ int spec_verify_noalloc(int B, int N, int V, int dtype, const void* target_logit
   w.blk_tok = reinterpret_cast<int*>(base + c.btok);
   w.err = reinterpret_cast<unsigned*>(base + c.err);
   w.arrivals = reinterpret_cast<unsigned*>(base + c.arr);
+  w.late = nullptr;  // tree walks only
   w.dbg_accept = reinterpret_cast<float*>(base + c.acc);
   w.dbg_logz = reinterpret_cast<float*>(base + c.logz);
 

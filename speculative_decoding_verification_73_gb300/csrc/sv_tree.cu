@@ -67,6 +67,7 @@ constexpr int kNoNode = INT_MAX;
 template <typename T, bool kVecPath>
 __global__ void __launch_bounds__(kThreads, kSpanMinBlocks) tree_rowstats_kernel(TreeProblem p,
                                                                                    Workspace w) {
+  allow_dependents();  // the walk may be scheduled behind the last wave
   const int S1 = w.S1;
   const int per = 2 * (p.M + 1);
   const int row = blockIdx.x / S1;
@@ -101,7 +102,10 @@ __global__ void __launch_bounds__(kThreads, kSpanMinBlocks) tree_rowstats_kernel
     out = greedy ? span_partial_vec<T, true, false>(base, beg, end, k, -1, nullptr)
                  : span_partial_vec<T, false, false>(base, beg, end, k, -1, nullptr);
   }
-  if (threadIdx.x == 0) w.partials[static_cast<size_t>(row) * S1 + span] = out;
+  if (threadIdx.x == 0) {
+    out.tag = p.epoch;
+    st_partial_relaxed(w.partials + static_cast<size_t>(row) * S1 + span, out);
+  }
 }
 
 // ------------------------------------------------------------ the walk
@@ -160,13 +164,22 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   const Partial* req_parts = w.partials + static_cast<size_t>(b) * 2 * (M + 1) * S1;
   const Partial* tparts = req_parts + static_cast<size_t>(i) * S1;
   const Partial* dparts = req_parts + static_cast<size_t>(M + 1 + i) * S1;
+  // Every partial this thread may merge is requested now; which of them the
+  // walk needs is known once the topology is (a draft row only for a node
+  // with children), and those are then polled until they carry this call's
+  // tag (the grid of the row statistics may still be running).
+  const float4 empty = make_float4(-INFINITY, 0.f, __int_as_float(INT_MAX), 0.f);
   float4 tpre[kPre], dpre[kPre];
 #pragma unroll
   for (int j = 0; j < kPre; ++j) {
-    tpre[j] = partial_or_empty(tparts + j, is_node && mode != kModeInvalid && j < S1);
-    dpre[j] = partial_or_empty(dparts + j, is_node && use_draft && j < S1);
+    tpre[j] = (is_node && mode != kModeInvalid && j < S1) ? ld_partial_relaxed(tparts + j) : empty;
+    dpre[j] = (is_node && use_draft && j < S1) ? ld_partial_relaxed(dparts + j) : empty;
   }
-  if (i == 0) s_err = mode == kModeInvalid ? kErrTemp : 0u;
+  __shared__ int s_late;
+  if (i == 0) {
+    s_err = mode == kModeInvalid ? kErrTemp : 0u;
+    s_late = 0;
+  }
   s_first[i] = kNoNode;
   s_next[i] = kNoNode;
   s_par[i] = par;
@@ -194,17 +207,21 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
     zc = E::load1(static_cast<const T*>(p.target) + off);
     if (use_draft) yc = E::load1(static_cast<const T*>(p.draft) + off);
   }
+  Poll pl{p.epoch, kPollLimit, false};
+  const bool take_t = is_node && mode != kModeInvalid;
+  const bool take_d = is_node && use_draft && s_first[i] != kNoNode;
+  settle(tpre, tparts, take_t ? S1 : 0, dpre, dparts, take_d ? S1 : 0, pl);
   if (is_node && mode == kModeGreedy) {
-    const RowMax g = merge_greedy(tpre, tparts, S1);
+    const RowMax g = merge_greedy_by(tpre, S1, TaggedLoad{tparts, S1, &pl});
     s_gidx[i] = g.idx;
     if (!g.ok) atomicOr(&s_err, kErrLogit);
   } else if (is_node && sampled) {
-    const RowNorm q = merge_sampled(tpre, tparts, S1);
+    const RowNorm q = merge_sampled_by(tpre, S1, TaggedLoad{tparts, S1, &pl});
     s_cq[i] = q.c;
     s_sq[i] = q.s;
     if (!q.ok) atomicOr(&s_err, kErrLogit);
-    if (use_draft && s_first[i] != kNoNode) {
-      const RowNorm pn = merge_sampled(dpre, dparts, S1);
+    if (take_d) {
+      const RowNorm pn = merge_sampled_by(dpre, S1, TaggedLoad{dparts, S1, &pl});
       s_cp[i] = pn.c;
       s_sp[i] = pn.s;
       if (!pn.ok) atomicOr(&s_err, kErrLogit);
@@ -215,18 +232,30 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   }
   s_zc[i] = zc;
   s_yc[i] = yc;
+  if (pl.late) atomicOr(&s_late, 1);
   __syncthreads();
+  // A wait that ran out in one CTA fails the request in all of them: that
+  // CTA publishes it under the call's tag, and after a cluster barrier every
+  // CTA reads it back, so the cluster takes the same branch below (a CTA
+  // leaving alone would strand its peers' exchanges through its shared
+  // memory).
+  if (i == 0 && s_late)
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(w.late + b), "r"(p.epoch) : "memory");
+  cluster_sync();
+  unsigned late_tag;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(late_tag) : "l"(w.late + b) : "memory");
 
   int32_t* out_tok = p.out_tokens + static_cast<size_t>(b) * (M + 1);
   int32_t* out_path = p.out_path + static_cast<size_t>(b) * M;
-  const unsigned bits = s_err;
+  const unsigned bits = s_err | (late_tag == p.epoch ? kErrWait : 0u);
   if (bits) {
     // report the first failing check in the order temperature, topology,
-    // tokens, logits
+    // tokens, logits, wait
     const unsigned err = (bits & kErrTemp)    ? kErrTemp
                          : (bits & kErrTree)  ? kErrTree
                          : (bits & kErrToken) ? kErrToken
-                                              : kErrLogit;
+                         : (bits & kErrLogit) ? kErrLogit
+                                              : kErrWait;
     if (rank == 0) {
       if (is_node) out_tok[i] = -1;
       if (i < M) out_path[i] = -1;
@@ -496,7 +525,20 @@ cudaError_t launch_tree_t(const TreeProblem& p, const Workspace& w, cudaStream_t
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
     }
-    tree_walk_kernel<T, kVecPath><<<dim3(static_cast<unsigned>(blocks)), kST, smem, s>>>(p, w);
+    // Programmatic dependent launch: the clusters may be scheduled once
+    // every row-statistics CTA has started (all of them resident or done, so
+    // a walk polling for partials never holds back a CTA it waits for).
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kST);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tree_walk_kernel<T, kVecPath>, p, w);
   }
   return cudaGetLastError();
 }
