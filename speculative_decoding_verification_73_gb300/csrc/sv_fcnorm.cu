@@ -33,13 +33,16 @@ namespace {
 constexpr int kBM = 128, kBN = 256, kBK = 64;
 constexpr int kKG = kBK / 8;                       // core matrices along K per tile
 constexpr int kStages = 4;
-constexpr int kAhead = 2;                          // steps of loads in flight ahead of the MMAs
+#ifndef SV_FC_AHEAD
+#define SV_FC_AHEAD 2  // 3 measured slower: 246 against 281 TFLOP/s
+#endif
+constexpr int kAhead = SV_FC_AHEAD;                // steps of loads in flight ahead of the MMAs
 constexpr int kFcThreads = 256;
 constexpr int kABytes = kBM * kBK * 2;             // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;             // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;     // 48 KB
 constexpr int kTmemCols = kBN;                     // fp32 accumulator 128 lanes x 256 columns
-static_assert(kAhead + 2 <= kStages, "a stage is refilled only after the MMAs two steps back");
+static_assert(kAhead + 1 <= kStages, "a stage is refilled only after the MMAs that read it");
 constexpr uint32_t kWaitLimit = 1u << 26;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -219,7 +222,8 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_gemm_kernel(FcNormProblem p)
   int committed = -1;  // last k step whose MMAs were committed
   for (int kt = 0; kt < nk; ++kt) {
     // refill the stage of step kt + kAhead, last read by the MMAs of step
-    // kt + kAhead - kStages (<= kt - 2): wait for them first
+    // kt + kAhead - kStages (<= kt - 1, committed in an earlier iteration):
+    // wait for them first
     const int nxt = kt + kAhead;
     const int prev = nxt - kStages;
     if (prev >= 0 && nxt < nk) {
