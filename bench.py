@@ -14,7 +14,7 @@ copy bandwidth of the GPU.  Under torchrun each rank verifies its own batch
 bracketed by barriers and the slowest rank's time is used.
 
 --impl reference times the CPU oracle (float64, one host thread) on the same
-metric, a bounded sample of requests per step.
+metric, one draft position of oracle work per step.
 
 --path lazy measures spec_verify_lazy on the same batch64-bf16 workload
 (rows read only up to each request's first rejection); its roofline counts
@@ -277,7 +277,11 @@ def run_ours(args):
     achieved = bytes_per_launch / (rowstats_ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
 
-    # ---- end to end through the C ABI with host buffers (pinned), rank-local
+    # ---- end to end through the C ABI with host buffers (pinned), rank-local.
+    # Double-buffered: step i's inputs are copied on a copy stream into
+    # buffer i % 2 while the verify stream still runs step i - 1; the verify
+    # of step i waits for its copy, and a copy into a buffer waits for the
+    # verify that last read it.  Every copy and read-back is timed.
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 200))
     h_target = wl.target.pin_memory()
     h_draft = wl.draft.pin_memory()
@@ -286,17 +290,27 @@ def run_ours(args):
     h_out_t = torch.empty(B, N + 1, dtype=torch.int32).pin_memory()
     h_out_a = torch.empty(B, dtype=torch.int32).pin_memory()
     h_out_k = torch.empty(B, dtype=torch.int32).pin_memory()
-    d_target, d_draft = target[0], draft[0]
+    bufs = [(target[c % copies], draft[c % copies], torch.empty_like(tokens), torch.empty_like(temperature))
+            for c in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in (h_target, h_draft, h_tokens, h_temp))
     d2h = sum(t.numel() * t.element_size() for t in (h_out_t, h_out_a, h_out_k))
+    copy_stream = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
 
     def e2e_step(i):
-        d_target.copy_(h_target, non_blocking=True)
-        d_draft.copy_(h_draft, non_blocking=True)
-        tokens.copy_(h_tokens, non_blocking=True)
-        temperature.copy_(h_temp, non_blocking=True)
+        zb, yb, tb, pb = bufs[i % 2]
+        copy_stream.wait_event(consumed[i % 2])  # the verify two steps back is done with it
+        with torch.cuda.stream(copy_stream):
+            zb.copy_(h_target, non_blocking=True)
+            yb.copy_(h_draft, non_blocking=True)
+            tb.copy_(h_tokens, non_blocking=True)
+            pb.copy_(h_temp, non_blocking=True)
+        copied[i % 2].record(copy_stream)
+        stream.wait_event(copied[i % 2])
         (binding.spec_verify_lazy if lazy else binding.spec_verify)(
-            sv.ctx, d_target, d_draft, tokens, temperature, i, out_t, out_a, out_k)
+            sv.ctx, zb, yb, tb, pb, i, out_t, out_a, out_k)
+        consumed[i % 2].record(stream)
         h_out_t.copy_(out_t, non_blocking=True)
         h_out_a.copy_(out_a, non_blocking=True)
         h_out_k.copy_(out_k, non_blocking=True)
@@ -307,6 +321,7 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize(dev)
     ev0.record(stream)
+    copy_stream.wait_event(ev0)  # no copy of the timed steps starts before the clock
     for i in range(e2e_steps):
         e2e_step(i)
     ev1.record(stream)
@@ -464,18 +479,31 @@ def run_tree(args):
     achieved = bytes_per_launch / (rs_ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
 
-    # end to end with pinned host buffers, through the Python binding
+    # end to end with pinned host buffers, through the Python binding;
+    # double-buffered like the chain's (copies of step i on a copy stream
+    # while the tree verify of step i - 1 runs)
     e2e_steps = args.e2e_steps or max(3, min(args.steps, 200))
     hs = [t.pin_memory() for t in (wl.target, wl.draft, wl.parents, wl.tokens, wl.temperature)]
-    ds = [target[0], draft[0], parents, tokens, temperature]
+    dbufs = [[target[c % copies], draft[c % copies], torch.empty_like(parents), torch.empty_like(tokens),
+              torch.empty_like(temperature)] for c in range(2)]
     hout = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (out_t, out_p, out_a, out_k)]
     h2d = sum(t.numel() * t.element_size() for t in hs)
     d2h = sum(t.numel() * t.element_size() for t in hout)
+    copy_stream = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
 
     def e2e_step(i):
-        for h, d in zip(hs, ds):
-            d.copy_(h, non_blocking=True)
-        step(i, 0)
+        ds = dbufs[i % 2]
+        copy_stream.wait_event(consumed[i % 2])  # the verify two steps back is done with it
+        with torch.cuda.stream(copy_stream):
+            for h, d in zip(hs, ds):
+                d.copy_(h, non_blocking=True)
+        copied[i % 2].record(copy_stream)
+        stream.wait_event(copied[i % 2])
+        binding.spec_verify_tree(sv.ctx, wl.mode, ds[0], ds[1], ds[2], ds[3], ds[4], i,
+                                 out_t, out_p, out_a, out_k)
+        consumed[i % 2].record(stream)
         for h, d in zip(hout, (out_t, out_p, out_a, out_k)):
             h.copy_(d, non_blocking=True)
 
@@ -483,6 +511,7 @@ def run_tree(args):
         e2e_step(i)
     torch.cuda.synchronize(dev)
     ev0.record(stream)
+    copy_stream.wait_event(ev0)  # no copy of the timed steps starts before the clock
     for i in range(e2e_steps):
         e2e_step(i)
     ev1.record(stream)
