@@ -165,7 +165,7 @@ def test_mismatch_rate_over_many_seeds():
 # ------------------------------------------------------------------ shapes and edges
 
 SHAPES = [
-    # B, N, V, dtype     (row chunks: 16384 bf16 / 8192 f32 elements; sampler chunks half that)
+    # B, N, V, dtype     (row spans: 32768 bf16 / 16384 f32 elements; sampler blocks 8192)
     (1, 0, 1, "f32"),
     (3, 1, 3, "bf16"),          # scalar path (6 bytes per row)
     (5, 3, 8191, "bf16"),       # scalar path, one chunk minus one
@@ -176,6 +176,8 @@ SHAPES = [
     (33, 2, 24577, "bf16"),     # scalar path, several chunks
     (2, 0, 50000, "bf16"),      # bonus only
     (17, 6, 65536, "bf16"),
+    (4, 3, 150000, "f32"),      # ten spans per row: partials merged past the first four
+    (3, 2, 150001, "f32"),      # the same on the scalar path
 ]
 
 

@@ -77,6 +77,9 @@ CASES = {
     "wide-sampled-bf16": lambda: workloads.make_tree(8, 50000, "bf16", gen_seed=75, widths=(4, 3),
                                                      verify_seed=9),
     "root-only": lambda: workloads.make_tree(5, 4096, "f32", gen_seed=76, widths=(), verify_seed=1),
+    # seven spans per fp32 row: partials merged past the first four
+    "many-spans-sampled-f32": lambda: workloads.make_tree(4, 100000, "f32", gen_seed=79, widths=(3, 2),
+                                                          verify_seed=12),
 }
 
 
