@@ -9,12 +9,13 @@
 // square + eps) for RMSNorm) in fp32 and writes the normalised row, rounded
 // to bf16, into its third of the concatenated input X [T, 3d] (three passes
 // over a row that stays in L1/L2).  fc_gemm: a tcgen05 GEMM out = X W^T +
-// bias.  Each CTA owns a 128 x 256 output tile and walks K in steps of 64
-// through four shared-memory stages filled by cp.async in the canonical
-// K-major layout (8 x 16-byte core matrices, no swizzle), loads issued two
-// steps ahead; one thread issues four tcgen05.mma.kind::f16 (K = 16 each)
-// per step into an fp32 accumulator of 256 TMEM columns and commits them to
-// the stage's mbarrier, which frees the stage two steps later.  The
+// bias.  Each CTA owns a 256 x 256 output tile (two 128-row halves sharing
+// the B tile) and walks K in steps of 64 through three shared-memory stages
+// filled by cp.async in the canonical K-major layout (8 x 16-byte core
+// matrices, no swizzle), loads issued two steps ahead; one thread issues,
+// per step and half, four tcgen05.mma.kind::f16 (M = 128, K = 16 each) into
+// that half's fp32 accumulator of 256 TMEM columns and commits them to the
+// stage's mbarrier, which frees the stage for the loads of a later step.  The
 // epilogue reads the accumulator with tcgen05.ld, adds the bias and stores
 // bf16.  Every mbarrier wait is bounded; one that runs out sets an error bit
 // and the kernel still frees its TMEM.  (A first version normalised the A
@@ -30,18 +31,27 @@
 namespace sv {
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64;
+// kMW 128-row halves of the output tile per CTA, each its own MMA (M = 128)
+// and accumulator, all sharing the stage's B tile: kMW = 2 moves 64 KB per
+// K step for twice the MMAs of kMW = 1 (48 KB).
+#ifndef SV_FC_MW
+#define SV_FC_MW 2
+#endif
+constexpr int kMW = SV_FC_MW;
+constexpr int kBM = 128 * kMW, kBN = 256, kBK = 64;
 constexpr int kKG = kBK / 8;                       // core matrices along K per tile
-constexpr int kStages = 4;
+constexpr int kStages = kMW == 2 ? 3 : 4;          // 3 x 64 KB or 4 x 48 KB of shared memory
 #ifndef SV_FC_AHEAD
-#define SV_FC_AHEAD 2  // 3 measured slower: 246 against 281 TFLOP/s
+#define SV_FC_AHEAD 2  // 3 measured slower with kMW = 1: 246 against 281 TFLOP/s
 #endif
 constexpr int kAhead = SV_FC_AHEAD;                // steps of loads in flight ahead of the MMAs
 constexpr int kFcThreads = 256;
-constexpr int kABytes = kBM * kBK * 2;             // 16 KB
+constexpr int kABytes = kBM * kBK * 2;             // 16 KB per 128 rows
 constexpr int kBBytes = kBN * kBK * 2;             // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;     // 48 KB
-constexpr int kTmemCols = kBN;                     // fp32 accumulator 128 lanes x 256 columns
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kHalfABytes = 128 / 8 * kKG * 128;   // offset of rows 128.. in the A tile
+constexpr int kTmemCols = kBN * kMW;               // fp32 accumulators: 128 lanes x 256 columns each
+static_assert(kMW == 1 || kMW == 2, "one or two 128-row halves");
 static_assert(kAhead + 1 <= kStages, "a stage is refilled only after the MMAs that read it");
 constexpr uint32_t kWaitLimit = 1u << 26;
 
@@ -216,7 +226,7 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_gemm_kernel(FcNormProblem p)
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = s_tmem;
-  const uint32_t idesc = mma_idesc(kBM, kBN);
+  const uint32_t idesc = mma_idesc(128, kBN);
 
   bool ok = true;
   int committed = -1;  // last k step whose MMAs were committed
@@ -245,14 +255,17 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_gemm_kernel(FcNormProblem p)
       const unsigned char* sB = sA + kABytes;
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint64_t da = smem_desc(smem_u32(sA) + kk * 256, 128, kKG * 128);
         const uint64_t db = smem_desc(smem_u32(sB) + kk * 256, 128, kKG * 128);
         const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-            "l"(da), "l"(db), "r"(idesc), "r"(acc)
-            : "memory");
+#pragma unroll
+        for (int h = 0; h < kMW; ++h) {  // half h: A rows 128h.., accumulator columns 256h..
+          const uint64_t da = smem_desc(smem_u32(sA) + h * kHalfABytes + kk * 256, 128, kKG * 128);
+          asm volatile(
+              "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem + h * kBN),
+              "l"(da), "l"(db), "r"(idesc), "r"(acc)
+              : "memory");
+        }
       }
       asm volatile(
           "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -271,15 +284,16 @@ __global__ void __launch_bounds__(kFcThreads, 1) fc_gemm_kernel(FcNormProblem p)
   }
   ok = __syncthreads_and(ok);
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  if (ok && nk > 0) {
-    // warp w reads TMEM lanes 32 (w % 4) .. + 31 (its rows) and column half w / 4
+  for (int h = 0; h < kMW && ok && nk > 0; ++h) {
+    // warp w reads TMEM lanes 32 (w % 4) .. + 31 (its rows of half h) and
+    // column half w / 4 of that half's accumulator
     const int lane_base = (warp & 3) * 32;
-    const int m = lane_base + (tid & 31);
+    const int m = h * 128 + lane_base + (tid & 31);
     const int t = m0 + m;
     const int cbase = (warp >> 2) * (kBN / 2);
     for (int c = 0; c < kBN / 2; c += 16) {
       uint32_t r[16];
-      const uint32_t addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + cbase + c;
+      const uint32_t addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + h * kBN + cbase + c;
       asm volatile(
           "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
           "%15}, [%16];"
