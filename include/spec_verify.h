@@ -67,7 +67,8 @@ extern "C" {
 /* Bits of the device error word (spec_verify_get_error).  A request that
  * fails a device check gets out_tokens = -1 everywhere, out_accept_len = -1
  * and out_kv_len = 0; the checks run in the order temperature, tokens,
- * logits and only the first failing one is recorded for the request. */
+ * (a bounded wait that ran out,) logits and only the first failing one is
+ * recorded for the request. */
 #define SV_ERRBIT_TEMP   1u
 #define SV_ERRBIT_TOKEN  2u
 #define SV_ERRBIT_LOGIT  4u
@@ -388,6 +389,19 @@ int spec_verify_launches_per_call(void);
  */
 int spec_verify_debug_philox(uint64_t seed, const uint32_t* ctr3, uint32_t* out4, int n,
                              void* cuda_stream);
+
+/*
+ * spec_verify_debug_skip_row_stats -- test hook for the bounded waits.  With
+ * on != 0, the following spec_verify / spec_verify_tree calls on the context
+ * launch their sampling (walk) kernel alone, without the row-statistics
+ * kernel, so no partial statistics of those calls ever arrive: every poll
+ * for them runs out (about a second), each request with a valid temperature
+ * and valid tokens (and topology) is failed with SV_ERRBIT_WAIT, and
+ * spec_verify_get_error returns SV_ETIMEOUT.  on == 0 restores normal calls;
+ * the context stays usable throughout.  Host-side only: enqueues nothing.
+ * Returns SV_OK or SV_EINVAL.
+ */
+int spec_verify_debug_skip_row_stats(spec_verify_ctx* ctx, int on);
 
 /*
  * spec_verify_debug_seek_calls -- test hook.  Sets the context's count of

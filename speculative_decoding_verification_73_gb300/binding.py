@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(_PKG, "libspecverify.so")
 
 (SV_OK, SV_EINVAL, SV_EBADTEMP, SV_EBADTOKEN, SV_EBADLOGIT, SV_ECUDA, SV_ESCRATCH, SV_EBADTREE,
  SV_EBADKV, SV_ETIMEOUT) = range(10)
-SV_ERRBIT_TEMP, SV_ERRBIT_TOKEN, SV_ERRBIT_LOGIT, SV_ERRBIT_TREE, SV_ERRBIT_KV = 1, 2, 4, 8, 16
+SV_ERRBIT_TEMP, SV_ERRBIT_TOKEN, SV_ERRBIT_LOGIT, SV_ERRBIT_TREE, SV_ERRBIT_KV, SV_ERRBIT_WAIT = 1, 2, 4, 8, 16, 32
 SV_KV_SCRATCH, SV_KV_INPLACE = 0, 1
 SV_NORM_NONE, SV_NORM_LAYER, SV_NORM_RMS = 0, 1, 2
 SV_TREE_SAMPLED, SV_TREE_TOPK = 0, 1
@@ -34,7 +34,7 @@ EXPORTS = (
     "spec_verify_profile", "spec_verify_profile_read", "spec_verify_launches_per_call",
     "spec_verify_debug_philox", "spec_verify_destroy", "spec_verify_strerror",
     "spec_verify_noalloc", "spec_verify_tree", "spec_verify_kv_commit", "spec_verify_lazy",
-    "spec_verify_fc_norm", "spec_verify_debug_seek_calls",
+    "spec_verify_fc_norm", "spec_verify_debug_seek_calls", "spec_verify_debug_skip_row_stats",
 )
 
 _lib = None
@@ -68,6 +68,7 @@ def load():
     lib.spec_verify_launches_per_call.argtypes = []
     lib.spec_verify_debug_philox.argtypes = [c_u64, c_void, c_void, c_int, c_void]
     lib.spec_verify_debug_seek_calls.argtypes = [c_void, ctypes.c_uint32]
+    lib.spec_verify_debug_skip_row_stats.argtypes = [c_void, c_int]
     lib.spec_verify_destroy.argtypes = [c_void]
     lib.spec_verify_lazy.argtypes = list(lib.spec_verify.argtypes)
     lib.spec_verify_fc_norm.argtypes = [c_void, c_int, c_int, c_int, c_int, ctypes.c_float, c_void,
@@ -372,6 +373,11 @@ class SpecVerify:
 
     def get_error(self):
         return spec_verify_get_error(self.ctx)
+
+    def debug_skip_row_stats(self, on):
+        """Test hook: walk kernels alone (see spec_verify_debug_skip_row_stats)."""
+        _check(load().spec_verify_debug_skip_row_stats(self.ctx, 1 if on else 0),
+               "spec_verify_debug_skip_row_stats")
 
     def debug_seek_calls(self, calls):
         """Test hook: set the context's call count (see spec_verify_debug_seek_calls)."""

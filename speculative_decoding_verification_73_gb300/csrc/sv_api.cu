@@ -30,6 +30,7 @@ struct spec_verify_ctx {
   unsigned epoch;
   size_t part_bytes;  // bytes of the partials region
   size_t late_bytes;  // bytes of the tree walk's timeout tags
+  int skip_rowstats;  // test hook: calls launch their walk kernel alone
 };
 
 namespace {
@@ -227,7 +228,7 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
     if (ev == nullptr) return SV_ECUDA;
     if (cudaEventRecord(ev[0], ctx->stream) != cudaSuccess) return SV_ECUDA;
   }
-  if (sv::launch_rowstats(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess)
+  if (!ctx->skip_rowstats && sv::launch_rowstats(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess)
     return SV_ECUDA;
   if (ev && cudaEventRecord(ev[1], ctx->stream) != cudaSuccess) return SV_ECUDA;
   if (sv::launch_sample(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
@@ -286,7 +287,8 @@ int spec_verify_tree(spec_verify_ctx* ctx, int B, int M, int V, int mode,
     if (ev == nullptr) return SV_ECUDA;
     if (cudaEventRecord(ev[0], ctx->stream) != cudaSuccess) return SV_ECUDA;
   }
-  if (sv::launch_tree_rowstats(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
+  if (!ctx->skip_rowstats && sv::launch_tree_rowstats(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess)
+    return SV_ECUDA;
   if (ev && cudaEventRecord(ev[1], ctx->stream) != cudaSuccess) return SV_ECUDA;
   if (sv::launch_tree_walk(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
   if (ev) {
@@ -472,6 +474,12 @@ int spec_verify_destroy(spec_verify_ctx* ctx) {
 /* Test hook: Philox4x32-10 words for n counters (c0, c1, c2, 0) under a
  * 64-bit seed, computed by the same device function the walk uses.
  * ctr3: device [n, 3] uint32; out4: device [n, 4] uint32. */
+int spec_verify_debug_skip_row_stats(spec_verify_ctx* ctx, int on) {
+  if (ctx == nullptr) return SV_EINVAL;
+  ctx->skip_rowstats = on != 0;
+  return SV_OK;
+}
+
 int spec_verify_debug_seek_calls(spec_verify_ctx* ctx, uint32_t calls) {
   if (ctx == nullptr) return SV_EINVAL;
   ctx->epoch = calls;

@@ -250,12 +250,13 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   const unsigned bits = s_err | (late_tag == p.epoch ? kErrWait : 0u);
   if (bits) {
     // report the first failing check in the order temperature, topology,
-    // tokens, logits, wait
+    // tokens, wait, logits (a wait that ran out leaves the partials that the
+    // logit check reads unread)
     const unsigned err = (bits & kErrTemp)    ? kErrTemp
                          : (bits & kErrTree)  ? kErrTree
                          : (bits & kErrToken) ? kErrToken
-                         : (bits & kErrLogit) ? kErrLogit
-                                              : kErrWait;
+                         : (bits & kErrWait)  ? kErrWait
+                                              : kErrLogit;
     if (rank == 0) {
       if (is_node) out_tok[i] = -1;
       if (i < M) out_path[i] = -1;

@@ -283,13 +283,15 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
   if (pl.late) atomicOr(&s_late, 1);
   __syncthreads();
 
+  // checks of the inputs first; a wait that ran out comes before the logit
+  // check, whose partials it leaves unread
   unsigned err = 0;
   if (mode == kModeInvalid)
     err = kErrTemp;
-  else if (s_late)
-    err = kErrWait;
   else if (s_bad_token)
     err = kErrToken;
+  else if (s_late)
+    err = kErrWait;
   else if (s_bad_logit)
     err = kErrLogit;
 

@@ -7,6 +7,8 @@ partials) and the counter's wrap past 2^32 - 1 all have to give exactly the
 results of a fresh context on the same inputs.
 """
 
+import time
+
 import pytest
 import torch
 
@@ -95,4 +97,51 @@ def test_call_counter_wrap():
         for a, b in zip(got, ref):
             assert torch.equal(a, b), i
         assert ctx.get_error() == ref_err == (0, 0)
+    ctx.close()
+
+
+def test_chain_waits_run_out_without_row_statistics():
+    """No row statistics ever come: the sampler's bounded polls run out, every
+    request with a valid temperature fails with the wait bit, and the context
+    gives a fresh context's results on the next normal call."""
+    wl = workloads.make_random(6, 3, 5000, "bf16", gen_seed=321, temps=(0.0, 1.0), verify_seed=1)
+    wl.temperature[5] = -1.0  # an input error still wins over the wait
+    ctx = binding.SpecVerify(MAX_B, MAX_N, MAX_V, torch.bfloat16)
+    ctx.debug_skip_row_stats(True)
+    t0 = time.time()
+    toks, acc, kv = _host(ctx(*_inputs(wl), 5))
+    elapsed = time.time() - t0
+    code, bits = ctx.get_error()
+    assert code == binding.SV_EBADTEMP and bits == binding.SV_ERRBIT_WAIT | binding.SV_ERRBIT_TEMP
+    assert (acc == -1).all() and (kv == 0).all() and (toks == -1).all()
+    assert elapsed < 60
+    ctx.debug_skip_row_stats(False)
+    wl.temperature[5] = 1.0
+    got = _host(ctx(*_inputs(wl), 5))
+    ref, ref_err = _fresh(wl, 5)
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
+    assert ctx.get_error() == ref_err == (0, 0)
+    ctx.close()
+
+
+def test_tree_waits_run_out_without_row_statistics():
+    """The same for the tree walk: the cluster fails each request together."""
+    tree = workloads.make_tree(5, 5000, "bf16", gen_seed=322, widths=(2, 2), temps=(0.0, 1.0), verify_seed=2)
+    ctx = binding.SpecVerify(MAX_B, MAX_N, MAX_V, torch.bfloat16)
+    args = (tree.target.cuda(), tree.draft.cuda(), tree.parents.cuda(), tree.tokens.cuda(),
+            tree.temperature.cuda(), 9, tree.mode)
+    ctx.debug_skip_row_stats(True)
+    toks, path, acc, kv = _host(ctx.tree(*args))
+    code, bits = ctx.get_error()
+    assert code == binding.SV_ETIMEOUT and bits == binding.SV_ERRBIT_WAIT
+    assert (acc == -1).all() and (kv == 0).all() and (toks == -1).all() and (path == -1).all()
+    ctx.debug_skip_row_stats(False)
+    got = _host(ctx.tree(*args))
+    assert ctx.get_error() == (0, 0)
+    fresh = binding.SpecVerify(MAX_B, MAX_N, MAX_V, torch.bfloat16)
+    ref = _host(fresh.tree(*args))
+    fresh.close()
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)
     ctx.close()
