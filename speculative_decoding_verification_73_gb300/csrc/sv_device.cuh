@@ -124,6 +124,10 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // since the last commit; wait_pending(n) returns once at most n of this
 // thread's groups are still in flight (n a constant after unrolling).
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kN>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(kN) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_pending(int n) {
   switch (n) {
     case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;

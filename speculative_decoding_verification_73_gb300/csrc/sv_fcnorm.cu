@@ -161,11 +161,6 @@ __device__ __forceinline__ void cp_async16_or_zero(void* smem_dst, const void* g
                "l"(gmem_src), "r"(valid ? 16 : 0)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int kN>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(kN) : "memory");
-}
 
 // Loads of K step kt into a stage: X rows m0.., W rows n0.., 8 chunks of 16
 // bytes each.  Chunk q goes to row (q / 64) * 8 + q % 8 and column chunk

@@ -186,6 +186,13 @@ __device__ __forceinline__ void settle(float4 (&a)[kN], const Partial* pa, int n
   if (pending()) pl.late = true;
 }
 
+// The same for one array.
+template <int kN>
+__device__ __forceinline__ void settle(float4 (&a)[kN], const Partial* pa, int na, Poll& pl) {
+  float4 none[kN];
+  settle(a, pa, na, none, pa, 0, pl);
+}
+
 // Batch loader for merge_*_by: every load issued, then the batch settled.
 struct TaggedLoad {
   const Partial* parts;
@@ -196,7 +203,7 @@ struct TaggedLoad {
     for (int i = 0; i < kBatch; ++i)
       pt[i] = i0 + i < n ? ld_partial_relaxed(parts + i0 + i)
                          : make_float4(-INFINITY, 0.f, __int_as_float(INT_MAX), 0.f);
-    settle(pt, parts + i0, n - i0, pt, parts + i0, 0, *pl);
+    settle(pt, parts + i0, n - i0, *pl);
   }
 };
 
