@@ -122,5 +122,41 @@ __device__ __forceinline__ void seg_sums(const T* z, const T* y, bool need_y, in
   }
 }
 
+// seg_sums over a level-1 block staged in shared memory in the layout of
+// staged_at (bz, by: the block's staged rows; cbeg, cend: its tokens).  The
+// same values summed in the same order as seg_sums, so the sums are equal
+// bit for bit.
+template <typename T, typename F>
+__device__ __forceinline__ void seg_sums_staged(const T* bz, const T* by, bool need_y, int cbeg, int cend,
+                                                F f, float& h0, float& h1) {
+  using E = Elem<T>;
+  constexpr int kVec = E::kVec;
+  constexpr int kVecs = kSegTok / kVec;
+  h0 = 0.f;
+  h1 = 0.f;
+  const int t0 = cbeg + static_cast<int>(threadIdx.x) * kSegTok;
+  uint4 zv[kVecs], yv[kVecs];
+#pragma unroll
+  for (int i = 0; i < kVecs; ++i) {
+    const bool in = t0 + i * kVec < cend;
+    const int at = (i * kST + static_cast<int>(threadIdx.x)) * kVec;
+    zv[i] = in ? *reinterpret_cast<const uint4*>(bz + at) : make_uint4(0, 0, 0, 0);
+    yv[i] = (in && need_y) ? *reinterpret_cast<const uint4*>(by + at) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int i = 0; i < kVecs; ++i) {
+    float part = 0.f;
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+      const int t = t0 + i * kVec + e;
+      if (t < cend) part += f(E::get(zv[i], e), need_y ? E::get(yv[i], e) : 0.f, t);
+    }
+    if (i < kVecs / 2)
+      h0 += part;
+    else
+      h1 += part;
+  }
+}
+
 }  // namespace
 }  // namespace sv

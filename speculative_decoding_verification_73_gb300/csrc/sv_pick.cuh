@@ -15,6 +15,18 @@ constexpr int kL3 = kLevel1 / kLevel3;   // level-3 blocks per level-1 block (51
 constexpr int kL3PerL2 = kLevel2 / kLevel3;  // 16
 static_assert(kSegTok == 2 * kLevel3, "two level-3 blocks per thread");
 
+// Staged layout of a level-1 block in shared memory: thread t owns tokens
+// [32t, 32t + 32), and its i-th 16-byte vector sits at element
+// (i * kST + t) * kVec, so the vector accesses of a warp (copies in, reads
+// out) cover 512 consecutive bytes and meet no bank conflict.  staged_at
+// maps a token offset in the block to its element.
+template <typename T>
+__device__ __forceinline__ int staged_at(int e) {
+  constexpr int kVec = Elem<T>::kVec;
+  const int th = e / kSegTok, r = e - th * kSegTok;
+  return ((r / kVec) * kST + th) * kVec + (r % kVec);
+}
+
 __device__ __forceinline__ float cta_sum(float v, float* scratch) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);

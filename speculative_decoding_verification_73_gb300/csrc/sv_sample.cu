@@ -151,18 +151,6 @@ __device__ __forceinline__ float staged1(const __nv_bfloat16* p) {
   return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(p)) << 16);
 }
 
-// Staged layout of a level-1 block: thread t owns tokens [32t, 32t + 32),
-// and its i-th 16-byte vector sits at element (i * kST + t) * kVec, so the
-// vector accesses of a warp (copies in, reads out) cover 512 consecutive
-// bytes and meet no bank conflict.  staged_at maps a token offset in the
-// block to its element.
-template <typename T>
-__device__ __forceinline__ int staged_at(int e) {
-  constexpr int kVec = Elem<T>::kVec;
-  const int th = e / kSegTok, r = e - th * kSegTok;
-  return ((r / kVec) * kST + th) * kVec + (r % kVec);
-}
-
 // Stage this thread's tokens [32t, 32t + 32) of the level-1 block starting at
 // cbeg into sz / sy; vectors at or past cend get -inf.
 template <typename T>

@@ -329,10 +329,12 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
     for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster, ++bi) {
       const int cbeg = c * kLevel1, cend = min(V, cbeg + kLevel1);
       constexpr int kVec = Elem<T>::kVec;
-      for (int e = i * kSegTok; e < i * kSegTok + kSegTok; e += kVec) {
+      for (int v = 0; v < kSegTok / kVec; ++v) {  // the layout of staged_at
+        const int e = i * kSegTok + v * kVec;
+        const int at = bi * kLevel1 + (v * kST + i) * kVec;
         if (cbeg + e < cend) {
-          cp_async16(sz + bi * kLevel1 + e, z + cbeg + e);
-          if (with_y) cp_async16(sy + bi * kLevel1 + e, y + cbeg + e);
+          cp_async16(sz + at, z + cbeg + e);
+          if (with_y) cp_async16(sy + at, y + cbeg + e);
         }
       }
     }
@@ -417,8 +419,8 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
       for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster, ++bi) {
         float h0, h1;
         const int cbeg = c * kLevel1;
-        seg_sums<T, kVecPath, decltype(lf), true>(sz + bi * kLevel1 - cbeg, sy + bi * kLevel1 - cbeg, true,
-                                                  cbeg + i * kSegTok, min(V, cbeg + kLevel1), lf, h0, h1);
+        seg_sums_staged<T>(sz + bi * kLevel1, sy + bi * kLevel1, true, cbeg, min(V, cbeg + kLevel1), lf, h0,
+                           h1);
         acc += h0 + h1;
       }
     } else {
@@ -469,13 +471,16 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
     float h0, h1, mass;
     int cand;
     if (staging) {
-      const T* bz = sz + bi * kLevel1 - cbeg;
-      const T* by = sy + bi * kLevel1 - cbeg;
-      seg_sums<T, kVecPath, decltype(rf), true>(bz, by, need_y, cbeg + i * kSegTok, cend, rf, h0, h1);
+      const T* bz = sz + bi * kLevel1;
+      const T* by = sy + bi * kLevel1;
+      seg_sums_staged<T>(bz, by, need_y, cbeg, cend, rf, h0, h1);
       cand = block_pick(
           h0, h1, cbeg, cend, job,
-          [&](int t) { return law.r(staged_elem(bz + t), need_y ? staged_elem(by + t) : 0.f, t); }, sc,
-          &mass);
+          [&](int t) {
+            const int e = staged_at<T>(t - cbeg);
+            return law.r(staged_elem(bz + e), need_y ? staged_elem(by + e) : 0.f, t);
+          },
+          sc, &mass);
     } else {
       seg_sums<T, kVecPath>(z, y, need_y, cbeg + i * kSegTok, cend, rf, h0, h1);
       cand = block_pick(
