@@ -158,5 +158,66 @@ __device__ __forceinline__ void seg_sums_staged(const T* bz, const T* by, bool n
   }
 }
 
+// The sums of law.r over this thread's 32 staged tokens of a block, as
+// seg_sums_staged gives them, with the q / p / residual of kQ and kSampled
+// evaluated two tokens at a time by the paired float instructions (each
+// lane performs the scalar law's operations, so every token's value and the
+// sums are the same bit for bit); kTopk takes the scalar law.
+template <typename T>
+__device__ __forceinline__ void law_sums_staged(const NodeLaw& law, const T* bz, const T* by, bool need_y,
+                                                int cbeg, int cend, float& h0, float& h1) {
+  if (law.kind == NodeLaw::kTopk) {
+    seg_sums_staged<T>(bz, by, need_y, cbeg, cend, [&](float zt, float yt, int t) { return law.r(zt, yt, t); },
+                       h0, h1);
+    return;
+  }
+  using E = Elem<T>;
+  constexpr int kVec = E::kVec;
+  constexpr int kVecs = kSegTok / kVec;
+  h0 = 0.f;
+  h1 = 0.f;
+  const bool sampled = law.kind == NodeLaw::kSampled;
+  const uint64_t k2 = f2pack(law.k, law.k);
+  const uint64_t nq2 = f2pack(-law.cq, -law.cq), iq2 = f2pack(law.inv_sq, law.inv_sq);
+  const uint64_t np2 = f2pack(-law.cp, -law.cp), ip2 = f2pack(law.inv_sp, law.inv_sp);
+  const uint64_t nc2 = f2pack(-law.c, -law.c);
+  const int t0 = cbeg + static_cast<int>(threadIdx.x) * kSegTok;
+  uint4 zv[kVecs], yv[kVecs];
+#pragma unroll
+  for (int i = 0; i < kVecs; ++i) {
+    const bool in = t0 + i * kVec < cend;
+    const int at = (i * kST + static_cast<int>(threadIdx.x)) * kVec;
+    zv[i] = in ? *reinterpret_cast<const uint4*>(bz + at) : make_uint4(0, 0, 0, 0);
+    yv[i] = (in && need_y) ? *reinterpret_cast<const uint4*>(by + at) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int i = 0; i < kVecs; ++i) {
+    float rv[kVec];
+#pragma unroll
+    for (int e = 0; e < E::kPairs; ++e) {
+      float a0, a1;
+      f2unpack(f2fma(E::pair(zv[i], e), k2, nq2), a0, a1);
+      uint64_t v2 = f2mul(f2pack(ex2(a0), ex2(a1)), iq2);  // q
+      if (sampled) {
+        float b0, b1;
+        f2unpack(f2fma(E::pair(yv[i], e), k2, np2), b0, b1);
+        const uint64_t p2 = f2mul(f2pack(ex2(b0), ex2(b1)), ip2);
+        float w0, w1;
+        f2unpack(f2fma(nc2, p2, v2), w0, w1);  // q - c p
+        v2 = f2pack(fmaxf(w0, 0.f) * law.scale, fmaxf(w1, 0.f) * law.scale);
+      }
+      f2unpack(v2, rv[2 * e], rv[2 * e + 1]);
+    }
+    float part = 0.f;
+#pragma unroll
+    for (int e = 0; e < kVec; ++e)
+      if (t0 + i * kVec + e < cend) part += rv[e];
+    if (i < kVecs / 2)
+      h0 += part;
+    else
+      h1 += part;
+  }
+}
+
 }  // namespace
 }  // namespace sv

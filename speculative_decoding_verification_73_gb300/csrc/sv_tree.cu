@@ -419,7 +419,7 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
       for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster, ++bi) {
         float h0, h1;
         const int cbeg = c * kLevel1;
-        seg_sums_staged<T>(sz + bi * kLevel1, sy + bi * kLevel1, true, cbeg, min(V, cbeg + kLevel1), lf, h0,
+        law_sums_staged<T>(law, sz + bi * kLevel1, sy + bi * kLevel1, true, cbeg, min(V, cbeg + kLevel1), h0,
                            h1);
         acc += h0 + h1;
       }
@@ -473,7 +473,7 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
     if (staging) {
       const T* bz = sz + bi * kLevel1;
       const T* by = sy + bi * kLevel1;
-      seg_sums_staged<T>(bz, by, need_y, cbeg, cend, rf, h0, h1);
+      law_sums_staged<T>(law, bz, by, need_y, cbeg, cend, h0, h1);
       cand = block_pick(
           h0, h1, cbeg, cend, job,
           [&](int t) {
