@@ -185,3 +185,37 @@ def test_error_order():
     yy[0, 6, 0] = np.nan
     r = ot.verify_tree(z, yy, wl.parents.numpy(), wl.tokens.numpy(), [1.0], **args)
     assert r.errors == 0
+
+
+@pytest.mark.parametrize("shape", ["random", "star", "line"])
+def test_255_node_trees_walk_validly(shape):
+    """Trees of the largest size a context takes (255 draft nodes): the
+    accepted path descends from the root along parent links, the emitted
+    tokens are the path's tokens then one drawn token, and the lengths
+    agree; greedy requests descend exactly while a child holds the argmax."""
+    kw = {"random": {"m": 255}, "star": {"widths": (255,)}, "line": {"widths": (1,) * 255}}[shape]
+    wl = workloads.make_tree(3, 1000, "f32", gen_seed=91, temps=(0.0, 0.7, 1.0), sigma=(0.0, 0.3),
+                             verify_seed=4, **kw)
+    res = ot.verify_tree(*wl.raw(), wl.parents.numpy(), wl.tokens.numpy(), wl.temperature.numpy(), 4,
+                           wl.dtype, wl.mode)
+    par, toks = wl.parents.numpy(), wl.tokens.numpy()
+    z, _ = wl.raw()
+    for b in range(3):
+        assert res.request_errors[b] == 0
+        a = int(res.accept_len[b])
+        assert res.kv_len[b] == a + 1
+        path = [int(x) for x in res.path[b][:a]]
+        assert all(x == -1 for x in res.path[b][a:])
+        node = 0
+        for c in path:
+            assert int(par[b, c - 1]) == node  # a child of the current node
+            node = c
+        emitted = [int(x) for x in res.tokens[b]]
+        assert emitted[:a] == [int(toks[b, c - 1]) for c in path]
+        assert 0 <= emitted[a] < 1000 and all(x == -1 for x in emitted[a + 1:])
+        if float(wl.temperature[b]) == 0.0:
+            # the walk stops at the first node none of whose children is the argmax
+            rows = np.asarray(z[b], dtype=np.float64)
+            kids = [i + 1 for i in range(par.shape[1]) if int(par[b, i]) == node]
+            g = int(np.argmax(rows[node]))
+            assert emitted[a] == g and all(int(toks[b, c - 1]) != g for c in kids)
