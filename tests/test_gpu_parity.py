@@ -192,6 +192,12 @@ def test_max_drafts():
     check(wl)
 
 
+def test_max_drafts_bf16_two_spans():
+    # every walk thread holds a row pair, each row two spans
+    wl = workloads.make_random(2, 255, 40000, "bf16", gen_seed=6, temps=(0.0, 1.0), sigma=(0.0, 0.05))
+    check(wl)
+
+
 def test_batch_of_zero_is_a_noop():
     ctx = binding.SpecVerify(4, 3, 100, torch.float32)
     z = torch.zeros(0, 4, 100, device="cuda")
