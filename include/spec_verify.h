@@ -21,10 +21,17 @@
  *
  * Random numbers: Philox4x32-10 (Salmon et al., "Parallel Random Numbers:
  * As Easy as 1, 2, 3", SC'11) with key = (seed low 32 bits, seed high 32
- * bits) and counter = (b, j, draw, 0); draw 0 is the accept test at 1-based
- * position j, draw 1 is the correction at j* or the bonus at j = N+1;
- * u = (word0 >> 8) * 2^-24.  Samples use the inverse CDF in vocabulary
- * order: the smallest t whose running sum exceeds u times the total.
+ * bits) and counter = (b, j, draw, 0); a word w gives the uniform
+ * (w >> 8) * 2^-24.  Draw 0 is the accept test at 1-based position j and
+ * uses word 0.  Draw 1 is the correction at j* or the bonus at j = N+1 and
+ * uses all four words, u_1..u_4, in a grouped inverse CDF: the vocabulary
+ * is cut into blocks of 8192 consecutive tokens (level 1), each block into
+ * blocks of 256 (level 2), those into blocks of 16 (level 3) and those into
+ * single tokens (level 4); level l picks, among the sub-blocks of the block
+ * chosen so far, the smallest index whose running mass exceeds u_l times
+ * their total mass (the last sub-block with mass if rounding leaves none).
+ * The token is drawn exactly from the normalised residual (or q), since the
+ * levels' conditional masses multiply to its probability.
  *
  * Layout: every tensor is dense row-major, caller-owned DEVICE memory
  * (cudaMalloc / torch CUDA tensors on the context's device).  Logits are
@@ -402,6 +409,22 @@ int spec_verify_debug_philox(uint64_t seed, const uint32_t* ctr3, uint32_t* out4
  * Returns SV_OK or SV_EINVAL.
  */
 int spec_verify_debug_skip_row_stats(spec_verify_ctx* ctx, int on);
+
+/*
+ * spec_verify_debug_late_cta -- test hook for a wait that runs out in one
+ * sampler CTA of a request while the request's other CTAs finish.  With
+ * cta >= 0, the following spec_verify calls on the context make the sampling
+ * kernel's CTA number `cta` of every request (a request has one CTA per two
+ * level-1 blocks of 8192 tokens for bfloat16 logits, one per block for
+ * float32; CTA 0 also writes the walk's outputs) act as if its poll for the
+ * row statistics ran out.  A sampled request with such a CTA is failed as a
+ * whole (out_tokens -1, out_accept_len -1, out_kv_len 0, SV_ERRBIT_WAIT);
+ * the counters the request's CTAs share carry the call's sequence number,
+ * so a later call on the context is not disturbed.  cta == -1 restores
+ * normal calls.  Host-side only: enqueues nothing.  Returns SV_OK or
+ * SV_EINVAL.
+ */
+int spec_verify_debug_late_cta(spec_verify_ctx* ctx, int cta);
 
 /*
  * spec_verify_debug_seek_calls -- test hook.  Sets the context's count of

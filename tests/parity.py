@@ -84,7 +84,9 @@ def check_quota(mismatches, positions):
 
 
 def rel_close(gpu, ref, rtol=WINDOW):
-    """|gpu - ref| <= rtol * max(|ref|, 1) elementwise, NaN where ref is NaN."""
+    """Row log-normalisers: |gpu - ref| <= rtol * max(|ref|, 1) elementwise,
+    NaN where ref is NaN.  A logZ has magnitude near the row's largest
+    scaled logit, so this is a relative bound wherever |logZ| >= 1."""
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     nan = np.isnan(ref)
@@ -101,6 +103,39 @@ def max_rel(gpu, ref):
     if not m.any():
         return 0.0
     return float(np.max(np.abs(gpu[m] - ref[m]) / np.maximum(np.abs(ref[m]), 1.0)))
+
+
+# Smallest normal float32.  An acceptance probability below it is a float32
+# subnormal on the GPU (or flushes to zero), whose spacing is no longer
+# relative to the value; such a threshold is also below the 2^-24 step of
+# the uniforms, so it decides like 0 for every uniform but u = 0.
+FLT_MIN_NORMAL = 2.0 ** -126
+
+
+def prob_close(gpu, ref, rtol=WINDOW):
+    """Acceptance probabilities min(1, q(d)/p(d)): |gpu - ref| <= rtol * |ref|
+    elementwise (relative, as the method statement fixes), NaN where ref is
+    NaN; an absolute FLT_MIN_NORMAL is allowed on top only for references
+    below FLT_MIN_NORMAL (exact zeros must come back as zeros)."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    nan = np.isnan(ref)
+    if not np.array_equal(nan, np.isnan(gpu)):
+        return False
+    g, r = gpu[~nan], ref[~nan]
+    floor = np.where(np.abs(r) < FLT_MIN_NORMAL, FLT_MIN_NORMAL, 0.0)
+    return bool(np.all(np.abs(g - r) <= rtol * np.abs(r) + floor))
+
+
+def max_prob_rel(gpu, ref):
+    """Largest relative error of acceptance probabilities with a normal
+    float32 reference (for the assertion message)."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    m = ~np.isnan(ref) & (np.abs(ref) >= FLT_MIN_NORMAL)
+    if not m.any():
+        return 0.0
+    return float(np.max(np.abs(gpu[m] - ref[m]) / np.abs(ref[m])))
 
 
 def run_tree_oracle(wl, seed=None):
