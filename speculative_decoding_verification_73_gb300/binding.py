@@ -35,6 +35,7 @@ EXPORTS = (
     "spec_verify_debug_philox", "spec_verify_destroy", "spec_verify_strerror",
     "spec_verify_noalloc", "spec_verify_tree", "spec_verify_kv_commit", "spec_verify_lazy",
     "spec_verify_fc_norm", "spec_verify_debug_seek_calls", "spec_verify_debug_skip_row_stats",
+    "spec_verify_debug_late_cta",
 )
 
 _lib = None
@@ -69,6 +70,7 @@ def load():
     lib.spec_verify_debug_philox.argtypes = [c_u64, c_void, c_void, c_int, c_void]
     lib.spec_verify_debug_seek_calls.argtypes = [c_void, ctypes.c_uint32]
     lib.spec_verify_debug_skip_row_stats.argtypes = [c_void, c_int]
+    lib.spec_verify_debug_late_cta.argtypes = [c_void, c_int]
     lib.spec_verify_destroy.argtypes = [c_void]
     lib.spec_verify_lazy.argtypes = list(lib.spec_verify.argtypes)
     lib.spec_verify_fc_norm.argtypes = [c_void, c_int, c_int, c_int, c_int, ctypes.c_float, c_void,
@@ -378,6 +380,11 @@ class SpecVerify:
         """Test hook: walk kernels alone (see spec_verify_debug_skip_row_stats)."""
         _check(load().spec_verify_debug_skip_row_stats(self.ctx, 1 if on else 0),
                "spec_verify_debug_skip_row_stats")
+
+    def debug_late_cta(self, cta):
+        """Test hook: sampler CTA `cta` of every request acts as if its wait
+        ran out; -1 = off (see spec_verify_debug_late_cta)."""
+        _check(load().spec_verify_debug_late_cta(self.ctx, int(cta)), "spec_verify_debug_late_cta")
 
     def debug_seek_calls(self, calls):
         """Test hook: set the context's call count (see spec_verify_debug_seek_calls)."""

@@ -30,7 +30,9 @@ struct spec_verify_ctx {
   unsigned epoch;
   size_t part_bytes;  // bytes of the partials region
   size_t late_bytes;  // bytes of the tree walk's timeout tags
+  size_t arr_bytes;   // bytes of the sampler's epoch-tagged arrival words
   int skip_rowstats;  // test hook: calls launch their walk kernel alone
+  int late_cta;       // test hook: sampler CTA that acts as if its waits ran out
 };
 
 namespace {
@@ -80,7 +82,8 @@ cudaEvent_t* profile_slot(spec_verify_ctx* ctx) {
 int next_epoch(spec_verify_ctx* ctx, unsigned* epoch) {
   if (++ctx->epoch == 0) {
     if (cudaMemsetAsync(ctx->w.partials, 0, ctx->part_bytes, ctx->stream) != cudaSuccess ||
-        cudaMemsetAsync(ctx->w.late, 0, ctx->late_bytes, ctx->stream) != cudaSuccess)
+        cudaMemsetAsync(ctx->w.late, 0, ctx->late_bytes, ctx->stream) != cudaSuccess ||
+        cudaMemsetAsync(ctx->w.arrivals, 0, ctx->arr_bytes, ctx->stream) != cudaSuccess)
       return SV_ECUDA;
     ctx->epoch = 1;
   }
@@ -128,6 +131,7 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   ctx->max_V = max_V;
   ctx->dtype = dtype;
   ctx->stream = static_cast<cudaStream_t>(cuda_stream);
+  ctx->late_cta = -1;
   if (cudaGetDevice(&ctx->device) != cudaSuccess) {
     delete ctx;
     return SV_ECUDA;
@@ -149,7 +153,7 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   const size_t o_err = off;
   off = align_up(off + sizeof(unsigned), 256);
   const size_t o_arr = off;
-  off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
+  off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned long long), 256);
   const size_t o_late = off;
   off = align_up(off + static_cast<size_t>(max_B) * sizeof(unsigned), 256);
   // the error word, arrival counters and tree-walk timeout tags start at zero
@@ -168,7 +172,8 @@ int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int
   ctx->w.chunk_sums = reinterpret_cast<float*>(base + o_sums);
   ctx->w.blk_tok = reinterpret_cast<int*>(base + o_btok);
   ctx->w.err = reinterpret_cast<unsigned*>(base + o_err);
-  ctx->w.arrivals = reinterpret_cast<unsigned*>(base + o_arr);
+  ctx->w.arrivals = reinterpret_cast<unsigned long long*>(base + o_arr);
+  ctx->arr_bytes = static_cast<size_t>(max_B) * sizeof(unsigned long long);
   ctx->w.late = reinterpret_cast<unsigned*>(base + o_late);
   ctx->late_bytes = static_cast<size_t>(max_B) * sizeof(unsigned);
   ctx->w.dbg_accept = reinterpret_cast<float*>(base + o_acc);
@@ -218,6 +223,7 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
   sv::Workspace w = ctx->w;
   w.S1 = ceil_div(V, sv::row_chunk_elems(ctx->dtype));
   w.S3 = ceil_div(V, sv::sample_chunk_elems(ctx->dtype));
+  p.debug_late_cta = ctx->late_cta;
   // A fresh tag per call: the sampler of this call takes a partial only once
   // it carries this tag, never one left by an earlier call.
   if (next_epoch(ctx, &p.epoch) != SV_OK) return SV_ECUDA;
@@ -471,12 +477,15 @@ int spec_verify_destroy(spec_verify_ctx* ctx) {
   return rc;
 }
 
-/* Test hook: Philox4x32-10 words for n counters (c0, c1, c2, 0) under a
- * 64-bit seed, computed by the same device function the walk uses.
- * ctr3: device [n, 3] uint32; out4: device [n, 4] uint32. */
 int spec_verify_debug_skip_row_stats(spec_verify_ctx* ctx, int on) {
   if (ctx == nullptr) return SV_EINVAL;
   ctx->skip_rowstats = on != 0;
+  return SV_OK;
+}
+
+int spec_verify_debug_late_cta(spec_verify_ctx* ctx, int cta) {
+  if (ctx == nullptr || cta < -1) return SV_EINVAL;
+  ctx->late_cta = cta;
   return SV_OK;
 }
 
@@ -486,6 +495,9 @@ int spec_verify_debug_seek_calls(spec_verify_ctx* ctx, uint32_t calls) {
   return SV_OK;
 }
 
+/* Test hook: Philox4x32-10 words for n counters (c0, c1, c2, 0) under a
+ * 64-bit seed, computed by the same device function the walk uses.
+ * ctr3: device [n, 3] uint32; out4: device [n, 4] uint32. */
 int spec_verify_debug_philox(uint64_t seed, const uint32_t* ctr3, uint32_t* out4, int n,
                              void* cuda_stream) {
   if (n < 0 || (n > 0 && (ctr3 == nullptr || out4 == nullptr))) return SV_EINVAL;

@@ -77,6 +77,7 @@ struct Partial {
 constexpr int kJobNone = 0;
 constexpr int kJobResidual = 1;
 constexpr int kJobBonus = 2;
+constexpr int kJobLate = 3;  // a sampled request whose wait ran out in this CTA
 
 // What the walk leaves for the sampler (in shared memory of each CTA).
 //   q_t = 2^(z_t*k - cq) * inv_sq,  p_t = 2^(y_t*k - cp) * inv_sp
@@ -100,6 +101,8 @@ struct Problem {
   int32_t* out_accept;       // [B]
   int32_t* out_kv;           // [B]
   unsigned epoch;            // tag of this call's row-statistics partials (never 0)
+  int debug_late_cta = -1;   // test hook: the sampler CTA (index within its request)
+                             // that acts as if its waits ran out; -1 = none
 };
 
 struct TreeProblem {
@@ -150,7 +153,8 @@ struct Workspace {
   float* chunk_sums;     // [B, S3]: residual mass of each level-1 block
   int* blk_tok;          // [B, S3]: the token each level-1 block would give
   unsigned* err;         // [1], OR of kErr* bits (starts at zero)
-  unsigned* arrivals;    // [B]: sampler CTAs done per request (zero between calls)
+  unsigned long long* arrivals;  // [B]: sampler arrivals per request, (epoch << 32) |
+                                 // late bit 31 | count: a word of an earlier call counts 0
   unsigned* late;        // [B]: tree walk: the call's tag once a wait of the request ran out
   float* dbg_accept;     // [B, N]
   float* dbg_logz;       // [B, 2N+1]

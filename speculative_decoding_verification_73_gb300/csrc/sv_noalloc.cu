@@ -70,7 +70,7 @@ Carve carve(size_t B, size_t N, int s1, int s3) {
   c.err = off;
   off = align_up(off + sizeof(unsigned), 256);
   c.arr = off;
-  off = align_up(off + B * sizeof(unsigned), 256);
+  off = align_up(off + B * sizeof(unsigned long long), 256);
   c.acc = off;
   off = align_up(off + B * (N > 0 ? N : 1) * sizeof(float), 256);
   c.logz = off;
@@ -122,7 +122,7 @@ int spec_verify_noalloc(int B, int N, int V, int dtype, const void* target_logit
   w.chunk_sums = reinterpret_cast<float*>(base + c.sums);
   w.blk_tok = reinterpret_cast<int*>(base + c.btok);
   w.err = reinterpret_cast<unsigned*>(base + c.err);
-  w.arrivals = reinterpret_cast<unsigned*>(base + c.arr);
+  w.arrivals = reinterpret_cast<unsigned long long*>(base + c.arr);
   w.late = nullptr;  // tree walks only
   w.dbg_accept = reinterpret_cast<float*>(base + c.acc);
   w.dbg_logz = reinterpret_cast<float*>(base + c.logz);

@@ -29,11 +29,14 @@
 // level-2 mass per eight threads, the level-1 mass per CTA) and picks the
 // block's candidate token at levels 2-4 with u_2..u_4, as if level 1 had
 // chosen this block.  It stores (level-1 mass, candidate) and counts itself
-// in the request's arrival counter; the CTA that arrives last picks level 1
-// over the blocks' masses with u_1, writes the chosen block's candidate, and
-// resets the counter for the next call.  No CTA waits for another.  If the
-// residual has no mass anywhere, that last CTA redoes every block with q
-// alone.
+// in the request's arrival word (tagged with the call's epoch, so nothing
+// needs resetting between calls); the CTA that arrives last picks level 1
+// over the blocks' masses with u_1 and writes the chosen block's candidate.
+// No CTA waits for another.  If the residual has no mass anywhere, that last
+// CTA redoes every block with q alone.  A CTA whose wait for the row
+// statistics ran out evaluates nothing but still counts in, marking the
+// word; the last CTA then fails the whole request (SV_ERRBIT_WAIT), so a
+// request is either sampled from every block or failed.
 //
 // r_t = max(q_t - p_t, 0) with q_t = 2^(z_t k - c_q) / s_q and likewise p_t,
 // evaluated two tokens at a time with the paired float instructions.  Its
@@ -64,6 +67,29 @@ constexpr int blocks_per_cta() {
 template <typename T>
 constexpr int stage_bytes() {
   return 2 * blocks_per_cta<T>() * kLevel1 * static_cast<int>(sizeof(T));
+}
+
+// Arrival counting of a request's sampler CTAs.  The word holds the call's
+// epoch in its high half, so a count left by an earlier call (a CTA that
+// stopped before counting in) reads as zero and never makes a later call's
+// CTA think it arrived last; no reset is needed.  Bit 31 records that some
+// CTA of the request gave up waiting.  Returns the word's low half after
+// this CTA's arrival.
+constexpr unsigned kArrivalCount = 0x7fffffffu;
+__device__ __forceinline__ unsigned count_in(unsigned long long* word, unsigned epoch, bool late) {
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(word);
+  // every failed exchange means another CTA of the request counted in, so
+  // the loop ends after at most one round per CTA of the request; the bound
+  // is only a guard (giving up leaves this CTA not the last)
+  for (int tries = 0; tries < (1 << 16); ++tries) {
+    const unsigned low = static_cast<unsigned>(old >> 32) == epoch ? static_cast<unsigned>(old) : 0u;
+    const unsigned now = ((low & kArrivalCount) + 1u) | (low & ~kArrivalCount) | (late ? ~kArrivalCount : 0u);
+    const unsigned long long want = static_cast<unsigned long long>(epoch) << 32 | now;
+    const unsigned long long seen = atomicCAS(word, old, want);
+    if (seen == old) return now;
+    old = seen;
+  }
+  return 0u;
 }
 
 // r for the tokens of one 16-byte vector of each row; rv[e] gets token e.
@@ -226,10 +252,11 @@ __global__ void __launch_bounds__(kST, 3) sample_kernel(Problem p, Workspace w) 
   const int G = (S3 + kB - 1) / kB;  // CTAs per request
   const int b = blockIdx.x / G;
   const int g = blockIdx.x - b * G;
-  walk_request<T>(p, w, b, g == 0, &s_job);
+  walk_request<T>(p, w, b, g == 0, &s_job, g == p.debug_late_cta);
   __syncthreads();
   const Job job = s_job;
-  if (job.kind == kJobNone) return;  // identical in every CTA of the request
+  if (job.kind == kJobNone) return;  // nothing to sample for this request
+  const bool late = job.kind == kJobLate;
   const int N = p.N, V = p.V;
   const T* z = static_cast<const T*>(p.target) + (static_cast<size_t>(b) * (N + 1) + job.row) * V;
   const T* y = job.kind == kJobResidual
@@ -241,7 +268,9 @@ __global__ void __launch_bounds__(kST, 3) sample_kernel(Problem p, Workspace w) 
   const int c0 = g * kB;
   const int nb = min(kB, S3 - c0);
 
-  if (kVecPath) {
+  if (late) {
+    // this CTA's wait ran out: no blocks, it only counts in (below)
+  } else if (kVecPath) {
     T* sz = reinterpret_cast<T*>(s_rows);
     T* sy = sz + kB * kLevel1;
     // one group of copies per block, so block i is reduced while the
@@ -290,13 +319,23 @@ __global__ void __launch_bounds__(kST, 3) sample_kernel(Problem p, Workspace w) 
   }
   if (threadIdx.x == 0) {
     __threadfence();  // publish before counting in
-    const unsigned before = atomicAdd(w.arrivals + b, 1u);
-    s_last = before == static_cast<unsigned>(G - 1);
-    if (s_last) w.arrivals[b] = 0u;  // every CTA of the request has counted in
+    const unsigned state = count_in(w.arrivals + b, p.epoch, late);
+    s_last = (state & kArrivalCount) == static_cast<unsigned>(G) ? 1 + (state >> 31) : 0;
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();  // see the other CTAs' masses and candidates
+  if (s_last == 2) {
+    // Some CTA of the request gave up waiting for its row statistics, so
+    // not every block was evaluated: the request fails as a whole.
+    if (threadIdx.x <= N) p.out_tokens[static_cast<size_t>(b) * (N + 1) + threadIdx.x] = -1;
+    if (threadIdx.x == 0) {
+      p.out_accept[b] = -1;
+      p.out_kv[b] = 0;
+      atomicOr(w.err, kErrWait);
+    }
+    return;
+  }
 
   // Level 1 over the blocks' masses; with at most 32 blocks lane i fetches
   // block i's candidate together with its mass.

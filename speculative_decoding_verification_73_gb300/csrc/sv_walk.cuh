@@ -207,9 +207,11 @@ struct TaggedLoad {
   }
 };
 
+// force_late: the test hook that makes this CTA act as if its waits ran out.
 template <typename T>
 __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& w, int b,
-                                             bool write_outputs, Job* job_out) {
+                                             bool write_outputs, Job* job_out,
+                                             bool force_late = false) {
   const int j = threadIdx.x;
   const int N = p.N, V = p.V;
   const bool row_thread = j <= N;
@@ -287,7 +289,7 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
       if (!pn.ok) atomicOr(&s_bad_logit, 1);
     }
   }
-  if (pl.late) atomicOr(&s_late, 1);
+  if (pl.late || force_late) atomicOr(&s_late, 1);
   __syncthreads();
 
   // checks of the inputs first; a wait that ran out comes before the logit
@@ -330,7 +332,9 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
         if (err) atomicOr(w.err, err);
       }
     }
-    if (j == 0) job_out->kind = kJobNone;
+    // a sampled request whose wait ran out here still counts in with the
+    // sampler's other CTAs of the request (see sv_sample.cu)
+    if (j == 0) job_out->kind = (err == kErrWait && mode == kModeSampled) ? kJobLate : kJobNone;
     return;
   }
 

@@ -145,3 +145,36 @@ def test_tree_waits_run_out_without_row_statistics():
     for a, b in zip(got, ref):
         assert torch.equal(a, b)
     ctx.close()
+
+
+@pytest.mark.parametrize("cta", [0, 1, 4])
+def test_one_sampler_cta_gives_up_while_the_others_finish(cta):
+    """One sampler CTA of every request acts as if its wait for the row
+    statistics ran out, while the request's other CTAs finish their blocks
+    and count in (V = 70000 bf16: five CTAs per request).  Every sampled
+    request fails as a whole with the wait bit (greedy requests too when
+    the CTA is 0, the one that walks them); the next normal calls on the
+    same context give a fresh context's results, so nothing the CTAs share
+    outlives the call."""
+    wl = workloads.make_random(12, 5, 70000, "bf16", gen_seed=323, temps=(0.0, 1.0), verify_seed=3)
+    sampled = (wl.temperature > 0).numpy()
+    assert sampled.any() and (~sampled).any()
+    ctx = binding.SpecVerify(12, 5, 70000, torch.bfloat16)
+    ctx.debug_late_cta(cta)
+    toks, acc, kv = _host(ctx(*_inputs(wl), 7))
+    code, bits = ctx.get_error()
+    assert code == binding.SV_ETIMEOUT and bits == binding.SV_ERRBIT_WAIT
+    failed = sampled if cta > 0 else sampled | ~sampled
+    assert (acc[failed] == -1).all() and (kv[failed] == 0).all() and (toks[failed] == -1).all()
+    ref, ref_err = _fresh(wl, 7)
+    assert ref_err == (0, 0)
+    for a, b in zip((toks, acc, kv), ref):
+        assert torch.equal(a[~failed], b[~failed])
+    ctx.debug_late_cta(-1)
+    for seed in (7, 8):
+        got = _host(ctx(*_inputs(wl), seed))
+        ref, ref_err = _fresh(wl, seed)
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b), seed
+        assert ctx.get_error() == ref_err == (0, 0)
+    ctx.close()

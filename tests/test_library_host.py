@@ -68,6 +68,7 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert lib.spec_verify_debug_philox(0, None, None, 0, None) == binding.SV_OK
     assert lib.spec_verify_debug_seek_calls(None, 5) == binding.SV_EINVAL
     assert lib.spec_verify_debug_skip_row_stats(None, 1) == binding.SV_EINVAL
+    assert lib.spec_verify_debug_late_cta(None, 1) == binding.SV_EINVAL
     assert lib.spec_verify_tree(None, 1, 1, 1, 0, None, None, None, None, None, 0, None, None, None,
                                 None) == binding.SV_EINVAL
     assert lib.spec_verify_kv_commit(None, 0, 1, 1, 1, 1, 16, None, None, None, None, None, 0) \
