@@ -31,7 +31,9 @@ def test_reference_arm_prints_one_contract_line():
     assert d["metric"] == "verified draft positions/sec" and d["unit"] == "positions/s"
     assert d["higher_is_better"] is True and d["value"] > 0
     cb = d["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == d["value"] and cb["sample"]
+    bench = _bench()
+    assert cb["kind"] == "oracle" and cb["cores"] == bench.host_cores() and cb["value"] == d["value"]
+    assert cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == "batch64-bf16"
@@ -51,3 +53,20 @@ def test_whole_job_rate_counts_every_rank():
     bench = _bench()
     # 448 positions per rank-step, 100 steps, 2 ranks, slowest rank 5 ms
     assert bench.whole_job_rate(448, 100, 2, 5.0) == 448 * 100 * 2 / 0.005
+
+
+def test_oracle_host_times_one_thread_and_every_core():
+    """The oracle timing of the cpu_baseline and per-config keys: a saved
+    workload, one thread here, then a spawned process per core."""
+    sys.path.insert(0, ROOT)
+    import bench  # importable by name, so the spawned workers find its functions
+    from speculative_decoding_verification_73_gb300 import workloads
+    host = bench.OracleHost()
+    try:
+        host.start()
+        out = host.time_requests("tiny-f32", workloads.tiny_f32(), budget_s=0.3)
+    finally:
+        host.close()
+    assert out["cores"] == bench.host_cores() and out["value"] > 0 and out["unit"] == bench.UNIT
+    assert out["single_thread"]["cores"] == 1 and out["single_thread"]["value"] > 0
+    assert not os.path.exists(host.dir)
