@@ -7,23 +7,32 @@
 // Two kernels.  fcnorm_prep: one warp per (token, segment) computes the
 // row's mean and 1/sqrt(var + eps) (LayerNorm; mean 0 and 1/sqrt(mean
 // square + eps) for RMSNorm) in fp32 and writes the normalised row, rounded
-// to bf16, into its third of the concatenated input X [T, 3d] (three passes
-// over a row that stays in L1/L2).  fc_gemm: a tcgen05 GEMM out = X W^T +
-// bias.  Each CTA owns a 256 x 256 output tile (two 128-row halves sharing
-// the B tile) and walks K in steps of 64 through three shared-memory stages
-// filled by cp.async in the canonical K-major layout (8 x 16-byte core
-// matrices, no swizzle), loads issued two steps ahead; one thread issues,
-// per step and half, four tcgen05.mma.kind::f16 (M = 128, K = 16 each) into
-// that half's fp32 accumulator of 256 TMEM columns and commits them to the
-// stage's mbarrier, which frees the stage for the loads of a later step.  The
-// epilogue reads the accumulator with tcgen05.ld, adds the bias and stores
-// bf16.  Every mbarrier wait is bounded; one that runs out sets an error bit
-// and the kernel still frees its TMEM.  (A first version normalised the A
-// tile on the fly inside the GEMM, with each step's loads issued only after
-// the previous step's MMAs: 150 TFLOP/s on T = d = d_out = 4096; writing X
-// costs one more pass over the hidden states and lets the GEMM pipeline.)
+// to bf16, into its third of the concatenated input X [T, 3d].  fc_gemm: a
+// persistent tcgen05 GEMM out = X W^T + bias, one CTA per SM walking
+// 128 x 256 output tiles, with its warps split by role:
+//   * warp 0 (one lane) loads: for each K step of 64 it waits until the
+//     stage is free, then fetches the 128 x 64 tile of X and the 256 x 64
+//     tile of W with two TMA tensor copies (cp.async.bulk.tensor, 128-byte
+//     swizzle) completing on the stage's "full" barrier;
+//   * warp 1 (one lane) multiplies: for each K step it waits for the stage,
+//     issues four tcgen05.mma.kind::f16 (M = 128, N = 256, K = 16) into one
+//     of two fp32 accumulators of 256 TMEM columns, and commits them to the
+//     stage's "empty" barrier (the stage is refilled once they are done);
+//     after the tile's last step it commits to the accumulator's "full"
+//     barrier;
+//   * warps 2-5 drain: they wait for an accumulator, read it with tcgen05.ld
+//     (each warp its quarter of the 128 lanes, one output row per thread),
+//     add the bias, store bf16 rows and release the accumulator, while the
+//     MMAs of the next tile already fill the other one.
+// So loads, MMAs and the epilogue overlap without any CTA-wide barrier in the
+// loop.  Tiles go m-block by m-block (all n-blocks of the first 128 rows,
+// then the next), so the CTAs working at one time share their X tiles and
+// W stays in L2.  Every barrier wait is bounded; one that runs out sets
+// SV_ERRBIT_WAIT, stops the CTA's loop, waits (bounded) for the copies and
+// MMAs it started, and frees its TMEM.
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "sv_device.cuh"
@@ -31,43 +40,19 @@
 namespace sv {
 namespace {
 
-// kMW 128-row halves of the output tile per CTA, each its own MMA (M = 128)
-// and accumulator, all sharing the stage's B tile: kMW = 2 moves 64 KB per
-// K step for twice the MMAs of kMW = 1 (48 KB).
-#ifndef SV_FC_MW
-#define SV_FC_MW 2
-#endif
-constexpr int kMW = SV_FC_MW;
-constexpr int kBM = 128 * kMW, kBN = 256, kBK = 64;
-constexpr int kKG = kBK / 8;                       // core matrices along K per tile
-constexpr int kStages = kMW == 2 ? 3 : 4;          // 3 x 64 KB or 4 x 48 KB of shared memory
-#ifndef SV_FC_AHEAD
-#define SV_FC_AHEAD 2  // 3 measured slower with kMW = 1: 246 against 281 TFLOP/s
-#endif
-constexpr int kAhead = SV_FC_AHEAD;                // steps of loads in flight ahead of the MMAs
-constexpr int kFcThreads = 256;
-constexpr int kABytes = kBM * kBK * 2;             // 16 KB per 128 rows
-constexpr int kBBytes = kBN * kBK * 2;             // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kHalfABytes = 128 / 8 * kKG * 128;   // offset of rows 128.. in the A tile
-constexpr int kTmemCols = kBN * kMW;               // fp32 accumulators: 128 lanes x 256 columns each
-static_assert(kMW == 1 || kMW == 2, "one or two 128-row halves");
-static_assert(kAhead + 1 <= kStages, "a stage is refilled only after the MMAs that read it");
+constexpr int kBM = 128, kBN = 256, kBK = 64;   // output tile, K step (64 bf16 = one 128-byte row)
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;          // 16 KB
+constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
+constexpr int kAccCols = kBN;                   // fp32 accumulator: 128 lanes x 256 columns
+constexpr int kTmemCols = 2 * kAccCols;         // two accumulators
+constexpr int kFcThreads = 192;                 // loads, MMAs, four epilogue warps
+constexpr int kEpiThreads = 128;
 constexpr uint32_t kWaitLimit = 1u << 26;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-// Shared-memory matrix descriptor: start address, leading (K-direction) and
-// stride (M/N-direction) byte offsets between core matrices, descriptor
-// version 1, no swizzle.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = static_cast<uint64_t>((addr & 0x3FFFF) >> 4);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  return d;
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
@@ -152,185 +137,264 @@ __global__ void fcnorm_prep_kernel(FcNormProblem p) {
   }
 }
 
+
 // --------------------------------------------------------------- the GEMM
 
-// 16-byte cp.async that writes zeros instead of reading when !valid.
-__device__ __forceinline__ void cp_async16_or_zero(void* smem_dst, const void* gmem_src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
-               "l"(gmem_src), "r"(valid ? 16 : 0)
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: rows of 128 bytes in atoms of 8 rows (1024 bytes apart
+// along M/N), descriptor version 1, swizzle mode 2 (128 bytes).  The K
+// offset inside the 128-byte row is added to the start address.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+  uint64_t d = static_cast<uint64_t>((addr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;              // leading offset (unused with this swizzle)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;      // stride offset: 8 rows of 128 bytes
+  d |= static_cast<uint64_t>(1) << 46;              // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;              // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
 }
 
-// Loads of K step kt into a stage: X rows m0.., W rows n0.., 8 chunks of 16
-// bytes each.  Chunk q goes to row (q / 64) * 8 + q % 8 and column chunk
-// (q / 8) % 8: eight consecutive threads fill one 16-byte column of eight
-// rows (eight distinct bank groups of a core matrix: no shared-memory bank
-// conflict), and a warp reads 64 contiguous bytes from each of eight rows.
-__device__ __forceinline__ int chunk_row(int q) { return (q >> 6) * 8 + (q & 7); }
-__device__ __forceinline__ int chunk_col(int q) { return (q >> 3) & 7; }
-
-__device__ __forceinline__ void load_stage(const FcNormProblem& p, unsigned char* stage, int m0, int n0,
-                                           int kt) {
-  const int K = 3 * p.d;
-  const int k0 = kt * kBK;
-  unsigned char* sA = stage;
-  unsigned char* sB = stage + kABytes;
-  for (int q = threadIdx.x; q < kBM * kKG; q += kFcThreads) {
-    const int m = chunk_row(q), c = chunk_col(q);
-    const bool in = m0 + m < p.T;
-    const __nv_bfloat16* src = p.x + static_cast<size_t>(in ? m0 + m : 0) * K + k0 + c * 8;
-    cp_async16_or_zero(sA + (m >> 3) * (kKG * 128) + c * 128 + (m & 7) * 16, src, in);
-  }
-  for (int q = threadIdx.x; q < kBN * kKG; q += kFcThreads) {
-    const int n = chunk_row(q), c = chunk_col(q);
-    const bool in = n0 + n < p.d_out;
-    const __nv_bfloat16* src = p.w + static_cast<size_t>(in ? n0 + n : 0) * K + k0 + c * 8;
-    cp_async16_or_zero(sB + (n >> 3) * (kKG * 128) + c * 128 + (n & 7) * 16, src, in);
-  }
+// 2-D TMA tensor copy of the box at (x, y) (x = K element offset, a multiple
+// of 64; y = row) into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
 }
 
-__global__ void __launch_bounds__(kFcThreads, 1) fc_gemm_kernel(FcNormProblem p) {
-  extern __shared__ __align__(1024) unsigned char smem[];
-  __shared__ __align__(8) uint64_t s_bar[kStages];
-  __shared__ uint32_t s_tmem;
-  __shared__ int s_fail;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM;
-  const int nk = 3 * p.d / kBK;
+__device__ __forceinline__ void tile_of(int t, int n_tiles_n, int& m0, int& n0) {
+  const int mb = t / n_tiles_n;
+  m0 = mb * kBM;
+  n0 = (t - mb * n_tiles_n) * kBN;
+}
 
-  if (tid == 0) {
-    s_fail = 0;
-    for (int s = 0; s < kStages; ++s)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar[s])) : "memory");
+struct GemmShared {
+  uint64_t full[kStages], empty[kStages];   // stage loaded / stage free
+  uint64_t acc_full[2], acc_empty[2];       // accumulator ready / drained
+  uint32_t tmem;
+  int abort;
+};
+
+__global__ void __launch_bounds__(kFcThreads, 1)
+    fc_gemm_kernel(FcNormProblem p, const __grid_constant__ CUtensorMap map_x,
+                   const __grid_constant__ CUtensorMap map_w) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // stages 1024-byte aligned (the swizzle atom); the runtime guarantees 16
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ GemmShared sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = 3 * p.d;
+  const int nk = K / kBK;
+  const int n_tiles_n = (p.d_out + kBN - 1) / kBN;
+  const int n_tiles = ((p.T + kBM - 1) / kBM) * n_tiles_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sh.acc_full[a], 1);
+      mbar_init(&sh.acc_empty[a], kEpiThreads);
+    }
+    sh.abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&s_tmem)),
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sh.tmem)),
                  "n"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-#pragma unroll
-  for (int a = 0; a < kAhead; ++a) {
-    if (a < nk) load_stage(p, smem + a * kStageBytes, m0, n0, a);
-    cp_async_commit();
-  }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const uint32_t tmem = s_tmem;
-  const uint32_t idesc = mma_idesc(128, kBN);
+  const uint32_t tmem = sh.tmem;
+  volatile int* abort = &sh.abort;
 
-  bool ok = true;
-  int committed = -1;  // last k step whose MMAs were committed
-  for (int kt = 0; kt < nk; ++kt) {
-    // refill the stage of step kt + kAhead, last read by the MMAs of step
-    // kt + kAhead - kStages (<= kt - 1, committed in an earlier iteration):
-    // wait for them first
-    const int nxt = kt + kAhead;
-    const int prev = nxt - kStages;
-    if (prev >= 0 && nxt < nk) {
-      if (!mbar_wait(smem_u32(&s_bar[prev % kStages]), static_cast<uint32_t>((prev / kStages) & 1)))
-        s_fail = 1;
+  if (warp == 0) {
+    // ---------------- loads
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < n_tiles && !*abort; t += gridDim.x) {
+        int m0, n0;
+        tile_of(t, n_tiles_n, m0, n0);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = static_cast<int>(it % kStages);
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!mbar_wait(smem_u32(&sh.empty[s]), ph ^ 1u)) {
+            *abort = 1;
+            break;
+          }
+          unsigned char* st = smem + s * kStageBytes;
+          mbar_expect_tx(&sh.full[s], kStageBytes);
+          tma_load_2d(st, &map_x, kb * kBK, m0, &sh.full[s]);
+          tma_load_2d(st + kABytes, &map_w, kb * kBK, n0, &sh.full[s]);
+        }
+      }
+      // copies into this CTA's shared memory must have landed before it
+      // can leave: wait (bounded) for the last use of every stage
+      for (uint32_t q = it > kStages ? it - kStages : 0; q < it; ++q)
+        mbar_wait(smem_u32(&sh.full[q % kStages]), (q / kStages) & 1u);
     }
-    if (nxt < nk) load_stage(p, smem + (nxt % kStages) * kStageBytes, m0, n0, nxt);
-    cp_async_commit();
-    cp_async_wait_group<kAhead>();  // this thread's loads of step kt have landed
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor core
-    __syncthreads();
-    if (s_fail) {
-      ok = false;
-      break;
+  } else if (warp == 1) {
+    // ---------------- MMAs
+    if (lane == 0) {
+      const uint32_t idesc = mma_idesc(kBM, kBN);
+      uint32_t it = 0, lt = 0;
+      bool issued = false;
+      uint64_t* last_commit = nullptr;
+      uint32_t last_phase = 0;
+      for (int t = blockIdx.x; t < n_tiles && !*abort; t += gridDim.x, ++lt) {
+        const uint32_t a = lt & 1u, aph = (lt >> 1) & 1u;
+        if (!mbar_wait(smem_u32(&sh.acc_empty[a]), aph ^ 1u)) {
+          *abort = 1;
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t acc = tmem + a * kAccCols;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = static_cast<int>(it % kStages);
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!mbar_wait(smem_u32(&sh.full[s]), ph)) {
+            *abort = 1;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t sa = smem_u32(smem + s * kStageBytes);
+          const uint64_t da = sw128_desc(sa), db = sw128_desc(sa + kABytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // K slice kk: 16 elements = 32 bytes further along the swizzled row
+            const uint32_t accumulate = (kb > 0 || kk > 0) ? 1u : 0u;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(acc),
+                "l"(da + 2 * kk), "l"(db + 2 * kk), "r"(idesc), "r"(accumulate)
+                : "memory");
+          }
+          asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                           smem_u32(&sh.empty[s]))
+                       : "memory");
+          issued = true;
+          last_commit = &sh.empty[s];
+          last_phase = ph;
+        }
+        if (*abort) break;
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                         smem_u32(&sh.acc_full[a]))
+                     : "memory");
+      }
+      // the tensor core must be done with TMEM and the stages before they go
+      if (issued && *abort) mbar_wait(smem_u32(last_commit), last_phase);
     }
-    if (tid == 0) {
+  } else {
+    // ---------------- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    uint32_t lt = 0;
+    for (int t = blockIdx.x; t < n_tiles && !*abort; t += gridDim.x, ++lt) {
+      const uint32_t a = lt & 1u, aph = (lt >> 1) & 1u;
+      if (!mbar_wait(smem_u32(&sh.acc_full[a]), aph)) {
+        *abort = 1;
+        break;
+      }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const unsigned char* sA = smem + (kt % kStages) * kStageBytes;
-      const unsigned char* sB = sA + kABytes;
+      int m0, n0;
+      tile_of(t, n_tiles_n, m0, n0);
+      const int tok = m0 + row;
+      const uint32_t base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * kAccCols;
+#pragma unroll 1
+      for (int c = 0; c < kBN; c += 32) {
+        uint32_t r[32];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+              "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+              "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+              "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+            : "r"(base + c));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        const int n = n0 + c;
+        if (tok < p.T && n < p.d_out) {
+          float y[32];
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint64_t db = smem_desc(smem_u32(sB) + kk * 256, 128, kKG * 128);
-        const uint32_t acc = (kt > 0 || kk > 0) ? 1u : 0u;
+          for (int j = 0; j < 32; ++j)
+            y[j] = __uint_as_float(r[j]) + (p.bias != nullptr && n + j < p.d_out ? __ldg(p.bias + n + j) : 0.f);
+          __nv_bfloat16* out = p.out + static_cast<size_t>(tok) * p.d_out + n;
+          if (n + 32 <= p.d_out && p.out_vec) {
+            uint4* o = reinterpret_cast<uint4*>(out);
 #pragma unroll
-        for (int h = 0; h < kMW; ++h) {  // half h: A rows 128h.., accumulator columns 256h..
-          const uint64_t da = smem_desc(smem_u32(sA) + h * kHalfABytes + kk * 256, 128, kKG * 128);
-          asm volatile(
-              "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem + h * kBN),
-              "l"(da), "l"(db), "r"(idesc), "r"(acc)
-              : "memory");
+            for (int q = 0; q < 4; ++q)
+              o[q] = make_uint4(pack_bf16(y[8 * q], y[8 * q + 1]), pack_bf16(y[8 * q + 2], y[8 * q + 3]),
+                                pack_bf16(y[8 * q + 4], y[8 * q + 5]), pack_bf16(y[8 * q + 6], y[8 * q + 7]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (n + j < p.d_out) out[j] = __float2bfloat16_rn(y[j]);
+          }
         }
       }
-      asm volatile(
-          "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-              smem_u32(&s_bar[kt % kStages]))
-          : "memory");
-    }
-    committed = kt;
-  }
-  cp_async_wait_group<0>();
-
-  // the last commit covers every MMA issued before it
-  if (ok && nk > 0) {
-    const int last = nk - 1;
-    if (!mbar_wait(smem_u32(&s_bar[last % kStages]), static_cast<uint32_t>((last / kStages) & 1)))
-      ok = false;
-  }
-  ok = __syncthreads_and(ok);
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  for (int h = 0; h < kMW && ok && nk > 0; ++h) {
-    // warp w reads TMEM lanes 32 (w % 4) .. + 31 (its rows of half h) and
-    // column half w / 4 of that half's accumulator
-    const int lane_base = (warp & 3) * 32;
-    const int m = h * 128 + lane_base + (tid & 31);
-    const int t = m0 + m;
-    const int cbase = (warp >> 2) * (kBN / 2);
-    for (int c = 0; c < kBN / 2; c += 16) {
-      uint32_t r[16];
-      const uint32_t addr = tmem + (static_cast<uint32_t>(lane_base) << 16) + h * kBN + cbase + c;
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-          "%15}, [%16];"
-          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-            "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-            "=r"(r[14]), "=r"(r[15])
-          : "r"(addr));
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      const int n = n0 + cbase + c;
-      if (t < p.T) {
-        float y[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          y[j] = __uint_as_float(r[j]) + (p.bias != nullptr && n + j < p.d_out ? __ldg(p.bias + n + j) : 0.f);
-        __nv_bfloat16* out = p.out + static_cast<size_t>(t) * p.d_out + n;
-        if (n + 16 <= p.d_out && p.out_vec) {
-          uint4* o = reinterpret_cast<uint4*>(out);
-          o[0] = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
-                            pack_bf16(y[6], y[7]));
-          o[1] = make_uint4(pack_bf16(y[8], y[9]), pack_bf16(y[10], y[11]), pack_bf16(y[12], y[13]),
-                            pack_bf16(y[14], y[15]));
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (n + j < p.d_out) out[j] = __float2bfloat16_rn(y[j]);
-        }
-      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      mbar_arrive(&sh.acc_empty[a]);
     }
   }
-  if (!ok && tid == 0) {
-    atomicOr(p.err, kErrWait);
-    // give the tensor core a last bounded chance to finish before the
-    // accumulator's columns are freed
-    if (committed >= 0)
-      mbar_wait(smem_u32(&s_bar[committed % kStages]),
-                static_cast<uint32_t>((committed / kStages) & 1));
-  }
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols)
-                 : "memory");
+  if (threadIdx.x == 0 && sh.abort) atomicOr(p.err, kErrWait);
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver once.
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_tiled() {
+  static EncodeTiled fn = nullptr;
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(f);
+  }
+  return fn;
+}
+
+// A bf16 matrix [rows, K] (row stride K elements, 16-byte aligned) read in
+// boxes of 64 x box_rows with the 128-byte swizzle; rows past the end read 0.
+bool make_map(CUtensorMap* map, const void* base, int K, int rows, int box_rows) {
+  EncodeTiled enc = encode_tiled();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t elem[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -341,11 +405,19 @@ cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s) {
   fcnorm_prep_kernel<<<(warps * 32 + 255) / 256, 256, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int smem = kStages * kStageBytes;
+  CUtensorMap map_x, map_w;
+  if (!make_map(&map_x, p.x, 3 * p.d, p.T, kBM) || !make_map(&map_w, p.w, 3 * p.d, p.d_out, kBN))
+    return cudaErrorInvalidValue;
+  const int smem = kStages * kStageBytes + 1024;  // + room to align the stages to 1024 bytes
   e = cudaFuncSetAttribute(fc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((p.d_out + kBN - 1) / kBN, (p.T + kBM - 1) / kBM);
-  fc_gemm_kernel<<<grid, kFcThreads, smem, s>>>(p);
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const int n_tiles = ((p.T + kBM - 1) / kBM) * ((p.d_out + kBN - 1) / kBN);
+  const int grid = n_tiles < sms ? n_tiles : sms;
+  fc_gemm_kernel<<<grid, kFcThreads, smem, s>>>(p, map_x, map_w);
   return cudaGetLastError();
 }
 

@@ -73,3 +73,27 @@ def test_selector_weights_return_the_normalised_segment():
     w[:, d:2 * d] = torch.eye(d, dtype=torch.float64)
     wl.weight = w.to(torch.bfloat16)
     run_case(wl, binding.SV_NORM_LAYER, with_bias=False, with_beta=True)
+
+
+def test_full_size_on_sampled_rows():
+    """T = d = d_out = 4096 (the benchmarked size, 32 x 16 output tiles of the
+    persistent GEMM, every CTA several tiles): 64 sampled tokens against the
+    oracle on those tokens alone (tokens are normalised independently)."""
+    T = d = d_out = 4096
+    wl = workloads.make_fcnorm(T, d, d_out, gen_seed=2026)
+    ctx = binding.SpecVerify(1, 1, 16, torch.float32)
+    h = [x.cuda() for x in wl.h]
+    out = binding.spec_verify_fc_norm(ctx.ctx, binding.SV_NORM_LAYER, *h, wl.weight.cuda(),
+                                      gamma=wl.gamma.cuda(), beta=wl.beta.cuda(), bias=wl.bias.cuda())
+    assert ctx.get_error() == (0, 0)
+    rows = np.sort(np.random.default_rng(4).choice(T, size=64, replace=False))
+    rows[0], rows[-1] = 0, T - 1
+    got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
+    hs = [_f64(x[torch.from_numpy(rows)]) for x in wl.h]
+    ref = ofc.fc_norm(*hs, _f64(wl.weight), binding.SV_NORM_LAYER, _f64(wl.gamma), _f64(wl.beta),
+                      _f64(wl.bias), 1e-5)
+    bound = ofc.abs_bound(*hs, _f64(wl.weight), binding.SV_NORM_LAYER, _f64(wl.gamma), _f64(wl.beta), 1e-5)
+    err = np.abs(got - ref)
+    tol = 2.0 ** -8 * (bound + np.abs(ref)) + 1e-6
+    assert (err <= tol).all(), f"worst error / tolerance {float((err / tol).max()):.3g}"
+    ctx.close()
