@@ -367,24 +367,27 @@ int spec_verify_debug_stats(spec_verify_ctx* ctx, int B, int N,
 
 /*
  * Kernel timing for benchmarks.  spec_verify_profile(ctx, every) with
- * every > 0 makes every every-th spec_verify call (the first, then each
- * every-th after it; 1 = all calls) record CUDA events around each kernel
- * it launches on the context's stream; every == 0 turns this off, and a
- * negative value is SV_EINVAL.  Events between the two kernels keep them
- * from overlapping, so recording a sample of the calls disturbs a timed
- * loop less.  spec_verify_profile_read waits for the stream and returns, for
- * the recorded calls since the last read, the summed device time in
- * milliseconds of each of the SV_NUM_KERNELS kernels and the number of
- * recorded calls; it then clears the sums.  Kernel 0 streams every logit row once (row statistics
- * and the draft tokens' logits); kernel 1 runs each request's accept/reject
- * walk and samples its correction or bonus token.
+ * every > 0 makes every every-th call of spec_verify, spec_verify_tree and
+ * spec_verify_lazy on the context (the first, then each every-th after it;
+ * 1 = all calls) record CUDA events around each kernel it launches on the
+ * context's stream; every == 0 turns this off, and a negative value is
+ * SV_EINVAL.  Events around kernels keep them from overlapping one another,
+ * so recording a sample of the calls disturbs a timed loop less.
+ * spec_verify_profile_read waits for the stream and returns, for the
+ * recorded calls since the last read, the summed device time in
+ * milliseconds of each of the SV_NUM_KERNELS kernel slots and the number of
+ * recorded calls; it then clears the sums.  For spec_verify slot 0 is the
+ * row-statistics kernel (every logit row streamed once, with the draft
+ * tokens' logits) and slot 1 the walk and draw kernel; for spec_verify_tree
+ * the same with the tree walk; spec_verify_lazy launches one kernel (slot 0;
+ * slot 1 reads 0).
  */
 #define SV_NUM_KERNELS 2
 int spec_verify_profile(spec_verify_ctx* ctx, int every);
 int spec_verify_profile_read(spec_verify_ctx* ctx, double* ms_per_kernel,
                              int* calls);
 
-/* Number of kernel launches one spec_verify call with B > 0 makes. */
+/* Number of kernel launches one spec_verify call with B > 0 makes (2). */
 int spec_verify_launches_per_call(void);
 
 /*

@@ -24,7 +24,7 @@ SV_F32, SV_BF16 = 0, 1
 SV_NUM_KERNELS = 2
 SV_MAX_N = 255
 SV_NOALLOC_SCRATCH_BYTES = 1 << 20
-KERNEL_NAMES = ("rowstats", "sample")
+KERNEL_NAMES = ("k0", "k1")  # profiling slots: row statistics, then walk and draws
 
 _DTYPE_CODE = {torch.float32: SV_F32, torch.bfloat16: SV_BF16}
 

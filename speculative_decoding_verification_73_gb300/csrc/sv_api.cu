@@ -410,6 +410,7 @@ int spec_verify_fc_norm(spec_verify_ctx* ctx, int T, int d, int d_out, int norm,
   p.bias = bias;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.out_vec = aligned16(out) && d_out % 8 == 0;
+  p.gb_vec = (norm == SV_NORM_NONE || aligned16(gamma)) && (p.beta == nullptr || aligned16(p.beta));
   p.x = static_cast<__nv_bfloat16*>(xbuf);
   p.err = ctx->w.err;
   return sv::launch_fcnorm(p, ctx->stream) == cudaSuccess ? SV_OK : SV_ECUDA;

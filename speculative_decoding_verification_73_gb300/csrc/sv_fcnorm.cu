@@ -83,14 +83,92 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__global__ void fcnorm_prep_kernel(FcNormProblem p) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= p.T * 3) return;
-  const int t = warp / 3, s = warp - t * 3;
+// Widened bf16 pair of a 32-bit word (element 2i of the 16 bytes is the
+// low half of word i).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// One warp per (token, segment) row of d elements, the row held in
+// registers: lane l keeps 16-byte vectors l, l + 32, ... (kVpl of them at
+// most, d <= 256 kVpl), so the row is read from global memory once, the
+// mean and the variance come from the registers (two passes, fp32, the
+// same order of additions as a loop over the vectors), and the normalised
+// row is written once.  Rows longer than 256 kVpl take the loop form below.
+template <int kVpl>
+__device__ __forceinline__ void prep_row_regs(const FcNormProblem& p, const __nv_bfloat16* h,
+                                              __nv_bfloat16* x, const float* g, const float* bt, int lane) {
+  const int nvec = p.d / 8;
+  uint4 v[kVpl];
+#pragma unroll
+  for (int i = 0; i < kVpl; ++i) {
+    const int q = lane + 32 * i;
+    v[i] = q < nvec ? *reinterpret_cast<const uint4*>(h + 8 * q) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float mu = 0.f, rstd = 1.f;
+  if (p.norm != kNormNone) {
+    if (p.norm == kNormLayer) {
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < kVpl; ++i) {
+        if (lane + 32 * i < nvec) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) sum += Elem<__nv_bfloat16>::get(v[i], e);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+      mu = sum / static_cast<float>(p.d);
+    }
+    float sq = 0.f;
+#pragma unroll
+    for (int i = 0; i < kVpl; ++i) {
+      if (lane + 32 * i < nvec) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float y = Elem<__nv_bfloat16>::get(v[i], e) - mu;
+          sq = fmaf(y, y, sq);
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(kFull, sq, o);
+    rstd = rsqrtf(sq / static_cast<float>(p.d) + p.eps);
+  }
+#pragma unroll
+  for (int i = 0; i < kVpl; ++i) {
+    const int q = lane + 32 * i;
+    if (q >= nvec) continue;
+    uint4 o = v[i];
+    if (p.norm != kNormNone) {
+      const int f = 8 * q;
+      const float4 g0 = __ldg(reinterpret_cast<const float4*>(g + f));
+      const float4 g1 = __ldg(reinterpret_cast<const float4*>(g + f + 4));
+      float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
+      if (bt != nullptr) {
+        b0 = __ldg(reinterpret_cast<const float4*>(bt + f));
+        b1 = __ldg(reinterpret_cast<const float4*>(bt + f + 4));
+      }
+      const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+      const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float z = (Elem<__nv_bfloat16>::get(v[i], e) - mu) * rstd * gg[e];
+        if (bt != nullptr) z += bb[e];
+        y[e] = z;
+      }
+      o = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                     pack_bf16(y[6], y[7]));
+    }
+    *reinterpret_cast<uint4*>(x + 8 * q) = o;
+  }
+}
+
+// The same statistics and output for any row length, three passes over the
+// row (the later ones from L1 / L2).
+__device__ __forceinline__ void prep_row_loop(const FcNormProblem& p, const __nv_bfloat16* h,
+                                              __nv_bfloat16* x, const float* g, const float* bt, int lane) {
   const int d = p.d;
-  const __nv_bfloat16* h = (s == 0 ? p.h[0] : s == 1 ? p.h[1] : p.h[2]) + static_cast<size_t>(t) * d;
-  __nv_bfloat16* x = p.x + static_cast<size_t>(t) * 3 * d + static_cast<size_t>(s) * d;
   float mu = 0.f, rstd = 1.f;
   if (p.norm != kNormNone) {
     if (p.norm == kNormLayer) {
@@ -117,8 +195,6 @@ __global__ void fcnorm_prep_kernel(FcNormProblem p) {
     for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(kFull, sq, o);
     rstd = rsqrtf(sq / static_cast<float>(d) + p.eps);
   }
-  const float* g = p.gamma + static_cast<size_t>(s) * d;
-  const float* bt = p.beta != nullptr ? p.beta + static_cast<size_t>(s) * d : nullptr;
   for (int f = lane * 8; f < d; f += 256) {
     const uint4 v = *reinterpret_cast<const uint4*>(h + f);
     uint4 o = v;
@@ -137,6 +213,23 @@ __global__ void fcnorm_prep_kernel(FcNormProblem p) {
   }
 }
 
+constexpr int kPrepVpl = 16;  // rows up to 4096 elements stay in registers
+
+__global__ void __launch_bounds__(256) fcnorm_prep_kernel(FcNormProblem p) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= p.T * 3) return;
+  const int t = warp / 3, s = warp - t * 3;
+  const int d = p.d;
+  const __nv_bfloat16* h = (s == 0 ? p.h[0] : s == 1 ? p.h[1] : p.h[2]) + static_cast<size_t>(t) * d;
+  __nv_bfloat16* x = p.x + static_cast<size_t>(t) * 3 * d + static_cast<size_t>(s) * d;
+  const float* g = p.norm != kNormNone ? p.gamma + static_cast<size_t>(s) * d : nullptr;
+  const float* bt = p.beta != nullptr ? p.beta + static_cast<size_t>(s) * d : nullptr;
+  if (d <= 256 * kPrepVpl && p.gb_vec)
+    prep_row_regs<kPrepVpl>(p, h, x, g, bt, lane);
+  else
+    prep_row_loop(p, h, x, g, bt, lane);
+}
 
 // --------------------------------------------------------------- the GEMM
 

@@ -142,6 +142,7 @@ struct FcNormProblem {
   const float* bias;           // [d_out] or nullptr
   __nv_bfloat16* out;          // [T, d_out]
   bool out_vec;                // rows of out 16-byte aligned
+  bool gb_vec;                 // gamma and beta (when given) 16-byte aligned
   __nv_bfloat16* x;            // [T, 3d]: the normalised, concatenated input (scratch)
   unsigned* err;
 };

@@ -55,6 +55,8 @@ CASES = [
     ("none-one-token", 1, 128, 256, binding.SV_NORM_NONE, True, False),
     ("layer-no-beta", 129, 192, 264, binding.SV_NORM_LAYER, False, False),
     ("layer-medium", 512, 1024, 1024, binding.SV_NORM_LAYER, True, True),
+    ("layer-wide-row", 33, 4160, 96, binding.SV_NORM_LAYER, True, True),   # rows past the register form
+    ("rms-widest-register-row", 40, 4096, 72, binding.SV_NORM_RMS, True, False),
 ]
 
 
