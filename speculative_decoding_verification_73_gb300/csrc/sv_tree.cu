@@ -121,9 +121,14 @@ template <typename T>
 constexpr int tree_stage_bytes() {
   return 2 * kStageBlocks * kLevel1 * static_cast<int>(sizeof(T));
 }
+// Build-time override: -DSV_TREE_STAGE=0 reads the rows from global memory
+// (L2 after the first pass) in every pass instead of staging them.
+#ifndef SV_TREE_STAGE
+#define SV_TREE_STAGE 1
+#endif
 template <typename T, bool kVecPath>
 constexpr bool tree_stages() {
-  return kVecPath && sizeof(T) == 2;
+  return SV_TREE_STAGE && kVecPath && sizeof(T) == 2;
 }
 
 template <typename T, bool kVecPath>
