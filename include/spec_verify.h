@@ -85,8 +85,7 @@ extern "C" {
 #define SV_ERRBIT_WAIT   32u  /* a bounded device wait ran out */
 
 /* ---- logit element types ---------------------------------------------- */
-#define SV_F32   0
-#define SV_BF16  1
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;  /* int-sized in the C ABI */
 
 /* Limits of one context. */
 #define SV_MAX_N 255            /* drafts per request                       */
@@ -111,7 +110,7 @@ typedef struct spec_verify_ctx spec_verify_ctx;   /* opaque, library-owned */
  * spec_verify_tree with up to max_N draft nodes per tree.  Returns SV_OK, SV_EINVAL or SV_ECUDA.
  */
 int spec_verify_init(spec_verify_ctx** ctx, int max_B, int max_N, int max_V,
-                     int dtype, void* cuda_stream);
+                     sv_dtype dtype, void* cuda_stream);
 
 /*
  * spec_verify -- one batched verify step.
@@ -186,7 +185,7 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V,
  * enqueued) or SV_ECUDA.
  */
 #define SV_NOALLOC_SCRATCH_BYTES (1u << 20)
-int spec_verify_noalloc(int B, int N, int V, int dtype,
+int spec_verify_noalloc(int B, int N, int V, sv_dtype dtype,
                         const void* target_logits, const void* draft_logits,
                         const int32_t* draft_tokens, const float* temperature,
                         uint64_t seed, int32_t* out_tokens,

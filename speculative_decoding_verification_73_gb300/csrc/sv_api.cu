@@ -117,7 +117,7 @@ const char* spec_verify_strerror(int code) {
 
 int spec_verify_launches_per_call(void) { return SV_NUM_KERNELS; }
 
-int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, int dtype,
+int spec_verify_init(spec_verify_ctx** out, int max_B, int max_N, int max_V, sv_dtype dtype,
                      void* cuda_stream) {
   if (out == nullptr) return SV_EINVAL;
   *out = nullptr;

@@ -40,12 +40,12 @@
 namespace sv {
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64;   // output tile, K step (64 bf16 = one 128-byte row)
+constexpr int kBM = 128, kBNMax = 256, kBK = 64;  // output tile (kBM x bn, bn <= 256), K step
 constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;          // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;          // 32 KB
+constexpr int kBBytes = kBNMax * kBK * 2;       // 32 KB room for the W tile
 constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
-constexpr int kAccCols = kBN;                   // fp32 accumulator: 128 lanes x 256 columns
+constexpr int kAccCols = kBNMax;                // fp32 accumulator slot: 128 lanes x 256 columns
 constexpr int kTmemCols = 2 * kAccCols;         // two accumulators
 constexpr int kFcThreads = 192;                 // loads, MMAs, four epilogue warps
 constexpr int kEpiThreads = 128;
@@ -269,10 +269,10 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-__device__ __forceinline__ void tile_of(int t, int n_tiles_n, int& m0, int& n0) {
+__device__ __forceinline__ void tile_of(int t, int n_tiles_n, int bn, int& m0, int& n0) {
   const int mb = t / n_tiles_n;
   m0 = mb * kBM;
-  n0 = (t - mb * n_tiles_n) * kBN;
+  n0 = (t - mb * n_tiles_n) * bn;
 }
 
 struct GemmShared {
@@ -284,7 +284,7 @@ struct GemmShared {
 
 __global__ void __launch_bounds__(kFcThreads, 1)
     fc_gemm_kernel(FcNormProblem p, const __grid_constant__ CUtensorMap map_x,
-                   const __grid_constant__ CUtensorMap map_w) {
+                   const __grid_constant__ CUtensorMap map_w, int bn) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // stages 1024-byte aligned (the swizzle atom); the runtime guarantees 16
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(kFcThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = 3 * p.d;
   const int nk = K / kBK;
-  const int n_tiles_n = (p.d_out + kBN - 1) / kBN;
+  const int n_tiles_n = (p.d_out + bn - 1) / bn;
   const int n_tiles = ((p.T + kBM - 1) / kBM) * n_tiles_n;
 
   if (threadIdx.x == 0) {
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kFcThreads, 1)
       uint32_t it = 0;
       for (int t = blockIdx.x; t < n_tiles && !*abort; t += gridDim.x) {
         int m0, n0;
-        tile_of(t, n_tiles_n, m0, n0);
+        tile_of(t, n_tiles_n, bn, m0, n0);
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = static_cast<int>(it % kStages);
           const uint32_t ph = (it / kStages) & 1u;
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kFcThreads, 1)
             break;
           }
           unsigned char* st = smem + s * kStageBytes;
-          mbar_expect_tx(&sh.full[s], kStageBytes);
+          mbar_expect_tx(&sh.full[s], kABytes + bn * kBK * 2);
           tma_load_2d(st, &map_x, kb * kBK, m0, &sh.full[s]);
           tma_load_2d(st + kABytes, &map_w, kb * kBK, n0, &sh.full[s]);
         }
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kFcThreads, 1)
   } else if (warp == 1) {
     // ---------------- MMAs
     if (lane == 0) {
-      const uint32_t idesc = mma_idesc(kBM, kBN);
+      const uint32_t idesc = mma_idesc(kBM, bn);
       uint32_t it = 0, lt = 0;
       bool issued = false;
       uint64_t* last_commit = nullptr;
@@ -411,11 +411,11 @@ __global__ void __launch_bounds__(kFcThreads, 1)
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       int m0, n0;
-      tile_of(t, n_tiles_n, m0, n0);
+      tile_of(t, n_tiles_n, bn, m0, n0);
       const int tok = m0 + row;
       const uint32_t base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * kAccCols;
 #pragma unroll 1
-      for (int c = 0; c < kBN; c += 32) {
+      for (int c = 0; c < bn; c += 32) {
         uint32_t r[32];
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -490,6 +490,26 @@ bool make_map(CUtensorMap* map, const void* base, int K, int rows, int box_rows)
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output tile width: of 256, 224, 192, 160 and 128 columns (multiples of
+// 32 for the epilogue, at most the 256 columns of an accumulator slot) the
+// one whose busiest CTA does the least work, ceil(tiles / SMs) x width (the
+// widest on a tie): 4096 x 4096 on 152 SMs takes 224 (608 tiles, four full
+// rounds) rather than 256 (512 tiles, the last of four rounds a third full).
+int tile_width(int T, int d_out, int sms) {
+  const int mt = (T + kBM - 1) / kBM;
+  int best = kBNMax;
+  long long best_cost = -1;
+  for (int bn = kBNMax; bn >= 128; bn -= 32) {
+    const long long tiles = static_cast<long long>(mt) * ((d_out + bn - 1) / bn);
+    const long long cost = (tiles + sms - 1) / sms * bn;
+    if (best_cost < 0 || cost < best_cost) {
+      best = bn;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 }  // namespace
 
 cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s) {
@@ -498,19 +518,20 @@ cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s) {
   fcnorm_prep_kernel<<<(warps * 32 + 255) / 256, 256, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  CUtensorMap map_x, map_w;
-  if (!make_map(&map_x, p.x, 3 * p.d, p.T, kBM) || !make_map(&map_w, p.w, 3 * p.d, p.d_out, kBN))
-    return cudaErrorInvalidValue;
-  const int smem = kStages * kStageBytes + 1024;  // + room to align the stages to 1024 bytes
-  e = cudaFuncSetAttribute(fc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
       (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
     return e;
-  const int n_tiles = ((p.T + kBM - 1) / kBM) * ((p.d_out + kBN - 1) / kBN);
+  const int bn = tile_width(p.T, p.d_out, sms);
+  CUtensorMap map_x, map_w;
+  if (!make_map(&map_x, p.x, 3 * p.d, p.T, kBM) || !make_map(&map_w, p.w, 3 * p.d, p.d_out, bn))
+    return cudaErrorInvalidValue;
+  const int smem = kStages * kStageBytes + 1024;  // + room to align the stages to 1024 bytes
+  e = cudaFuncSetAttribute(fc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int n_tiles = ((p.T + kBM - 1) / kBM) * ((p.d_out + bn - 1) / bn);
   const int grid = n_tiles < sms ? n_tiles : sms;
-  fc_gemm_kernel<<<grid, kFcThreads, smem, s>>>(p, map_x, map_w);
+  fc_gemm_kernel<<<grid, kFcThreads, smem, s>>>(p, map_x, map_w, bn);
   return cudaGetLastError();
 }
 

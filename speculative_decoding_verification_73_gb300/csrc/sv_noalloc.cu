@@ -97,7 +97,7 @@ void* scratch_on_current_device() {
 
 extern "C" {
 
-int spec_verify_noalloc(int B, int N, int V, int dtype, const void* target_logits,
+int spec_verify_noalloc(int B, int N, int V, sv_dtype dtype, const void* target_logits,
                         const void* draft_logits, const int32_t* draft_tokens,
                         const float* temperature, uint64_t seed, int32_t* out_tokens,
                         int32_t* out_accept_len, int32_t* out_kv_len, void* cuda_stream) {

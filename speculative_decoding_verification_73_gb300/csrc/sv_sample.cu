@@ -240,8 +240,14 @@ __device__ int block_candidate_global(const T* z, const T* y, int cbeg, int V, c
       mass);
 }
 
+// Resident CTAs per SM the sampler is built for (its registers per thread
+// follow); build-time override -DSV_SAMPLE_MINB=<n>.
+#ifndef SV_SAMPLE_MINB
+#define SV_SAMPLE_MINB 3
+#endif
+
 template <typename T, bool kVecPath>
-__global__ void __launch_bounds__(kST, 3) sample_kernel(Problem p, Workspace w) {
+__global__ void __launch_bounds__(kST, SV_SAMPLE_MINB) sample_kernel(Problem p, Workspace w) {
   constexpr int kB = blocks_per_cta<T>();
   extern __shared__ __align__(16) unsigned char s_rows[];  // staged rows (vector path)
   __shared__ BlockScratch scs[kB];

@@ -99,3 +99,13 @@ def test_full_size_on_sampled_rows():
     tol = 2.0 ** -8 * (bound + np.abs(ref)) + 1e-6
     assert (err <= tol).all(), f"worst error / tolerance {float((err / tol).max()):.3g}"
     ctx.close()
+
+
+@pytest.mark.parametrize("T,d_out", [(640, 3872), (640, 4832), (640, 5792), (1280, 3392), (128, 256)])
+def test_every_tile_width(T, d_out):
+    """The GEMM picks its output tile width (256, 224, 192, 160 or 128
+    columns) from the shape and the SM count; on a 152-SM GB300 these shapes
+    take 160, 192, 224, 256 and 128 columns respectively (ragged last tiles
+    included).  A narrow d keeps each case quick."""
+    wl = workloads.make_fcnorm(T, 64, d_out, gen_seed=T + d_out)
+    run_case(wl, binding.SV_NORM_LAYER, True, True)
