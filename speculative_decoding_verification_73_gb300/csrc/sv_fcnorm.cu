@@ -214,8 +214,13 @@ __device__ __forceinline__ void prep_row_loop(const FcNormProblem& p, const __nv
 }
 
 constexpr int kPrepVpl = 16;  // rows up to 4096 elements stay in registers
+// Resident CTAs per SM the normalisation kernel is built for.
+#ifndef SV_PREP_MINB
+#define SV_PREP_MINB 2
+#endif
 
-__global__ void __launch_bounds__(256) fcnorm_prep_kernel(FcNormProblem p) {
+__global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_kernel(FcNormProblem p) {
+  allow_dependents();  // the GEMM's CTAs may be scheduled as this grid drains
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= p.T * 3) return;
@@ -325,6 +330,9 @@ __global__ void __launch_bounds__(kFcThreads, 1)
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
+      // X is written by the normalisation grid before this one (this grid
+      // is its programmatic dependent): wait for it before the first load
+      wait_for_prerequisite();
       uint32_t it = 0;
       for (int t = blockIdx.x; t < n_tiles && !*abort; t += gridDim.x) {
         int m0, n0;
@@ -531,8 +539,19 @@ cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int n_tiles = ((p.T + kBM - 1) / kBM) * ((p.d_out + bn - 1) / bn);
   const int grid = n_tiles < sms ? n_tiles : sms;
-  fc_gemm_kernel<<<grid, kFcThreads, smem, s>>>(p, map_x, map_w, bn);
-  return cudaGetLastError();
+  // A programmatic dependent of the normalisation grid: its prologue (barrier
+  // set-up, TMEM allocation) overlaps that grid's tail; its loads wait.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kFcThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fc_gemm_kernel, p, map_x, map_w, bn);
 }
 
 }  // namespace sv
