@@ -188,6 +188,17 @@ def test_shapes_mixed_temperatures(B, N, V, dtype):
     check(wl)
 
 
+@pytest.mark.parametrize("B,N,V,dtype", [(3, 2, 300000, "bf16"), (2, 3, 270000, "f32")])
+def test_more_than_32_level1_blocks(B, N, V, dtype):
+    """37 (bf16) and 33 (fp32) level-1 blocks of 8192 tokens: the last
+    sampler CTA picks level 1 over more than 32 masses (the tiled pass of the
+    warp pick) and fetches the chosen block's candidate by index; sampled
+    requests only, three verify seeds each."""
+    wl = workloads.make_random(B, N, V, dtype, gen_seed=V % 1000 + B, verify_seed=V, temps=(0.7, 1.0))
+    for seed in range(3):
+        check(wl, seed=seed, stats=(seed == 0))
+
+
 def test_max_drafts():
     wl = workloads.make_random(3, 255, 96, "f32", gen_seed=5, temps=(0.0, 1.0, 2.0), sigma=(0.0, 0.05))
     check(wl)
