@@ -14,20 +14,22 @@
 // commit would pass S, read outside the window, or whose kept positions do
 // not rise is left unchanged and flagged.
 //
-// kv_commit_kernel: at most kKvCtasPerSm CTAs per SM take the (layer,
-// sequence) entries in turn; one thread per 16-byte column copies the kept
-// positions eight at a time (eight loads in flight per thread) -- a plain
-// bandwidth-bound copy with coalesced 16-byte accesses (consecutive
-// threads, consecutive columns).  kv_advance_kernel
+// kv_commit_kernel: a grid of at most kKvCtasPerSm CTAs per SM (40
+// registers, six resident per SM) takes the (layer, sequence) entries in
+// turn; one thread per 16-byte column copies the kept positions four at a
+// time (four loads in flight per thread) -- a plain bandwidth-bound copy
+// with coalesced 16-byte accesses (consecutive threads, consecutive
+// columns).  kv_advance_kernel
 // then moves the lengths: a second grid, launched with programmatic
 // dependent launch so that it is resident while the copy drains, whose
 // griddepcontrol.wait returns only once the copy grid has completed and its
 // writes are visible -- so no CTA of the copy can read a length already
 // advanced.  The copy is itself a programmatic dependent of the grid before
 // it and waits for that grid the same way.  (Measured per commit of 32
-// layers x 64 sequences x 4 KB: 14.73 us with 8 CTAs per SM, 16.96 with 4,
-// 15.40 with one CTA per entry; a CTA per sequence and group of four layers
-// 18.1 us; one launch whose last CTA advances the lengths 16.9 us.)
+// layers x 64 sequences x 4 KB: 13.44 us as built; eight entries per batch
+// at 74 registers, 3 CTAs per SM: 14.73 us; four per batch at 32 registers:
+// 14.58 us; a CTA per sequence and group of four layers 18.1 us; one launch
+// whose last CTA advances the lengths 16.9 us.)
 
 #include <cstdint>
 
@@ -37,11 +39,20 @@ namespace sv {
 namespace {
 
 constexpr int kKvThreads = 256;
-constexpr int kKvBatch = 8;
+// Kept entries copied per batch (loads in flight per thread), and resident
+// CTAs per SM the copy kernel is built for; build-time overrides
+// -DSV_KV_BATCH=<n>, -DSV_KV_MINB=<n>.
+#ifndef SV_KV_BATCH
+#define SV_KV_BATCH 4
+#endif
+#ifndef SV_KV_MINB
+#define SV_KV_MINB 6
+#endif
+constexpr int kKvBatch = SV_KV_BATCH;
 // CTAs per SM of the copy grid (more items than that are taken in turn);
 // build-time override -DSV_KV_CTAS_PER_SM=<n>.
 #ifndef SV_KV_CTAS_PER_SM
-#define SV_KV_CTAS_PER_SM 8
+#define SV_KV_CTAS_PER_SM 12
 #endif
 constexpr int kKvCtasPerSm = SV_KV_CTAS_PER_SM;
 
@@ -116,7 +127,7 @@ __device__ __forceinline__ void commit_item(const KvProblem& p, long long item, 
 // The copy grid: at most kKvCtasPerSm CTAs per SM, each taking the
 // (layer, sequence, column slice) items in turn.
 template <bool kScratch>
-__global__ void __launch_bounds__(kKvThreads) kv_commit_kernel(KvProblem p) {
+__global__ void __launch_bounds__(kKvThreads, SV_KV_MINB) kv_commit_kernel(KvProblem p) {
   // Launched as a programmatic dependent of whatever precedes it: wait for
   // that grid (it may be the verify step writing kv_len, or the previous
   // commit's length update) before reading anything.
