@@ -88,41 +88,47 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// One warp per (token, segment) row of d elements, the row held in
-// registers: lane l keeps 16-byte vectors l, l + 32, ... (kVpl of them at
-// most, d <= 256 kVpl), so the row is read from global memory once, the
-// mean and the variance come from the registers (two passes, fp32, the
-// same order of additions as a loop over the vectors), and the normalised
-// row is written once.  Rows longer than 256 kVpl take the loop form below.
-template <int kVpl>
-__device__ __forceinline__ void prep_row_regs(const FcNormProblem& p, const __nv_bfloat16* h,
-                                              __nv_bfloat16* x, const float* g, const float* bt, int lane) {
+// Two warps per (token, segment) row of d <= 4096 elements, the row held in
+// registers: warp half h of the row keeps, in lane l, the 16-byte vectors
+// 256 h + l + 32 i (i < kPrepVpl), so the row is read from global memory
+// once; each warp sums its half, the two halves' sums meet in shared memory
+// (the same two numbers added in the same order by both warps), then the
+// same for the squared deviations, and each warp writes its half of the
+// normalised row.  Half the registers of a warp per row, so twice the warps
+// hide the loads' latency.  Every thread of the CTA reaches its barriers.
+constexpr int kPrepVpl = 8;           // vectors per lane and warp
+constexpr int kPrepRowsPerCta = 4;    // 8 warps, two per row
+__device__ __forceinline__ void prep_row_split(const FcNormProblem& p, const __nv_bfloat16* h,
+                                               __nv_bfloat16* x, const float* g, const float* bt, bool live,
+                                               int half, int lane, float* s_part) {
   const int nvec = p.d / 8;
-  uint4 v[kVpl];
+  const int wl = threadIdx.x >> 5;
+  uint4 v[kPrepVpl];
 #pragma unroll
-  for (int i = 0; i < kVpl; ++i) {
-    const int q = lane + 32 * i;
-    v[i] = q < nvec ? *reinterpret_cast<const uint4*>(h + 8 * q) : make_uint4(0u, 0u, 0u, 0u);
+  for (int i = 0; i < kPrepVpl; ++i) {
+    const int q = 256 * half + lane + 32 * i;
+    v[i] = (live && q < nvec) ? *reinterpret_cast<const uint4*>(h + 8 * q) : make_uint4(0u, 0u, 0u, 0u);
   }
   float mu = 0.f, rstd = 1.f;
   if (p.norm != kNormNone) {
     if (p.norm == kNormLayer) {
       float sum = 0.f;
 #pragma unroll
-      for (int i = 0; i < kVpl; ++i) {
-        if (lane + 32 * i < nvec) {
+      for (int i = 0; i < kPrepVpl; ++i) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) sum += Elem<__nv_bfloat16>::get(v[i], e);
-        }
+        for (int e = 0; e < 8; ++e) sum += Elem<__nv_bfloat16>::get(v[i], e);  // zeros past the row
       }
 #pragma unroll
       for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-      mu = sum / static_cast<float>(p.d);
+      if (lane == 0) s_part[wl] = sum;
+      __syncthreads();
+      mu = (s_part[wl & ~1] + s_part[wl | 1]) / static_cast<float>(p.d);
+      __syncthreads();  // both warps of the pair have read s_part
     }
     float sq = 0.f;
 #pragma unroll
-    for (int i = 0; i < kVpl; ++i) {
-      if (lane + 32 * i < nvec) {
+    for (int i = 0; i < kPrepVpl; ++i) {
+      if (256 * half + lane + 32 * i < nvec) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float y = Elem<__nv_bfloat16>::get(v[i], e) - mu;
@@ -132,11 +138,14 @@ __device__ __forceinline__ void prep_row_regs(const FcNormProblem& p, const __nv
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(kFull, sq, o);
-    rstd = rsqrtf(sq / static_cast<float>(p.d) + p.eps);
+    if (lane == 0) s_part[wl] = sq;
+    __syncthreads();
+    rstd = rsqrtf((s_part[wl & ~1] + s_part[wl | 1]) / static_cast<float>(p.d) + p.eps);
   }
+  if (!live) return;
 #pragma unroll
-  for (int i = 0; i < kVpl; ++i) {
-    const int q = lane + 32 * i;
+  for (int i = 0; i < kPrepVpl; ++i) {
+    const int q = 256 * half + lane + 32 * i;
     if (q >= nvec) continue;
     uint4 o = v[i];
     if (p.norm != kNormNone) {
@@ -213,14 +222,31 @@ __device__ __forceinline__ void prep_row_loop(const FcNormProblem& p, const __nv
   }
 }
 
-constexpr int kPrepVpl = 16;  // rows up to 4096 elements stay in registers
-// Resident CTAs per SM the normalisation kernel is built for.
+// Resident CTAs per SM the normalisation kernels are built for.
 #ifndef SV_PREP_MINB
-#define SV_PREP_MINB 2
+#define SV_PREP_MINB 4
 #endif
 
-__global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_kernel(FcNormProblem p) {
+// Rows of at most 4096 elements (and 16-byte aligned gamma / beta): two
+// warps per row, four rows per CTA.
+__global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_split_kernel(FcNormProblem p) {
   allow_dependents();  // the GEMM's CTAs may be scheduled as this grid drains
+  __shared__ float s_part[8];
+  const int wl = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kPrepRowsPerCta + (wl >> 1);
+  const bool live = row < p.T * 3;
+  const int t = live ? row / 3 : 0, s = live ? row - t * 3 : 0;
+  const int d = p.d;
+  const __nv_bfloat16* h = (s == 0 ? p.h[0] : s == 1 ? p.h[1] : p.h[2]) + static_cast<size_t>(t) * d;
+  __nv_bfloat16* x = p.x + static_cast<size_t>(t) * 3 * d + static_cast<size_t>(s) * d;
+  const float* g = p.norm != kNormNone ? p.gamma + static_cast<size_t>(s) * d : nullptr;
+  const float* bt = p.beta != nullptr ? p.beta + static_cast<size_t>(s) * d : nullptr;
+  prep_row_split(p, h, x, g, bt, live, wl & 1, lane, s_part);
+}
+
+// Any other row: one warp per row, three passes.
+__global__ void __launch_bounds__(256) fcnorm_prep_kernel(FcNormProblem p) {
+  allow_dependents();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= p.T * 3) return;
@@ -230,10 +256,7 @@ __global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_kernel(FcNormPr
   __nv_bfloat16* x = p.x + static_cast<size_t>(t) * 3 * d + static_cast<size_t>(s) * d;
   const float* g = p.norm != kNormNone ? p.gamma + static_cast<size_t>(s) * d : nullptr;
   const float* bt = p.beta != nullptr ? p.beta + static_cast<size_t>(s) * d : nullptr;
-  if (d <= 256 * kPrepVpl && p.gb_vec)
-    prep_row_regs<kPrepVpl>(p, h, x, g, bt, lane);
-  else
-    prep_row_loop(p, h, x, g, bt, lane);
+  prep_row_loop(p, h, x, g, bt, lane);
 }
 
 // --------------------------------------------------------------- the GEMM
@@ -522,8 +545,11 @@ int tile_width(int T, int d_out, int sms) {
 
 cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s) {
   if (p.T <= 0 || p.d_out <= 0) return cudaSuccess;
-  const int warps = p.T * 3;
-  fcnorm_prep_kernel<<<(warps * 32 + 255) / 256, 256, 0, s>>>(p);
+  const int rows = p.T * 3;
+  if (p.d <= 2 * 256 * kPrepVpl && p.gb_vec)
+    fcnorm_prep_split_kernel<<<(rows + kPrepRowsPerCta - 1) / kPrepRowsPerCta, 256, 0, s>>>(p);
+  else
+    fcnorm_prep_kernel<<<(rows * 32 + 255) / 256, 256, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
