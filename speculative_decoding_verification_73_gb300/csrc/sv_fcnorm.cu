@@ -96,17 +96,34 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // same for the squared deviations, and each warp writes its half of the
 // normalised row.  Half the registers of a warp per row, so twice the warps
 // hide the loads' latency.  Every thread of the CTA reaches its barriers.
-constexpr int kPrepVpl = 8;           // vectors per lane and warp
-constexpr int kPrepRowsPerCta = 4;    // 8 warps, two per row
+// Build-time override -DSV_PREP_SPLIT=<warps per row> (2 or 4).
+#ifndef SV_PREP_SPLIT
+#define SV_PREP_SPLIT 2
+#endif
+constexpr int kPrepSplit = SV_PREP_SPLIT;          // warps per row
+constexpr int kPrepVpl = 16 / kPrepSplit;          // vectors per lane and warp
+constexpr int kPrepRowsPerCta = 8 / kPrepSplit;    // 8 warps per CTA
+static_assert(kPrepSplit == 2 || kPrepSplit == 4, "a row split over 2 or 4 warps");
+// The row's total of one per-warp partial each, in warp order (the same
+// additions in every warp of the row).
+__device__ __forceinline__ float row_total(const float* s_part, int wl) {
+  const int first = wl - wl % kPrepSplit;
+  float t = s_part[first];
+#pragma unroll
+  for (int k = 1; k < kPrepSplit; ++k) t += s_part[first + k];
+  return t;
+}
+
 __device__ __forceinline__ void prep_row_split(const FcNormProblem& p, const __nv_bfloat16* h,
                                                __nv_bfloat16* x, const float* g, const float* bt, bool live,
                                                int half, int lane, float* s_part) {
+  constexpr int kSpan = 32 * kPrepVpl;  // vectors of the row per warp
   const int nvec = p.d / 8;
   const int wl = threadIdx.x >> 5;
   uint4 v[kPrepVpl];
 #pragma unroll
   for (int i = 0; i < kPrepVpl; ++i) {
-    const int q = 256 * half + lane + 32 * i;
+    const int q = kSpan * half + lane + 32 * i;
     v[i] = (live && q < nvec) ? *reinterpret_cast<const uint4*>(h + 8 * q) : make_uint4(0u, 0u, 0u, 0u);
   }
   float mu = 0.f, rstd = 1.f;
@@ -122,13 +139,13 @@ __device__ __forceinline__ void prep_row_split(const FcNormProblem& p, const __n
       for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
       if (lane == 0) s_part[wl] = sum;
       __syncthreads();
-      mu = (s_part[wl & ~1] + s_part[wl | 1]) / static_cast<float>(p.d);
-      __syncthreads();  // both warps of the pair have read s_part
+      mu = row_total(s_part, wl) / static_cast<float>(p.d);
+      __syncthreads();  // every warp of the row has read s_part
     }
     float sq = 0.f;
 #pragma unroll
     for (int i = 0; i < kPrepVpl; ++i) {
-      if (256 * half + lane + 32 * i < nvec) {
+      if (kSpan * half + lane + 32 * i < nvec) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float y = Elem<__nv_bfloat16>::get(v[i], e) - mu;
@@ -140,12 +157,12 @@ __device__ __forceinline__ void prep_row_split(const FcNormProblem& p, const __n
     for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(kFull, sq, o);
     if (lane == 0) s_part[wl] = sq;
     __syncthreads();
-    rstd = rsqrtf((s_part[wl & ~1] + s_part[wl | 1]) / static_cast<float>(p.d) + p.eps);
+    rstd = rsqrtf(row_total(s_part, wl) / static_cast<float>(p.d) + p.eps);
   }
   if (!live) return;
 #pragma unroll
   for (int i = 0; i < kPrepVpl; ++i) {
-    const int q = 256 * half + lane + 32 * i;
+    const int q = kSpan * half + lane + 32 * i;
     if (q >= nvec) continue;
     uint4 o = v[i];
     if (p.norm != kNormNone) {
@@ -233,7 +250,7 @@ __global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_split_kernel(Fc
   allow_dependents();  // the GEMM's CTAs may be scheduled as this grid drains
   __shared__ float s_part[8];
   const int wl = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kPrepRowsPerCta + (wl >> 1);
+  const int row = blockIdx.x * kPrepRowsPerCta + wl / kPrepSplit;
   const bool live = row < p.T * 3;
   const int t = live ? row / 3 : 0, s = live ? row - t * 3 : 0;
   const int d = p.d;
@@ -241,7 +258,7 @@ __global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_split_kernel(Fc
   __nv_bfloat16* x = p.x + static_cast<size_t>(t) * 3 * d + static_cast<size_t>(s) * d;
   const float* g = p.norm != kNormNone ? p.gamma + static_cast<size_t>(s) * d : nullptr;
   const float* bt = p.beta != nullptr ? p.beta + static_cast<size_t>(s) * d : nullptr;
-  prep_row_split(p, h, x, g, bt, live, wl & 1, lane, s_part);
+  prep_row_split(p, h, x, g, bt, live, wl % kPrepSplit, lane, s_part);
 }
 
 // Any other row: one warp per row, three passes.
@@ -546,7 +563,7 @@ int tile_width(int T, int d_out, int sms) {
 cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s) {
   if (p.T <= 0 || p.d_out <= 0) return cudaSuccess;
   const int rows = p.T * 3;
-  if (p.d <= 2 * 256 * kPrepVpl && p.gb_vec)
+  if (p.d <= 8 * 32 * kPrepVpl * kPrepSplit && p.gb_vec)
     fcnorm_prep_split_kernel<<<(rows + kPrepRowsPerCta - 1) / kPrepRowsPerCta, 256, 0, s>>>(p);
   else
     fcnorm_prep_kernel<<<(rows * 32 + 255) / 256, 256, 0, s>>>(p);
