@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 
 #include "sv_device.cuh"
+#include "sv_mbar.cuh"
 
 namespace sv {
 namespace {
@@ -49,31 +50,12 @@ constexpr int kAccCols = kBNMax;                // fp32 accumulator slot: 128 la
 constexpr int kTmemCols = 2 * kAccCols;         // two accumulators
 constexpr int kFcThreads = 192;                 // loads, MMAs, four epilogue warps
 constexpr int kEpiThreads = 128;
-constexpr uint32_t kWaitLimit = 1u << 26;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
 
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
 // K-major, M x N.
 __device__ __forceinline__ uint32_t mma_idesc(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(m >> 4) << 24);
-}
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
 }
 
 // --------------------------------------------------------------- normalisation
@@ -291,19 +273,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
   return d;
 }
 
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
 // 2-D TMA tensor copy of the box at (x, y) (x = K element offset, a multiple
 // of 64; y = row) into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -351,7 +320,7 @@ __global__ void __launch_bounds__(kFcThreads, 1)
       mbar_init(&sh.acc_empty[a], kEpiThreads);
     }
     sh.abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&sh.tmem)),

@@ -76,16 +76,121 @@ __device__ Partial chunk_partial_scalar(const T* row, int beg, int end, bool gre
 // ------------------------------------------------------------------ online
 
 // One CTA reduces one span of kSpanBytes of a row in a single pass: thread t
-// reads 16-byte vectors t, t + kThreads, ... of the span in groups of kGroup,
-// the next group's loads issued before the current group is reduced, and
-// keeps a running maximum with its sum rescaled whenever the maximum grows
-// (or, for a greedy row, the running maximum and its lowest index).  The
-// threads' states are merged once at the end.  kFull: the span is complete,
-// so no vector needs a bounds check.  Exponent arguments and sums use the
-// paired float instructions, two elements per instruction.
-// kSmem: `row` + beg points to a copy of the span staged in shared memory
-// (plain loads) instead of global memory (streaming loads); the arithmetic
-// is the same either way.
+// reads 16-byte vectors t, t + kThreads, ... of the span in groups of kGroup
+// and keeps a running maximum with its sum rescaled whenever the maximum
+// grows (or, for a greedy row, the running maximum and its lowest index).
+// The threads' states are merged once at the end.  Exponent arguments and
+// sums use the paired float instructions, two elements per instruction.
+// The per-thread state, the per-group update and the final merge are
+// written out separately below, so that the order of operations that every
+// span partial depends on reads in one place.
+
+struct SpanAcc {
+  float m;      // running maximum (raw logits)
+  float c;      // fl(m k), the exponent reference of the sum
+  uint64_t s2;  // sum of 2^(x k - c), two lanes
+  bool bad;     // a NaN / +inf / out-of-range maximum was seen
+  int idx;      // greedy: lowest index holding m
+};
+
+__device__ __forceinline__ SpanAcc span_acc_init() {
+  SpanAcc a;
+  a.m = -INFINITY;
+  a.c = -INFINITY;
+  a.s2 = f2pack(0.f, 0.f);
+  a.bad = false;
+  a.idx = INT_MAX;
+  return a;
+}
+
+// Fold group gi of this thread's vectors (vector i of the group is span
+// vector threadIdx.x + (gi kGroup + i) kThreads) into the state.  A vector
+// past the span's end must hold -inf words.  The thread whose vector holds
+// the draft token d stores its logit at *tok_out.
+template <typename T, bool kGreedy, bool kFull>
+__device__ __forceinline__ void span_group(SpanAcc& a, const uint4 (&g)[kGroup], int beg, int end, int gi,
+                                           uint64_t k2, float k, int d, float* tok_out) {
+  using E = Elem<T>;
+  constexpr int kVec = E::kVec;
+  if (!kGreedy) {
+#pragma unroll
+    for (int u = 0; u < kGroup; ++u) {
+      const int e0 = beg + (static_cast<int>(threadIdx.x) + (gi * kGroup + u) * kThreads) * kVec;
+      if (d >= e0 && d < e0 + kVec && (kFull || d < end)) *tok_out = E::get(g[u], d - e0);
+    }
+  }
+  float gm = E::vmax_nan(g[0]);
+#pragma unroll
+  for (int u = 1; u < kGroup; ++u) gm = fmax_nan(gm, E::vmax_nan(g[u]));
+  if (gm != gm) a.bad = true;
+  if (kGreedy) {
+    if (gm > a.m) {  // strict: an equal value later in the row keeps the earlier index
+      a.m = gm;
+      a.idx = INT_MAX;
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) {
+          if (a.idx == INT_MAX && E::get(g[u], e) == gm)
+            a.idx = beg + (static_cast<int>(threadIdx.x) + (gi * kGroup + u) * kThreads) * kVec + e;
+        }
+      }
+    }
+  } else {
+    if (gm > a.m) {
+      const float cn = gm * k;
+      if (gm == INFINITY || !(fabsf(cn) <= 3.40282347e38f)) a.bad = true;
+      const float r = a.c > -INFINITY ? ex2(a.c - cn) : 0.f;
+      a.s2 = f2mul(a.s2, f2pack(r, r));
+      a.c = cn;
+      a.m = gm;
+    }
+    if (a.m > -INFINITY && !a.bad) {
+      const uint64_t nc2 = f2pack(-a.c, -a.c);
+#pragma unroll
+      for (int u = 0; u < kGroup; ++u) {
+#pragma unroll
+        for (int e = 0; e < E::kPairs; ++e) {
+          float a0, a1;
+          f2unpack(f2fma(E::pair(g[u], e), k2, nc2), a0, a1);
+          a.s2 = f2add(a.s2, f2pack(ex2(a0), ex2(a1)));
+        }
+      }
+    }
+  }
+}
+
+// Merge the threads' states into the span's partial (every thread of the
+// CTA gets it).  red_f, red_g, red_i: kThreads/32 slots each.
+template <bool kGreedy>
+__device__ __forceinline__ Partial span_finish(const SpanAcc& a, float* red_f, float* red_g, int* red_i) {
+  Partial out;
+  out.tag = 0;
+  if (kGreedy) {
+    const float best = block_max_nan(a.bad ? __int_as_float(0x7fc00000) : a.m, red_f);
+    out.idx = block_min_int(a.m == best ? a.idx : INT_MAX, red_i);
+    out.a = best;
+    out.s = (best != best) ? __int_as_float(0x7fc00000) : 0.f;
+  } else {
+    float s_lo, s_hi;
+    f2unpack(a.s2, s_lo, s_hi);
+    const float s = s_lo + s_hi;
+    // merge (c, s) over the CTA; any bad thread makes the span bad
+    const float cmax = block_max_nan(a.bad ? __int_as_float(0x7fc00000) : a.c, red_f);
+    float part = 0.f;
+    if (cmax == cmax && cmax > -INFINITY && a.c > -INFINITY) part = s * ex2(a.c - cmax);
+    const float tot = block_sum(part, red_g);
+    out.a = cmax;
+    out.s = (cmax != cmax) ? __int_as_float(0x7fc00000) : (cmax > -INFINITY ? tot : 0.f);
+    out.idx = 0;
+  }
+  return out;
+}
+
+// The span [beg, end) of a row, read from global memory (the next group's
+// loads issued before the current group is reduced) or, kSmem, from a copy
+// staged in shared memory at `row` + beg (plain loads).  kFull: the span is
+// complete, so no vector needs a bounds check.
 template <typename T, bool kGreedy, bool kFull, bool kSmem = false>
 __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int end, float k, int d,
                                                     float* tok_out) {
@@ -106,11 +211,7 @@ __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int e
     const int v = threadIdx.x + u * kThreads;
     buf[0][u] = (kFull || v < nv) ? (kSmem ? vp[v] : ld_stream16(vp + v)) : pad;
   }
-  float m = -INFINITY;      // running maximum (raw logits)
-  float c = -INFINITY;      // fl(m k), the exponent reference of the sum
-  uint64_t s2 = f2pack(0.f, 0.f);  // sum of 2^(x k - c), two lanes
-  bool bad = false;         // a NaN / +inf / out-of-range maximum was seen
-  int idx = INT_MAX;        // greedy: lowest index holding m
+  SpanAcc acc = span_acc_init();
   const uint64_t k2 = f2pack(k, k);
 #pragma unroll
   for (int gi = 0; gi < kGroups; ++gi) {
@@ -122,75 +223,9 @@ __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int e
         buf[cur ^ 1][u] = (kFull || v < nv) ? (kSmem ? vp[v] : ld_stream16(vp + v)) : pad;
       }
     }
-    if (!kGreedy) {
-      // the thread whose vector holds the draft token stores its logit
-#pragma unroll
-      for (int u = 0; u < kGroup; ++u) {
-        const int e0 = beg + (threadIdx.x + (gi * kGroup + u) * kThreads) * kVec;
-        if (d >= e0 && d < e0 + kVec && (kFull || d < end)) *tok_out = E::get(buf[cur][u], d - e0);
-      }
-    }
-    float gm = E::vmax_nan(buf[cur][0]);
-#pragma unroll
-    for (int u = 1; u < kGroup; ++u) gm = fmax_nan(gm, E::vmax_nan(buf[cur][u]));
-    if (gm != gm) bad = true;
-    if (kGreedy) {
-      if (gm > m) {  // strict: an equal value later in the row keeps the earlier index
-        m = gm;
-        idx = INT_MAX;
-#pragma unroll
-        for (int u = 0; u < kGroup; ++u) {
-#pragma unroll
-          for (int e = 0; e < kVec; ++e) {
-            if (idx == INT_MAX && E::get(buf[cur][u], e) == gm)
-              idx = beg + (threadIdx.x + (gi * kGroup + u) * kThreads) * kVec + e;
-          }
-        }
-      }
-    } else {
-      if (gm > m) {
-        const float cn = gm * k;
-        if (gm == INFINITY || !(fabsf(cn) <= 3.40282347e38f)) bad = true;
-        const float r = c > -INFINITY ? ex2(c - cn) : 0.f;
-        s2 = f2mul(s2, f2pack(r, r));
-        c = cn;
-        m = gm;
-      }
-      if (m > -INFINITY && !bad) {
-        const uint64_t nc2 = f2pack(-c, -c);
-#pragma unroll
-        for (int u = 0; u < kGroup; ++u) {
-#pragma unroll
-          for (int e = 0; e < E::kPairs; ++e) {
-            float a0, a1;
-            f2unpack(f2fma(E::pair(buf[cur][u], e), k2, nc2), a0, a1);
-            s2 = f2add(s2, f2pack(ex2(a0), ex2(a1)));
-          }
-        }
-      }
-    }
+    span_group<T, kGreedy, kFull>(acc, buf[cur], beg, end, gi, k2, k, d, tok_out);
   }
-  Partial out;
-  out.tag = 0;
-  if (kGreedy) {
-    const float best = block_max_nan(bad ? __int_as_float(0x7fc00000) : m, red_f);
-    out.idx = block_min_int(m == best ? idx : INT_MAX, red_i);
-    out.a = best;
-    out.s = (best != best) ? __int_as_float(0x7fc00000) : 0.f;
-  } else {
-    float s_lo, s_hi;
-    f2unpack(s2, s_lo, s_hi);
-    const float s = s_lo + s_hi;
-    // merge (c, s) over the CTA; any bad thread makes the span bad
-    const float cmax = block_max_nan(bad ? __int_as_float(0x7fc00000) : c, red_f);
-    float part = 0.f;
-    if (cmax == cmax && cmax > -INFINITY && c > -INFINITY) part = s * ex2(c - cmax);
-    const float tot = block_sum(part, red_g);
-    out.a = cmax;
-    out.s = (cmax != cmax) ? __int_as_float(0x7fc00000) : (cmax > -INFINITY ? tot : 0.f);
-    out.idx = 0;
-  }
-  return out;
+  return span_finish<kGreedy>(acc, red_f, red_g, red_i);
 }
 
 }  // namespace
