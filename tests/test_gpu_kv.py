@@ -106,3 +106,68 @@ def test_full_size_commit_32_layers():
     seq = torch.randint(0, S - W, (B,), generator=torch.Generator().manual_seed(11), dtype=torch.int32)
     assert _commit_both(ctx, binding.SV_KV_SCRATCH, cache, scratch, seq, kv) == 0
     ctx.close()
+
+
+def _commit_chain(ctx, mode, cache, scratch_list, seq, kv_list, path_list=None):
+    """Several commits back to back on one context (no host sync between
+    them), against the oracle applied in the same order."""
+    want, want_len = cache.numpy().copy(), seq.numpy().copy()
+    d_cache, d_seq = cache.cuda(), seq.cuda()
+    for i, kv in enumerate(kv_list):
+        scratch = None if scratch_list is None else scratch_list[i]
+        path = None if path_list is None else path_list[i]
+        want, want_len, _ = okv.commit(mode, want, want_len, kv.numpy(),
+                                       scratch=None if scratch is None else scratch.numpy(),
+                                       path=None if path is None else path.numpy())
+        binding.spec_verify_kv_commit(ctx.ctx, mode, d_cache, d_seq, kv.cuda(),
+                                      scratch=None if scratch is None else scratch.cuda(),
+                                      path=None if path is None else path.cuda())
+    code, bits = ctx.get_error()
+    assert bits == 0, bits
+    np.testing.assert_array_equal(d_seq.cpu().numpy(), want_len)
+    np.testing.assert_array_equal(d_cache.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("E", [48, 8192], ids=["one-slice", "two-slices"])
+def test_back_to_back_commits_advance_each_length_once(E):
+    """Four commits issued back to back (no host sync): each one's lengths
+    move exactly once, after every layer's copy has read them; entries of
+    one column slice and of two 4 KB slices."""
+    ctx = binding.SpecVerify(8, 4, 64, torch.float32)
+    L, B, S, W = 3, 5, 40, 5
+    cache = _bytes((L, B, S, E), 21)
+    g = torch.Generator().manual_seed(22)
+    scratch = [_bytes((L, B, W, E), 23 + i) for i in range(4)]
+    kv = [torch.randint(0, W + 1, (B,), generator=g, dtype=torch.int32) for _ in range(4)]
+    seq = torch.randint(0, 8, (B,), generator=g, dtype=torch.int32)
+    _commit_chain(ctx, binding.SV_KV_SCRATCH, cache, scratch, seq, kv)
+    ctx.close()
+
+
+def test_back_to_back_in_place_commits_between_verify_calls():
+    """In-place commits driven by tree paths, with verify calls on the same
+    context in between (the calls share the context's sequence numbers)."""
+    B, M, V = 4, 6, 96
+    ctx = binding.SpecVerify(B, M, V, torch.float32)
+    L, S, E = 2, 48, 32
+    cache = _bytes((L, B, S, E), 31)
+    seq = torch.tensor([0, 5, 9, 2], dtype=torch.int32)
+    g = torch.Generator().manual_seed(32)
+    want, want_len = cache.numpy().copy(), seq.numpy().copy()
+    d_cache, d_seq = cache.cuda(), seq.cuda()
+    z = torch.randn(B, M + 1, V, generator=g).cuda()
+    tok = torch.randint(0, V, (B, M), generator=g, dtype=torch.int32).cuda()
+    temp = torch.ones(B).cuda()
+    for i in range(3):
+        ctx(z, z[:, :M].contiguous(), tok, temp, i)  # a chain verify in between
+        path = torch.tensor([[1, 3, -1, -1, -1, -1], [2, -1, -1, -1, -1, -1],
+                             [1, 2, 4, -1, -1, -1], [-1] * 6], dtype=torch.int32)
+        kv = torch.tensor([3, 2, 4, 1], dtype=torch.int32)
+        want, want_len, err = okv.commit(binding.SV_KV_INPLACE, want, want_len, kv.numpy(), path=path.numpy())
+        assert err == 0
+        binding.spec_verify_kv_commit(ctx.ctx, binding.SV_KV_INPLACE, d_cache, d_seq, kv.cuda(), path=path.cuda())
+    code, bits = ctx.get_error()
+    assert bits == 0, bits
+    np.testing.assert_array_equal(d_seq.cpu().numpy(), want_len)
+    np.testing.assert_array_equal(d_cache.cpu().numpy(), want)
+    ctx.close()
