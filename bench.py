@@ -1066,7 +1066,10 @@ def bf16_peak():
         return 1900.0, "fallback"
 
 
-def fcnorm_setup(dev, stream, rank=0):
+def fcnorm_setup(dev, stream, rank=0, norm="layernorm"):
+    """FC-norm at T = d = d_out = 4096; norm "layernorm" (the workload the
+    row is measured on) or "none" (EAGLE-3's plain concatenation: the GEMM
+    reads the hidden states directly)."""
     import torch
     from speculative_decoding_verification_73_gb300 import binding, workloads
     T, d, d_out = 4096, 4096, 4096
@@ -1077,34 +1080,44 @@ def fcnorm_setup(dev, stream, rank=0):
     xbuf = torch.empty(T, 3 * d, dtype=torch.bfloat16, device=dev)
     sv = binding.SpecVerify(1, 1, 16, torch.float32, stream=stream, device=dev)
 
+    layer = norm == "layernorm"
+
     def step(i=0):
-        binding.spec_verify_fc_norm(sv.ctx, binding.SV_NORM_LAYER, *h, w, gamma=g, beta=b, bias=bias,
+        binding.spec_verify_fc_norm(sv.ctx, binding.SV_NORM_LAYER if layer else binding.SV_NORM_NONE, *h, w,
+                                    gamma=g if layer else None, beta=b if layer else None, bias=bias,
                                     out=out, xbuf=xbuf)
 
-    return sv, step, 2.0 * T * 3 * d * d_out, {"T": T, "d": d, "d_out": d_out, "norm": "layernorm"}
+    return sv, step, 2.0 * T * 3 * d * d_out, {"T": T, "d": d, "d_out": d_out, "norm": norm}
 
 
 def fcnorm_summary(dev, stream, steps=30, warmup=3):
     import torch
     from speculative_decoding_verification_73_gb300 import binding
-    sv, step, flops, shape = fcnorm_setup(dev, stream)
-    for _ in range(warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    us = ev0.elapsed_time(ev1) / steps * 1e3
-    code, _ = sv.get_error()
-    assert code == 0, binding.strerror(code)
-    sv.close()
     peak, kind = bf16_peak()
-    tf = flops / (us * 1e-6) / 1e12
-    return dict(workload=FC_WORKLOAD, us_per_call=us, steps=steps, flops_per_call=flops, tflops=tf,
-                tensor_frac=tf / peak, peak_kind=f"{kind} cuBLAS bf16 burst", **shape)
+    res = {}
+    for norm in ("layernorm", "none"):
+        sv, step, flops, shape = fcnorm_setup(dev, stream, norm=norm)
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        us = ev0.elapsed_time(ev1) / steps * 1e3
+        code, _ = sv.get_error()
+        assert code == 0, binding.strerror(code)
+        sv.close()
+        tf = flops / (us * 1e-6) / 1e12
+        if norm == "layernorm":
+            res = dict(workload=FC_WORKLOAD, us_per_call=us, steps=steps, flops_per_call=flops, tflops=tf,
+                       tensor_frac=tf / peak, peak_kind=f"{kind} cuBLAS bf16 burst", **shape)
+        else:
+            res["norm_none"] = dict(us_per_call=us, tflops=tf, tensor_frac=tf / peak,
+                                    launches=1, note="the GEMM alone, reading the three hidden states")
+    return res
 
 
 def run_fcnorm(args):

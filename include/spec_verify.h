@@ -325,13 +325,16 @@ int spec_verify_kv_commit(spec_verify_ctx* ctx, int mode, int L, int B, int S, i
  *   bias          [d_out] float32 or NULL
  *   out           [T, d_out] bfloat16 (caller-owned)
  *   xbuf          [T, 3 d] bfloat16 scratch (caller-owned, 16-byte aligned):
- *                 receives the normalised, concatenated input
+ *                 for LayerNorm / RMSNorm it receives the normalised,
+ *                 concatenated input, which the GEMM then reads; with
+ *                 SV_NORM_NONE the GEMM reads the hidden states themselves
+ *                 and xbuf is left untouched
  * Statistics in float32; the normalised inputs are rounded to bfloat16 and
  * multiplied on the tensor cores (tcgen05, fp32 accumulation in tensor
- * memory); the output is rounded to bfloat16.  Two kernel launches on the
- * context's stream.  Returns SV_OK, SV_EINVAL (nothing enqueued) or
- * SV_ECUDA; a device wait that ran out is reported by spec_verify_get_error
- * as SV_ETIMEOUT.
+ * memory); the output is rounded to bfloat16.  One kernel launch on the
+ * context's stream for SV_NORM_NONE, two otherwise.  Returns SV_OK,
+ * SV_EINVAL (nothing enqueued) or SV_ECUDA; a device wait that ran out is
+ * reported by spec_verify_get_error as SV_ETIMEOUT.
  */
 #define SV_NORM_NONE  0
 #define SV_NORM_LAYER 1

@@ -4,14 +4,17 @@
 // 3.1": LayerNorm on each of the three target hidden states before the FC;
 // the EAGLE 3.1 news page speaks of RMSNorm; no norm is EAGLE-3).
 //
-// Two kernels.  fcnorm_prep: one warp per (token, segment) computes the
-// row's mean and 1/sqrt(var + eps) (LayerNorm; mean 0 and 1/sqrt(mean
-// square + eps) for RMSNorm) in fp32 and writes the normalised row, rounded
-// to bf16, into its third of the concatenated input X [T, 3d].  fc_gemm: a
-// persistent tcgen05 GEMM out = X W^T + bias, one CTA per SM walking
-// 128 x 256 output tiles, with its warps split by role:
+// fcnorm_prep (LayerNorm / RMSNorm): two warps (one for rows past 4096
+// elements) per (token, segment) compute the row's mean and
+// 1/sqrt(var + eps) (LayerNorm; mean 0 and 1/sqrt(mean square + eps) for
+// RMSNorm) in fp32 and write the normalised row, rounded to bf16, into its
+// third of the concatenated input X [T, 3d].  fc_gemm: a persistent tcgen05
+// GEMM out = X W^T + bias -- with no normalisation it reads the three
+// hidden states themselves, K step kb from the state kb / (d / 64), and
+// nothing runs before it -- one CTA per SM walking 128 x bn output tiles
+// (bn <= 256), with its warps split by role:
 //   * warp 0 (one lane) loads: for each K step of 64 it waits until the
-//     stage is free, then fetches the 128 x 64 tile of X and the 256 x 64
+//     stage is free, then fetches the 128 x 64 input tile and the bn x 64
 //     tile of W with two TMA tensor copies (cp.async.bulk.tensor, 128-byte
 //     swizzle) completing on the stage's "full" barrier;
 //   * warp 1 (one lane) multiplies: for each K step it waits for the stage,
@@ -50,6 +53,9 @@ constexpr int kAccCols = kBNMax;                // fp32 accumulator slot: 128 la
 constexpr int kTmemCols = 2 * kAccCols;         // two accumulators
 constexpr int kFcThreads = 192;                 // loads, MMAs, four epilogue warps
 constexpr int kEpiThreads = 128;
+// Where the GEMM's input tiles come from.
+constexpr int kGemmX = 0;       // X [T, 3d], written by the normalisation grid before
+constexpr int kGemmDirect = 1;  // the three hidden states themselves (no normalisation)
 
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
 // K-major, M x N.
@@ -65,10 +71,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-// Widened bf16 pair of a 32-bit word (element 2i of the 16 bytes is the
-// low half of word i).
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // Two warps per (token, segment) row of d <= 4096 elements, the row held in
 // registers: warp half h of the row keeps, in lane l, the 16-byte vectors
@@ -296,8 +298,12 @@ struct GemmShared {
   int abort;
 };
 
+// map_a0..2: the input tiles -- X (kGemmX: map_a0 only, K = 3d) or the
+// three hidden states [T, d] (K step kb of segment kb / (d / 64)).
+template <int kMode>
 __global__ void __launch_bounds__(kFcThreads, 1)
-    fc_gemm_kernel(FcNormProblem p, const __grid_constant__ CUtensorMap map_x,
+    fc_gemm_kernel(FcNormProblem p, const __grid_constant__ CUtensorMap map_a0,
+                   const __grid_constant__ CUtensorMap map_a1, const __grid_constant__ CUtensorMap map_a2,
                    const __grid_constant__ CUtensorMap map_w, int bn) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // stages 1024-byte aligned (the swizzle atom); the runtime guarantees 16
@@ -310,6 +316,7 @@ __global__ void __launch_bounds__(kFcThreads, 1)
   const int n_tiles_n = (p.d_out + bn - 1) / bn;
   const int n_tiles = ((p.T + kBM - 1) / kBM) * n_tiles_n;
 
+  const int kps = p.d / kBK;  // K steps per hidden state
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sh.full[s], 1);
@@ -337,10 +344,15 @@ __global__ void __launch_bounds__(kFcThreads, 1)
   if (warp == 0) {
     // ---------------- loads
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_x)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a0)) : "memory");
+      if (kMode != kGemmX) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a1)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_a2)) : "memory");
+      }
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&map_w)) : "memory");
-      // X is written by the normalisation grid before this one (this grid
-      // is its programmatic dependent): wait for it before the first load
+      // kGemmX: X is written by the normalisation grid before this one (this
+      // grid is its programmatic dependent): wait for it before the first
+      // load.  (kGemmDirect is launched plainly: this returns at once.)
       wait_for_prerequisite();
       uint32_t it = 0;
       for (int t = blockIdx.x; t < n_tiles && !*abort; t += gridDim.x) {
@@ -354,8 +366,11 @@ __global__ void __launch_bounds__(kFcThreads, 1)
             break;
           }
           unsigned char* st = smem + s * kStageBytes;
+          const int seg = kMode == kGemmX ? 0 : kb / kps;
+          const int xa = kMode == kGemmX ? kb * kBK : (kb - seg * kps) * kBK;
+          const CUtensorMap* ma = seg == 0 ? &map_a0 : seg == 1 ? &map_a1 : &map_a2;
           mbar_expect_tx(&sh.full[s], kABytes + bn * kBK * 2);
-          tma_load_2d(st, &map_x, kb * kBK, m0, &sh.full[s]);
+          tma_load_2d(st, ma, xa, m0, &sh.full[s]);
           tma_load_2d(st + kABytes, &map_w, kb * kBK, n0, &sh.full[s]);
         }
       }
@@ -527,27 +542,17 @@ int tile_width(int T, int d_out, int sms) {
   return best;
 }
 
-}  // namespace
+// Build-time switch -DSV_FC_DIRECT=0: SV_NORM_NONE also goes through X.
+#ifndef SV_FC_DIRECT
+#define SV_FC_DIRECT 1
+#endif
 
-cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s) {
-  if (p.T <= 0 || p.d_out <= 0) return cudaSuccess;
-  const int rows = p.T * 3;
-  if (p.d <= 8 * 32 * kPrepVpl * kPrepSplit && p.gb_vec)
-    fcnorm_prep_split_kernel<<<(rows + kPrepRowsPerCta - 1) / kPrepRowsPerCta, 256, 0, s>>>(p);
-  else
-    fcnorm_prep_kernel<<<(rows * 32 + 255) / 256, 256, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
-      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return e;
-  const int bn = tile_width(p.T, p.d_out, sms);
-  CUtensorMap map_x, map_w;
-  if (!make_map(&map_x, p.x, 3 * p.d, p.T, kBM) || !make_map(&map_w, p.w, 3 * p.d, p.d_out, bn))
-    return cudaErrorInvalidValue;
+template <int kMode>
+cudaError_t launch_gemm(const FcNormProblem& p, const CUtensorMap& a0, const CUtensorMap& a1,
+                        const CUtensorMap& a2, const CUtensorMap& w, int bn, int sms, bool dependent,
+                        cudaStream_t s) {
   const int smem = kStages * kStageBytes + 1024;  // + room to align the stages to 1024 bytes
-  e = cudaFuncSetAttribute(fc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(fc_gemm_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int n_tiles = ((p.T + kBM - 1) / kBM) * ((p.d_out + bn - 1) / bn);
   const int grid = n_tiles < sms ? n_tiles : sms;
@@ -562,8 +567,41 @@ cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s) {
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fc_gemm_kernel, p, map_x, map_w, bn);
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, fc_gemm_kernel<kMode>, p, a0, a1, a2, w, bn);
+}
+
+}  // namespace
+
+// SV_NORM_NONE: kGemmDirect, the GEMM alone, reading the hidden states.
+// LayerNorm / RMSNorm: the normalisation grid writes X, then kGemmX.
+cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s) {
+  if (p.T <= 0 || p.d_out <= 0) return cudaSuccess;
+  const int rows = p.T * 3;
+  const bool direct = SV_FC_DIRECT && p.norm == kNormNone;
+  cudaError_t e;
+  if (!direct) {
+    if (p.d <= 8 * 32 * kPrepVpl * kPrepSplit && p.gb_vec)
+      fcnorm_prep_split_kernel<<<(rows + kPrepRowsPerCta - 1) / kPrepRowsPerCta, 256, 0, s>>>(p);
+    else
+      fcnorm_prep_kernel<<<(rows * 32 + 255) / 256, 256, 0, s>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  const int bn = tile_width(p.T, p.d_out, sms);
+  CUtensorMap a0, a1, a2, w;
+  if (!make_map(&w, p.w, 3 * p.d, p.d_out, bn)) return cudaErrorInvalidValue;
+  if (!direct) {
+    if (!make_map(&a0, p.x, 3 * p.d, p.T, kBM)) return cudaErrorInvalidValue;
+    return launch_gemm<kGemmX>(p, a0, a0, a0, w, bn, sms, true, s);
+  }
+  if (!make_map(&a0, p.h[0], p.d, p.T, kBM) || !make_map(&a1, p.h[1], p.d, p.T, kBM) ||
+      !make_map(&a2, p.h[2], p.d, p.T, kBM))
+    return cudaErrorInvalidValue;
+  return launch_gemm<kGemmDirect>(p, a0, a1, a2, w, bn, sms, false, s);
 }
 
 }  // namespace sv

@@ -25,10 +25,21 @@ def _f64(t):
     return t.to(torch.float64).numpy()
 
 
-def run_case(wl, norm, with_bias=True, with_beta=True, eps=1e-5):
+def _misaligned(t):
+    """A copy of t on the GPU whose data starts 4 bytes past a 16-byte boundary."""
+    flat = torch.empty(t.numel() + 1, dtype=t.dtype, device="cuda")
+    flat[1:] = t.reshape(-1).cuda()
+    view = flat[1:].view(t.shape)
+    assert view.data_ptr() % 16 != 0
+    return view
+
+
+def run_case(wl, norm, with_bias=True, with_beta=True, eps=1e-5, misalign_gamma=False):
     ctx = binding.SpecVerify(1, 1, 16, torch.float32)
     h = [x.cuda() for x in wl.h]
-    gamma = wl.gamma.cuda() if norm != binding.SV_NORM_NONE else None
+    gamma = None
+    if norm != binding.SV_NORM_NONE:
+        gamma = _misaligned(wl.gamma) if misalign_gamma else wl.gamma.cuda()
     beta = wl.beta.cuda() if (norm == binding.SV_NORM_LAYER and with_beta) else None
     bias = wl.bias.cuda() if with_bias else None
     out = binding.spec_verify_fc_norm(ctx.ctx, norm, *h, wl.weight.cuda(), gamma=gamma, beta=beta,
@@ -57,6 +68,8 @@ CASES = [
     ("layer-medium", 512, 1024, 1024, binding.SV_NORM_LAYER, True, True),
     ("layer-wide-row", 33, 4160, 96, binding.SV_NORM_LAYER, True, True),   # rows past the register form
     ("rms-widest-register-row", 40, 4096, 72, binding.SV_NORM_RMS, True, False),
+    ("none-medium", 300, 512, 640, binding.SV_NORM_NONE, True, False),    # 3 x 8 K steps, ragged T
+    ("rms-medium", 257, 1024, 512, binding.SV_NORM_RMS, False, False),
 ]
 
 
@@ -65,6 +78,13 @@ def test_fc_norm_matches_oracle(name, T, d, d_out, norm, bias, beta):
     wl = workloads.make_fcnorm(T, d, d_out, gen_seed=sum(map(ord, name)))
     worst = run_case(wl, norm, bias, beta)
     print(f"{name}: worst error / tolerance {worst:.3f}")
+
+
+def test_gamma_not_16_byte_aligned():
+    """gamma off a 16-byte boundary: the one-warp-per-row normalisation
+    (scalar gamma / beta loads) writes X before the GEMM."""
+    wl = workloads.make_fcnorm(96, 256, 192, gen_seed=77)
+    run_case(wl, binding.SV_NORM_LAYER, True, True, misalign_gamma=True)
 
 
 def test_selector_weights_return_the_normalised_segment():
