@@ -45,10 +45,11 @@ namespace sv {
 namespace {
 
 constexpr int kBM = 128, kBNMax = 256, kBK = 64;  // output tile (kBM x bn, bn <= 256), K step
-constexpr int kStages = 4;
+constexpr int kMaxStages = 8;  // the ring holds as many stages as fit (see gemm_stages)
 constexpr int kABytes = kBM * kBK * 2;          // 16 KB
-constexpr int kBBytes = kBNMax * kBK * 2;       // 32 KB room for the W tile
-constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
+// One stage: the 128 x 64 input tile, then the bn x 64 W tile, rounded up
+// to the 1024-byte swizzle atom (44 KB for bn = 224, 48 KB for 256).
+__host__ __device__ constexpr int stage_bytes(int bn) { return (kABytes + bn * kBK * 2 + 1023) / 1024 * 1024; }
 constexpr int kAccCols = kBNMax;                // fp32 accumulator slot: 128 lanes x 256 columns
 constexpr int kTmemCols = 2 * kAccCols;         // two accumulators
 constexpr int kFcThreads = 192;                 // loads, MMAs, four epilogue warps
@@ -292,7 +293,7 @@ __device__ __forceinline__ void tile_of(int t, int n_tiles_n, int bn, int& m0, i
 }
 
 struct GemmShared {
-  uint64_t full[kStages], empty[kStages];   // stage loaded / stage free
+  uint64_t full[kMaxStages], empty[kMaxStages];  // stage loaded / stage free
   uint64_t acc_full[2], acc_empty[2];       // accumulator ready / drained
   uint32_t tmem;
   int abort;
@@ -304,7 +305,8 @@ template <int kMode>
 __global__ void __launch_bounds__(kFcThreads, 1)
     fc_gemm_kernel(FcNormProblem p, const __grid_constant__ CUtensorMap map_a0,
                    const __grid_constant__ CUtensorMap map_a1, const __grid_constant__ CUtensorMap map_a2,
-                   const __grid_constant__ CUtensorMap map_w, int bn) {
+                   const __grid_constant__ CUtensorMap map_w, int bn, int stages) {
+  const int sbytes = stage_bytes(bn);
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // stages 1024-byte aligned (the swizzle atom); the runtime guarantees 16
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(kFcThreads, 1)
 
   const int kps = p.d / kBK;  // K steps per hidden state
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_init(&sh.full[s], 1);
       mbar_init(&sh.empty[s], 1);
     }
@@ -359,13 +361,13 @@ __global__ void __launch_bounds__(kFcThreads, 1)
         int m0, n0;
         tile_of(t, n_tiles_n, bn, m0, n0);
         for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = static_cast<int>(it % kStages);
-          const uint32_t ph = (it / kStages) & 1u;
+          const int s = static_cast<int>(it % stages);
+          const uint32_t ph = (it / stages) & 1u;
           if (!mbar_wait(smem_u32(&sh.empty[s]), ph ^ 1u)) {
             *abort = 1;
             break;
           }
-          unsigned char* st = smem + s * kStageBytes;
+          unsigned char* st = smem + s * sbytes;
           const int seg = kMode == kGemmX ? 0 : kb / kps;
           const int xa = kMode == kGemmX ? kb * kBK : (kb - seg * kps) * kBK;
           const CUtensorMap* ma = seg == 0 ? &map_a0 : seg == 1 ? &map_a1 : &map_a2;
@@ -376,8 +378,8 @@ __global__ void __launch_bounds__(kFcThreads, 1)
       }
       // copies into this CTA's shared memory must have landed before it
       // can leave: wait (bounded) for the last use of every stage
-      for (uint32_t q = it > kStages ? it - kStages : 0; q < it; ++q)
-        mbar_wait(smem_u32(&sh.full[q % kStages]), (q / kStages) & 1u);
+      for (uint32_t q = it > stages ? it - stages : 0; q < it; ++q)
+        mbar_wait(smem_u32(&sh.full[q % stages]), (q / stages) & 1u);
     }
   } else if (warp == 1) {
     // ---------------- MMAs
@@ -396,14 +398,14 @@ __global__ void __launch_bounds__(kFcThreads, 1)
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t acc = tmem + a * kAccCols;
         for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = static_cast<int>(it % kStages);
-          const uint32_t ph = (it / kStages) & 1u;
+          const int s = static_cast<int>(it % stages);
+          const uint32_t ph = (it / stages) & 1u;
           if (!mbar_wait(smem_u32(&sh.full[s]), ph)) {
             *abort = 1;
             break;
           }
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          const uint32_t sa = smem_u32(smem + s * kStageBytes);
+          const uint32_t sa = smem_u32(smem + s * sbytes);
           const uint64_t da = sw128_desc(sa), db = sw128_desc(sa + kABytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -542,6 +544,19 @@ int tile_width(int T, int d_out, int sms) {
   return best;
 }
 
+// Stages of the ring for tile width bn: as many as fit in max_smem bytes of
+// shared memory with the 1024 bytes of alignment room and the barriers
+// (at most kMaxStages; build-time cap -DSV_FC_STAGES=<n>).
+#ifndef SV_FC_STAGES
+#define SV_FC_STAGES kMaxStages
+#endif
+int gemm_stages(int bn, int max_smem) {
+  const int room = max_smem - 1024 - static_cast<int>(sizeof(GemmShared));
+  const int n = room / stage_bytes(bn);
+  const int cap = SV_FC_STAGES < kMaxStages ? SV_FC_STAGES : kMaxStages;
+  return n < cap ? n : cap;
+}
+
 // Build-time switch -DSV_FC_DIRECT=0: SV_NORM_NONE also goes through X.
 #ifndef SV_FC_DIRECT
 #define SV_FC_DIRECT 1
@@ -551,8 +566,16 @@ template <int kMode>
 cudaError_t launch_gemm(const FcNormProblem& p, const CUtensorMap& a0, const CUtensorMap& a1,
                         const CUtensorMap& a2, const CUtensorMap& w, int bn, int sms, bool dependent,
                         cudaStream_t s) {
-  const int smem = kStages * kStageBytes + 1024;  // + room to align the stages to 1024 bytes
-  cudaError_t e = cudaFuncSetAttribute(fc_gemm_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int dev = 0, max_smem = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+    return e;
+  // as many stages as fit beside the barriers: five of 44 KB for bn = 224
+  const int stages = gemm_stages(bn, max_smem);
+  if (stages < 2) return cudaErrorInvalidValue;
+  const int smem = stages * stage_bytes(bn) + 1024;  // + room to align the stages to 1024 bytes
+  e = cudaFuncSetAttribute(fc_gemm_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int n_tiles = ((p.T + kBM - 1) / kBM) * ((p.d_out + bn - 1) / bn);
   const int grid = n_tiles < sms ? n_tiles : sms;
@@ -568,7 +591,7 @@ cudaError_t launch_gemm(const FcNormProblem& p, const CUtensorMap& a0, const CUt
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, fc_gemm_kernel<kMode>, p, a0, a1, a2, w, bn);
+  return cudaLaunchKernelEx(&cfg, fc_gemm_kernel<kMode>, p, a0, a1, a2, w, bn, stages);
 }
 
 }  // namespace
