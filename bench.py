@@ -22,8 +22,9 @@ On one GPU the line also carries, unless --no-extras:
               every call, and the oracle on each on one thread and on every
               host core;
   rows_f      short measurements of the tree verify (tree222-bf16), the KV
-              commit (32 layers x 64 sequences x 4 KB) and the FC-norm fusion
-              (T = d = d_out = 4096).
+              commit (32 layers x 64 sequences x 4 KB), the FC-norm fusion
+              (T = d = d_out = 4096) and the lazy verify against the eager
+              one (batch64-bf16 and lowaccept64-bf16).
 cpu_baseline is the oracle on the headline workload, on every host core
 (one process per core, one request per task) and on one thread.
 
@@ -590,6 +591,7 @@ def run_ours(args):
             "tree": tree_summary(dev, stream, peak),
             "kv_commit": kv_summary(dev, stream, peak),
             "fc_norm": fcnorm_summary(dev, stream),
+            "lazy": lazy_summary(lib, dev, stream),
         }
     sv.close()
     if host is not None:
@@ -960,6 +962,44 @@ def kv_setup(dev, stream, copies, rank=0):
              "kv_len_sum": int(sum(max(int(n), 0) for n in kv_host)),
              "l2": f"{copies} rotating scratch windows of {L * B * W * E / 1e6:.0f} MB"}
     return sv, step, moved, shape
+
+
+LAZY_WORKLOADS = ("batch64-bf16", "lowaccept64-bf16")
+
+
+def lazy_summary(lib, dev, stream, steps=300, warmup=20):
+    """spec_verify against spec_verify_lazy per step on batch64-bf16 and on
+    lowaccept64-bf16 (drafter far from the target), three rotating input
+    copies; the lazy walk reads rows only up to each request's first
+    rejection, so it pays when few drafts are accepted."""
+    import torch
+    from speculative_decoding_verification_73_gb300 import binding, workloads
+    res = {}
+    for name in LAZY_WORKLOADS:
+        wl = workloads.batch64_bf16() if name == "batch64-bf16" else workloads.low_accept_bf16()
+        B, N, V = wl.shape
+        sv = binding.SpecVerify(B, N, V, torch.bfloat16, stream=stream, device=dev)
+        entry = {}
+        for lazy in (False, True):
+            step, bufs = direct_chain(lib, sv, wl, dev, copies=3, lazy=lazy)
+            for i in range(warmup):
+                step(i)
+            torch.cuda.synchronize(dev)
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for i in range(steps):
+                step(warmup + i)
+            ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            entry["lazy_us_per_step" if lazy else "eager_us_per_step"] = ev0.elapsed_time(ev1) / steps * 1e3
+            entry["mean_accepted"] = float(bufs["out"][1].float().mean())
+            del bufs
+        code, _ = sv.get_error()
+        assert code == 0, binding.strerror(code)
+        sv.close()
+        entry.update(B=B, N=N, V=V, steps=steps)
+        res[name] = entry
+    return res
 
 
 def kv_summary(dev, stream, peak, steps=500, warmup=20):

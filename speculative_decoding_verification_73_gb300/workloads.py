@@ -196,6 +196,15 @@ def batch64_bf16(verify_seed=0, gen_seed=1003):
                      sigma=sig, temperatures=temps, name="batch64-bf16")
 
 
+def low_accept_bf16(verify_seed=0, sigma=3.0):
+    """B=64, N=7, V=128256, bf16, every request at T 1 with draft noise
+    sigma 3 (the drafter far from the target: most requests reject their
+    first draft) -- the regime where reading rows only up to the first
+    rejection pays."""
+    return make_zipf(64, 7, 128256, "bf16", gen_seed=4242, verify_seed=verify_seed, sigma=sigma,
+                     temperatures=1.0, name="lowaccept64-bf16")
+
+
 def mixture_bf16(verify_seed=0):
     """B=16, N=3, V=163840, bf16: half of the 64 target rows peaked (top-1
     mass 0.95 over a Zipf-0.8 base), half flat Zipf-0.8; sigma 0.4; T 1."""

@@ -46,6 +46,7 @@ LAZY_CASES = {
     "random-f32-ragged": lambda: workloads.make_random(12, 5, 3001, "f32", gen_seed=92, verify_seed=2),
     "mixture-bf16": workloads.mixture_bf16,
     "batch64-bf16": workloads.batch64_bf16,
+    "lowaccept64-bf16": workloads.low_accept_bf16,
     "no-drafts": lambda: workloads.make_random(6, 0, 5000, "f32", gen_seed=93),
 }
 
