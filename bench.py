@@ -575,6 +575,10 @@ def run_ours(args):
         "clocks": clk,
     }
     if extras and not lazy:
+        rp = read_stream_peak(dev, stream, bytes_per_launch)
+        line["roofline"]["read_peak"] = rp
+        line["roofline"]["frac_of_read_peak"] = achieved / rp["gb_per_s"]
+        line["roofline"]["frac_of_read_at_step_bytes"] = achieved / rp["at_step_bytes"]["gb_per_s"]
         per = {WORKLOAD: {"B": B, "N": N, "V": V, "logits": "bf16",
                           "us_per_step": elapsed_ms / args.steps * 1e3, "steps": args.steps,
                           "positions_per_s": value, "bytes_read_per_step": bytes_per_launch,
@@ -962,6 +966,42 @@ def kv_setup(dev, stream, copies, rank=0):
              "kv_len_sum": int(sum(max(int(n), 0) for n in kv_host)),
              "l2": f"{copies} rotating scratch windows of {L * B * W * E / 1e6:.0f} MB"}
     return sv, step, moved, shape
+
+
+def read_stream_peak(dev, stream, step_bytes, big=4 << 30):
+    """The achievable streaming-read bandwidth on this GPU, by the library's
+    read-stream hook (one plain read kernel per call): on a 4 GiB buffer
+    (median of 10 single reads), and on buffers of the step's own size
+    (3 rotating copies larger than L2 together, 300 back-to-back reads, the
+    way the row statistics are timed), which carries the same fixed launch,
+    ramp and drain cost per launch."""
+    import torch
+    from speculative_decoding_verification_73_gb300 import binding
+    out = torch.zeros(1, dtype=torch.int64, device=dev)
+
+    def timed(bufs, reps):
+        for i in range(3):
+            binding.spec_verify_debug_read_stream(bufs[i % len(bufs)], out, stream)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(reps):
+            binding.spec_verify_debug_read_stream(bufs[i % len(bufs)], out, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+
+    buf = torch.ones(big, dtype=torch.uint8, device=dev)
+    ms_big = statistics.median(timed([buf], 1) for _ in range(10))
+    del buf
+    n = step_bytes // 16 * 16
+    bufs = [torch.ones(n, dtype=torch.uint8, device=dev) for _ in range(3)]
+    ms_step = timed(bufs, 300)
+    del bufs
+    return {"gb_per_s": big / (ms_big * 1e-3) / 1e9, "bytes": big,
+            "at_step_bytes": {"gb_per_s": n / (ms_step * 1e-3) / 1e9, "us": ms_step * 1e3, "bytes": n},
+            "kernel": "spec_verify_debug_read_stream (8 CTAs per SM, 16-byte non-allocating loads)",
+            "note": "context for the roofline; 'peak' stays the measured copy bandwidth"}
 
 
 LAZY_WORKLOADS = ("batch64-bf16", "lowaccept64-bf16")

@@ -403,6 +403,21 @@ int spec_verify_debug_philox(uint64_t seed, const uint32_t* ctr3, uint32_t* out4
                              void* cuda_stream);
 
 /*
+ * spec_verify_debug_read_stream -- measurement hook: the achievable
+ * streaming-read bandwidth of this GPU, for the row statistics' roofline
+ * (the survey's measurement row asks for a plain streaming-read kernel on
+ * the same box beside the nominal peak).  Reads the `bytes` bytes at buf
+ * (device, 16-byte aligned, bytes a multiple of 16) once with 16-byte
+ * non-allocating loads from a grid of 8 CTAs per SM (one kernel launch and
+ * nothing else), and adds the sum of the buffer's 64-bit little-endian
+ * words to the device word *out_sum, modulo 2^64, so no read can be
+ * dropped (the caller clears *out_sum).  Enqueued on cuda_stream.  Returns
+ * SV_OK, SV_EINVAL or SV_ECUDA.
+ */
+int spec_verify_debug_read_stream(const void* buf, size_t bytes, uint64_t* out_sum,
+                                  void* cuda_stream);
+
+/*
  * spec_verify_debug_skip_row_stats -- test hook for the bounded waits.  With
  * on != 0, the following spec_verify / spec_verify_tree calls on the context
  * launch their sampling (walk) kernel alone, without the row-statistics

@@ -32,7 +32,7 @@ _DTYPE_CODE = {torch.float32: SV_F32, torch.bfloat16: SV_BF16}
 EXPORTS = (
     "spec_verify_init", "spec_verify", "spec_verify_get_error", "spec_verify_debug_stats",
     "spec_verify_profile", "spec_verify_profile_read", "spec_verify_launches_per_call",
-    "spec_verify_debug_philox", "spec_verify_destroy", "spec_verify_strerror",
+    "spec_verify_debug_philox", "spec_verify_debug_read_stream", "spec_verify_destroy", "spec_verify_strerror",
     "spec_verify_noalloc", "spec_verify_tree", "spec_verify_kv_commit", "spec_verify_lazy",
     "spec_verify_fc_norm", "spec_verify_debug_seek_calls", "spec_verify_debug_skip_row_stats",
     "spec_verify_debug_late_cta",
@@ -68,6 +68,7 @@ def load():
                                              ctypes.POINTER(c_int)]
     lib.spec_verify_launches_per_call.argtypes = []
     lib.spec_verify_debug_philox.argtypes = [c_u64, c_void, c_void, c_int, c_void]
+    lib.spec_verify_debug_read_stream.argtypes = [c_void, ctypes.c_size_t, c_void, c_void]
     lib.spec_verify_debug_seek_calls.argtypes = [c_void, ctypes.c_uint32]
     lib.spec_verify_debug_skip_row_stats.argtypes = [c_void, c_int]
     lib.spec_verify_debug_late_cta.argtypes = [c_void, c_int]
@@ -327,6 +328,21 @@ def spec_verify_debug_philox(seed, counters, stream=None):
                                            _ptr(ctr), _ptr(out), int(n), _stream_handle(stream)),
            "spec_verify_debug_philox")
     return out.to(torch.int64) & 0xFFFFFFFF
+
+
+def spec_verify_debug_read_stream(buf, out=None, stream=None):
+    """Read the CUDA tensor buf (contiguous, 16-byte aligned, a multiple of
+    16 bytes) once on the device, adding the sum of its 64-bit words modulo
+    2^64 to the one-element int64 CUDA tensor out (a new zeroed one when
+    None); returns out."""
+    if not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    nbytes = buf.numel() * buf.element_size()
+    if out is None:
+        out = torch.zeros(1, dtype=torch.int64, device=buf.device)
+    _check(load().spec_verify_debug_read_stream(_ptr(buf), int(nbytes), _ptr(out), _stream_handle(stream)),
+           "spec_verify_debug_read_stream")
+    return out
 
 
 def spec_verify_destroy(ctx):

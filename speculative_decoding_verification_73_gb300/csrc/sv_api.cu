@@ -508,4 +508,13 @@ int spec_verify_debug_philox(uint64_t seed, const uint32_t* ctr3, uint32_t* out4
              : SV_ECUDA;
 }
 
+int spec_verify_debug_read_stream(const void* buf, size_t bytes, uint64_t* out_sum, void* cuda_stream) {
+  if (out_sum == nullptr || bytes % 16 != 0 || (bytes > 0 && (buf == nullptr || !aligned16(buf))))
+    return SV_EINVAL;
+  return sv::launch_read_stream(buf, bytes, reinterpret_cast<unsigned long long*>(out_sum),
+                                static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess
+             ? SV_OK
+             : SV_ECUDA;
+}
+
 }  // extern "C"

@@ -175,6 +175,7 @@ cudaError_t launch_tree_walk(int dtype, bool vec, const TreeProblem& p, const Wo
 cudaError_t launch_kv_commit(const KvProblem& p, cudaStream_t s);
 cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s);
 cudaError_t launch_lazy(int dtype, bool vec, const Problem& p, const Workspace& w, cudaStream_t s);
+cudaError_t launch_read_stream(const void* buf, size_t bytes, unsigned long long* out, cudaStream_t s);
 cudaError_t launch_philox_probe(unsigned long long seed, const uint32_t* ctr3, uint32_t* out4,
                                 int n, cudaStream_t s);
 

@@ -1,5 +1,8 @@
-// Test hook: Philox4x32-10 words computed by the device function the walk
-// and the sampler use, for checking against an independent implementation.
+// Test hooks: Philox4x32-10 words computed by the device function the walk
+// and the sampler use, for checking against an independent implementation;
+// and a plain streaming read of a buffer (the achievable read bandwidth the
+// row statistics are compared with), folding what it reads into a checksum
+// so that no load can be dropped.
 
 #include "sv_device.cuh"
 
@@ -18,7 +21,40 @@ __global__ void philox_probe_kernel(unsigned long long seed, const uint32_t* ctr
   out4[4 * i + 3] = r.w;
 }
 
+// Sum of the buffer's 64-bit words (mod 2^64): every thread reads 16-byte
+// vectors i, i + stride, ... with non-allocating loads, four in flight, and
+// each warp adds its total to *out once.
+__global__ void __launch_bounds__(256) read_stream_kernel(const uint4* __restrict__ src, size_t n16,
+                                                          unsigned long long* out) {
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  unsigned long long acc = 0;
+  auto fold = [](const uint4& v) {
+    return (static_cast<unsigned long long>(v.y) << 32 | v.x) + (static_cast<unsigned long long>(v.w) << 32 | v.z);
+  };
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = ld_stream16(src + i), b = ld_stream16(src + i + stride);
+    const uint4 c = ld_stream16(src + i + 2 * stride), d = ld_stream16(src + i + 3 * stride);
+    acc += fold(a) + fold(b) + fold(c) + fold(d);
+  }
+  for (; i < n16; i += stride) acc += fold(ld_stream16(src + i));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+  if ((threadIdx.x & 31) == 0) atomicAdd(out, acc);
+}
+
 }  // namespace
+
+cudaError_t launch_read_stream(const void* buf, size_t bytes, unsigned long long* out, cudaStream_t s) {
+  if (bytes == 0) return cudaSuccess;
+  cudaError_t e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+      (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  read_stream_kernel<<<sms * 8, 256, 0, s>>>(static_cast<const uint4*>(buf), bytes / 16, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_philox_probe(unsigned long long seed, const uint32_t* ctr3, uint32_t* out4,
                                 int n, cudaStream_t s) {
