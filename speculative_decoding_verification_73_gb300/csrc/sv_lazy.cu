@@ -10,8 +10,9 @@
 // pass per position.
 //
 // One cluster of kLazyCluster CTAs per request.  For each position the
-// cluster splits the row pair's 64 KB spans among its CTAs, stages each span
-// in shared memory and reduces it with the chain's span reduction
+// cluster splits the row pair's 64 KB spans among its CTAs, brings each span
+// on chip at once (most of it staged in shared memory, the rest in
+// registers) and reduces it with the chain's per-group span arithmetic
 // (sv_span.cuh; the span holding the draft token also stores its logit),
 // stores the partials in the chain's workspace layout, and meets at a
 // cluster barrier; then every CTA merges
