@@ -1,4 +1,4 @@
-"""FC-norm on the GPU (stats kernel + tcgen05 GEMM) through the C ABI against
+"""FC-norm on the GPU (normalisation kernel + tcgen05 GEMM) through the C ABI against
 the float64 oracle, within the bound that bf16 rounding of the normalised
 inputs and of the output implies: |gpu - ref| <= 2^-8 (sum_k |x_k||w_k| +
 |ref|)."""
@@ -97,24 +97,29 @@ def test_selector_weights_return_the_normalised_segment():
     run_case(wl, binding.SV_NORM_LAYER, with_bias=False, with_beta=True)
 
 
-def test_full_size_on_sampled_rows():
-    """T = d = d_out = 4096 (the benchmarked size, 32 x 16 output tiles of the
-    persistent GEMM, every CTA several tiles): 64 sampled tokens against the
-    oracle on those tokens alone (tokens are normalised independently)."""
+@pytest.mark.parametrize("norm", [binding.SV_NORM_LAYER, binding.SV_NORM_NONE], ids=["layernorm", "none"])
+def test_full_size_on_sampled_rows(norm):
+    """T = d = d_out = 4096 (the benchmarked size, 32 m-blocks of output
+    tiles of the persistent GEMM, every CTA several tiles), through X and
+    straight from the hidden states: 64 sampled tokens against the oracle on
+    those tokens alone (tokens are normalised independently)."""
     T = d = d_out = 4096
     wl = workloads.make_fcnorm(T, d, d_out, gen_seed=2026)
     ctx = binding.SpecVerify(1, 1, 16, torch.float32)
     h = [x.cuda() for x in wl.h]
-    out = binding.spec_verify_fc_norm(ctx.ctx, binding.SV_NORM_LAYER, *h, wl.weight.cuda(),
-                                      gamma=wl.gamma.cuda(), beta=wl.beta.cuda(), bias=wl.bias.cuda())
+    layer = norm == binding.SV_NORM_LAYER
+    out = binding.spec_verify_fc_norm(ctx.ctx, norm, *h, wl.weight.cuda(),
+                                      gamma=wl.gamma.cuda() if layer else None,
+                                      beta=wl.beta.cuda() if layer else None, bias=wl.bias.cuda())
     assert ctx.get_error() == (0, 0)
     rows = np.sort(np.random.default_rng(4).choice(T, size=64, replace=False))
     rows[0], rows[-1] = 0, T - 1
     got = out[torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
     hs = [_f64(x[torch.from_numpy(rows)]) for x in wl.h]
-    ref = ofc.fc_norm(*hs, _f64(wl.weight), binding.SV_NORM_LAYER, _f64(wl.gamma), _f64(wl.beta),
-                      _f64(wl.bias), 1e-5)
-    bound = ofc.abs_bound(*hs, _f64(wl.weight), binding.SV_NORM_LAYER, _f64(wl.gamma), _f64(wl.beta), 1e-5)
+    g = _f64(wl.gamma) if layer else None
+    bt = _f64(wl.beta) if layer else None
+    ref = ofc.fc_norm(*hs, _f64(wl.weight), norm, g, bt, _f64(wl.bias), 1e-5)
+    bound = ofc.abs_bound(*hs, _f64(wl.weight), norm, g, bt, 1e-5)
     err = np.abs(got - ref)
     tol = 2.0 ** -8 * (bound + np.abs(ref)) + 1e-6
     assert (err <= tol).all(), f"worst error / tolerance {float((err / tol).max()):.3g}"
@@ -122,10 +127,13 @@ def test_full_size_on_sampled_rows():
 
 
 @pytest.mark.parametrize("T,d_out", [(640, 3872), (640, 4832), (640, 5792), (1280, 3392), (128, 256)])
-def test_every_tile_width(T, d_out):
+@pytest.mark.parametrize("norm", [binding.SV_NORM_LAYER, binding.SV_NORM_NONE], ids=["layernorm", "none"])
+def test_every_tile_width(T, d_out, norm):
     """The GEMM picks its output tile width (256, 224, 192, 160 or 128
-    columns) from the shape and the SM count; on a 152-SM GB300 these shapes
-    take 160, 192, 224, 256 and 128 columns respectively (ragged last tiles
-    included).  A narrow d keeps each case quick."""
+    columns) from the shape and the SM count, and its ring depth from the
+    width; on a 152-SM GB300 these shapes take 160, 192, 224, 256 and 128
+    columns respectively (ragged last tiles included), through X
+    (LayerNorm) and straight from the hidden states (no normalisation).  A
+    narrow d keeps each case quick."""
     wl = workloads.make_fcnorm(T, 64, d_out, gen_seed=T + d_out)
-    run_case(wl, binding.SV_NORM_LAYER, True, True)
+    run_case(wl, norm, True, norm == binding.SV_NORM_LAYER)
