@@ -59,7 +59,7 @@ constexpr int kLazyCluster = SV_LAZY_CLUSTER;  // CTAs per request
 #define SV_LAZY_STAGE_VECS 12
 #endif
 constexpr int kSpanVecs = kSpanBytes / 16 / kThreads;  // vectors per thread of a span
-constexpr int kStagedVecs = SV_LAZY_STAGE_VECS;
+constexpr int kStagedVecs = SV_LAZY_STAGE_VECS < kSpanVecs ? SV_LAZY_STAGE_VECS : kSpanVecs;
 constexpr int kHeldVecs = kSpanVecs - kStagedVecs;      // held in registers
 constexpr int kLazyStageBytes = kStagedVecs * kThreads * 16;
 static_assert(kStagedVecs >= 1 && kStagedVecs <= kSpanVecs, "staged vectors per thread");

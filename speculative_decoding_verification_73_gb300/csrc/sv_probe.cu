@@ -22,8 +22,9 @@ __global__ void philox_probe_kernel(unsigned long long seed, const uint32_t* ctr
 }
 
 // Sum of the buffer's 64-bit words (mod 2^64): every thread reads 16-byte
-// vectors i, i + stride, ... with non-allocating loads, four in flight, and
-// each warp adds its total to *out once.
+// vectors i, i + stride, ... with non-allocating loads, four in flight; the
+// CTA adds up its threads' totals and adds the result to *out once (one
+// atomic per CTA, so the atomics on the one word stay few).
 __global__ void __launch_bounds__(256) read_stream_kernel(const uint4* __restrict__ src, size_t n16,
                                                           unsigned long long* out) {
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
@@ -40,7 +41,15 @@ __global__ void __launch_bounds__(256) read_stream_kernel(const uint4* __restric
   for (; i < n16; i += stride) acc += fold(ld_stream16(src + i));
 #pragma unroll
   for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
-  if ((threadIdx.x & 31) == 0) atomicAdd(out, acc);
+  __shared__ unsigned long long s_warp[256 / 32];
+  if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long t = 0;
+#pragma unroll
+    for (int w = 0; w < 256 / 32; ++w) t += s_warp[w];
+    atomicAdd(out, t);
+  }
 }
 
 }  // namespace
