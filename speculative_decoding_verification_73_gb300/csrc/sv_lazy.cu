@@ -86,6 +86,7 @@ __device__ __forceinline__ Partial reduce_span_split(const T* row, int beg, int 
   cp_async_wait_all();  // thread t reads back exactly the vectors it copied
   SpanAcc acc = span_acc_init();
   const uint64_t k2 = f2pack(k, k);
+  const TokAt ta = kGreedy ? TokAt{-1, 0, 0} : tok_at<T>(beg, end, d);
 #pragma unroll
   for (int gi = 0; gi < kSpanVecs / kGroup; ++gi) {
     uint4 g[kGroup];
@@ -98,7 +99,7 @@ __device__ __forceinline__ Partial reduce_span_split(const T* row, int beg, int 
       else
         g[u] = held[i - kStagedVecs];
     }
-    span_group<T, kGreedy, false>(acc, g, beg, end, gi, k2, k, d, tok);
+    span_group<T, kGreedy>(acc, g, beg, gi, k2, k, ta, tok);
   }
   return span_finish<kGreedy>(acc, red_f, red_g, red_i);
 }

@@ -103,21 +103,45 @@ __device__ __forceinline__ SpanAcc span_acc_init() {
   return a;
 }
 
+// Where the draft token d sits among this thread's vectors of the span
+// [beg, end): group gi, vector u of the group, element e (gi = -1 if this
+// thread does not hold it), worked out once per span.
+struct TokAt {
+  int gi, u, e;
+};
+
+template <typename T>
+__device__ __forceinline__ TokAt tok_at(int beg, int end, int d) {
+  constexpr int kVec = Elem<T>::kVec;
+  TokAt t{-1, 0, 0};
+  if (d >= beg && d < end) {
+    const int r = d - beg;
+    const int v = r / kVec;
+    if (v % kThreads == static_cast<int>(threadIdx.x)) {
+      const int i = v / kThreads;
+      t.gi = i / kGroup;
+      t.u = i - t.gi * kGroup;
+      t.e = r - v * kVec;
+    }
+  }
+  return t;
+}
+
 // Fold group gi of this thread's vectors (vector i of the group is span
 // vector threadIdx.x + (gi kGroup + i) kThreads) into the state.  A vector
 // past the span's end must hold -inf words.  The thread whose vector holds
-// the draft token d stores its logit at *tok_out.
-template <typename T, bool kGreedy, bool kFull>
-__device__ __forceinline__ void span_group(SpanAcc& a, const uint4 (&g)[kGroup], int beg, int end, int gi,
-                                           uint64_t k2, float k, int d, float* tok_out) {
+// the draft token (ta, from tok_at) stores its logit at *tok_out.
+template <typename T, bool kGreedy>
+__device__ __forceinline__ void span_group(SpanAcc& a, const uint4 (&g)[kGroup], int beg, int gi, uint64_t k2,
+                                           float k, const TokAt& ta, float* tok_out) {
   using E = Elem<T>;
   constexpr int kVec = E::kVec;
-  if (!kGreedy) {
+  if (!kGreedy && gi == ta.gi) {
+    uint4 v = g[0];
 #pragma unroll
-    for (int u = 0; u < kGroup; ++u) {
-      const int e0 = beg + (static_cast<int>(threadIdx.x) + (gi * kGroup + u) * kThreads) * kVec;
-      if (d >= e0 && d < e0 + kVec && (kFull || d < end)) *tok_out = E::get(g[u], d - e0);
-    }
+    for (int u = 1; u < kGroup; ++u)
+      if (u == ta.u) v = g[u];
+    *tok_out = E::get(v, ta.e);
   }
   float gm = E::vmax_nan(g[0]);
 #pragma unroll
@@ -213,6 +237,7 @@ __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int e
   }
   SpanAcc acc = span_acc_init();
   const uint64_t k2 = f2pack(k, k);
+  const TokAt ta = kGreedy ? TokAt{-1, 0, 0} : tok_at<T>(beg, end, d);
 #pragma unroll
   for (int gi = 0; gi < kGroups; ++gi) {
     const int cur = gi & 1;
@@ -223,7 +248,7 @@ __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int e
         buf[cur ^ 1][u] = (kFull || v < nv) ? (kSmem ? vp[v] : ld_stream16(vp + v)) : pad;
       }
     }
-    span_group<T, kGreedy, kFull>(acc, buf[cur], beg, end, gi, k2, k, d, tok_out);
+    span_group<T, kGreedy>(acc, buf[cur], beg, gi, k2, k, ta, tok_out);
   }
   return span_finish<kGreedy>(acc, red_f, red_g, red_i);
 }
