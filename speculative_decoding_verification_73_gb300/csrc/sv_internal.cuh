@@ -154,8 +154,8 @@ struct Workspace {
   float* chunk_sums;     // [B, S3]: residual mass of each level-1 block
   int* blk_tok;          // [B, S3]: the token each level-1 block would give
   unsigned* err;         // [1], OR of kErr* bits (starts at zero)
-  unsigned long long* arrivals;  // [B]: sampler arrivals per request, (epoch << 32) |
-                                 // late bit 31 | count: a word of an earlier call counts 0
+  unsigned long long* arrivals;  // [B]: sampler arrivals per request, (late arrivals << 32) |
+                                 // count; zero between calls (the last CTA clears it)
   unsigned* late;        // [B]: tree walk: the call's tag once a wait of the request ran out
   float* dbg_accept;     // [B, N]
   float* dbg_logz;       // [B, 2N+1]

@@ -69,27 +69,18 @@ constexpr int stage_bytes() {
   return 2 * blocks_per_cta<T>() * kLevel1 * static_cast<int>(sizeof(T));
 }
 
-// Arrival counting of a request's sampler CTAs.  The word holds the call's
-// epoch in its high half, so a count left by an earlier call (a CTA that
-// stopped before counting in) reads as zero and never makes a later call's
-// CTA think it arrived last; no reset is needed.  Bit 31 records that some
-// CTA of the request gave up waiting.  Returns the word's low half after
-// this CTA's arrival.
-constexpr unsigned kArrivalCount = 0x7fffffffu;
-__device__ __forceinline__ unsigned count_in(unsigned long long* word, unsigned epoch, bool late) {
-  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(word);
-  // every failed exchange means another CTA of the request counted in, so
-  // the loop ends after at most one round per CTA of the request; the bound
-  // is only a guard (giving up leaves this CTA not the last)
-  for (int tries = 0; tries < (1 << 16); ++tries) {
-    const unsigned low = static_cast<unsigned>(old >> 32) == epoch ? static_cast<unsigned>(old) : 0u;
-    const unsigned now = ((low & kArrivalCount) + 1u) | (low & ~kArrivalCount) | (late ? ~kArrivalCount : 0u);
-    const unsigned long long want = static_cast<unsigned long long>(epoch) << 32 | now;
-    const unsigned long long seen = atomicCAS(word, old, want);
-    if (seen == old) return now;
-    old = seen;
-  }
-  return 0u;
+// Arrival counting of a request's sampler CTAs: each adds 1 to the
+// request's word (plus kLateUnit when its wait for the row statistics ran
+// out) with one atomic, and the CTA whose arrival brings the count to the
+// request's CTA total is the last; it clears the word for the next call.
+// Every CTA of a sampled request counts in exactly once (a CTA that gave up
+// waiting counts in as late), so the last one always does, and a call never
+// meets a count left by an earlier one.  Returns the word after this CTA's
+// arrival: the count in the low half, the late arrivals in the high half.
+constexpr unsigned long long kLateUnit = 1ull << 32;
+__device__ __forceinline__ unsigned long long count_in(unsigned long long* word, bool late) {
+  const unsigned long long inc = late ? kLateUnit + 1ull : 1ull;
+  return atomicAdd(word, inc) + inc;
 }
 
 // r for the tokens of one 16-byte vector of each row; rv[e] gets token e.
@@ -325,8 +316,10 @@ __global__ void __launch_bounds__(kST, SV_SAMPLE_MINB) sample_kernel(Problem p, 
   }
   if (threadIdx.x == 0) {
     __threadfence();  // publish before counting in
-    const unsigned state = count_in(w.arrivals + b, p.epoch, late);
-    s_last = (state & kArrivalCount) == static_cast<unsigned>(G) ? 1 + (state >> 31) : 0;
+    const unsigned long long state = count_in(w.arrivals + b, late);
+    const bool last = static_cast<unsigned>(state) == static_cast<unsigned>(G);
+    s_last = last ? 1 + ((state >> 32) != 0 ? 1 : 0) : 0;
+    if (last) w.arrivals[b] = 0;  // every CTA of the request has counted in
   }
   __syncthreads();
   if (!s_last) return;
