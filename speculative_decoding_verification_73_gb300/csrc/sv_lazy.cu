@@ -14,8 +14,10 @@
 // on chip at once (most of it staged in shared memory, the rest in
 // registers) and reduces it with the chain's per-group span arithmetic
 // (sv_span.cuh; the span holding the draft token also stores its logit),
-// stores the partials in the chain's workspace layout, and meets at a
-// cluster barrier; then every CTA merges
+// keeps the partials in its shared memory (rows of more than kLazyMaxS1
+// spans: in the chain's workspace layout), and meets at a cluster barrier;
+// then every CTA gathers the position's partials from its peers through
+// distributed shared memory and merges
 // the same partials and takes the same accept decision, with the walk's
 // arithmetic, so the results are those of spec_verify bit for bit.  The
 // final token is drawn like the tree walk's: per level-1 block the mass and
@@ -122,6 +124,54 @@ __device__ __forceinline__ RowNorm merge_row(const Partial* parts, int n) {
   return merge_sampled(pre, parts, n);
 }
 
+// The same merges over partials gathered into this CTA's shared memory
+// (plain loads; the merge arithmetic is the same).
+__device__ __forceinline__ float4 partial_local(const Partial* at, bool take) {
+  return take ? *reinterpret_cast<const float4*>(at) : make_float4(-INFINITY, 0.f, __int_as_float(INT_MAX), 0.f);
+}
+
+__device__ __forceinline__ RowNorm merge_row_local(const Partial* parts, int n) {
+  float4 pre[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) pre[i] = partial_local(parts + i, i < n);
+  return merge_sampled_by(pre, n, [&](int i0, float4(&pt)[kBatch]) {
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) pt[i] = partial_local(parts + i0 + i, i0 + i < n);
+  });
+}
+
+__device__ __forceinline__ RowMax merge_row_greedy_local(const Partial* parts, int n) {
+  float4 pre[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) pre[i] = partial_local(parts + i, i < n);
+  return merge_greedy_by(pre, n, [&](int i0, float4(&pt)[kBatch]) {
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) pt[i] = partial_local(parts + i0 + i, i0 + i < n);
+  });
+}
+
+// 16 bytes at `local`'s place in the shared memory of cluster CTA `rank`
+// (16-byte aligned).
+__device__ __forceinline__ float4 ld_dsmem16(const void* local, unsigned rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+
+// Rows of up to kLazyMaxS1 spans exchange their partials through
+// distributed shared memory (each CTA keeps the partials of its own spans
+// of the position in double-buffered slots; after the cluster barrier every
+// CTA gathers the row pair's); longer rows go through the workspace.
+constexpr int kLazyMaxS1 = 32;
+constexpr int kLazySlots = (2 * kLazyMaxS1 + kLazyCluster - 1) / kLazyCluster;  // items per CTA
+
 __device__ __forceinline__ RowMax merge_row_greedy(const Partial* parts, int n) {
   float4 pre[kPre];
 #pragma unroll
@@ -141,6 +191,9 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kThreads,
   __shared__ float s_law[5];  // k, cq, inv_sq, cp, inv_sp of the draw
   __shared__ float s_u[4];
   __shared__ int s_kind;
+  __shared__ __align__(16) Partial s_own[2][kLazySlots];  // this CTA's spans of a position, by parity
+  __shared__ float s_owntok[2][kLazySlots];               // their token logits
+  __shared__ __align__(16) Partial s_gather[2 * kLazyMaxS1];  // the position's row pair, gathered
   const int b = blockIdx.x / kLazyCluster;
   const unsigned rank = cluster_rank();
   const int N = p.N, V = p.V, S1 = w.S1;
@@ -165,6 +218,8 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kThreads,
   Partial* parts = w.partials + static_cast<size_t>(b) * per * S1;
   float* tok_logit = w.tok_logit + static_cast<size_t>(b) * per;
   int a = N;
+  const bool dsm = S1 <= kLazyMaxS1;  // partials through distributed shared memory
+  constexpr int kSpanElems = kSpanBytes / static_cast<int>(sizeof(T));
   if (!err) {
     for (int j = 1; j <= N + 1; ++j) {
       const bool last = j == N + 1;
@@ -172,22 +227,38 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kThreads,
       const bool with_draft = !greedy && !last;
       const int nitems = with_draft ? 2 * S1 : S1;
       const int d = last ? -1 : toks[j - 1];
-      for (int it = static_cast<int>(rank); it < nitems; it += kLazyCluster) {
+      const int par = j & 1;
+      for (int it = static_cast<int>(rank), li = 0; it < nitems; it += kLazyCluster, ++li) {
         const bool dr = it >= S1;
         const int span = dr ? it - S1 : it;
         const int slot = dr ? N + 1 + trow : trow;
         const T* row = dr ? static_cast<const T*>(p.draft) + (static_cast<size_t>(b) * N + trow) * V
                           : static_cast<const T*>(p.target) + (static_cast<size_t>(b) * (N + 1) + trow) * V;
-        const Partial out = reduce_row_span<T, kVecPath>(row, span, V, greedy, k, greedy ? -1 : d,
-                                                         tok_logit + slot, reinterpret_cast<T*>(s_stage));
-        if (tid == 0) parts[static_cast<size_t>(slot) * S1 + span] = out;
+        float* tokp = dsm ? &s_owntok[par][li] : tok_logit + slot;
+        const Partial out = reduce_row_span<T, kVecPath>(row, span, V, greedy, k, greedy ? -1 : d, tokp,
+                                                         reinterpret_cast<T*>(s_stage));
+        if (tid == 0) {
+          if (dsm)
+            s_own[par][li] = out;
+          else
+            parts[static_cast<size_t>(slot) * S1 + span] = out;
+        }
       }
-      __threadfence();
+      if (!dsm) __threadfence();
       cluster_sync();  // the step's partials and token logits are stored
+      if (dsm) {
+        // item i (span i of the target row, then of the draft row) is in
+        // slot i / kLazyCluster of CTA i % kLazyCluster
+        if (tid < nitems)
+          *reinterpret_cast<float4*>(&s_gather[tid]) =
+              ld_dsmem16(&s_own[par][tid / kLazyCluster], static_cast<unsigned>(tid % kLazyCluster));
+        __syncthreads();
+      }
       if (tid == 0) {
         int state = kGo;
         if (greedy) {
-          const RowMax g = merge_row_greedy(parts + static_cast<size_t>(trow) * S1, S1);
+          const RowMax g = dsm ? merge_row_greedy_local(s_gather, S1)
+                               : merge_row_greedy(parts + static_cast<size_t>(trow) * S1, S1);
           if (!g.ok) {
             state = kStopError;
           } else if (last || d != g.idx) {
@@ -196,15 +267,25 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kThreads,
             s_a = j - 1;
           }
         } else {
-          const RowNorm q = merge_row(parts + static_cast<size_t>(trow) * S1, S1);
+          const RowNorm q = dsm ? merge_row_local(s_gather, S1) : merge_row(parts + static_cast<size_t>(trow) * S1, S1);
           RowNorm pn{0.f, 1.f, true};
-          if (with_draft) pn = merge_row(parts + static_cast<size_t>(N + 1 + trow) * S1, S1);
+          if (with_draft)
+            pn = dsm ? merge_row_local(s_gather + S1, S1)
+                     : merge_row(parts + static_cast<size_t>(N + 1 + trow) * S1, S1);
           if (!q.ok || !pn.ok) {
             state = kStopError;
           } else {
             bool accepted = !last;
             if (!last) {
-              const float zd = __ldcg(tok_logit + trow), yd = __ldcg(tok_logit + N + 1 + trow);
+              float zd, yd;
+              if (dsm) {  // the items holding d: span d / kSpanElems of each row
+                const int it_z = d / kSpanElems, it_y = S1 + d / kSpanElems;
+                zd = ld_dsmem(&s_owntok[par][it_z / kLazyCluster], static_cast<unsigned>(it_z % kLazyCluster));
+                yd = ld_dsmem(&s_owntok[par][it_y / kLazyCluster], static_cast<unsigned>(it_y % kLazyCluster));
+              } else {
+                zd = __ldcg(tok_logit + trow);
+                yd = __ldcg(tok_logit + N + 1 + trow);
+              }
               if (yd != -INFINITY) {  // p(d) > 0
                 const float lr = fmaf(zd - yd, k, -(q.c - pn.c)) + log2f(pn.s / q.s);
                 accepted = philox_uniform(p.seed, b, j, 0) < fminf(1.f, exp2f(lr));
@@ -229,6 +310,9 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kThreads,
       __syncthreads();
       if (s_state != kGo) break;
     }
+    // no CTA leaves (or reuses a slot) while another may still read its
+    // shared memory
+    cluster_sync();
     if (s_state == kStopError) err = kErrLogit;
     a = s_a;
   }
