@@ -344,8 +344,16 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kThreads,
     const int S3 = w.S3;
     float* masses = w.chunk_sums + static_cast<size_t>(b) * S3;
     int* cands = w.blk_tok + static_cast<size_t>(b) * S3;
+    // the blocks' masses and candidates reach rank 0 through distributed
+    // shared memory (block c in slot c / kLazyCluster of CTA c % kLazyCluster)
+    // when they fit the slots, else through the workspace
+    constexpr int kPickSlots = 16;
+    __shared__ float s_bmass[kPickSlots];
+    __shared__ float s_bcand[kPickSlots];  // the candidate token's bits
+    const bool dsm_pick = S3 <= kPickSlots * kLazyCluster;
     auto rf = [&](float zt, float yt, int t) { return law.r(zt, yt, t); };
-    for (int c = static_cast<int>(rank); c < S3; c += kLazyCluster) {
+    int bi = 0;
+    for (int c = static_cast<int>(rank); c < S3; c += kLazyCluster, ++bi) {
       const int cbeg = c * kLevel1, cend = min(V, cbeg + kLevel1);
       float h0, h1, mass;
       seg_sums<T, kVecPath>(z, y, need_y, cbeg + tid * kSegTok, cend, rf, h0, h1);
@@ -353,18 +361,38 @@ __global__ void __cluster_dims__(kLazyCluster, 1, 1) __launch_bounds__(kThreads,
           h0, h1, cbeg, cend, job,
           [&](int t) { return law.r(E::load1(z + t), need_y ? E::load1(y + t) : 0.f, t); }, sc, &mass);
       if (tid == 0) {
-        masses[c] = mass;
-        cands[c] = cand;
+        if (dsm_pick) {
+          s_bmass[bi] = mass;
+          s_bcand[bi] = __int_as_float(cand);
+        } else {
+          masses[c] = mass;
+          cands[c] = cand;
+        }
       }
     }
-    __threadfence();
-    cluster_sync();  // every block's mass and candidate are stored
-    if (rank != 0) return;
-    if (tid < 32) {
-      const int c1 = warp_pick([&](int i) { return __ldcg(masses + i); }, S3, job.u[0]);
-      if (tid == 0) s_final = c1 >= 0 ? __ldcg(cands + c1) : -1;
+    if (dsm_pick) {
+      cluster_sync();  // every block's mass and candidate are in its CTA's shared memory
+      if (rank == 0 && tid < 32) {
+        const int c1 = warp_pick(
+            [&](int i) { return ld_dsmem(&s_bmass[i / kLazyCluster], static_cast<unsigned>(i % kLazyCluster)); },
+            S3, job.u[0]);
+        if (tid == 0)
+          s_final = c1 >= 0 ? __float_as_int(ld_dsmem(&s_bcand[c1 / kLazyCluster],
+                                                      static_cast<unsigned>(c1 % kLazyCluster)))
+                            : -1;
+      }
+      cluster_sync();  // rank 0 has read the other CTAs' shared memory
+      if (rank != 0) return;
+    } else {
+      __threadfence();
+      cluster_sync();  // every block's mass and candidate are stored
+      if (rank != 0) return;
+      if (tid < 32) {
+        const int c1 = warp_pick([&](int i) { return __ldcg(masses + i); }, S3, job.u[0]);
+        if (tid == 0) s_final = c1 >= 0 ? __ldcg(cands + c1) : -1;
+      }
+      __syncthreads();
     }
-    __syncthreads();
     if (s_final < 0 && need_y) {
       // the residual has no mass (float32 rounding only): draw from q
       const NodeLaw lq{NodeLaw::kQ, s_law[0], s_law[1], s_law[2], 0.f, 0.f, 1.f, 1.f, 0, nullptr};

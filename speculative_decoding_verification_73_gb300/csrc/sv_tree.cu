@@ -468,6 +468,13 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   const Job job = s_job;
   float* masses = w.chunk_sums + static_cast<size_t>(b) * S3;
   int* cands = w.blk_tok + static_cast<size_t>(b) * S3;
+  // the blocks' masses and candidates reach rank 0 through distributed
+  // shared memory (block c in slot c / kTreeCluster of CTA c % kTreeCluster)
+  // when they fit the slots, else through the workspace
+  constexpr int kPickSlots = 16;
+  __shared__ float s_bmass[kPickSlots];
+  __shared__ float s_bcand[kPickSlots];  // the candidate token's bits
+  const bool dsm_pick = S3 <= kPickSlots * kTreeCluster;
   auto rf = [&](float zt, float yt, int t) { return law.r(zt, yt, t); };
   if (staging) stage_node(node, need_y);
   int bi = 0;
@@ -493,18 +500,38 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
           [&](int t) { return law.r(E::load1(z + t), need_y ? E::load1(y + t) : 0.f, t); }, sc, &mass);
     }
     if (i == 0) {
-      masses[c] = mass;
-      cands[c] = cand;
+      if (dsm_pick) {
+        s_bmass[bi] = mass;
+        s_bcand[bi] = __int_as_float(cand);
+      } else {
+        masses[c] = mass;
+        cands[c] = cand;
+      }
     }
   }
-  __threadfence();
-  cluster_sync();  // every block's mass and candidate are stored
-  if (rank != 0) return;
-  if (i < 32) {
-    const int c1 = warp_pick([&](int j) { return __ldcg(masses + j); }, S3, job.u[0]);
-    if (i == 0) s_child = c1 >= 0 ? __ldcg(cands + c1) : 0;
+  if (dsm_pick) {
+    cluster_sync();  // every block's mass and candidate are in its CTA's shared memory
+    if (rank == 0 && i < 32) {
+      const int c1 = warp_pick(
+          [&](int j) { return ld_dsmem(&s_bmass[j / kTreeCluster], static_cast<unsigned>(j % kTreeCluster)); },
+          S3, job.u[0]);
+      if (i == 0)
+        s_child = c1 >= 0 ? __float_as_int(ld_dsmem(&s_bcand[c1 / kTreeCluster],
+                                                    static_cast<unsigned>(c1 % kTreeCluster)))
+                          : 0;
+    }
+    cluster_sync();  // rank 0 has read the other CTAs' shared memory
+    if (rank != 0) return;
+  } else {
+    __threadfence();
+    cluster_sync();  // every block's mass and candidate are stored
+    if (rank != 0) return;
+    if (i < 32) {
+      const int c1 = warp_pick([&](int j) { return __ldcg(masses + j); }, S3, job.u[0]);
+      if (i == 0) s_child = c1 >= 0 ? __ldcg(cands + c1) : 0;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   const int plen = s_plen;
   if (is_node) {
     if (i < plen)
