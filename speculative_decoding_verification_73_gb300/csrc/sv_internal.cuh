@@ -78,6 +78,7 @@ constexpr int kJobNone = 0;
 constexpr int kJobResidual = 1;
 constexpr int kJobBonus = 2;
 constexpr int kJobLate = 3;  // a sampled request whose wait ran out in this CTA
+constexpr int kJobFailed = 4;  // a sampled request failed by its inputs (token, logit)
 
 // What the walk leaves for the sampler (in shared memory of each CTA).
 //   q_t = 2^(z_t*k - cq) * inv_sq,  p_t = 2^(y_t*k - cp) * inv_sp

@@ -29,14 +29,18 @@
 // level-2 mass per eight threads, the level-1 mass per CTA) and picks the
 // block's candidate token at levels 2-4 with u_2..u_4, as if level 1 had
 // chosen this block.  It stores (level-1 mass, candidate) and counts itself
-// in the request's arrival word (tagged with the call's epoch, so nothing
-// needs resetting between calls); the CTA that arrives last picks level 1
-// over the blocks' masses with u_1 and writes the chosen block's candidate.
-// No CTA waits for another.  If the residual has no mass anywhere, that last
-// CTA redoes every block with q alone.  A CTA whose wait for the row
-// statistics ran out evaluates nothing but still counts in, marking the
-// word; the last CTA then fails the whole request (SV_ERRBIT_WAIT), so a
-// request is either sampled from every block or failed.
+// in the request's arrival word with one atomic add; the CTA that arrives
+// last picks level 1 over the blocks' masses with u_1, writes the chosen
+// block's candidate and clears the word for the next call.  No CTA waits
+// for another.  If the residual has no mass anywhere, that last CTA redoes
+// every block with q alone.  A CTA whose wait for the row statistics ran
+// out evaluates nothing but still counts in, marking the word; the last CTA
+// then fails the whole request (SV_ERRBIT_WAIT), so a request is either
+// sampled from every block or failed.  A CTA whose walk found the request's
+// inputs bad (a token out of range, a logit that is NaN or +inf) evaluates
+// nothing either and counts in unmarked: the walk has already failed the
+// request, and every CTA of it counts in, so the word is clear after every
+// call.
 //
 // r_t = max(q_t - p_t, 0) with q_t = 2^(z_t k - c_q) / s_q and likewise p_t,
 // evaluated two tokens at a time with the paired float instructions.  Its
@@ -74,8 +78,9 @@ constexpr int stage_bytes() {
 // out) with one atomic, and the CTA whose arrival brings the count to the
 // request's CTA total is the last; it clears the word for the next call.
 // Every CTA of a sampled request counts in exactly once (a CTA that gave up
-// waiting counts in as late), so the last one always does, and a call never
-// meets a count left by an earlier one.  Returns the word after this CTA's
+// waiting counts in as late, one whose walk failed the request as failed),
+// so the last one always does, and a call never meets a count left by an
+// earlier one.  Returns the word after this CTA's
 // arrival: the count in the low half, the late arrivals in the high half.
 constexpr unsigned long long kLateUnit = 1ull << 32;
 __device__ __forceinline__ unsigned long long count_in(unsigned long long* word, bool late) {
@@ -254,6 +259,8 @@ __global__ void __launch_bounds__(kST, SV_SAMPLE_MINB) sample_kernel(Problem p, 
   const Job job = s_job;
   if (job.kind == kJobNone) return;  // nothing to sample for this request
   const bool late = job.kind == kJobLate;
+  // the walk failed the request and wrote its outputs; the CTA only counts in
+  const bool failed = job.kind == kJobFailed;
   const int N = p.N, V = p.V;
   const T* z = static_cast<const T*>(p.target) + (static_cast<size_t>(b) * (N + 1) + job.row) * V;
   const T* y = job.kind == kJobResidual
@@ -265,8 +272,8 @@ __global__ void __launch_bounds__(kST, SV_SAMPLE_MINB) sample_kernel(Problem p, 
   const int c0 = g * kB;
   const int nb = min(kB, S3 - c0);
 
-  if (late) {
-    // this CTA's wait ran out: no blocks, it only counts in (below)
+  if (late || failed) {
+    // no blocks: the CTA only counts in (below)
   } else if (kVecPath) {
     T* sz = reinterpret_cast<T*>(s_rows);
     T* sy = sz + kB * kLevel1;
@@ -318,11 +325,14 @@ __global__ void __launch_bounds__(kST, SV_SAMPLE_MINB) sample_kernel(Problem p, 
     __threadfence();  // publish before counting in
     const unsigned long long state = count_in(w.arrivals + b, late);
     const bool last = static_cast<unsigned>(state) == static_cast<unsigned>(G);
-    s_last = last ? 1 + ((state >> 32) != 0 ? 1 : 0) : 0;
+    // 0: not last; 1: last, sample; 2: last, some CTA's wait ran out;
+    // 3: last, the walk failed the request (then no CTA sampled, and only a
+    // CTA whose wait ran out can have seen otherwise)
+    s_last = !last ? 0 : (state >> 32) != 0 ? 2 : failed ? 3 : 1;
     if (last) w.arrivals[b] = 0;  // every CTA of the request has counted in
   }
   __syncthreads();
-  if (!s_last) return;
+  if (s_last == 0 || s_last == 3) return;
   __threadfence();  // see the other CTAs' masses and candidates
   if (s_last == 2) {
     // Some CTA of the request gave up waiting for its row statistics, so

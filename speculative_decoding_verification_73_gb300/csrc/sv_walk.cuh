@@ -332,9 +332,11 @@ __device__ __forceinline__ void walk_request(const Problem& p, const Workspace& 
         if (err) atomicOr(w.err, err);
       }
     }
-    // a sampled request whose wait ran out here still counts in with the
-    // sampler's other CTAs of the request (see sv_sample.cu)
-    if (j == 0) job_out->kind = (err == kErrWait && mode == kModeSampled) ? kJobLate : kJobNone;
+    // every sampler CTA of a sampled request counts in, whatever stopped it
+    // (see sv_sample.cu): a wait that ran out is this CTA's alone, so the
+    // request's other CTAs may have reached the logit check instead
+    if (j == 0)
+      job_out->kind = mode != kModeSampled ? kJobNone : (err == kErrWait ? kJobLate : kJobFailed);
     return;
   }
 

@@ -178,3 +178,33 @@ def test_one_sampler_cta_gives_up_while_the_others_finish(cta):
             assert torch.equal(a, b), seed
         assert ctx.get_error() == ref_err == (0, 0)
     ctx.close()
+
+
+@pytest.mark.parametrize("cta", [1, 4])
+def test_sampler_cta_gives_up_on_a_request_with_a_bad_logit(cta):
+    """One sampler CTA of every request acts as if its wait ran out, on a
+    batch where two sampled requests also carry a NaN / +inf logit: that
+    CTA stops at the wait, its peers at the logit check.  Each failed
+    request's CTAs still all count in, so the next normal calls on the same
+    context (clean inputs) give a fresh context's results and no error."""
+    wl = workloads.make_random(12, 5, 70000, "bf16", gen_seed=324, temps=(0.0, 1.0), verify_seed=3)
+    sampled = (wl.temperature > 0).numpy()
+    bad = [int(b) for b in sampled.nonzero()[0][:2]]
+    assert len(bad) == 2 and (~sampled).any()
+    target = wl.target.clone()
+    target[bad[0], 1, 12345] = float("nan")
+    target[bad[1], 0, 69999] = float("inf")
+    ctx = binding.SpecVerify(12, 5, 70000, torch.bfloat16)
+    ctx.debug_late_cta(cta)
+    toks, acc, kv = _host(ctx(target.cuda(), wl.draft.cuda(), wl.tokens.cuda(), wl.temperature.cuda(), 7))
+    code, bits = ctx.get_error()
+    assert bits & binding.SV_ERRBIT_WAIT and bits & binding.SV_ERRBIT_LOGIT, (code, bits)
+    assert (acc[sampled] == -1).all() and (kv[sampled] == 0).all() and (toks[sampled] == -1).all()
+    ctx.debug_late_cta(-1)
+    for seed in (7, 8):
+        got = _host(ctx(*_inputs(wl), seed))
+        ref, ref_err = _fresh(wl, seed)
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b), seed
+        assert ctx.get_error() == ref_err == (0, 0)
+    ctx.close()
