@@ -29,13 +29,15 @@
 // tree_walk_kernel gives each request a cluster of kTreeCluster CTAs.  Every
 // CTA merges the partials of all rows and fetches the logits of every child
 // at its token (thread i holds node i), then all of them run the same walk:
-// one thread decides, and each rejection in SAMPLED mode triggers a pass in
-// which every CTA sums max(r(t) - p(t), 0) over its share of the vocabulary
-// and the cluster's partial sums are exchanged through distributed shared
-// memory after a cluster barrier, so every CTA holds the same normaliser.
-// The final draw computes, per level-1 block, the block's mass and the token
-// levels 2-4 would pick in it (each CTA its own blocks), then rank 0 picks
-// level 1.  All arithmetic is float32; each CTA takes the same decisions
+// one thread decides, and each rejection in SAMPLED mode of a child that has
+// a later sibling triggers a pass in which every CTA sums max(r(t) - p(t), 0)
+// over its share of the vocabulary and the cluster's partial sums are
+// exchanged through distributed shared memory after a cluster barrier, so
+// every CTA holds the same normaliser for that sibling's test.  After the
+// last sibling is rejected no pass runs: the draw is scale-free and needs
+// only the new residual's offset, known already.  The final draw computes,
+// per level-1 block, the block's mass and the token levels 2-4 would pick in
+// it (each CTA its own blocks), then rank 0 picks level 1.  All arithmetic is float32; each CTA takes the same decisions
 // from the same numbers, so the cluster stays in step.
 
 #include <climits>
@@ -147,6 +149,11 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   __shared__ unsigned s_err;
   __shared__ int s_node, s_depth, s_child, s_m, s_plen, s_act;
   __shared__ float s_rej_mass, s_c, s_d;  // s_c, s_d: c_m and D_m of the residual
+  // after the node's last child is rejected: c_m before that rejection, and
+  // whether D of the new residual is still unknown (no pass was run)
+  __shared__ float s_cprev;
+  __shared__ int s_tentative;
+  __shared__ float s_cmass;  // the sum of this CTA's level-1 block masses in the draw
 
   const int b = blockIdx.x / kTreeCluster;
   const unsigned rank = cluster_rank();
@@ -312,6 +319,7 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
     s_rej_mass = 0.f;
     s_c = 0.f;
     s_d = 1.f;
+    s_tentative = 0;
   }
   __syncthreads();
   const bool topk = p.mode == kTreeTopk;
@@ -399,7 +407,20 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
           s_c = 0.f;
           s_d = 1.f;
         } else if (!topk) {
-          act = kActPass;
+          if (s_next[c] == kNoNode) {
+            // The node's last child: the draw that follows is scale-free, so
+            // it needs c_{m+1} = c_m + D_m but not D_{m+1}, and no pass runs.
+            // Should (q - c_{m+1} p)_+ have no mass anywhere, the draw finds
+            // out and falls back to r_m, as a pass would have left it.
+            s_cprev = s_c;
+            s_c = s_c + s_d;
+            s_m = m + 1;
+            s_child = kNoNode;
+            s_tentative = 1;
+            act = kActResidual;
+          } else {
+            act = kActPass;
+          }
         }
       }
       s_act = act;
@@ -457,12 +478,6 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   const int node = s_node;
   const int depth = s_depth;
   const bool bonus = s_act == kActBonus;
-  // a draw is scale-free: r_m is taken as (q - c_m p)_+ without the 1 / D_m
-  const NodeLaw law{bonus ? NodeLaw::kQ : (topk ? NodeLaw::kTopk : NodeLaw::kSampled), k,
-                    s_cq[node], 1.f / s_sq[node], s_cp[node], 1.f / s_sp[node], s_c, 1.f, s_m, s_rej};
-  const bool need_y = law.kind == NodeLaw::kSampled && s_m > 0;
-  const T* z = zbase + static_cast<size_t>(node) * V;
-  const T* y = ybase + static_cast<size_t>(node) * V;
   if (i == 0) philox_uniforms4(p.seed, b, depth, 1, s_job.u);
   __syncthreads();
   const Job job = s_job;
@@ -475,42 +490,66 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   __shared__ float s_bmass[kPickSlots];
   __shared__ float s_bcand[kPickSlots];  // the candidate token's bits
   const bool dsm_pick = S3 <= kPickSlots * kTreeCluster;
-  auto rf = [&](float zt, float yt, int t) { return law.r(zt, yt, t); };
-  if (staging) stage_node(node, need_y);
-  int bi = 0;
-  for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster, ++bi) {
-    const int cbeg = c * kLevel1, cend = min(V, cbeg + kLevel1);
-    float h0, h1, mass;
-    int cand;
-    if (staging) {
-      const T* bz = sz + bi * kLevel1;
-      const T* by = sy + bi * kLevel1;
-      law_sums_staged<T>(law, bz, by, need_y, cbeg, cend, h0, h1);
-      cand = block_pick(
-          h0, h1, cbeg, cend, job,
-          [&](int t) {
-            const int e = staged_at<T>(t - cbeg);
-            return law.r(staged_elem(bz + e), need_y ? staged_elem(by + e) : 0.f, t);
-          },
-          sc, &mass);
-    } else {
-      seg_sums<T, kVecPath>(z, y, need_y, cbeg + i * kSegTok, cend, rf, h0, h1);
-      cand = block_pick(
-          h0, h1, cbeg, cend, job,
-          [&](int t) { return law.r(E::load1(z + t), need_y ? E::load1(y + t) : 0.f, t); }, sc, &mass);
-    }
-    if (i == 0) {
-      if (dsm_pick) {
-        s_bmass[bi] = mass;
-        s_bcand[bi] = __int_as_float(cand);
+  while (true) {
+    // a draw is scale-free: r_m is taken as (q - c_m p)_+ without the 1 / D_m
+    const NodeLaw law{bonus ? NodeLaw::kQ : (topk ? NodeLaw::kTopk : NodeLaw::kSampled), k,
+                      s_cq[node], 1.f / s_sq[node], s_cp[node], 1.f / s_sp[node], s_c, 1.f, s_m, s_rej};
+    const bool need_y = law.kind == NodeLaw::kSampled && s_m > 0;
+    const T* z = zbase + static_cast<size_t>(node) * V;
+    const T* y = ybase + static_cast<size_t>(node) * V;
+    auto rf = [&](float zt, float yt, int t) { return law.r(zt, yt, t); };
+    if (staging) stage_node(node, need_y);
+    int bi = 0;
+    float cmass = 0.f;  // thread 0: the masses of this CTA's blocks
+    for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster, ++bi) {
+      const int cbeg = c * kLevel1, cend = min(V, cbeg + kLevel1);
+      float h0, h1, mass;
+      int cand;
+      if (staging) {
+        const T* bz = sz + bi * kLevel1;
+        const T* by = sy + bi * kLevel1;
+        law_sums_staged<T>(law, bz, by, need_y, cbeg, cend, h0, h1);
+        cand = block_pick(
+            h0, h1, cbeg, cend, job,
+            [&](int t) {
+              const int e = staged_at<T>(t - cbeg);
+              return law.r(staged_elem(bz + e), need_y ? staged_elem(by + e) : 0.f, t);
+            },
+            sc, &mass);
       } else {
-        masses[c] = mass;
-        cands[c] = cand;
+        seg_sums<T, kVecPath>(z, y, need_y, cbeg + i * kSegTok, cend, rf, h0, h1);
+        cand = block_pick(
+            h0, h1, cbeg, cend, job,
+            [&](int t) { return law.r(E::load1(z + t), need_y ? E::load1(y + t) : 0.f, t); }, sc, &mass);
+      }
+      if (i == 0) {
+        cmass += mass;
+        if (dsm_pick) {
+          s_bmass[bi] = mass;
+          s_bcand[bi] = __int_as_float(cand);
+        } else {
+          masses[c] = mass;
+          cands[c] = cand;
+        }
       }
     }
+    if (i == 0) s_cmass = cmass;
+    if (!dsm_pick) __threadfence();
+    cluster_sync();  // every block's mass and candidate are stored
+    if (!s_tentative) break;
+    // no pass ran for the last rejection: fall back to r_m if the new
+    // residual has no mass in any CTA (the same answer in every CTA)
+    const float cm = i < kTreeCluster ? ld_dsmem(&s_cmass, static_cast<unsigned>(i)) : 0.f;
+    const bool has_mass = __syncthreads_or(cm > 0.f) != 0;
+    cluster_sync();  // every CTA has read the others' sums
+    if (has_mass) break;
+    if (i == 0) {
+      s_c = s_cprev;
+      s_tentative = 0;
+    }
+    __syncthreads();
   }
   if (dsm_pick) {
-    cluster_sync();  // every block's mass and candidate are in its CTA's shared memory
     if (rank == 0 && i < 32) {
       const int c1 = warp_pick(
           [&](int j) { return ld_dsmem(&s_bmass[j / kTreeCluster], static_cast<unsigned>(j % kTreeCluster)); },
@@ -523,8 +562,6 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
     cluster_sync();  // rank 0 has read the other CTAs' shared memory
     if (rank != 0) return;
   } else {
-    __threadfence();
-    cluster_sync();  // every block's mass and candidate are stored
     if (rank != 0) return;
     if (i < 32) {
       const int c1 = warp_pick([&](int j) { return __ldcg(masses + j); }, S3, job.u[0]);
