@@ -332,29 +332,35 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   T* sy = sz + kStageBlocks * kLevel1;              // the same for y
   if (i == 0) s_staged = -1;
   __syncthreads();
-  // Stage this CTA's blocks of the node's rows (z, and y when read) unless
-  // they are staged already; every thread copies the vectors it will sum.
-  auto stage_node = [&](int node, bool with_y) {
-    if (s_staged == node) return;
+  // Issue this CTA's copies of the node's rows (z, and y when read) into the
+  // staging buffer unless they are staged already: one group of copies per
+  // level-1 block slot (kStageBlocks groups, empty ones included), so a
+  // thread starts on its own vectors of block 0 while block 1's are still
+  // arriving.  Before reading its vectors of slot bi a thread waits for its
+  // own copies with cp_async_wait_pending(kStageBlocks - 1 - bi); other
+  // threads' vectors are read only after a CTA barrier.  Thread 0 records
+  // the node in s_staged after the caller's next CTA barrier (every thread
+  // has read s_staged by then).
+  auto stage_issue = [&](int node, bool with_y) {
+    const bool fresh = s_staged != node;
     const T* z = zbase + static_cast<size_t>(node) * V;
     const T* y = ybase + static_cast<size_t>(node) * V;
-    int bi = 0;
-    for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster, ++bi) {
-      const int cbeg = c * kLevel1, cend = min(V, cbeg + kLevel1);
-      constexpr int kVec = Elem<T>::kVec;
-      for (int v = 0; v < kSegTok / kVec; ++v) {  // the layout of staged_at
-        const int e = i * kSegTok + v * kVec;
-        const int at = bi * kLevel1 + (v * kST + i) * kVec;
-        if (cbeg + e < cend) {
-          cp_async16(sz + at, z + cbeg + e);
-          if (with_y) cp_async16(sy + at, y + cbeg + e);
+    int c = static_cast<int>(rank);
+    for (int bi = 0; bi < kStageBlocks; ++bi, c += kTreeCluster) {
+      if (fresh && c < S3) {
+        const int cbeg = c * kLevel1, cend = min(V, cbeg + kLevel1);
+        constexpr int kVec = Elem<T>::kVec;
+        for (int v = 0; v < kSegTok / kVec; ++v) {  // the layout of staged_at
+          const int e = i * kSegTok + v * kVec;
+          const int at = bi * kLevel1 + (v * kST + i) * kVec;
+          if (cbeg + e < cend) {
+            cp_async16(sz + at, z + cbeg + e);
+            if (with_y) cp_async16(sy + at, y + cbeg + e);
+          }
         }
       }
+      cp_async_commit();
     }
-    cp_async_wait_all();
-    __syncthreads();
-    if (i == 0) s_staged = node;
-    __syncthreads();
   };
   int pass = 0;
   while (true) {
@@ -440,11 +446,12 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
     float acc = 0.f;
     auto lf = [&](float zt, float yt, int t) { return law.r(zt, yt, t); };
     if (staging) {
-      stage_node(node, true);
+      stage_issue(node, true);
       int bi = 0;
       for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster, ++bi) {
         float h0, h1;
         const int cbeg = c * kLevel1;
+        cp_async_wait_pending(kStageBlocks - 1 - bi);  // this thread's copies of slot bi
         law_sums_staged<T>(law, sz + bi * kLevel1, sy + bi * kLevel1, true, cbeg, min(V, cbeg + kLevel1), h0,
                            h1);
         acc += h0 + h1;
@@ -458,7 +465,10 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
       }
     }
     acc = cta_sum(acc, sc.red);
-    if (i == 0) s_part[pass & 1] = acc;
+    if (i == 0) {
+      s_part[pass & 1] = acc;
+      if (staging) s_staged = node;
+    }
     cluster_sync();
     if (i == 0) {
       float total = 0.f;
@@ -498,7 +508,7 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
     const T* z = zbase + static_cast<size_t>(node) * V;
     const T* y = ybase + static_cast<size_t>(node) * V;
     auto rf = [&](float zt, float yt, int t) { return law.r(zt, yt, t); };
-    if (staging) stage_node(node, need_y);
+    if (staging) stage_issue(node, need_y);
     int bi = 0;
     float cmass = 0.f;  // thread 0: the masses of this CTA's blocks
     for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster, ++bi) {
@@ -508,6 +518,7 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
       if (staging) {
         const T* bz = sz + bi * kLevel1;
         const T* by = sy + bi * kLevel1;
+        cp_async_wait_pending(kStageBlocks - 1 - bi);  // this thread's copies of slot bi
         law_sums_staged<T>(law, bz, by, need_y, cbeg, cend, h0, h1);
         cand = block_pick(
             h0, h1, cbeg, cend, job,
@@ -536,6 +547,7 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
     if (i == 0) s_cmass = cmass;
     if (!dsm_pick) __threadfence();
     cluster_sync();  // every block's mass and candidate are stored
+    if (staging && i == 0) s_staged = node;
     if (!s_tentative) break;
     // no pass ran for the last rejection: fall back to r_m if the new
     // residual has no mass in any CTA (the same answer in every CTA)
