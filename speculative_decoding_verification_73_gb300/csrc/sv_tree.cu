@@ -144,7 +144,8 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   __shared__ float s_cq[kMaxNodes], s_sq[kMaxNodes], s_cp[kMaxNodes], s_sp[kMaxNodes];
   __shared__ float s_zc[kMaxNodes], s_yc[kMaxNodes];
   __shared__ float s_part[2];
-  __shared__ BlockScratch sc;
+  __shared__ BlockScratch scs[2];  // the draw's two staged blocks; scs[0] otherwise
+  BlockScratch& sc = scs[0];
   __shared__ Job s_job;
   __shared__ unsigned s_err;
   __shared__ int s_node, s_depth, s_child, s_m, s_plen, s_act;
@@ -327,7 +328,13 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   const T* ybase = use_draft ? static_cast<const T*>(p.draft) + static_cast<size_t>(b) * (M + 1) * V
                              : zbase;
   const int S3 = w.S3;
-  const bool staging = tree_stages<T, kVecPath>() && S3 <= kStageBlocks * kTreeCluster;
+  // this CTA's level-1 blocks: the nbpc consecutive blocks from cfirst (the
+  // layout of the chain sampler's blocks, so a one-child tree draws from the
+  // same per-block masses in the same order)
+  const int nbpc = (S3 + kTreeCluster - 1) / kTreeCluster;
+  const int cfirst = static_cast<int>(rank) * nbpc;
+  const int clast = min(S3, cfirst + nbpc);
+  const bool staging = tree_stages<T, kVecPath>() && nbpc <= kStageBlocks;
   T* sz = reinterpret_cast<T*>(s_stage_raw);        // [kStageBlocks][kLevel1] of z
   T* sy = sz + kStageBlocks * kLevel1;              // the same for y
   if (i == 0) s_staged = -1;
@@ -345,9 +352,8 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
     const bool fresh = s_staged != node;
     const T* z = zbase + static_cast<size_t>(node) * V;
     const T* y = ybase + static_cast<size_t>(node) * V;
-    int c = static_cast<int>(rank);
-    for (int bi = 0; bi < kStageBlocks; ++bi, c += kTreeCluster) {
-      if (fresh && c < S3) {
+    for (int bi = 0, c = cfirst; bi < kStageBlocks; ++bi, ++c) {
+      if (fresh && c < clast) {
         const int cbeg = c * kLevel1, cend = min(V, cbeg + kLevel1);
         constexpr int kVec = Elem<T>::kVec;
         for (int v = 0; v < kSegTok / kVec; ++v) {  // the layout of staged_at
@@ -448,7 +454,7 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
     if (staging) {
       stage_issue(node, true);
       int bi = 0;
-      for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster, ++bi) {
+      for (int c = cfirst; c < clast; ++c, ++bi) {
         float h0, h1;
         const int cbeg = c * kLevel1;
         cp_async_wait_pending(kStageBlocks - 1 - bi);  // this thread's copies of slot bi
@@ -457,7 +463,7 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
         acc += h0 + h1;
       }
     } else {
-      for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster) {
+      for (int c = cfirst; c < clast; ++c) {
         float h0, h1;
         seg_sums<T, kVecPath>(z, y, true, c * kLevel1 + i * kSegTok, min(V, (c + 1) * kLevel1), lf, h0,
                               h1);
@@ -494,12 +500,12 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   float* masses = w.chunk_sums + static_cast<size_t>(b) * S3;
   int* cands = w.blk_tok + static_cast<size_t>(b) * S3;
   // the blocks' masses and candidates reach rank 0 through distributed
-  // shared memory (block c in slot c / kTreeCluster of CTA c % kTreeCluster)
-  // when they fit the slots, else through the workspace
+  // shared memory (block c in slot c % nbpc of CTA c / nbpc) when they fit
+  // the slots, else through the workspace
   constexpr int kPickSlots = 16;
   __shared__ float s_bmass[kPickSlots];
   __shared__ float s_bcand[kPickSlots];  // the candidate token's bits
-  const bool dsm_pick = S3 <= kPickSlots * kTreeCluster;
+  const bool dsm_pick = nbpc <= kPickSlots;
   while (true) {
     // a draw is scale-free: r_m is taken as (q - c_m p)_+ without the 1 / D_m
     const NodeLaw law{bonus ? NodeLaw::kQ : (topk ? NodeLaw::kTopk : NodeLaw::kSampled), k,
@@ -509,38 +515,60 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
     const T* y = ybase + static_cast<size_t>(node) * V;
     auto rf = [&](float zt, float yt, int t) { return law.r(zt, yt, t); };
     if (staging) stage_issue(node, need_y);
-    int bi = 0;
     float cmass = 0.f;  // thread 0: the masses of this CTA's blocks
-    for (int c = static_cast<int>(rank); c < S3; c += kTreeCluster, ++bi) {
-      const int cbeg = c * kLevel1, cend = min(V, cbeg + kLevel1);
-      float h0, h1, mass;
-      int cand;
-      if (staging) {
-        const T* bz = sz + bi * kLevel1;
-        const T* by = sy + bi * kLevel1;
+    if (staging) {
+      // both staged blocks' sums, then their picks with one set of CTA barriers
+      const int nb = max(0, clast - cfirst);
+      float h0[kStageBlocks], h1[kStageBlocks], mass[kStageBlocks];
+      int cand[kStageBlocks];
+#pragma unroll
+      for (int bi = 0; bi < kStageBlocks; ++bi) {
+        h0[bi] = 0.f;
+        h1[bi] = 0.f;
         cp_async_wait_pending(kStageBlocks - 1 - bi);  // this thread's copies of slot bi
-        law_sums_staged<T>(law, bz, by, need_y, cbeg, cend, h0, h1);
-        cand = block_pick(
-            h0, h1, cbeg, cend, job,
-            [&](int t) {
-              const int e = staged_at<T>(t - cbeg);
-              return law.r(staged_elem(bz + e), need_y ? staged_elem(by + e) : 0.f, t);
-            },
-            sc, &mass);
-      } else {
+        if (bi < nb) {
+          const int cbeg = (cfirst + bi) * kLevel1;
+          law_sums_staged<T>(law, sz + bi * kLevel1, sy + bi * kLevel1, need_y, cbeg, min(V, cbeg + kLevel1),
+                             h0[bi], h1[bi]);
+        }
+      }
+      blocks_pick<kStageBlocks>(
+          h0, h1, cfirst * kLevel1, V, nb, job,
+          [&](int bb, int t) {
+            const int e = bb * kLevel1 + staged_at<T>(t - (cfirst + bb) * kLevel1);
+            return law.r(staged_elem(sz + e), need_y ? staged_elem(sy + e) : 0.f, t);
+          },
+          scs, mass, cand);
+      if (i == 0) {
+        for (int bi = 0; bi < nb; ++bi) {
+          cmass += mass[bi];
+          if (dsm_pick) {
+            s_bmass[bi] = mass[bi];
+            s_bcand[bi] = __int_as_float(cand[bi]);
+          } else {
+            masses[cfirst + bi] = mass[bi];
+            cands[cfirst + bi] = cand[bi];
+          }
+        }
+      }
+    } else {
+      int bi = 0;
+      for (int c = cfirst; c < clast; ++c, ++bi) {
+        const int cbeg = c * kLevel1, cend = min(V, cbeg + kLevel1);
+        float h0, h1, mass;
         seg_sums<T, kVecPath>(z, y, need_y, cbeg + i * kSegTok, cend, rf, h0, h1);
-        cand = block_pick(
+        const int cand = block_pick(
             h0, h1, cbeg, cend, job,
             [&](int t) { return law.r(E::load1(z + t), need_y ? E::load1(y + t) : 0.f, t); }, sc, &mass);
-      }
-      if (i == 0) {
-        cmass += mass;
-        if (dsm_pick) {
-          s_bmass[bi] = mass;
-          s_bcand[bi] = __int_as_float(cand);
-        } else {
-          masses[c] = mass;
-          cands[c] = cand;
+        if (i == 0) {
+          cmass += mass;
+          if (dsm_pick) {
+            s_bmass[bi] = mass;
+            s_bcand[bi] = __int_as_float(cand);
+          } else {
+            masses[c] = mass;
+            cands[c] = cand;
+          }
         }
       }
     }
@@ -564,11 +592,10 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   if (dsm_pick) {
     if (rank == 0 && i < 32) {
       const int c1 = warp_pick(
-          [&](int j) { return ld_dsmem(&s_bmass[j / kTreeCluster], static_cast<unsigned>(j % kTreeCluster)); },
+          [&](int j) { return ld_dsmem(&s_bmass[j % nbpc], static_cast<unsigned>(j / nbpc)); },
           S3, job.u[0]);
       if (i == 0)
-        s_child = c1 >= 0 ? __float_as_int(ld_dsmem(&s_bcand[c1 / kTreeCluster],
-                                                    static_cast<unsigned>(c1 % kTreeCluster)))
+        s_child = c1 >= 0 ? __float_as_int(ld_dsmem(&s_bcand[c1 % nbpc], static_cast<unsigned>(c1 / nbpc)))
                           : 0;
     }
     cluster_sync();  // rank 0 has read the other CTAs' shared memory
