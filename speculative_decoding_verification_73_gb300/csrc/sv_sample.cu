@@ -15,8 +15,9 @@
 // rounding leaves none).  The law is exactly r / sum(r), and every decision
 // compares a uniform against at most a few dozen float32 edges.
 //
-// Grid: one CTA per request and group of blocks_per_cta() level-1 blocks,
-// request-major, launched with programmatic dependent launch: it becomes
+// Grid: one CTA per request and group of blocks_per_cta() level-1 blocks
+// (one block per CTA when the batch is small enough that the grid would
+// leave SMs idle), request-major, launched with programmatic dependent launch: it becomes
 // resident once every row-statistics CTA has started, while that grid
 // drains, and never waits for the grid as a whole.  The walk polls the tags
 // of its own request's partials instead, so the requests whose rows were
@@ -68,10 +69,19 @@ template <typename T>
 constexpr int blocks_per_cta() {
   return sizeof(T) == 2 ? SV_SAMPLE_BF16_BLOCKS : 1;
 }
-template <typename T>
+template <typename T, int kB>
 constexpr int stage_bytes() {
-  return 2 * blocks_per_cta<T>() * kLevel1 * static_cast<int>(sizeof(T));
+  return 2 * kB * kLevel1 * static_cast<int>(sizeof(T));
 }
+// A batch whose sampler grid at blocks_per_cta() blocks per CTA would leave
+// most SMs idle takes one block per CTA instead (twice the CTAs, half the
+// staging and arithmetic each): when the one-block grid has at most
+// SV_SAMPLE_SMALL_PER_SM CTAs per SM (mixture-bf16, B 16 at V 163840: 23-25
+// against 27.2 us per call; batch64-bf16 keeps two blocks per CTA).
+// Build-time override -DSV_SAMPLE_SMALL_PER_SM=<n> (0: never).
+#ifndef SV_SAMPLE_SMALL_PER_SM
+#define SV_SAMPLE_SMALL_PER_SM 3
+#endif
 
 // Arrival counting of a request's sampler CTAs: each adds 1 to the
 // request's word (plus kLateUnit when its wait for the row statistics ran
@@ -242,9 +252,8 @@ __device__ int block_candidate_global(const T* z, const T* y, int cbeg, int V, c
 #define SV_SAMPLE_MINB 3
 #endif
 
-template <typename T, bool kVecPath>
+template <typename T, bool kVecPath, int kB>
 __global__ void __launch_bounds__(kST, SV_SAMPLE_MINB) sample_kernel(Problem p, Workspace w) {
-  constexpr int kB = blocks_per_cta<T>();
   extern __shared__ __align__(16) unsigned char s_rows[];  // staged rows (vector path)
   __shared__ BlockScratch scs[kB];
   BlockScratch& sc = scs[0];
@@ -384,17 +393,16 @@ __global__ void __launch_bounds__(kST, SV_SAMPLE_MINB) sample_kernel(Problem p, 
   if (threadIdx.x == 0) p.out_tokens[static_cast<size_t>(b) * (N + 1) + job.row] = sc.tok;
 }
 
-template <typename T, bool kVecPath>
-cudaError_t launch_sample_t(const Problem& p, const Workspace& w, cudaStream_t s) {
-  constexpr int kB = blocks_per_cta<T>();
+template <typename T, bool kVecPath, int kB>
+cudaError_t launch_sample_k(const Problem& p, const Workspace& w, cudaStream_t s) {
   const long long blocks = static_cast<long long>(p.B) * ((w.S3 + kB - 1) / kB);
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  const int smem = kVecPath ? stage_bytes<T>() : 0;
+  const int smem = kVecPath ? stage_bytes<T, kB>() : 0;
   if (kVecPath) {
     // above the default 48 KB of dynamic shared memory: opt in (cheap, idempotent)
-    const cudaError_t e =
-        cudaFuncSetAttribute(sample_kernel<T, kVecPath>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const cudaError_t e = cudaFuncSetAttribute(sample_kernel<T, kVecPath, kB>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
   }
   // Programmatic dependent launch: the grid may be scheduled once every
@@ -410,7 +418,22 @@ cudaError_t launch_sample_t(const Problem& p, const Workspace& w, cudaStream_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, sample_kernel<T, kVecPath>, p, w);
+  return cudaLaunchKernelEx(&cfg, sample_kernel<T, kVecPath, kB>, p, w);
+}
+
+template <typename T, bool kVecPath>
+cudaError_t launch_sample_t(const Problem& p, const Workspace& w, cudaStream_t s) {
+  constexpr int kB = blocks_per_cta<T>();
+  if (kB > 1 && SV_SAMPLE_SMALL_PER_SM > 0) {
+    int dev = 0, sms = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    if (static_cast<long long>(p.B) * w.S3 <= static_cast<long long>(sms) * SV_SAMPLE_SMALL_PER_SM)
+      return launch_sample_k<T, kVecPath, 1>(p, w, s);
+  }
+  return launch_sample_k<T, kVecPath, kB>(p, w, s);
 }
 
 }  // namespace
