@@ -48,6 +48,10 @@ LAZY_CASES = {
     "batch64-bf16": workloads.batch64_bf16,
     "lowaccept64-bf16": workloads.low_accept_bf16,
     "no-drafts": lambda: workloads.make_random(6, 0, 5000, "f32", gen_seed=93),
+    # 34 spans and 135 level-1 blocks per row: partials, token logits and the
+    # draw's masses go through the workspace instead of distributed shared memory
+    "huge-vocabulary-bf16": lambda: workloads.make_random(3, 3, 1100000, "bf16", gen_seed=96, verify_seed=5,
+                                                          temps=(0.7, 1.0)),
 }
 
 

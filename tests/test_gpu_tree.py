@@ -80,6 +80,15 @@ CASES = {
     # seven spans per fp32 row: partials merged past the first four
     "many-spans-sampled-f32": lambda: workloads.make_tree(4, 100000, "f32", gen_seed=79, widths=(3, 2),
                                                           verify_seed=12),
+    # 21 level-1 blocks of bf16: three per CTA, so the rows are not staged and
+    # each block is picked on its own
+    "three-blocks-per-cta-bf16": lambda: workloads.make_tree(6, 170000, "bf16", gen_seed=86,
+                                                             widths=(2, 2, 2), temps=(0.7, 1.0),
+                                                             verify_seed=13),
+    # 135 level-1 blocks: the draw's masses and candidates go through the
+    # workspace instead of distributed shared memory
+    "huge-vocabulary-bf16": lambda: workloads.make_tree(2, 1100000, "bf16", gen_seed=87, widths=(2, 2),
+                                                        temps=(0.7, 1.0), verify_seed=14),
 }
 
 
