@@ -4,7 +4,7 @@
 // 3.1": LayerNorm on each of the three target hidden states before the FC;
 // the EAGLE 3.1 news page speaks of RMSNorm; no norm is EAGLE-3).
 //
-// fcnorm_prep (LayerNorm / RMSNorm): two warps (one for rows past 4096
+// fcnorm_prep (LayerNorm / RMSNorm): four warps (one for rows past 4096
 // elements) per (token, segment) compute the row's mean and
 // 1/sqrt(var + eps) (LayerNorm; mean 0 and 1/sqrt(mean square + eps) for
 // RMSNorm) in fp32 and write the normalised row, rounded to bf16, into its
@@ -73,17 +73,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 
-// Two warps per (token, segment) row of d <= 4096 elements, the row held in
-// registers: warp half h of the row keeps, in lane l, the 16-byte vectors
-// 256 h + l + 32 i (i < kPrepVpl), so the row is read from global memory
-// once; each warp sums its half, the two halves' sums meet in shared memory
-// (the same two numbers added in the same order by both warps), then the
-// same for the squared deviations, and each warp writes its half of the
-// normalised row.  Half the registers of a warp per row, so twice the warps
-// hide the loads' latency.  Every thread of the CTA reaches its barriers.
-// Build-time override -DSV_PREP_SPLIT=<warps per row> (2 or 4).
+// kPrepSplit warps per (token, segment) row of d <= 4096 elements, the row
+// held in registers: warp h of the row keeps, in lane l, the 16-byte vectors
+// 32 kPrepVpl h + l + 32 i (i < kPrepVpl), so the row is read from global
+// memory once; each warp sums its part, the parts' sums meet in shared
+// memory (the same numbers added in the same order by every warp of the
+// row), then the same for the squared deviations, and each warp writes its
+// part of the normalised row.  Four warps per row at 40 registers (six CTAs
+// per SM) measured 319.7 us per LayerNorm call at T = d = d_out = 4096,
+// against 322.1 with two warps per row at 64 registers (four per SM) and
+// 327.6 with four per row at 32 registers.  Every thread of the CTA reaches
+// its barriers.  Build-time override -DSV_PREP_SPLIT=<warps per row> (2 or 4).
 #ifndef SV_PREP_SPLIT
-#define SV_PREP_SPLIT 2
+#define SV_PREP_SPLIT 4
 #endif
 constexpr int kPrepSplit = SV_PREP_SPLIT;          // warps per row
 constexpr int kPrepVpl = 16 / kPrepSplit;          // vectors per lane and warp
@@ -226,11 +228,11 @@ __device__ __forceinline__ void prep_row_loop(const FcNormProblem& p, const __nv
 
 // Resident CTAs per SM the normalisation kernels are built for.
 #ifndef SV_PREP_MINB
-#define SV_PREP_MINB 4
+#define SV_PREP_MINB 6
 #endif
 
-// Rows of at most 4096 elements (and 16-byte aligned gamma / beta): two
-// warps per row, four rows per CTA.
+// Rows of at most 4096 elements (and 16-byte aligned gamma / beta):
+// kPrepSplit warps per row, 8 / kPrepSplit rows per CTA.
 __global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_split_kernel(FcNormProblem p) {
   allow_dependents();  // the GEMM's CTAs may be scheduled as this grid drains
   __shared__ float s_part[8];
