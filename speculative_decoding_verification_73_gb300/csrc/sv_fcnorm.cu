@@ -4,11 +4,12 @@
 // 3.1": LayerNorm on each of the three target hidden states before the FC;
 // the EAGLE 3.1 news page speaks of RMSNorm; no norm is EAGLE-3).
 //
-// fcnorm_prep (LayerNorm / RMSNorm): four warps (one for rows past 4096
-// elements) per (token, segment) compute the row's mean and
-// 1/sqrt(var + eps) (LayerNorm; mean 0 and 1/sqrt(mean square + eps) for
-// RMSNorm) in fp32 and write the normalised row, rounded to bf16, into its
-// third of the concatenated input X [T, 3d].  fc_gemm: a persistent tcgen05
+// fcnorm_prep (LayerNorm / RMSNorm): for each (token, segment) row the
+// row's mean and 1/sqrt(var + eps) (LayerNorm; mean 0 and
+// 1/sqrt(mean square + eps) for RMSNorm) in fp32, and the normalised row,
+// rounded to bf16, written into its third of the concatenated input
+// X [T, 3d] -- a CTA per four tokens of one segment (one warp per row past
+// 4096 elements).  fc_gemm: a persistent tcgen05
 // GEMM out = X W^T + bias -- with no normalisation it reads the three
 // hidden states themselves, K step kb from the state kb / (d / 64), and
 // nothing runs before it -- one CTA per SM walking 128 x bn output tiles
@@ -73,108 +74,33 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 
-// kPrepSplit warps per (token, segment) row of d <= 4096 elements, the row
-// held in registers: warp h of the row keeps, in lane l, the 16-byte vectors
-// 32 kPrepVpl h + l + 32 i (i < kPrepVpl), so the row is read from global
-// memory once; each warp sums its part, the parts' sums meet in shared
-// memory (the same numbers added in the same order by every warp of the
-// row), then the same for the squared deviations, and each warp writes its
-// part of the normalised row.  Four warps per row at 40 registers (six CTAs
-// per SM) measured 319.7 us per LayerNorm call at T = d = d_out = 4096,
-// against 322.1 with two warps per row at 64 registers (four per SM) and
-// 327.6 with four per row at 32 registers.  Every thread of the CTA reaches
-// its barriers.  Build-time override -DSV_PREP_SPLIT=<warps per row> (2 or 4).
-#ifndef SV_PREP_SPLIT
-#define SV_PREP_SPLIT 4
-#endif
-constexpr int kPrepSplit = SV_PREP_SPLIT;          // warps per row
-constexpr int kPrepVpl = 16 / kPrepSplit;          // vectors per lane and warp
-constexpr int kPrepRowsPerCta = 8 / kPrepSplit;    // 8 warps per CTA
-static_assert(kPrepSplit == 2 || kPrepSplit == 4, "a row split over 2 or 4 warps");
-// The row's total of one per-warp partial each, in warp order (the same
-// additions in every warp of the row).
-__device__ __forceinline__ float row_total(const float* s_part, int wl) {
-  const int first = wl - wl % kPrepSplit;
-  float t = s_part[first];
+// Rows of d <= 4096 elements with 16-byte aligned gamma / beta: one CTA
+// normalises kPrepRows consecutive tokens of one segment.  Warp w holds, in
+// lane l, the 16-byte vectors 64 w + 32 i + l (i < 2) of each of those rows,
+// so every element is read from global memory once; each warp sums its part
+// of every row, the parts meet in shared memory (added in warp order, the
+// same in every warp), then the same for the squared deviations.  Since a
+// warp holds the same columns of all the CTA's rows, it loads each gamma /
+// beta vector once and applies it to every row: the loads of gamma / beta
+// (four times the bytes of the row vector they scale) kept the kernel bound
+// by L1 when every warp had its own row.
+constexpr int kPrepRows = 4;   // tokens of one segment per CTA
+constexpr int kPrepVec = 2;    // vectors per lane and row: 8 warps x 32 lanes x 2 x 8 = 4096 columns
+constexpr int kPrepMaxD = 8 * 32 * kPrepVec * 8;
+
+__device__ __forceinline__ float vsum8(const uint4& v) {
+  float t = 0.f;
 #pragma unroll
-  for (int k = 1; k < kPrepSplit; ++k) t += s_part[first + k];
+  for (int e = 0; e < 8; ++e) t += Elem<__nv_bfloat16>::get(v, e);  // zeros past the row
   return t;
 }
 
-__device__ __forceinline__ void prep_row_split(const FcNormProblem& p, const __nv_bfloat16* h,
-                                               __nv_bfloat16* x, const float* g, const float* bt, bool live,
-                                               int half, int lane, float* s_part) {
-  constexpr int kSpan = 32 * kPrepVpl;  // vectors of the row per warp
-  const int nvec = p.d / 8;
-  const int wl = threadIdx.x >> 5;
-  uint4 v[kPrepVpl];
+// The CTA's total of one per-warp partial each, in warp order.
+__device__ __forceinline__ float warps_total(const float* s_part) {
+  float t = s_part[0];
 #pragma unroll
-  for (int i = 0; i < kPrepVpl; ++i) {
-    const int q = kSpan * half + lane + 32 * i;
-    v[i] = (live && q < nvec) ? *reinterpret_cast<const uint4*>(h + 8 * q) : make_uint4(0u, 0u, 0u, 0u);
-  }
-  float mu = 0.f, rstd = 1.f;
-  if (p.norm != kNormNone) {
-    if (p.norm == kNormLayer) {
-      float sum = 0.f;
-#pragma unroll
-      for (int i = 0; i < kPrepVpl; ++i) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sum += Elem<__nv_bfloat16>::get(v[i], e);  // zeros past the row
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-      if (lane == 0) s_part[wl] = sum;
-      __syncthreads();
-      mu = row_total(s_part, wl) / static_cast<float>(p.d);
-      __syncthreads();  // every warp of the row has read s_part
-    }
-    float sq = 0.f;
-#pragma unroll
-    for (int i = 0; i < kPrepVpl; ++i) {
-      if (kSpan * half + lane + 32 * i < nvec) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float y = Elem<__nv_bfloat16>::get(v[i], e) - mu;
-          sq = fmaf(y, y, sq);
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(kFull, sq, o);
-    if (lane == 0) s_part[wl] = sq;
-    __syncthreads();
-    rstd = rsqrtf(row_total(s_part, wl) / static_cast<float>(p.d) + p.eps);
-  }
-  if (!live) return;
-#pragma unroll
-  for (int i = 0; i < kPrepVpl; ++i) {
-    const int q = kSpan * half + lane + 32 * i;
-    if (q >= nvec) continue;
-    uint4 o = v[i];
-    if (p.norm != kNormNone) {
-      const int f = 8 * q;
-      const float4 g0 = __ldg(reinterpret_cast<const float4*>(g + f));
-      const float4 g1 = __ldg(reinterpret_cast<const float4*>(g + f + 4));
-      float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
-      if (bt != nullptr) {
-        b0 = __ldg(reinterpret_cast<const float4*>(bt + f));
-        b1 = __ldg(reinterpret_cast<const float4*>(bt + f + 4));
-      }
-      const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-      const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-      float y[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float z = (Elem<__nv_bfloat16>::get(v[i], e) - mu) * rstd * gg[e];
-        if (bt != nullptr) z += bb[e];
-        y[e] = z;
-      }
-      o = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
-                     pack_bf16(y[6], y[7]));
-    }
-    *reinterpret_cast<uint4*>(x + 8 * q) = o;
-  }
+  for (int w = 1; w < 8; ++w) t += s_part[w];
+  return t;
 }
 
 // The same statistics and output for any row length, three passes over the
@@ -226,26 +152,116 @@ __device__ __forceinline__ void prep_row_loop(const FcNormProblem& p, const __nv
   }
 }
 
-// Resident CTAs per SM the normalisation kernels are built for.
+// Resident CTAs per SM the normalisation kernel of short rows is built for.
 #ifndef SV_PREP_MINB
-#define SV_PREP_MINB 6
+#define SV_PREP_MINB 4
 #endif
 
-// Rows of at most 4096 elements (and 16-byte aligned gamma / beta):
-// kPrepSplit warps per row, 8 / kPrepSplit rows per CTA.
-__global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_split_kernel(FcNormProblem p) {
+__global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_rows_kernel(FcNormProblem p) {
   allow_dependents();  // the GEMM's CTAs may be scheduled as this grid drains
-  __shared__ float s_part[8];
+  __shared__ float s_part[kPrepRows][8];
   const int wl = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kPrepRowsPerCta + wl / kPrepSplit;
-  const bool live = row < p.T * 3;
-  const int t = live ? row / 3 : 0, s = live ? row - t * 3 : 0;
-  const int d = p.d;
-  const __nv_bfloat16* h = (s == 0 ? p.h[0] : s == 1 ? p.h[1] : p.h[2]) + static_cast<size_t>(t) * d;
-  __nv_bfloat16* x = p.x + static_cast<size_t>(t) * 3 * d + static_cast<size_t>(s) * d;
-  const float* g = p.norm != kNormNone ? p.gamma + static_cast<size_t>(s) * d : nullptr;
-  const float* bt = p.beta != nullptr ? p.beta + static_cast<size_t>(s) * d : nullptr;
-  prep_row_split(p, h, x, g, bt, live, wl % kPrepSplit, lane, s_part);
+  const int groups = (p.T + kPrepRows - 1) / kPrepRows;
+  const int sg = blockIdx.x / groups;  // segment: h_early, h_mid, h_late
+  const int t0 = (blockIdx.x - sg * groups) * kPrepRows;
+  const int d = p.d, nvec = d / 8;
+  const __nv_bfloat16* h = sg == 0 ? p.h[0] : sg == 1 ? p.h[1] : p.h[2];
+  uint4 v[kPrepRows][kPrepVec];
+#pragma unroll
+  for (int r = 0; r < kPrepRows; ++r) {
+#pragma unroll
+    for (int i = 0; i < kPrepVec; ++i) {
+      const int q = 64 * wl + 32 * i + lane;
+      const int t = t0 + r;
+      v[r][i] = (t < p.T && q < nvec) ? *reinterpret_cast<const uint4*>(h + static_cast<size_t>(t) * d + 8 * q)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  float mu[kPrepRows], rstd[kPrepRows];
+#pragma unroll
+  for (int r = 0; r < kPrepRows; ++r) {
+    mu[r] = 0.f;
+    rstd[r] = 1.f;
+  }
+  if (p.norm != kNormNone) {
+    if (p.norm == kNormLayer) {
+#pragma unroll
+      for (int r = 0; r < kPrepRows; ++r) {
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < kPrepVec; ++i) sum += vsum8(v[r][i]);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
+        if (lane == 0) s_part[r][wl] = sum;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int r = 0; r < kPrepRows; ++r) mu[r] = warps_total(s_part[r]) / static_cast<float>(d);
+      __syncthreads();  // every warp has read s_part
+    }
+#pragma unroll
+    for (int r = 0; r < kPrepRows; ++r) {
+      float sq = 0.f;
+#pragma unroll
+      for (int i = 0; i < kPrepVec; ++i) {
+        if (64 * wl + 32 * i + lane < nvec) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float y = Elem<__nv_bfloat16>::get(v[r][i], e) - mu[r];
+            sq = fmaf(y, y, sq);
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(kFull, sq, o);
+      if (lane == 0) s_part[r][wl] = sq;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kPrepRows; ++r)
+      rstd[r] = rsqrtf(warps_total(s_part[r]) / static_cast<float>(d) + p.eps);
+  }
+  const float* g = p.norm != kNormNone ? p.gamma + static_cast<size_t>(sg) * d : nullptr;
+  const float* bt = p.beta != nullptr ? p.beta + static_cast<size_t>(sg) * d : nullptr;
+  __nv_bfloat16* x = p.x + static_cast<size_t>(sg) * d;
+#pragma unroll
+  for (int i = 0; i < kPrepVec; ++i) {
+    const int q = 64 * wl + 32 * i + lane;
+    if (q >= nvec) continue;
+    float gg[8], bb[8];
+    if (p.norm != kNormNone) {
+      const int f = 8 * q;
+      const float4 g0 = __ldg(reinterpret_cast<const float4*>(g + f));
+      const float4 g1 = __ldg(reinterpret_cast<const float4*>(g + f + 4));
+      float4 b0 = make_float4(0.f, 0.f, 0.f, 0.f), b1 = b0;
+      if (bt != nullptr) {
+        b0 = __ldg(reinterpret_cast<const float4*>(bt + f));
+        b1 = __ldg(reinterpret_cast<const float4*>(bt + f + 4));
+      }
+      gg[0] = g0.x; gg[1] = g0.y; gg[2] = g0.z; gg[3] = g0.w;
+      gg[4] = g1.x; gg[5] = g1.y; gg[6] = g1.z; gg[7] = g1.w;
+      bb[0] = b0.x; bb[1] = b0.y; bb[2] = b0.z; bb[3] = b0.w;
+      bb[4] = b1.x; bb[5] = b1.y; bb[6] = b1.z; bb[7] = b1.w;
+    }
+#pragma unroll
+    for (int r = 0; r < kPrepRows; ++r) {
+      const int t = t0 + r;
+      if (t >= p.T) continue;
+      uint4 o = v[r][i];
+      if (p.norm != kNormNone) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float z = (Elem<__nv_bfloat16>::get(v[r][i], e) - mu[r]) * rstd[r] * gg[e];
+          if (bt != nullptr) z += bb[e];
+          y[e] = z;
+        }
+        o = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                       pack_bf16(y[6], y[7]));
+      }
+      *reinterpret_cast<uint4*>(x + static_cast<size_t>(t) * 3 * d + 8 * q) = o;
+    }
+  }
 }
 
 // Any other row: one warp per row, three passes.
@@ -606,8 +622,8 @@ cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s) {
   const bool direct = SV_FC_DIRECT && p.norm == kNormNone;
   cudaError_t e;
   if (!direct) {
-    if (p.d <= 8 * 32 * kPrepVpl * kPrepSplit && p.gb_vec)
-      fcnorm_prep_split_kernel<<<(rows + kPrepRowsPerCta - 1) / kPrepRowsPerCta, 256, 0, s>>>(p);
+    if (p.d <= kPrepMaxD && p.gb_vec)
+      fcnorm_prep_rows_kernel<<<3 * ((p.T + kPrepRows - 1) / kPrepRows), 256, 0, s>>>(p);
     else
       fcnorm_prep_kernel<<<(rows * 32 + 255) / 256, 256, 0, s>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
