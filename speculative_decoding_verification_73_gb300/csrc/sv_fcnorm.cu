@@ -177,6 +177,8 @@ __global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_rows_kernel(FcN
                                       : make_uint4(0u, 0u, 0u, 0u);
     }
   }
+  // the arithmetic in pairs of floats (paired float instructions)
+  using E = Elem<__nv_bfloat16>;
   float mu[kPrepRows], rstd[kPrepRows];
 #pragma unroll
   for (int r = 0; r < kPrepRows; ++r) {
@@ -187,9 +189,15 @@ __global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_rows_kernel(FcN
     if (p.norm == kNormLayer) {
 #pragma unroll
       for (int r = 0; r < kPrepRows; ++r) {
-        float sum = 0.f;
+        uint64_t s2 = f2pack(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < kPrepVec; ++i) sum += vsum8(v[r][i]);
+        for (int i = 0; i < kPrepVec; ++i) {
+#pragma unroll
+          for (int e = 0; e < E::kPairs; ++e) s2 = f2add(s2, E::pair(v[r][i], e));  // zeros past the row
+        }
+        float lo, hi;
+        f2unpack(s2, lo, hi);
+        float sum = lo + hi;
 #pragma unroll
         for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
         if (lane == 0) s_part[r][wl] = sum;
@@ -201,17 +209,21 @@ __global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_rows_kernel(FcN
     }
 #pragma unroll
     for (int r = 0; r < kPrepRows; ++r) {
-      float sq = 0.f;
+      const uint64_t nmu2 = f2pack(-mu[r], -mu[r]);
+      uint64_t q2 = f2pack(0.f, 0.f);
 #pragma unroll
       for (int i = 0; i < kPrepVec; ++i) {
         if (64 * wl + 32 * i + lane < nvec) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float y = Elem<__nv_bfloat16>::get(v[r][i], e) - mu[r];
-            sq = fmaf(y, y, sq);
+          for (int e = 0; e < E::kPairs; ++e) {
+            const uint64_t y2 = f2add(E::pair(v[r][i], e), nmu2);
+            q2 = f2fma(y2, y2, q2);
           }
         }
       }
+      float lo, hi;
+      f2unpack(q2, lo, hi);
+      float sq = lo + hi;
 #pragma unroll
       for (int o = 16; o; o >>= 1) sq += __shfl_xor_sync(kFull, sq, o);
       if (lane == 0) s_part[r][wl] = sq;
@@ -228,7 +240,8 @@ __global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_rows_kernel(FcN
   for (int i = 0; i < kPrepVec; ++i) {
     const int q = 64 * wl + 32 * i + lane;
     if (q >= nvec) continue;
-    float gg[8], bb[8];
+    // gamma and beta of the vector's 8 columns, as 4 pairs each
+    uint64_t g2[4], b2[4];
     if (p.norm != kNormNone) {
       const int f = 8 * q;
       const float4 g0 = __ldg(reinterpret_cast<const float4*>(g + f));
@@ -238,10 +251,14 @@ __global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_rows_kernel(FcN
         b0 = __ldg(reinterpret_cast<const float4*>(bt + f));
         b1 = __ldg(reinterpret_cast<const float4*>(bt + f + 4));
       }
-      gg[0] = g0.x; gg[1] = g0.y; gg[2] = g0.z; gg[3] = g0.w;
-      gg[4] = g1.x; gg[5] = g1.y; gg[6] = g1.z; gg[7] = g1.w;
-      bb[0] = b0.x; bb[1] = b0.y; bb[2] = b0.z; bb[3] = b0.w;
-      bb[4] = b1.x; bb[5] = b1.y; bb[6] = b1.z; bb[7] = b1.w;
+      g2[0] = f2pack(g0.x, g0.y);
+      g2[1] = f2pack(g0.z, g0.w);
+      g2[2] = f2pack(g1.x, g1.y);
+      g2[3] = f2pack(g1.z, g1.w);
+      b2[0] = f2pack(b0.x, b0.y);
+      b2[1] = f2pack(b0.z, b0.w);
+      b2[2] = f2pack(b1.x, b1.y);
+      b2[3] = f2pack(b1.z, b1.w);
     }
 #pragma unroll
     for (int r = 0; r < kPrepRows; ++r) {
@@ -249,15 +266,17 @@ __global__ void __launch_bounds__(256, SV_PREP_MINB) fcnorm_prep_rows_kernel(FcN
       if (t >= p.T) continue;
       uint4 o = v[r][i];
       if (p.norm != kNormNone) {
-        float y[8];
+        // y = (x - mu) (rstd gamma) + beta
+        const uint64_t nmu2 = f2pack(-mu[r], -mu[r]), rs2 = f2pack(rstd[r], rstd[r]);
+        uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float z = (Elem<__nv_bfloat16>::get(v[r][i], e) - mu[r]) * rstd[r] * gg[e];
-          if (bt != nullptr) z += bb[e];
-          y[e] = z;
+        for (int e = 0; e < E::kPairs; ++e) {
+          const uint64_t y2 = f2fma(f2add(E::pair(v[r][i], e), nmu2), f2mul(rs2, g2[e]), b2[e]);
+          float lo, hi;
+          f2unpack(y2, lo, hi);
+          w[e] = pack_bf16(lo, hi);
         }
-        o = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
-                       pack_bf16(y[6], y[7]));
+        o = make_uint4(w[0], w[1], w[2], w[3]);
       }
       *reinterpret_cast<uint4*>(x + static_cast<size_t>(t) * 3 * d + 8 * q) = o;
     }
