@@ -731,7 +731,7 @@ def tree222(verify_seed=0):
                                verify_seed=verify_seed, name=TREE_WORKLOAD)
 
 
-def tree_setup(dev, stream, wl, copies):
+def tree_setup(dev, stream, wl, copies, lazy=False):
     import torch
     from speculative_decoding_verification_73_gb300 import binding
     B, M, V = wl.shape
@@ -746,9 +746,60 @@ def tree_setup(dev, stream, wl, copies):
     def step(i, c=None):
         c = i % copies if c is None else c
         binding.spec_verify_tree(sv.ctx, wl.mode, target[c], draft[c], parents, tokens, temperature,
-                                 i, *outs)
+                                 i, *outs, lazy=lazy)
 
     return sv, step, (target, draft, parents, tokens, temperature), outs
+
+
+def tree_lazy_bytes(wl, outs, step, seeds=8):
+    """Bytes the lazy tree walk reads per call, averaged over `seeds` calls:
+    the target row of every node on each request's walked path (root, then
+    the accepted nodes) and, for a sampled request, the draft row of each of
+    those nodes that has children."""
+    from speculative_decoding_verification_73_gb300 import binding
+    B, M, V = wl.shape
+    par = wl.parents.numpy()
+    inner = [set(int(v) for v in par[b]) for b in range(B)]  # nodes that have children
+    temp = wl.temperature.numpy()
+    row = V * wl.target.element_size()
+    total = 0
+    for i in range(seeds):
+        step(i, 0)
+        path, acc = outs[1].cpu().numpy(), outs[2].cpu().numpy()
+        for b in range(B):
+            nodes = [0] + [int(n) for n in path[b, : max(int(acc[b]), 0)]]
+            total += len(nodes) * row
+            if temp[b] > 0 and wl.mode == binding.SV_TREE_SAMPLED:
+                total += sum(1 for n in nodes if n in inner[b]) * row
+    return total // seeds
+
+
+def tree_lazy_summary(dev, stream, steps=200, warmup=10, copies=3):
+    """spec_verify_tree_lazy on tree222-bf16: device time per call (three
+    rotating input copies, so rows come from HBM), verified nodes per second
+    and the bytes its walks read."""
+    import torch
+    from speculative_decoding_verification_73_gb300 import binding
+    wl = tree222()
+    B, M, V = wl.shape
+    sv, step, _, outs = tree_setup(dev, stream, wl, copies, lazy=True)
+    nbytes = tree_lazy_bytes(wl, outs, step)
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(steps):
+        step(warmup + i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = ev0.elapsed_time(ev1) / steps * 1e3
+    code, _ = sv.get_error()
+    assert code == 0, binding.strerror(code)
+    sv.close()
+    return {"workload": TREE_WORKLOAD, "us_per_step": us, "steps": steps,
+            "verified_nodes_per_s": B * M / (us * 1e-6), "bytes_read_per_step": nbytes,
+            "launches": 1, "l2": f"{copies} rotating input copies of {wl.bytes_read() / 1e6:.0f} MB"}
 
 
 def tree_summary(dev, stream, peak, steps=200, warmup=10):
@@ -780,7 +831,8 @@ def tree_summary(dev, stream, peak, steps=200, warmup=10):
             "kernel_us": {"tree_rowstats": rs, "tree_walk": kern["k1"]},
             "roofline": {"kernel": "tree_rowstats", "achieved_gbs": nbytes / (rs * 1e-6) / 1e9,
                          "frac": nbytes / (rs * 1e-6) / 1e9 / peak},
-            "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB per call)"}
+            "l2": f"inputs larger than L2 ({nbytes / 1e6:.0f} MB per call)",
+            "lazy": tree_lazy_summary(dev, stream)}
 
 
 def run_tree(args):
@@ -905,6 +957,8 @@ def run_tree(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = tree_cpu_baseline(wl, budget_s=12.0)
     sv.close()
+    if world == 1:
+        line["lazy"] = tree_lazy_summary(dev, stream)
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:

@@ -248,6 +248,29 @@ int spec_verify_tree(spec_verify_ctx* ctx, int B, int M, int V, int mode,
                      int32_t* out_accept_len, int32_t* out_kv_len);
 
 /*
+ * spec_verify_tree_lazy -- spec_verify_tree reading only the rows its walk
+ * reaches (the lesson's "Invariant: Leviathan rejection sampling": a node's
+ * children are tested against that node's rows alone, so the rows of nodes
+ * the walk never reaches do not influence the result): when the walk
+ * arrives at a node, the node's target row (and, in SV_TREE_SAMPLED mode,
+ * its draft row if it has children) is reduced on the spot.  Same
+ * arguments, layout, uniforms and outputs as spec_verify_tree; on valid
+ * inputs the outputs are spec_verify_tree's bit for bit.  Errors: the
+ * temperature, the topology and every token are checked first; a row is
+ * checked only when the walk reads it, so a bad row of a node the walk
+ * never reaches is not an error (spec_verify_tree checks every row).
+ * Limit: rows of at most 32 spans of 64 KB (V <= 1048576 for SV_BF16,
+ * 524288 for SV_F32), else SV_EINVAL.  One kernel launch per call, no
+ * workspace traffic between kernels.
+ */
+int spec_verify_tree_lazy(spec_verify_ctx* ctx, int B, int M, int V, int mode,
+                          const void* target_logits, const void* draft_logits,
+                          const int32_t* parents, const int32_t* draft_tokens,
+                          const float* temperature, uint64_t seed,
+                          int32_t* out_tokens, int32_t* out_path,
+                          int32_t* out_accept_len, int32_t* out_kv_len);
+
+/*
  * spec_verify_lazy -- the same step as spec_verify (same arguments, same
  * outputs bit for bit on valid inputs), reading each request's rows only as
  * far as its walk goes: position j reads target row j-1 and draft row j-1

@@ -49,6 +49,11 @@ Readings of points the pages leave open:
   outside [0, i-1]), tokens (outside [0, V)), logits (every target row, and
   in SAMPLED mode the draft rows of nodes that have children, must be
   valid rows as in ``verify.row_is_valid``).
+* The lazy reading (``lazy=True``): the walk reads a node's rows only when
+  it reaches the node, and the rows of nodes it never reaches do not enter
+  the result (a node's children are tested against that node's rows
+  alone), so only the rows it reads are checked: the same outputs on valid
+  inputs, and a bad row off the walked path is not an error.
 
 Floating point is float64; ``node_law`` drives the same accept and
 residual code with exact ``fractions.Fraction`` arrays for the pins.
@@ -183,9 +188,29 @@ def draws(seed, b):
     return draw
 
 
-def verify_request(z_raw, y_raw, parents, tokens, temperature, seed, b, dtype, mode):
+class _BadRow(Exception):
+    """A row the lazy walk read is not a valid row."""
+
+
+class _RowsOnUse:
+    """Rows widened, checked and transformed when the walk first reads them
+    (the lazy reading)."""
+
+    def __init__(self, raw, dtype, make):
+        self.raw, self.dtype, self.make, self.cache = raw, dtype, make, {}
+
+    def __getitem__(self, r):
+        if r not in self.cache:
+            x = logits_to_f64(self.raw[r], self.dtype)
+            if not row_is_valid(x):
+                raise _BadRow
+            self.cache[r] = self.make(x)
+        return self.cache[r]
+
+
+def verify_request(z_raw, y_raw, parents, tokens, temperature, seed, b, dtype, mode, lazy=False):
     """One request: z_raw [M+1, V], y_raw [M+1, V] (None in TOPK mode or at
-    T = 0), parents [M], tokens [M].
+    T = 0), parents [M], tokens [M]; ``lazy`` selects the lazy reading.
 
     Returns (err_bit, emitted, path, accepted, kv_len, decisions).
     """
@@ -201,6 +226,17 @@ def verify_request(z_raw, y_raw, parents, tokens, temperature, seed, b, dtype, m
     tokens = [int(x) for x in np.asarray(tokens).reshape(-1)[:m]]
     if any(x < 0 or x >= vocab for x in tokens):
         return ERR_TOKEN, None, None, None, None, []
+    if lazy:
+        try:
+            if t == 0.0:
+                emitted, path, a, kv = greedy_walk(_RowsOnUse(z_raw, dtype, lambda x: x), parents, tokens)
+                return 0, emitted, path, a, kv, []
+            q_rows = _RowsOnUse(z_raw, dtype, lambda x: softmax(x, t))
+            p_rows = _RowsOnUse(y_raw, dtype, lambda x: softmax(x, t)) if mode == SAMPLED else None
+            emitted, path, a, kv, dec = walk(q_rows, p_rows, parents, tokens, mode, draws(seed, b))
+            return 0, emitted, path, a, kv, dec
+        except _BadRow:
+            return ERR_LOGIT, None, None, None, None, []
     z = logits_to_f64(z_raw, dtype)
     if not all(row_is_valid(z[r]) for r in range(m + 1)):
         return ERR_LOGIT, None, None, None, None, []
@@ -233,10 +269,12 @@ class TreeResult:
         self.decisions = [[] for _ in range(batch)]
 
 
-def verify_tree(target, draft, parents, tokens, temperature, seed, dtype, mode):
+def verify_tree(target, draft, parents, tokens, temperature, seed, dtype, mode, lazy=False):
     """Batched tree verify: target [B, M+1, V], draft [B, M+1, V] (None when
-    unused), parents [B, M], tokens [B, M], temperature [B], 64-bit seed.
-    Failed requests get tokens and path -1, accept_len -1, kv_len 0."""
+    unused), parents [B, M], tokens [B, M], temperature [B], 64-bit seed;
+    ``lazy`` selects the lazy reading (rows checked only where the walk
+    reads them).  Failed requests get tokens and path -1, accept_len -1,
+    kv_len 0."""
     target = np.asarray(target)
     batch, m1, _ = target.shape
     m = m1 - 1
@@ -247,7 +285,7 @@ def verify_tree(target, draft, parents, tokens, temperature, seed, dtype, mode):
     for b in range(batch):
         y_b = None if draft is None else np.asarray(draft[b])
         err, emitted, path, a, kv, dec = verify_request(
-            target[b], y_b, parents[b], tokens[b], temperature[b], seed, b, dtype, mode)
+            target[b], y_b, parents[b], tokens[b], temperature[b], seed, b, dtype, mode, lazy)
         if err:
             res.errors |= err
             res.request_errors[b] = err

@@ -33,7 +33,8 @@ EXPORTS = (
     "spec_verify_init", "spec_verify", "spec_verify_get_error", "spec_verify_debug_stats",
     "spec_verify_profile", "spec_verify_profile_read", "spec_verify_launches_per_call",
     "spec_verify_debug_philox", "spec_verify_debug_read_stream", "spec_verify_destroy", "spec_verify_strerror",
-    "spec_verify_noalloc", "spec_verify_tree", "spec_verify_kv_commit", "spec_verify_lazy",
+    "spec_verify_noalloc", "spec_verify_tree", "spec_verify_tree_lazy", "spec_verify_kv_commit",
+    "spec_verify_lazy",
     "spec_verify_fc_norm", "spec_verify_debug_seek_calls", "spec_verify_debug_skip_row_stats",
     "spec_verify_debug_late_cta",
 )
@@ -80,6 +81,7 @@ def load():
                                           c_void, c_void, c_void, c_void, c_void, c_int]
     lib.spec_verify_tree.argtypes = [c_void, c_int, c_int, c_int, c_int, c_void, c_void, c_void,
                                      c_void, c_void, c_u64, c_void, c_void, c_void, c_void]
+    lib.spec_verify_tree_lazy.argtypes = list(lib.spec_verify_tree.argtypes)
     lib.spec_verify_noalloc.argtypes = [c_int, c_int, c_int, c_int, c_void, c_void, c_void, c_void,
                                         c_u64, c_void, c_void, c_void, c_void]
     lib.spec_verify_strerror.argtypes = [c_int]
@@ -183,9 +185,10 @@ def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, temperature, 
 
 
 def spec_verify_tree(ctx, mode, target_logits, draft_logits, parents, draft_tokens, temperature,
-                     seed, out_tokens, out_path, out_accept_len, out_kv_len):
+                     seed, out_tokens, out_path, out_accept_len, out_kv_len, lazy=False):
     """Enqueue one tree verify step; B, M, V are taken from ``target_logits``
-    [B, M+1, V].  ``draft_logits`` [B, M+1, V] may be None in TOPK mode."""
+    [B, M+1, V].  ``draft_logits`` [B, M+1, V] may be None in TOPK mode.
+    ``lazy`` calls spec_verify_tree_lazy (rows read only where the walk goes)."""
     B, m1, V = target_logits.shape
     M = m1 - 1
     logit_dt = (torch.float32, torch.bfloat16)
@@ -200,11 +203,12 @@ def spec_verify_tree(ctx, mode, target_logits, draft_logits, parents, draft_toke
     _require(out_tokens, "out_tokens", (B, m1), (torch.int32,))
     _require(out_accept_len, "out_accept_len", (B,), (torch.int32,))
     _require(out_kv_len, "out_kv_len", (B,), (torch.int32,))
-    _check(load().spec_verify_tree(ctx, int(B), int(M), int(V), int(mode), _ptr(target_logits),
-                                   _ptr(draft_logits), _ptr(parents), _ptr(draft_tokens),
-                                   _ptr(temperature), ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF),
-                                   _ptr(out_tokens), _ptr(out_path), _ptr(out_accept_len),
-                                   _ptr(out_kv_len)), "spec_verify_tree")
+    name = "spec_verify_tree_lazy" if lazy else "spec_verify_tree"
+    _check(getattr(load(), name)(ctx, int(B), int(M), int(V), int(mode), _ptr(target_logits),
+                                 _ptr(draft_logits), _ptr(parents), _ptr(draft_tokens),
+                                 _ptr(temperature), ctypes.c_uint64(int(seed) & 0xFFFFFFFFFFFFFFFF),
+                                 _ptr(out_tokens), _ptr(out_path), _ptr(out_accept_len),
+                                 _ptr(out_kv_len)), name)
 
 
 def spec_verify_kv_commit(ctx, mode, cache, seq_len, kv_len, scratch=None, path=None):
@@ -378,15 +382,16 @@ class SpecVerify:
         spec_verify_lazy(self.ctx, target, draft, tokens, temperature, seed, toks, acc, kv)
         return toks, acc, kv
 
-    def tree(self, target, draft, parents, tokens, temperature, seed, mode=SV_TREE_SAMPLED):
-        """Tree verify; returns (out_tokens [B, M+1], out_path [B, M],
-        out_accept_len [B], out_kv_len [B]) as CUDA tensors."""
+    def tree(self, target, draft, parents, tokens, temperature, seed, mode=SV_TREE_SAMPLED, lazy=False):
+        """Tree verify (``lazy``: spec_verify_tree_lazy); returns (out_tokens
+        [B, M+1], out_path [B, M], out_accept_len [B], out_kv_len [B]) as CUDA
+        tensors."""
         B, m1, _ = target.shape
         toks = self.out_tokens[: B * m1].view(B, m1)
         path = self.out_path[: B * (m1 - 1)].view(B, m1 - 1)
         acc, kv = self.out_accept[:B], self.out_kv[:B]
         spec_verify_tree(self.ctx, mode, target, draft, parents, tokens, temperature, seed,
-                         toks, path, acc, kv)
+                         toks, path, acc, kv, lazy=lazy)
         return toks, path, acc, kv
 
     def get_error(self):

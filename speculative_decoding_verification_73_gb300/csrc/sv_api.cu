@@ -245,15 +245,20 @@ int spec_verify(spec_verify_ctx* ctx, int B, int N, int V, const void* target_lo
   return SV_OK;
 }
 
-int spec_verify_tree(spec_verify_ctx* ctx, int B, int M, int V, int mode,
-                     const void* target_logits, const void* draft_logits, const int32_t* parents,
-                     const int32_t* draft_tokens, const float* temperature, uint64_t seed,
-                     int32_t* out_tokens, int32_t* out_path, int32_t* out_accept_len,
-                     int32_t* out_kv_len) {
+namespace {
+
+// spec_verify_tree and spec_verify_tree_lazy: the same checks and problem;
+// the eager form streams every row first, the lazy one only the rows its
+// walk reaches (rows of at most 32 spans).
+int tree_call(spec_verify_ctx* ctx, bool lazy, int B, int M, int V, int mode, const void* target_logits,
+              const void* draft_logits, const int32_t* parents, const int32_t* draft_tokens,
+              const float* temperature, uint64_t seed, int32_t* out_tokens, int32_t* out_path,
+              int32_t* out_accept_len, int32_t* out_kv_len) {
   if (ctx == nullptr) return SV_EINVAL;
   if (B < 0 || B > ctx->max_B || M < 0 || M > ctx->max_N || V < 1 || V > ctx->max_V ||
       (mode != SV_TREE_SAMPLED && mode != SV_TREE_TOPK))
     return SV_EINVAL;
+  if (lazy && ceil_div(V, sv::row_chunk_elems(ctx->dtype)) > sv::kTreeLazyMaxSpans) return SV_EINVAL;
   if (B == 0) return SV_OK;
   if (target_logits == nullptr || temperature == nullptr || out_tokens == nullptr ||
       out_accept_len == nullptr || out_kv_len == nullptr)
@@ -281,17 +286,28 @@ int spec_verify_tree(spec_verify_ctx* ctx, int B, int M, int V, int mode,
   p.out_path = out_path;
   p.out_accept = out_accept_len;
   p.out_kv = out_kv_len;
+  p.epoch = 0;
   sv::Workspace w = ctx->w;
   w.S1 = ceil_div(V, sv::row_chunk_elems(ctx->dtype));
   w.S3 = ceil_div(V, sv::sample_chunk_elems(ctx->dtype));
-  // the walk polls the tags of this call's partials
-  if (next_epoch(ctx, &p.epoch) != SV_OK) return SV_ECUDA;
+  // the eager walk polls the tags of this call's partials
+  if (!lazy && next_epoch(ctx, &p.epoch) != SV_OK) return SV_ECUDA;
 
   cudaEvent_t* ev = nullptr;
   if (ctx->profile_every > 0 && (ctx->profile_seen++ % ctx->profile_every) == 0) {
     ev = profile_slot(ctx);
     if (ev == nullptr) return SV_ECUDA;
     if (cudaEventRecord(ev[0], ctx->stream) != cudaSuccess) return SV_ECUDA;
+  }
+  if (lazy) {
+    if (sv::launch_tree_lazy(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess) return SV_ECUDA;
+    if (ev) {  // one kernel: its time is reported as kernel 0, kernel 1 gets ~0
+      if (cudaEventRecord(ev[1], ctx->stream) != cudaSuccess ||
+          cudaEventRecord(ev[2], ctx->stream) != cudaSuccess)
+        return SV_ECUDA;
+      ctx->recorded += 1;
+    }
+    return SV_OK;
   }
   if (!ctx->skip_rowstats && sv::launch_tree_rowstats(ctx->dtype, vec, p, w, ctx->stream) != cudaSuccess)
     return SV_ECUDA;
@@ -302,6 +318,26 @@ int spec_verify_tree(spec_verify_ctx* ctx, int B, int M, int V, int mode,
     ctx->recorded += 1;
   }
   return SV_OK;
+}
+
+}  // namespace
+
+int spec_verify_tree(spec_verify_ctx* ctx, int B, int M, int V, int mode,
+                     const void* target_logits, const void* draft_logits, const int32_t* parents,
+                     const int32_t* draft_tokens, const float* temperature, uint64_t seed,
+                     int32_t* out_tokens, int32_t* out_path, int32_t* out_accept_len,
+                     int32_t* out_kv_len) {
+  return tree_call(ctx, false, B, M, V, mode, target_logits, draft_logits, parents, draft_tokens, temperature,
+                   seed, out_tokens, out_path, out_accept_len, out_kv_len);
+}
+
+int spec_verify_tree_lazy(spec_verify_ctx* ctx, int B, int M, int V, int mode,
+                          const void* target_logits, const void* draft_logits, const int32_t* parents,
+                          const int32_t* draft_tokens, const float* temperature, uint64_t seed,
+                          int32_t* out_tokens, int32_t* out_path, int32_t* out_accept_len,
+                          int32_t* out_kv_len) {
+  return tree_call(ctx, true, B, M, V, mode, target_logits, draft_logits, parents, draft_tokens, temperature,
+                   seed, out_tokens, out_path, out_accept_len, out_kv_len);
 }
 
 int spec_verify_kv_commit(spec_verify_ctx* ctx, int mode, int L, int B, int S, int W,

@@ -173,6 +173,11 @@ cudaError_t launch_tree_rowstats(int dtype, bool vec, const TreeProblem& p, cons
                                  cudaStream_t s);
 cudaError_t launch_tree_walk(int dtype, bool vec, const TreeProblem& p, const Workspace& w,
                              cudaStream_t s);
+// The lazy tree walk alone (no row-statistics grid): rows of at most
+// kTreeLazyMaxSpans spans.
+constexpr int kTreeLazyMaxSpans = 32;
+cudaError_t launch_tree_lazy(int dtype, bool vec, const TreeProblem& p, const Workspace& w,
+                             cudaStream_t s);
 cudaError_t launch_kv_commit(const KvProblem& p, cudaStream_t s);
 cudaError_t launch_fcnorm(const FcNormProblem& p, cudaStream_t s);
 cudaError_t launch_lazy(int dtype, bool vec, const Problem& p, const Workspace& w, cudaStream_t s);

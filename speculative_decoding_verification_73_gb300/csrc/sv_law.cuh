@@ -37,6 +37,21 @@ __device__ __forceinline__ float ld_dsmem(const float* local, unsigned rank) {
   return v;
 }
 
+// 16 bytes at `local`'s place in the shared memory of cluster CTA `rank`
+// (16-byte aligned).
+__device__ __forceinline__ float4 ld_dsmem16(const void* local, unsigned rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+
 // ------------------------------------------------------------ distributions
 
 // The distribution a node's token is drawn from, or that its next child is

@@ -124,47 +124,6 @@ __device__ __forceinline__ RowNorm merge_row(const Partial* parts, int n) {
   return merge_sampled(pre, parts, n);
 }
 
-// The same merges over partials gathered into this CTA's shared memory
-// (plain loads; the merge arithmetic is the same).
-__device__ __forceinline__ float4 partial_local(const Partial* at, bool take) {
-  return take ? *reinterpret_cast<const float4*>(at) : make_float4(-INFINITY, 0.f, __int_as_float(INT_MAX), 0.f);
-}
-
-__device__ __forceinline__ RowNorm merge_row_local(const Partial* parts, int n) {
-  float4 pre[kPre];
-#pragma unroll
-  for (int i = 0; i < kPre; ++i) pre[i] = partial_local(parts + i, i < n);
-  return merge_sampled_by(pre, n, [&](int i0, float4(&pt)[kBatch]) {
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) pt[i] = partial_local(parts + i0 + i, i0 + i < n);
-  });
-}
-
-__device__ __forceinline__ RowMax merge_row_greedy_local(const Partial* parts, int n) {
-  float4 pre[kPre];
-#pragma unroll
-  for (int i = 0; i < kPre; ++i) pre[i] = partial_local(parts + i, i < n);
-  return merge_greedy_by(pre, n, [&](int i0, float4(&pt)[kBatch]) {
-#pragma unroll
-    for (int i = 0; i < kBatch; ++i) pt[i] = partial_local(parts + i0 + i, i0 + i < n);
-  });
-}
-
-// 16 bytes at `local`'s place in the shared memory of cluster CTA `rank`
-// (16-byte aligned).
-__device__ __forceinline__ float4 ld_dsmem16(const void* local, unsigned rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(remote)
-               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(local))), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(remote)
-               : "memory");
-  return v;
-}
-
 // Rows of up to kLazyMaxS1 spans exchange their partials through
 // distributed shared memory (each CTA keeps the partials of its own spans
 // of the position in double-buffered slots; after the cluster barrier every

@@ -60,6 +60,11 @@ namespace {
 #ifndef SV_TREE_MINB
 #define SV_TREE_MINB 2
 #endif
+// Resident CTAs per SM the lazy walk is built for (all the request clusters
+// of a 64-request batch at once at four).
+#ifndef SV_TREE_LAZY_MINB
+#define SV_TREE_LAZY_MINB 4
+#endif
 constexpr int kTreeCluster = SV_TREE_CLUSTER;
 constexpr int kMaxNodes = kST;  // root + up to 255 draft nodes, one thread each
 constexpr int kNoNode = INT_MAX;
@@ -133,8 +138,20 @@ constexpr bool tree_stages() {
   return SV_TREE_STAGE && kVecPath && sizeof(T) == 2;
 }
 
-template <typename T, bool kVecPath>
-__global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_TREE_MINB)
+// The lazy walk (kLazy) reads no row statistics: when the walk reaches a
+// node, the cluster reduces that node's target row (and its draft row, for
+// a node with children in SAMPLED mode) with the same span reduction as
+// tree_rowstats_kernel, one span per CTA at a time, and every CTA merges
+// the spans' partials gathered through distributed shared memory in span
+// order -- the numbers the eager walk merges, so the two take the same
+// decisions.  Rows of nodes the walk never reaches are neither read nor
+// checked.  Rows of at most kTreeLazyMaxS1 spans.
+constexpr int kTreeLazyMaxS1 = kTreeLazyMaxSpans;
+constexpr int kTreeLazySlots = (2 * kTreeLazyMaxS1 + kTreeCluster - 1) / kTreeCluster;  // items per CTA
+
+template <typename T, bool kVecPath, bool kLazy>
+__global__ void __cluster_dims__(kTreeCluster, 1, 1)
+    __launch_bounds__(kST, kLazy ? SV_TREE_LAZY_MINB : SV_TREE_MINB)
     tree_walk_kernel(TreeProblem p, Workspace w) {
   using E = Elem<T>;
   extern __shared__ __align__(16) unsigned char s_stage_raw[];
@@ -155,6 +172,11 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   __shared__ float s_cprev;
   __shared__ int s_tentative;
   __shared__ float s_cmass;  // the sum of this CTA's level-1 block masses in the draw
+  // lazy walk: this CTA's span partials of a node visit (double-buffered by
+  // visit parity) and the visit's partials gathered from the cluster
+  __shared__ __align__(16) Partial s_own[2][kLazy ? kTreeLazySlots : 1];
+  __shared__ __align__(16) Partial s_gather[kLazy ? 2 * kTreeLazyMaxS1 : 1];
+  __shared__ int s_visit, s_statnode, s_bad;
 
   const int b = blockIdx.x / kTreeCluster;
   const unsigned rank = cluster_rank();
@@ -185,8 +207,8 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   float4 tpre[kPre], dpre[kPre];
 #pragma unroll
   for (int j = 0; j < kPre; ++j) {
-    tpre[j] = (is_node && mode != kModeInvalid && j < S1) ? ld_partial_relaxed(tparts + j) : empty;
-    dpre[j] = (is_node && use_draft && j < S1) ? ld_partial_relaxed(dparts + j) : empty;
+    tpre[j] = (!kLazy && is_node && mode != kModeInvalid && j < S1) ? ld_partial_relaxed(tparts + j) : empty;
+    dpre[j] = (!kLazy && is_node && use_draft && j < S1) ? ld_partial_relaxed(dparts + j) : empty;
   }
   __shared__ int s_late;
   if (i == 0) {
@@ -223,8 +245,10 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   Poll pl{p.epoch, kPollLimit, false};
   const bool take_t = is_node && mode != kModeInvalid;
   const bool take_d = is_node && use_draft && s_first[i] != kNoNode;
-  settle(tpre, tparts, take_t ? S1 : 0, dpre, dparts, take_d ? S1 : 0, pl);
-  if (is_node && mode == kModeGreedy) {
+  if (!kLazy) settle(tpre, tparts, take_t ? S1 : 0, dpre, dparts, take_d ? S1 : 0, pl);
+  if (kLazy) {
+    // statistics come node by node, below
+  } else if (is_node && mode == kModeGreedy) {
     const RowMax g = merge_greedy_by(tpre, S1, TaggedLoad{tparts, S1, &pl});
     s_gidx[i] = g.idx;
     if (!g.ok) atomicOr(&s_err, kErrLogit);
@@ -252,15 +276,17 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   // CTA reads it back, so the cluster takes the same branch below (a CTA
   // leaving alone would strand its peers' exchanges through its shared
   // memory).
-  if (i == 0 && s_late)
-    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(w.late + b), "r"(p.epoch) : "memory");
-  cluster_sync();
-  unsigned late_tag;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(late_tag) : "l"(w.late + b) : "memory");
+  unsigned late_tag = 0;
+  if (!kLazy) {
+    if (i == 0 && s_late)
+      asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(w.late + b), "r"(p.epoch) : "memory");
+    cluster_sync();
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(late_tag) : "l"(w.late + b) : "memory");
+  }
 
   int32_t* out_tok = p.out_tokens + static_cast<size_t>(b) * (M + 1);
   int32_t* out_path = p.out_path + static_cast<size_t>(b) * M;
-  const unsigned bits = s_err | (late_tag == p.epoch ? kErrWait : 0u);
+  const unsigned bits = s_err | (!kLazy && late_tag == p.epoch ? kErrWait : 0u);
   if (bits) {
     // report the first failing check in the order temperature, topology,
     // tokens, wait, logits (a wait that ran out leaves the partials that the
@@ -280,6 +306,124 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
       }
     }
     return;  // identical in every CTA of the cluster
+  }
+
+  // ---- lazy walk: the statistics of one node's rows, reduced by the cluster
+  // (span it of the node's target row, then of its draft row, by CTA
+  // it % kTreeCluster), merged by thread 0 of every CTA into s_cq / s_sq /
+  // s_cp / s_sp (sampled) or s_gidx (greedy); s_bad if a row is bad
+  auto node_stats = [&](int node, bool greedy_row) {
+    const bool with_draft = !greedy_row && use_draft && s_first[node] != kNoNode;
+    const int nitems = with_draft ? 2 * S1 : S1;
+    const int par = s_visit & 1;
+    constexpr int kSpan = kSpanBytes / static_cast<int>(sizeof(T));
+    for (int it = static_cast<int>(rank), li = 0; it < nitems; it += kTreeCluster, ++li) {
+      const bool dr = it >= S1;
+      const int span = dr ? it - S1 : it;
+      const T* row = static_cast<const T*>(dr ? p.draft : p.target) + (static_cast<size_t>(b) * (M + 1) + node) * V;
+      const int beg = span * kSpan, end = min(V, beg + kSpan);
+      Partial out;
+      if (!kVecPath)
+        out = chunk_partial_scalar<T>(row, beg, end, greedy_row, k, -1, nullptr);
+      else if (end - beg == kSpan)
+        out = greedy_row ? span_partial_vec<T, true, true>(row, beg, end, k, -1, nullptr)
+                         : span_partial_vec<T, false, true>(row, beg, end, k, -1, nullptr);
+      else
+        out = greedy_row ? span_partial_vec<T, true, false>(row, beg, end, k, -1, nullptr)
+                         : span_partial_vec<T, false, false>(row, beg, end, k, -1, nullptr);
+      if (i == 0) s_own[par][li] = out;
+    }
+    cluster_sync();  // every CTA's partials of this visit are in its shared memory
+    if (i < nitems)
+      *reinterpret_cast<float4*>(&s_gather[i]) =
+          ld_dsmem16(&s_own[par][i / kTreeCluster], static_cast<unsigned>(i % kTreeCluster));
+    __syncthreads();
+    if (i == 0) {
+      bool bad;
+      if (greedy_row) {
+        const RowMax g = merge_row_greedy_local(s_gather, S1);
+        s_gidx[node] = g.idx;
+        bad = !g.ok;
+      } else {
+        const RowNorm q = merge_row_local(s_gather, S1);
+        s_cq[node] = q.c;
+        s_sq[node] = q.s;
+        bad = !q.ok;
+        if (with_draft) {
+          const RowNorm pn = merge_row_local(s_gather + S1, S1);
+          s_cp[node] = pn.c;
+          s_sp[node] = pn.s;
+          bad = bad || !pn.ok;
+        } else {
+          s_cp[node] = 0.f;
+          s_sp[node] = 1.f;
+        }
+      }
+      s_bad = bad ? 1 : 0;
+      s_visit += 1;
+    }
+    __syncthreads();
+  };
+  // a visited row is bad: the whole cluster fails the request (the same
+  // merged numbers in every CTA), after a cluster barrier so that no CTA
+  // leaves while a peer may still read its partial slots
+  auto fail_logit = [&]() {
+    cluster_sync();
+    if (rank == 0) {
+      if (is_node) out_tok[i] = -1;
+      if (i < M) out_path[i] = -1;
+      if (i == 0) {
+        p.out_accept[b] = -1;
+        p.out_kv[b] = 0;
+        atomicOr(w.err, kErrLogit);
+      }
+    }
+  };
+  if (kLazy && i == 0) {
+    s_visit = 0;
+    s_statnode = -1;
+  }
+
+  if (kLazy && mode == kModeGreedy) {
+    // every CTA walks: descend into the child whose token is the argmax of
+    // the node's target row (emitted tokens kept in s_rej)
+    if (i == 0) {
+      s_node = 0;
+      s_plen = 0;
+    }
+    __syncthreads();
+    while (true) {
+      node_stats(s_node, true);
+      if (s_bad) {
+        fail_logit();
+        return;
+      }
+      if (i == 0) {
+        const int node = s_node, g = s_gidx[node];
+        int c = s_first[node];
+        while (c != kNoNode && s_tok[c] != g) c = s_next[c];
+        s_rej[s_plen] = g;
+        if (c == kNoNode) {
+          s_act = 1;
+        } else {
+          s_path[s_plen++] = c;
+          s_node = c;
+          s_act = 0;
+        }
+      }
+      __syncthreads();
+      if (s_act) break;
+    }
+    cluster_sync();  // no CTA leaves while a peer may still read its partial slots
+    if (rank != 0) return;
+    const int plen = s_plen;
+    if (is_node) out_tok[i] = i <= plen ? s_rej[i] : -1;
+    if (i < M) out_path[i] = i < plen ? s_path[i] : -1;
+    if (i == 0) {
+      p.out_accept[b] = plen;
+      p.out_kv[b] = plen + 1;
+    }
+    return;
   }
 
   if (mode == kModeGreedy) {
@@ -334,7 +478,7 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   const int nbpc = (S3 + kTreeCluster - 1) / kTreeCluster;
   const int cfirst = static_cast<int>(rank) * nbpc;
   const int clast = min(S3, cfirst + nbpc);
-  const bool staging = tree_stages<T, kVecPath>() && nbpc <= kStageBlocks;
+  const bool staging = !kLazy && tree_stages<T, kVecPath>() && nbpc <= kStageBlocks;
   T* sz = reinterpret_cast<T*>(s_stage_raw);        // [kStageBlocks][kLevel1] of z
   T* sy = sz + kStageBlocks * kLevel1;              // the same for y
   if (i == 0) s_staged = -1;
@@ -370,6 +514,15 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1) __launch_bounds__(kST, SV_T
   };
   int pass = 0;
   while (true) {
+    if (kLazy && s_statnode != s_node) {
+      node_stats(s_node, false);  // the walk has just reached this node
+      if (s_bad) {
+        fail_logit();
+        return;
+      }
+      if (i == 0) s_statnode = s_node;
+      __syncthreads();
+    }
     if (i == 0) {
       const int node = s_node, c = s_child, m = s_m;
       int act = kActContinue;
@@ -635,7 +788,7 @@ cudaError_t launch_tree_t(const TreeProblem& p, const Workspace& w, cudaStream_t
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     const int smem = tree_stages<T, kVecPath>() ? tree_stage_bytes<T>() : 0;
     if (smem > 0) {
-      const cudaError_t e = cudaFuncSetAttribute(tree_walk_kernel<T, kVecPath>,
+      const cudaError_t e = cudaFuncSetAttribute(tree_walk_kernel<T, kVecPath, false>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;
     }
@@ -652,8 +805,17 @@ cudaError_t launch_tree_t(const TreeProblem& p, const Workspace& w, cudaStream_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tree_walk_kernel<T, kVecPath>, p, w);
+    return cudaLaunchKernelEx(&cfg, tree_walk_kernel<T, kVecPath, false>, p, w);
   }
+  return cudaGetLastError();
+}
+
+template <typename T, bool kVecPath>
+cudaError_t launch_tree_lazy_t(const TreeProblem& p, const Workspace& w, cudaStream_t s) {
+  const long long blocks = static_cast<long long>(p.B) * kTreeCluster;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffLL || w.S1 > kTreeLazyMaxS1) return cudaErrorInvalidConfiguration;
+  tree_walk_kernel<T, kVecPath, true><<<dim3(static_cast<unsigned>(blocks)), kST, 0, s>>>(p, w);
   return cudaGetLastError();
 }
 
@@ -665,6 +827,13 @@ cudaError_t launch_tree_rowstats(int dtype, bool vec, const TreeProblem& p, cons
     return vec ? launch_tree_t<__nv_bfloat16, true>(p, w, s, false)
                : launch_tree_t<__nv_bfloat16, false>(p, w, s, false);
   return vec ? launch_tree_t<float, true>(p, w, s, false) : launch_tree_t<float, false>(p, w, s, false);
+}
+
+cudaError_t launch_tree_lazy(int dtype, bool vec, const TreeProblem& p, const Workspace& w,
+                             cudaStream_t s) {
+  if (dtype == 1)
+    return vec ? launch_tree_lazy_t<__nv_bfloat16, true>(p, w, s) : launch_tree_lazy_t<__nv_bfloat16, false>(p, w, s);
+  return vec ? launch_tree_lazy_t<float, true>(p, w, s) : launch_tree_lazy_t<float, false>(p, w, s);
 }
 
 cudaError_t launch_tree_walk(int dtype, bool vec, const TreeProblem& p, const Workspace& w,

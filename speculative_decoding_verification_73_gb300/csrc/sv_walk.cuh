@@ -140,6 +140,32 @@ __device__ __forceinline__ RowMax merge_greedy(const float4 (&pre)[kPre], const 
   });
 }
 
+// The same merges over partials gathered into this CTA's shared memory
+// (plain loads; the merge arithmetic is the same).
+__device__ __forceinline__ float4 partial_local(const Partial* at, bool take) {
+  return take ? *reinterpret_cast<const float4*>(at) : make_float4(-INFINITY, 0.f, __int_as_float(INT_MAX), 0.f);
+}
+
+__device__ __forceinline__ RowNorm merge_row_local(const Partial* parts, int n) {
+  float4 pre[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) pre[i] = partial_local(parts + i, i < n);
+  return merge_sampled_by(pre, n, [&](int i0, float4(&pt)[kBatch]) {
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) pt[i] = partial_local(parts + i0 + i, i0 + i < n);
+  });
+}
+
+__device__ __forceinline__ RowMax merge_row_greedy_local(const Partial* parts, int n) {
+  float4 pre[kPre];
+#pragma unroll
+  for (int i = 0; i < kPre; ++i) pre[i] = partial_local(parts + i, i < n);
+  return merge_greedy_by(pre, n, [&](int i0, float4(&pt)[kBatch]) {
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) pt[i] = partial_local(parts + i0 + i, i0 + i < n);
+  });
+}
+
 // ------------------------------------------------------- tagged partials
 // The chain sampler does not wait for the row-statistics grid to end: each
 // partial it needs is read with a relaxed 128-bit load and used once its tag

@@ -23,14 +23,15 @@ def lib():
     return binding.load()
 
 
-def run_tree(wl, seed=None, ctx=None):
+def run_tree(wl, seed=None, ctx=None, lazy=False):
     B, M, V = wl.shape
     own = ctx is None
     if own:
         ctx = binding.SpecVerify(max(B, 1), max(M, 1), V, TORCH_DT[wl.dtype])
     draft = wl.draft.cuda() if wl.mode == binding.SV_TREE_SAMPLED else None
     toks, path, acc, kv = ctx.tree(wl.target.cuda(), draft, wl.parents.cuda(), wl.tokens.cuda(),
-                                   wl.temperature.cuda(), wl.seed if seed is None else seed, wl.mode)
+                                   wl.temperature.cuda(), wl.seed if seed is None else seed, wl.mode,
+                                   lazy=lazy)
     code, bits = ctx.get_error()
     out = (toks.cpu().numpy().copy(), path.cpu().numpy().copy(), acc.cpu().numpy().copy(),
            kv.cpu().numpy().copy(), code, bits)
@@ -175,3 +176,71 @@ def test_repeated_sibling_tokens(mode):
     for seed in (26, 27, 28):
         res, _ = check_tree(wl, seed, f"repeat mode {mode} seed {seed}")
         assert res.errors == 0
+
+
+# ------------------------------------------------------------------ lazy walk
+
+LAZY_NAMES = [n for n in CASES if n != "huge-vocabulary-bf16"]
+
+
+@pytest.mark.parametrize("name", LAZY_NAMES + ["222-full"])
+def test_lazy_tree_is_the_eager_tree_bit_for_bit(name):
+    """spec_verify_tree_lazy reduces each row the walk reaches with the same
+    span reduction as the eager row statistics and merges the same partials
+    in the same order: identical outputs on valid inputs (three seeds, one
+    context, eager and lazy calls interleaved)."""
+    wl = (workloads.make_tree(32, 128256, "bf16", gen_seed=77, widths=(2, 2, 2), verify_seed=11)
+          if name == "222-full" else CASES[name]())
+    B, M, V = wl.shape
+    ctx = binding.SpecVerify(max(B, 1), max(M, 1), V, TORCH_DT[wl.dtype])
+    for seed in (wl.seed, wl.seed + 1000, 2 ** 64 - 3):
+        eager = run_tree(wl, seed, ctx)
+        lazy = run_tree(wl, seed, ctx, lazy=True)
+        for a, b in zip(eager[:4], lazy[:4]):
+            assert np.array_equal(a, b), name
+        assert eager[4:] == lazy[4:] == (0, 0)
+    ctx.close()
+
+
+def test_lazy_tree_reads_only_the_walked_rows():
+    """Bad rows off every request's walked path (a NaN target row of a node
+    the walk never reaches, a +inf draft row of an unvisited inner node) are
+    not errors for the lazy walk: its outputs are those of the clean input,
+    and equal the oracle's lazy reading; the same inputs fail the eager walk.
+    A NaN in the root's row fails both."""
+    from oracle import tree as ot
+    wl = workloads.make_tree(16, 5000, "bf16", gen_seed=405, widths=(2, 2, 2), temps=(0.0, 1.0), verify_seed=3)
+    clean = run_tree(wl, 3)
+    assert clean[4:] == (0, 0)
+    B, M, V = wl.shape
+    par = wl.parents.numpy()
+    kids = [ot.children_of([int(v) for v in par[b]], M) for b in range(B)]
+    for b in range(B):
+        seen = {0} | {int(n) for n in clean[1][b] if n >= 0}
+        off = [n for n in range(1, M + 1) if n not in seen]
+        wl.target[b, off[0], 7] = float("nan")
+        inner_off = [n for n in off if kids[b][n]]
+        if inner_off and float(wl.temperature[b]) > 0:
+            wl.draft[b, inner_off[0], 11] = float("inf")
+    lazy = run_tree(wl, 3, lazy=True)
+    assert lazy[4:] == (0, 0)
+    for a, b in zip(clean[:4], lazy[:4]):
+        assert np.array_equal(a, b)
+    z, y = wl.raw()
+    res = ot.verify_tree(z, y, par, wl.tokens.numpy(), wl.temperature.numpy(), 3, wl.dtype, wl.mode, lazy=True)
+    assert res.errors == 0
+    compare_tree(res, *lazy[:4], wl.temperature.numpy(), "lazy-off-path")
+    eager = run_tree(wl, 3)
+    assert eager[5] == binding.SV_ERRBIT_LOGIT and (eager[2] == -1).all()
+    wl.target[:, 0, 5] = float("nan")
+    for lz in (False, True):
+        out = run_tree(wl, 3, lazy=lz)
+        assert out[5] == binding.SV_ERRBIT_LOGIT and (out[2] == -1).all() and (out[0] == -1).all()
+
+
+def test_lazy_tree_takes_rows_of_at_most_32_spans():
+    """Rows of more than 32 spans of 64 KB are refused before anything is
+    enqueued (SV_EINVAL); the eager walk takes them."""
+    wl = CASES["huge-vocabulary-bf16"]()
+    with pytest.raises(binding.SpecVerifyError):
+        run_tree(wl, lazy=True)

@@ -219,3 +219,59 @@ def test_255_node_trees_walk_validly(shape):
             kids = [i + 1 for i in range(par.shape[1]) if int(par[b, i]) == node]
             g = int(np.argmax(rows[node]))
             assert emitted[a] == g and all(int(toks[b, c - 1]) != g for c in kids)
+
+
+LAZY_CASES = [
+    dict(batch=12, vocab=3000, dtype="f32", gen_seed=401, widths=(2, 2, 2)),
+    dict(batch=12, vocab=3000, dtype="bf16", gen_seed=402, widths=(3, 2)),
+    dict(batch=10, vocab=2000, dtype="f32", gen_seed=403, m=20),
+    dict(batch=10, vocab=2000, dtype="bf16", gen_seed=404, widths=(2, 2), mode=workloads.TREE_TOPK),
+]
+
+
+@pytest.mark.parametrize("case", range(len(LAZY_CASES)))
+def test_lazy_reading_equals_the_eager_one_on_valid_rows(case):
+    """Reading a node's rows only when the walk reaches it changes nothing
+    on valid inputs (greedy, sampled and TOPK requests, fixed and random
+    topologies, three seeds)."""
+    wl = workloads.make_tree(**LAZY_CASES[case])
+    z, y = wl.raw()
+    for seed in (0, 7, 2 ** 64 - 1):
+        args = (z, y, wl.parents.numpy(), wl.tokens.numpy(), wl.temperature.numpy(), seed, wl.dtype, wl.mode)
+        e, l = ot.verify_tree(*args), ot.verify_tree(*args, lazy=True)
+        assert e.errors == l.errors == 0
+        for a, b in ((e.tokens, l.tokens), (e.path, l.path), (e.accept_len, l.accept_len), (e.kv_len, l.kv_len)):
+            assert np.array_equal(a, b)
+
+
+def test_lazy_reading_checks_only_the_rows_it_reads():
+    """A NaN in the target row (or +inf in the draft row) of a node the walk
+    never reaches fails the eager reading but not the lazy one, whose outputs
+    stay those of the clean input; the same NaN in the root's row fails both."""
+    wl = workloads.make_tree(16, 500, "f32", gen_seed=405, widths=(2, 2, 2), temps=(0.0, 1.0))
+    z, y = wl.raw()
+    par, tok, temp = wl.parents.numpy(), wl.tokens.numpy(), wl.temperature.numpy()
+    clean = ot.verify_tree(z, y, par, tok, temp, 3, "f32", ot.SAMPLED)
+    assert clean.errors == 0
+    zz, yy = z.copy(), y.copy()
+    kids = [ot.children_of([int(v) for v in par[b]], par.shape[1]) for b in range(par.shape[0])]
+    planted = 0
+    for b in range(par.shape[0]):
+        seen = {0} | {int(n) for n in clean.path[b] if n >= 0}
+        off = [n for n in range(1, par.shape[1] + 1) if n not in seen]
+        zz[b, off[0], 7] = np.nan
+        inner_off = [n for n in off if kids[b][n]]
+        if inner_off and temp[b] > 0:
+            yy[b, inner_off[0], 11] = np.inf
+        planted += 1
+    assert planted == par.shape[0]
+    eager = ot.verify_tree(zz, yy, par, tok, temp, 3, "f32", ot.SAMPLED)
+    lazy = ot.verify_tree(zz, yy, par, tok, temp, 3, "f32", ot.SAMPLED, lazy=True)
+    assert eager.errors == ov.ERR_LOGIT and (eager.accept_len == -1).all()
+    assert lazy.errors == 0
+    for a, b in ((clean.tokens, lazy.tokens), (clean.path, lazy.path), (clean.accept_len, lazy.accept_len)):
+        assert np.array_equal(a, b)
+    zr = z.copy()
+    zr[:, 0, 5] = np.nan
+    both = [ot.verify_tree(zr, y, par, tok, temp, 3, "f32", ot.SAMPLED, lazy=lz) for lz in (False, True)]
+    assert all(r.errors == ov.ERR_LOGIT and (r.accept_len == -1).all() for r in both)
