@@ -253,5 +253,61 @@ __device__ __forceinline__ Partial span_partial_vec(const T* row, int beg, int e
   return span_finish<kGreedy>(acc, red_f, red_g, red_i);
 }
 
+// The span [beg, end) of a row read through a ring in shared memory: each
+// thread fetches its own vectors with cp.async into its own slots kDepth
+// groups ahead of the group it reduces, so more of the span is in flight
+// than registers would hold (a thread reads only slots it filled itself,
+// after its own cp.async.wait_group: no CTA barrier).  `ring` holds
+// kDepth * kGroup * kThreads vectors.  The same partial as span_partial_vec
+// (same vectors per thread, same groups, same order).
+template <int kDepth>
+constexpr int span_ring_bytes() {
+  return kDepth * kGroup * kThreads * 16;
+}
+template <typename T, bool kGreedy, bool kFull, int kDepth>
+__device__ __forceinline__ Partial span_partial_ring(const T* row, int beg, int end, float k, int d,
+                                                     float* tok_out, uint4* ring) {
+  using E = Elem<T>;
+  constexpr int kVecs = kSpanBytes / 16 / kThreads;  // vectors per thread
+  constexpr int kGroups = kVecs / kGroup;
+  static_assert(kDepth >= 1 && kDepth <= 3 && kDepth <= kGroups, "ring depth");
+  __shared__ float red_f[kThreads / 32];
+  __shared__ float red_g[kThreads / 32];
+  __shared__ int red_i[kThreads / 32];
+  const uint4* vp = reinterpret_cast<const uint4*>(row + beg);
+  const int nv = kFull ? kVecs * kThreads : (end - beg) / E::kVec;
+  const uint4 pad = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+  auto slot = [&](int gi, int u) { return ring + ((gi % kDepth) * kGroup + u) * kThreads + threadIdx.x; };
+  auto issue = [&](int gi) {
+#pragma unroll
+    for (int u = 0; u < kGroup; ++u) {
+      const int v = threadIdx.x + (gi * kGroup + u) * kThreads;
+      if (kFull || v < nv)
+        cp_async16(slot(gi, u), vp + v);
+      else
+        *slot(gi, u) = pad;
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int gi = 0; gi < kDepth; ++gi) issue(gi);
+  SpanAcc acc = span_acc_init();
+  const uint64_t k2 = f2pack(k, k);
+  const TokAt ta = kGreedy ? TokAt{-1, 0, 0} : tok_at<T>(beg, end, d);
+#pragma unroll
+  for (int gi = 0; gi < kGroups; ++gi) {
+    cp_async_wait_group<kDepth - 1>();  // this thread's copies of group gi have landed
+    uint4 g[kGroup];
+#pragma unroll
+    for (int u = 0; u < kGroup; ++u) g[u] = *slot(gi, u);
+    if (gi + kDepth < kGroups)
+      issue(gi + kDepth);  // into the slot just read
+    else
+      cp_async_commit();  // an empty group keeps the count of groups in step
+    span_group<T, kGreedy>(acc, g, beg, gi, k2, k, ta, tok_out);
+  }
+  return span_finish<kGreedy>(acc, red_f, red_g, red_i);
+}
+
 }  // namespace
 }  // namespace sv

@@ -147,6 +147,12 @@ constexpr bool tree_stages() {
 // decisions.  Rows of nodes the walk never reaches are neither read nor
 // checked.  Rows of at most kTreeLazyMaxS1 spans.
 constexpr int kTreeLazyMaxS1 = kTreeLazyMaxSpans;
+// groups of loads in flight per thread in the lazy walk's span reductions
+// (a cp.async ring in dynamic shared memory)
+#ifndef SV_TREE_LAZY_RING
+#define SV_TREE_LAZY_RING 2
+#endif
+constexpr int kTreeLazyRing = SV_TREE_LAZY_RING;
 constexpr int kTreeLazySlots = (2 * kTreeLazyMaxS1 + kTreeCluster - 1) / kTreeCluster;  // items per CTA
 
 template <typename T, bool kVecPath, bool kLazy>
@@ -323,14 +329,15 @@ __global__ void __cluster_dims__(kTreeCluster, 1, 1)
       const T* row = static_cast<const T*>(dr ? p.draft : p.target) + (static_cast<size_t>(b) * (M + 1) + node) * V;
       const int beg = span * kSpan, end = min(V, beg + kSpan);
       Partial out;
+      uint4* ring = reinterpret_cast<uint4*>(s_stage_raw);
       if (!kVecPath)
         out = chunk_partial_scalar<T>(row, beg, end, greedy_row, k, -1, nullptr);
       else if (end - beg == kSpan)
-        out = greedy_row ? span_partial_vec<T, true, true>(row, beg, end, k, -1, nullptr)
-                         : span_partial_vec<T, false, true>(row, beg, end, k, -1, nullptr);
+        out = greedy_row ? span_partial_ring<T, true, true, kTreeLazyRing>(row, beg, end, k, -1, nullptr, ring)
+                         : span_partial_ring<T, false, true, kTreeLazyRing>(row, beg, end, k, -1, nullptr, ring);
       else
-        out = greedy_row ? span_partial_vec<T, true, false>(row, beg, end, k, -1, nullptr)
-                         : span_partial_vec<T, false, false>(row, beg, end, k, -1, nullptr);
+        out = greedy_row ? span_partial_ring<T, true, false, kTreeLazyRing>(row, beg, end, k, -1, nullptr, ring)
+                         : span_partial_ring<T, false, false, kTreeLazyRing>(row, beg, end, k, -1, nullptr, ring);
       if (i == 0) s_own[par][li] = out;
     }
     cluster_sync();  // every CTA's partials of this visit are in its shared memory
@@ -815,7 +822,8 @@ cudaError_t launch_tree_lazy_t(const TreeProblem& p, const Workspace& w, cudaStr
   const long long blocks = static_cast<long long>(p.B) * kTreeCluster;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL || w.S1 > kTreeLazyMaxS1) return cudaErrorInvalidConfiguration;
-  tree_walk_kernel<T, kVecPath, true><<<dim3(static_cast<unsigned>(blocks)), kST, 0, s>>>(p, w);
+  const int smem = kVecPath ? span_ring_bytes<kTreeLazyRing>() : 0;
+  tree_walk_kernel<T, kVecPath, true><<<dim3(static_cast<unsigned>(blocks)), kST, smem, s>>>(p, w);
   return cudaGetLastError();
 }
 
