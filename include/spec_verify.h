@@ -392,8 +392,9 @@ int spec_verify_debug_stats(spec_verify_ctx* ctx, int B, int N,
 
 /*
  * Kernel timing for benchmarks.  spec_verify_profile(ctx, every) with
- * every > 0 makes every every-th call of spec_verify, spec_verify_tree and
- * spec_verify_lazy on the context (the first, then each every-th after it;
+ * every > 0 makes every every-th call of spec_verify, spec_verify_tree,
+ * spec_verify_tree_lazy and spec_verify_lazy on the context (the first, then
+ * each every-th after it;
  * 1 = all calls) record CUDA events around each kernel it launches on the
  * context's stream; every == 0 turns this off, and a negative value is
  * SV_EINVAL.  Events around kernels keep them from overlapping one another,
@@ -404,8 +405,8 @@ int spec_verify_debug_stats(spec_verify_ctx* ctx, int B, int N,
  * recorded calls; it then clears the sums.  For spec_verify slot 0 is the
  * row-statistics kernel (every logit row streamed once, with the draft
  * tokens' logits) and slot 1 the walk and draw kernel; for spec_verify_tree
- * the same with the tree walk; spec_verify_lazy launches one kernel (slot 0;
- * slot 1 reads 0).
+ * the same with the tree walk; spec_verify_lazy and spec_verify_tree_lazy
+ * launch one kernel each (slot 0; slot 1 reads 0).
  */
 #define SV_NUM_KERNELS 2
 int spec_verify_profile(spec_verify_ctx* ctx, int every);
