@@ -183,14 +183,15 @@ def test_repeated_sibling_tokens(mode):
 LAZY_NAMES = [n for n in CASES if n != "huge-vocabulary-bf16"]
 
 
-@pytest.mark.parametrize("name", LAZY_NAMES + ["222-full"])
+@pytest.mark.parametrize("name", LAZY_NAMES + ["222-full"] + list(MAX_CASES))
 def test_lazy_tree_is_the_eager_tree_bit_for_bit(name):
     """spec_verify_tree_lazy reduces each row the walk reaches with the same
     span reduction as the eager row statistics and merges the same partials
     in the same order: identical outputs on valid inputs (three seeds, one
-    context, eager and lazy calls interleaved)."""
+    context, eager and lazy calls interleaved), up to 255-node trees (the
+    line tree's walks visit up to 256 nodes each)."""
     wl = (workloads.make_tree(32, 128256, "bf16", gen_seed=77, widths=(2, 2, 2), verify_seed=11)
-          if name == "222-full" else CASES[name]())
+          if name == "222-full" else MAX_CASES[name]() if name in MAX_CASES else CASES[name]())
     B, M, V = wl.shape
     ctx = binding.SpecVerify(max(B, 1), max(M, 1), V, TORCH_DT[wl.dtype])
     for seed in (wl.seed, wl.seed + 1000, 2 ** 64 - 3):
