@@ -428,9 +428,9 @@ int spec_verify_debug_philox(uint64_t seed, const uint32_t* ctr3, uint32_t* out4
 
 /*
  * spec_verify_debug_read_stream -- measurement hook: the achievable
- * streaming-read bandwidth of this GPU, for the row statistics' roofline
- * (the survey's measurement row asks for a plain streaming-read kernel on
- * the same box beside the nominal peak).  Reads the `bytes` bytes at buf
+ * streaming-read bandwidth of this GPU, reported beside the nominal and the
+ * measured copy peaks as the row statistics' size-matched reference (what a
+ * plain read of the same bytes achieves).  Reads the `bytes` bytes at buf
  * (device, 16-byte aligned, bytes a multiple of 16) once with 16-byte
  * non-allocating loads from a grid of 8 CTAs per SM (one kernel launch and
  * nothing else), and adds the sum of the buffer's 64-bit little-endian
