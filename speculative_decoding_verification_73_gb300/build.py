@@ -4,7 +4,7 @@
 
 Compiles every csrc/*.cu for sm_103a in parallel with nvcc, then links one
 shared library next to this file.  The CUDA runtime is linked statically,
-so the library only needs the driver at run time.
+so the library only needs the CUDA driver at run time.
 """
 
 import concurrent.futures
