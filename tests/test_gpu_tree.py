@@ -245,3 +245,26 @@ def test_lazy_tree_takes_rows_of_at_most_32_spans():
     wl = CASES["huge-vocabulary-bf16"]()
     with pytest.raises(binding.SpecVerifyError):
         run_tree(wl, lazy=True)
+
+
+def test_lazy_tree_errors_are_flagged_per_request():
+    """The eager error workload through the lazy walk: temperature, topology
+    and token errors as in spec_verify_tree (checked before the walk); the
+    +inf logit sits in node 2's row, an error only if that request's walk
+    reaches node 2 -- exactly the oracle's lazy reading."""
+    from oracle import tree as ot
+    wl = workloads.make_tree(6, 2048, "f32", gen_seed=78, widths=(2, 2), temps=(1.0,), verify_seed=2)
+    wl.temperature[0] = float("nan")
+    wl.parents[1, 3] = 5            # node 4 under node 5
+    wl.tokens[2, 0] = 2048          # out of range
+    wl.target[3, 2, 7] = float("inf")
+    wl.parents[4, 0] = -1
+    toks, path, acc, kv, code, bits = run_tree(wl, lazy=True)
+    z, y = wl.raw()
+    res = ot.verify_tree(z, y, wl.parents.numpy(), wl.tokens.numpy(), wl.temperature.numpy(), wl.seed,
+                         wl.dtype, wl.mode, lazy=True)
+    assert bits == res.errors
+    for b, bit in ((0, 1), (1, 8), (2, 2), (4, 8)):
+        assert res.request_errors[b] == bit
+        assert acc[b] == -1 and kv[b] == 0 and (toks[b] == -1).all() and (path[b] == -1).all()
+    compare_tree(res, toks, path, acc, kv, wl.temperature.numpy(), "lazy-errors")
