@@ -84,7 +84,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // beta vector once and applies it to every row: the loads of gamma / beta
 // (four times the bytes of the row vector they scale) kept the kernel bound
 // by L1 when every warp had its own row.
-constexpr int kPrepRows = 4;   // tokens of one segment per CTA
+// Tokens of one segment per CTA (build-time override -DSV_PREP_ROWS=<n>):
+// four at 64 registers (4 CTAs per SM) measured 314.8 us per LayerNorm call
+// at T = d = d_out = 4096, two at 40 registers (6 per SM) 316.1 us, two at
+// 58 registers (4 per SM) 319.7 us.
+#ifndef SV_PREP_ROWS
+#define SV_PREP_ROWS 4
+#endif
+constexpr int kPrepRows = SV_PREP_ROWS;
 constexpr int kPrepVec = 2;    // vectors per lane and row: 8 warps x 32 lanes x 2 x 8 = 4096 columns
 constexpr int kPrepMaxD = 8 * 32 * kPrepVec * 8;
 
