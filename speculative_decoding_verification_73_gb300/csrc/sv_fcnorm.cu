@@ -95,13 +95,6 @@ constexpr int kPrepRows = SV_PREP_ROWS;
 constexpr int kPrepVec = 2;    // vectors per lane and row: 8 warps x 32 lanes x 2 x 8 = 4096 columns
 constexpr int kPrepMaxD = 8 * 32 * kPrepVec * 8;
 
-__device__ __forceinline__ float vsum8(const uint4& v) {
-  float t = 0.f;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) t += Elem<__nv_bfloat16>::get(v, e);  // zeros past the row
-  return t;
-}
-
 // The CTA's total of one per-warp partial each, in warp order.
 __device__ __forceinline__ float warps_total(const float* s_part) {
   float t = s_part[0];
